@@ -1,0 +1,15 @@
+"""Float64 CPU oracle for the FLASH GAU forward (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and the
+two share no code.
+"""
+
+from .flash_gau import (  # noqa: F401
+    swish,
+    scale_offset,
+    relpos_bias,
+    chunk_scores,
+    flash_gau,
+    algorithmic_flops_per_token,
+)

@@ -1,0 +1,198 @@
+"""Float64 CPU oracle for the FLASH gated-attention-unit forward pass with
+mixed chunk attention.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plainly written
+definition that the CUDA path is checked against.  Only the test suite, the
+smoke check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py``
+may import it; the library itself never does, and it shares no code with the
+CUDA kernels.
+
+Sources ("the pages"):
+  [FLASH-blog]  "FLASH: Possibly the Most Interesting Efficient Transformer
+                Design in Recent Times" (kexue.fm, translated), sections
+                "Gated Attention", "Weak Attention", "Mixed Chunking".
+  [TQLT]        "Transformer Quality in Linear Time" (wikillm summary of
+                arXiv 2202.10447): Method, eq. 5, eq. 7, eq. 8, and the
+                gau_block / flash_block pseudocode.
+  [TQLT-zh]     "Transformer Quality in Linear Time" (papercache summary),
+                appendix D, Code 4 (relative position bias).
+
+Readings taken where the pages disagree or are silent:
+  * scores are scaled by 1/C inside relu^2, before the bias is added
+    ([TQLT] flash_block pseudocode; gau_block divides by the length N, which
+    is the same rule at C = T);
+  * the global term is the plain sum of chunk states of eq. 7 / eq. 8, times
+    a caller-chosen ``lin_scale`` (1 = eq. 7/8, 1/C = the listing's division,
+    0 = the LocalOnly ablation);
+  * b[i, j] = relpos[j - i + C - 1], the Toeplitz matrix the Code 4 listing
+    builds from 2C-1 weights, used for every C;
+  * the causal mask keeps the diagonal (j <= i) and is applied after relu^2;
+  * the causal global term of the first chunk is the empty sum, i.e. zero;
+  * no bias terms, norm, RoPE or residual (the layer as eq. 3-8 write it).
+
+Parity: every function here is pinned by tests/test_oracle.py against
+independent formulations (a scalar token loop, the full-length linear
+attention of the pages' associativity argument, a library Toeplitz
+constructor, the GLU special case, chunk-permutation invariance, golden
+fixtures derived by hand from the Code 4 listing).
+"""
+
+import numpy as np
+
+__all__ = [
+    "swish",
+    "scale_offset",
+    "relpos_bias",
+    "chunk_scores",
+    "flash_gau",
+    "algorithmic_flops_per_token",
+]
+
+
+def swish(x):
+    """SiLU / Swish, phi(x) = x * sigmoid(x) = x / (1 + exp(-x)).
+
+    [FLASH-blog] "Gated Attention": the paper applies Swish to U and V (and
+    [TQLT] gau_block applies it to the whole 2e+s projection, so to Z too).
+    Written as x / (1 + exp(-x)); for very negative x, exp(-x) overflows to
+    inf and the quotient is the correct limit -0.0.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def scale_offset(Z, gamma, beta):
+    """The four per-dimension affine heads of mixed chunk attention.
+
+    [TQLT] Method: queries and keys come from Z by a per-dimension scale and
+    offset; FLASH derives four heads Q_quad, K_quad, Q_lin, K_lin from the
+    same Z ([TQLT] "Mixed chunk attention"; [FLASH-blog] "Mixed Chunking").
+
+    Z: [..., s];  gamma, beta: [4, s] with rows (Q_quad, K_quad, Q_lin, K_lin).
+    Returns a tuple of four arrays shaped like Z.
+    """
+    Z = np.asarray(Z, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    return tuple(Z * gamma[h] + beta[h] for h in range(4))
+
+
+def relpos_bias(relpos, n):
+    """Relative position bias for one length-n window: a Toeplitz matrix
+    built from 2n-1 learned weights, b[i, j] = relpos[j - i + n - 1].
+
+    [TQLT-zh] appendix D, Code 4 (the n < 512 branch): the listing pads,
+    tiles, reshapes and slices the weight vector; worked by hand for n = 3
+    that yields row i = (w[2-i], w[3-i], w[4-i]), i.e. the index rule above
+    (tests/golden/relpos_toeplitz_n3.txt).
+    """
+    relpos = np.asarray(relpos, dtype=np.float64)
+    if relpos.shape != (2 * n - 1,):
+        raise ValueError("relpos must have 2n-1 entries")
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    return relpos[j - i + n - 1]
+
+
+def chunk_scores(q, k, bias, C, causal):
+    """Attention weights inside one chunk: A = relu^2(q k^T / C + b), with
+    entries above the diagonal set to zero when causal.
+
+    [TQLT] eq. 5 (relu^2 of scores plus relative bias) and the flash_block
+    pseudocode (division by C before the bias, lower-triangular mask applied
+    to the relu^2 kernel); [FLASH-blog] "Mixed Chunking" (decoders mask out
+    the upper triangle).
+    """
+    s = q @ k.T / C + bias
+    a = np.maximum(s, 0.0) ** 2
+    if causal:
+        a = np.tril(a)  # keeps j <= i
+    return a
+
+
+def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
+              lin_scale=1.0):
+    """FLASH GAU layer forward with mixed chunk attention, in float64.
+
+    Steps ([TQLT] Method and flash_block; [FLASH-blog] "Mixed Chunking"):
+      1. U = swish(X W_u), V = swish(X W_v), Z = swish(X W_z).
+      2. Q_quad, K_quad, Q_lin, K_lin = Z * gamma_h + beta_h.
+      3. Per chunk g of C tokens: Vq_g = relu^2(Q_quad,g K_quad,g^T / C + b) V_g
+         (upper triangle zeroed when causal).
+      4. State_g = K_lin,g^T V_g.
+      5. Prefix_g = sum_{h<g} State_h if causal (eq. 8), else sum_h State_h
+         (eq. 7).
+      6. Vl_g = lin_scale * Q_lin,g Prefix_g.
+      7. O_g = [U_g * (Vq_g + Vl_g)] W_o   ([TQLT] display after eq. 8).
+
+    X: [B, T, d]; W_u, W_v: [d, e]; W_z: [d, s]; W_o: [e, d];
+    gamma, beta: [4, s]; relpos: [2C-1]; T must be a multiple of C
+    ([FLASH-blog] "Mixed Chunking" assumes divisibility).
+
+    Returns (O, inter) with O: [B, T, d] float64 and ``inter`` a dict of the
+    intermediates U, V, Z, heads [4, B, T, s], state [B, G, s, e],
+    prefix [B, G, s, e], Vq, Vl, gated [B, T, e].
+    """
+    X = np.asarray(X, dtype=np.float64)
+    B, T, d = X.shape
+    if C <= 0 or T % C != 0:
+        raise ValueError("T must be a positive multiple of C")
+    G = T // C
+    e = W_u.shape[1]
+    s = W_z.shape[1]
+
+    U = swish(X @ np.asarray(W_u, dtype=np.float64))
+    V = swish(X @ np.asarray(W_v, dtype=np.float64))
+    Z = swish(X @ np.asarray(W_z, dtype=np.float64))
+    Qq, Kq, Ql, Kl = scale_offset(Z, gamma, beta)
+    bias = relpos_bias(relpos, C)
+
+    Vq = np.zeros((B, T, e))
+    state = np.zeros((B, G, s, e))
+    for b in range(B):
+        for g in range(G):
+            rows = slice(g * C, (g + 1) * C)
+            a = chunk_scores(Qq[b, rows], Kq[b, rows], bias, C, causal)
+            Vq[b, rows] = a @ V[b, rows]
+            state[b, g] = Kl[b, rows].T @ V[b, rows]
+
+    prefix = np.zeros((B, G, s, e))
+    for b in range(B):
+        total = np.zeros((s, e))
+        for g in range(G):
+            if causal:
+                prefix[b, g] = total  # strictly earlier chunks only
+            total = total + state[b, g]
+        if not causal:
+            prefix[b, :] = total
+
+    Vl = np.zeros((B, T, e))
+    for b in range(B):
+        for g in range(G):
+            rows = slice(g * C, (g + 1) * C)
+            Vl[b, rows] = lin_scale * (Ql[b, rows] @ prefix[b, g])
+
+    gated = U * (Vq + Vl)
+    O = gated @ np.asarray(W_o, dtype=np.float64)
+    inter = dict(U=U, V=V, Z=Z, heads=np.stack([Qq, Kq, Ql, Kl]),
+                 state=state, prefix=prefix, Vq=Vq, Vl=Vl, gated=gated)
+    return O, inter
+
+
+def algorithmic_flops_per_token(d, e, s, C, causal, quad_only=False):
+    """Floating-point operations the layer must do per token (one multiply
+    plus one add counted as two), excluding the masked upper triangle:
+
+      projection 2d(2e+s) + output 2ed + scores 2*Cbar*s + mixing 2*Cbar*e
+      + chunk state 2se + linear read-out 2se,
+
+    with Cbar = (C+1)/2 when causal (average visible keys per query) and C
+    otherwise; the two linear-term products are omitted for FLASH-Quad
+    (C = T, causal, no global term).
+    """
+    cbar = (C + 1) / 2.0 if causal else float(C)
+    f = 2 * d * (2 * e + s) + 2 * e * d + 2 * cbar * s + 2 * cbar * e
+    if not quad_only:
+        f += 4 * s * e
+    return f

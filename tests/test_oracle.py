@@ -1,0 +1,277 @@
+"""Pins for the float64 oracle, each against something other than the oracle
+itself: library routines, hand-derived golden fixtures, a scalar per-token
+formulation, the pages' associativity and cumulative-sum arguments, special
+cases that reduce the layer to a GLU or to FLASH-Quad, and invariants.
+CPU only."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+
+from oracle import flash_gau, relpos_bias, swish, algorithmic_flops_per_token
+from efficient_attention_transformer_gb300.synthetic import (
+    make_inputs, round_bf16)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load_index_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(t) for t in line.split()])
+    return np.array(rows)
+
+
+def _run(inp, C, causal, lin_scale=1.0):
+    return flash_gau(inp["X"], inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"],
+                     inp["gamma"], inp["beta"], inp["relpos"], C, causal,
+                     lin_scale)
+
+
+# ---------------------------------------------------------------- swish ----
+
+def test_swish_matches_scipy_expit():
+    x = np.concatenate([np.linspace(-30, 30, 2001), [0.0, -745.0, 800.0]])
+    ref = x * scipy.special.expit(x)
+    np.testing.assert_allclose(swish(x), ref, rtol=1e-14, atol=1e-300)
+    assert swish(0.0) == 0.0
+
+
+# ---------------------------------------------------- relative position ----
+
+@pytest.mark.parametrize("n,name", [(3, "relpos_toeplitz_n3.txt"),
+                                    (5, "relpos_toeplitz_n5.txt")])
+def test_relpos_golden_from_code4(n, name):
+    idx = _load_index_table(name)
+    w = np.arange(2 * n - 1, dtype=np.float64)
+    np.testing.assert_array_equal(relpos_bias(w, n), idx.astype(np.float64))
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 64])
+def test_relpos_matches_scipy_toeplitz(n):
+    w = np.random.default_rng(n).standard_normal(2 * n - 1)
+    # first column b[i, 0] = w[n-1-i]; first row b[0, j] = w[n-1+j]
+    ref = scipy.linalg.toeplitz(w[n - 1::-1], w[n - 1:])
+    np.testing.assert_array_equal(relpos_bias(w, n), ref)
+
+
+# ------------------------------------------------- scalar token loop -------
+
+def _brute_force(inp, C, causal, lin_scale):
+    """Per-token scalar restatement: every output element summed from its
+    inputs with Python floats; the global term is token-level linear
+    attention over tokens of strictly earlier chunks (causal) or all chunks
+    (non-causal), never through chunk states."""
+    X, Wu, Wv, Wz, Wo = (inp[k].tolist() for k in ("X", "W_u", "W_v", "W_z", "W_o"))
+    ga, be, rp = inp["gamma"].tolist(), inp["beta"].tolist(), inp["relpos"].tolist()
+    B, T, d = inp["X"].shape
+    e, s = inp["W_u"].shape[1], inp["W_z"].shape[1]
+
+    def sw(a):
+        return a / (1.0 + math.exp(-a))
+
+    def proj(x, W, n):
+        return [sw(sum(x[k] * W[k][j] for k in range(d))) for j in range(n)]
+
+    O = np.zeros((B, T, d))
+    for b in range(B):
+        u = [proj(X[b][t], Wu, e) for t in range(T)]
+        v = [proj(X[b][t], Wv, e) for t in range(T)]
+        z = [proj(X[b][t], Wz, s) for t in range(T)]
+        head = [[[z[t][k] * ga[h][k] + be[h][k] for k in range(s)]
+                 for t in range(T)] for h in range(4)]
+        qq, kq, ql, kl = head
+        for t in range(T):
+            g, i = divmod(t, C)
+            mix = [0.0] * e
+            for j in range(C):
+                if causal and j > i:
+                    continue
+                tj = g * C + j
+                sc = sum(qq[t][k] * kq[tj][k] for k in range(s)) / C + rp[j - i + C - 1]
+                a = max(sc, 0.0) ** 2
+                for c in range(e):
+                    mix[c] += a * v[tj][c]
+            for tp in range(T):
+                gp = tp // C
+                if causal and gp >= g:
+                    continue
+                w = lin_scale * sum(ql[t][k] * kl[tp][k] for k in range(s))
+                for c in range(e):
+                    mix[c] += w * v[tp][c]
+            for o in range(d):
+                O[b, t, o] = sum(u[t][c] * mix[c] * Wo[c][o] for c in range(e))
+    return O
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("T,C", [(12, 4), (6, 6), (8, 2)])
+def test_oracle_matches_scalar_token_loop(causal, T, C):
+    inp = make_inputs(B=2, T=T, d=3, e=5, s=2, C=C, dtype="fp32", seed=7)
+    # larger head scales so relu^2 is active on some pairs and off on others
+    inp["gamma"] = inp["gamma"] * 3.0
+    O, _ = _run(inp, C, causal, lin_scale=0.5)
+    ref = _brute_force(inp, C, causal, lin_scale=0.5)
+    np.testing.assert_allclose(O, ref, rtol=1e-11, atol=1e-12)
+
+
+# --------------------------------------------- special cases of the layer --
+
+def test_attention_identity_reduces_to_glu():
+    """A = I turns GAU into a GLU with Swish on both branches ("Gated
+    Attention" / "Joining Forces": O = (U * V) W_o).  A = I is reached through
+    the parameters: zero quadratic heads make Q K^T = 0, and a bias that is 1
+    on the diagonal and -1 elsewhere gives relu^2(b) = I; a zero linear query
+    removes the global term."""
+    C = 8
+    inp = make_inputs(B=2, T=32, d=16, e=24, s=8, C=C, dtype="fp32", seed=3)
+    inp["gamma"][[0, 1, 2]] = 0.0
+    inp["beta"][[0, 1, 2]] = 0.0
+    inp["relpos"] = -np.ones(2 * C - 1)
+    inp["relpos"][C - 1] = 1.0
+    for causal in (True, False):
+        O, _ = _run(inp, C, causal)
+        X = inp["X"]
+        hu, hv = X @ inp["W_u"], X @ inp["W_v"]
+        glu = (hu * scipy.special.expit(hu)) * (hv * scipy.special.expit(hv))
+        np.testing.assert_allclose(O, glu @ inp["W_o"], rtol=1e-12, atol=1e-13)
+
+
+def test_causal_first_chunk_has_no_global_term():
+    C = 16
+    inp = make_inputs(B=3, T=64, d=8, e=12, s=4, C=C, dtype="fp32", seed=5)
+    _, it = _run(inp, C, True)
+    assert np.all(it["prefix"][:, 0] == 0.0)
+    assert np.all(it["Vl"][:, :C] == 0.0)
+    assert np.any(it["Vl"][:, C:] != 0.0)
+
+
+def test_noncausal_global_term_is_full_linear_attention():
+    """Eq. 7 summed over chunks equals linear attention applied to the whole
+    sequence, (Q_lin K_lin^T) V ("Mixed Chunking": exactly equivalent)."""
+    C = 8
+    inp = make_inputs(B=2, T=40, d=8, e=12, s=6, C=C, dtype="fp32", seed=11)
+    _, it = _run(inp, C, False, lin_scale=0.25)
+    Ql, Kl = it["heads"][2], it["heads"][3]
+    for b in range(2):
+        ref = 0.25 * (Ql[b] @ Kl[b].T) @ it["V"][b]
+        np.testing.assert_allclose(it["Vl"][b], ref, rtol=1e-11, atol=1e-11)
+
+
+def test_causal_global_term_is_token_cumsum_at_chunk_ends():
+    """Eq. 8 equals token-level linear attention read at the end of the
+    previous chunk: M_t = M_{t-1} + K_t V_t^T (the cumulative-sum form of
+    section 3.1), and chunk g reads M at token gC - 1."""
+    C = 4
+    inp = make_inputs(B=2, T=24, d=6, e=7, s=5, C=C, dtype="fp32", seed=13)
+    _, it = _run(inp, C, True)
+    Ql, Kl, V = it["heads"][2], it["heads"][3], it["V"]
+    for b in range(2):
+        M = np.cumsum(Kl[b][:, :, None] * V[b][:, None, :], axis=0)  # [T, s, e]
+        for t in range(24):
+            g = t // C
+            ref = np.zeros(7) if g == 0 else Ql[b, t] @ M[g * C - 1]
+            np.testing.assert_allclose(it["Vl"][b, t], ref, rtol=1e-11, atol=1e-11)
+
+
+def test_noncausal_invariant_to_chunk_permutation():
+    """Local attention stays inside a chunk and eq. 7's global sum is
+    order-free, so permuting whole chunks of the input permutes the output
+    the same way."""
+    C, G = 8, 5
+    inp = make_inputs(B=2, T=C * G, d=8, e=10, s=4, C=C, dtype="fp32", seed=17)
+    O, _ = _run(inp, C, False)
+    perm = np.array([3, 0, 4, 2, 1])
+    rows = np.concatenate([np.arange(p * C, (p + 1) * C) for p in perm])
+    inp2 = dict(inp, X=inp["X"][:, rows])
+    O2, _ = _run(inp2, C, False)
+    np.testing.assert_allclose(O2, O[:, rows], rtol=1e-11, atol=1e-12)
+    # causal is NOT invariant: the global term depends on chunk order
+    Oc, _ = _run(inp, C, True)
+    Oc2, _ = _run(inp2, C, True)
+    assert not np.allclose(Oc2, Oc[:, rows])
+
+
+def test_zero_quadratic_heads_leave_only_global_term():
+    C = 8
+    inp = make_inputs(B=1, T=32, d=8, e=10, s=4, C=C, dtype="fp32", seed=19)
+    inp["gamma"][[0, 1]] = 0.0
+    inp["beta"][[0, 1]] = 0.0
+    inp["relpos"][:] = 0.0
+    O, it = _run(inp, C, True)
+    assert np.all(it["Vq"] == 0.0)
+    np.testing.assert_allclose(O, (it["U"] * it["Vl"]) @ inp["W_o"], rtol=1e-13)
+
+
+def test_large_negative_bias_switches_relu2_off():
+    C = 8
+    inp = make_inputs(B=1, T=16, d=8, e=6, s=4, C=C, dtype="fp32", seed=23)
+    inp["relpos"][:] = -1e3
+    _, it = _run(inp, C, False)
+    assert np.all(it["Vq"] == 0.0)
+
+
+def test_local_only_and_lin_scale_linearity():
+    C = 8
+    inp = make_inputs(B=2, T=32, d=8, e=10, s=4, C=C, dtype="fp32", seed=29)
+    O0, it0 = _run(inp, C, True, lin_scale=0.0)
+    assert np.all(it0["Vl"] == 0.0)
+    np.testing.assert_allclose(O0, (it0["U"] * it0["Vq"]) @ inp["W_o"], rtol=1e-13)
+    _, it1 = _run(inp, C, True, lin_scale=1.0)
+    _, it3 = _run(inp, C, True, lin_scale=3.0)
+    np.testing.assert_allclose(it3["Vl"], 3.0 * it1["Vl"], rtol=1e-12)
+
+
+def test_relu2_weights_nonnegative_and_masked():
+    C = 16
+    inp = make_inputs(B=1, T=32, d=8, e=6, s=4, C=C, dtype="fp32", seed=31)
+    inp["gamma"] = inp["gamma"] * 4.0
+    from oracle import chunk_scores, relpos_bias as rb
+    _, it = _run(inp, C, True)
+    a = chunk_scores(it["heads"][0][0, :C], it["heads"][1][0, :C],
+                     rb(inp["relpos"], C), C, True)
+    assert np.all(a >= 0.0)
+    assert np.all(np.triu(a, 1) == 0.0)
+    assert np.any(np.diag(a) > 0.0)
+
+
+def test_chunk_of_whole_sequence_causal_has_no_global_term():
+    """C = T: the layer degenerates to FLASH-Quad (appendix C.3), whose causal
+    output has no linear term at all."""
+    T = 16
+    inp = make_inputs(B=2, T=T, d=8, e=6, s=4, C=T, dtype="fp32", seed=37)
+    O, it = _run(inp, T, True)
+    assert np.all(it["Vl"] == 0.0)
+    np.testing.assert_allclose(O, (it["U"] * it["Vq"]) @ inp["W_o"], rtol=1e-13)
+
+
+def test_rejects_ragged_length():
+    inp = make_inputs(B=1, T=10, d=4, e=4, s=2, C=4, dtype="fp32", seed=0)
+    with pytest.raises(ValueError):
+        _run(inp, 4, True)
+
+
+# ------------------------------------------------------------ FLOP count --
+
+def test_flop_count_matches_operation_count():
+    """Counts multiply-adds of the tiny scalar formulation directly."""
+    d, e, s, C = 3, 5, 2, 4
+    for causal in (True, False):
+        visible = sum((i + 1) if causal else C for i in range(C)) / C
+        per_token = 2 * (d * (2 * e + s) + e * d + visible * s + visible * e + 2 * s * e)
+        assert algorithmic_flops_per_token(d, e, s, C, causal) == pytest.approx(per_token)
+    assert algorithmic_flops_per_token(768, 1536, 128, 256, True) == 8488576.0
+
+
+def test_bf16_rounding_is_nearest_even():
+    import torch
+    x = np.random.default_rng(0).standard_normal(10000) * 100
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(round_bf16(x), ref)
