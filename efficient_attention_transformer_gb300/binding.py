@@ -1,0 +1,217 @@
+"""ctypes binding of libflashgau (see include/flash_gau.h).
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity and their data pointers handed to the C entry points; every step
+of the computation runs in the library's CUDA kernels.  Loading fails loudly
+when the library has not been built.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+FP32 = 0
+BF16 = 1
+
+OK = 0
+EINVAL = -1
+ENOTSUP = -2
+EWORKSPACE = -3
+ECUDA = -4
+EDEVICE = -5
+ETIMEOUT = -6
+
+# Every function the header declares; the library must export all of them.
+EXPORTED = (
+    "flash_gau_workspace_layout_query",
+    "flash_gau_workspace_bytes",
+    "flash_gau_forward",
+    "flash_gau_forward_timed",
+    "flash_gau_num_stages",
+    "flash_gau_stage_name",
+    "flash_gau_workspace_status",
+    "flash_gau_strerror",
+    "flash_gau_version",
+)
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [
+        ("W_uvz", ctypes.c_void_p),
+        ("W_o", ctypes.c_void_p),
+        ("gamma", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p),
+        ("relpos", ctypes.c_void_p),
+        ("d", ctypes.c_int),
+        ("e", ctypes.c_int),
+        ("s", ctypes.c_int),
+        ("lin_scale", ctypes.c_float),
+    ]
+
+
+class WorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("total_bytes", "status", "U", "V", "heads", "state", "prefix", "gated")]
+
+
+class FlashGauError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("flash_gau status %d: %s" % (status, msg))
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (loaded on first use)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libflashgau.so is not built (expected at %s); call "
+                "efficient_attention_transformer_gb300.build.build()" % _LIB_PATH)
+        L = ctypes.CDLL(_LIB_PATH)
+        i, p, sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        L.flash_gau_workspace_layout_query.argtypes = [i, i, i, i, i, i, i, i,
+                                                       ctypes.POINTER(WorkspaceLayout)]
+        L.flash_gau_workspace_layout_query.restype = i
+        L.flash_gau_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights), i, i]
+        L.flash_gau_workspace_bytes.restype = sz
+        L.flash_gau_forward.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p, sz, p]
+        L.flash_gau_forward.restype = i
+        L.flash_gau_forward_timed.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p,
+                                              sz, p, ctypes.POINTER(p), i]
+        L.flash_gau_forward_timed.restype = i
+        L.flash_gau_num_stages.argtypes = [i, i]
+        L.flash_gau_num_stages.restype = i
+        L.flash_gau_stage_name.argtypes = [i, i, i]
+        L.flash_gau_stage_name.restype = ctypes.c_char_p
+        L.flash_gau_workspace_status.argtypes = [p, p]
+        L.flash_gau_workspace_status.restype = i
+        L.flash_gau_strerror.argtypes = [i]
+        L.flash_gau_strerror.restype = ctypes.c_char_p
+        L.flash_gau_version.argtypes = []
+        L.flash_gau_version.restype = i
+        _lib = L
+    return _lib
+
+
+def strerror(status):
+    return lib().flash_gau_strerror(status).decode()
+
+
+def _check(status):
+    if status != OK:
+        raise FlashGauError(status, strerror(status))
+
+
+def dtype_code(t):
+    if t == torch.float32:
+        return FP32
+    if t == torch.bfloat16:
+        return BF16
+    raise TypeError("io dtype must be float32 or bfloat16, got %s" % (t,))
+
+
+def workspace_layout(B, T, C, d, e, s, causal, dtype):
+    """Byte offsets of the intermediates, as a dict."""
+    L = WorkspaceLayout()
+    _check(lib().flash_gau_workspace_layout_query(B, T, C, d, e, s, int(bool(causal)),
+                                                  dtype, ctypes.byref(L)))
+    return {n: getattr(L, n) for n, _ in WorkspaceLayout._fields_}
+
+
+def num_stages(dtype, causal):
+    return lib().flash_gau_num_stages(dtype, int(bool(causal)))
+
+
+def stage_names(dtype, causal):
+    return [lib().flash_gau_stage_name(dtype, int(bool(causal)), k).decode()
+            for k in range(num_stages(dtype, causal))]
+
+
+def _dev_ptr(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+class GauWeights:
+    """Device-resident layer parameters in the layout the library expects."""
+
+    def __init__(self, W_uvz, W_o, gamma, beta, relpos, d, e, s, lin_scale=1.0):
+        self.W_uvz, self.W_o = W_uvz, W_o
+        self.gamma, self.beta, self.relpos = gamma, beta, relpos
+        self.d, self.e, self.s = int(d), int(e), int(s)
+        self.lin_scale = float(lin_scale)
+        self.dtype = dtype_code(W_uvz.dtype)
+        f32 = torch.float32
+        self.c = Weights(_dev_ptr(W_uvz, "W_uvz", W_uvz.dtype), _dev_ptr(W_o, "W_o", W_uvz.dtype),
+                         _dev_ptr(gamma, "gamma", f32), _dev_ptr(beta, "beta", f32),
+                         _dev_ptr(relpos, "relpos", f32), self.d, self.e, self.s,
+                         self.lin_scale)
+        if tuple(W_uvz.shape) != (d, 2 * e + s) or tuple(W_o.shape) != (e, d):
+            raise ValueError("weight shapes do not match d, e, s")
+        if tuple(gamma.shape) != (4, s) or tuple(beta.shape) != (4, s):
+            raise ValueError("gamma and beta must be [4, s]")
+
+    def workspace_bytes(self, B, T, C, causal):
+        n = lib().flash_gau_workspace_bytes(B, T, C, ctypes.byref(self.c), int(bool(causal)),
+                                            self.dtype)
+        if n == 0:
+            raise FlashGauError(EINVAL, "invalid or unsupported problem")
+        return n
+
+    def new_workspace(self, B, T, C, causal, device=None):
+        n = self.workspace_bytes(B, T, C, causal)
+        return torch.zeros(n, dtype=torch.uint8, device=device or self.W_uvz.device)
+
+
+def forward(X, weights, C, causal, out=None, workspace=None, stream=None,
+            stage_events=None):
+    """O = FLASH-GAU(X) through flash_gau_forward (or _timed when
+    stage_events, a list of torch.cuda.Event, is given).  X: [B, T, d]."""
+    if X.dim() != 3:
+        raise ValueError("X must be [B, T, d]")
+    B, T, d = X.shape
+    if d != weights.d:
+        raise ValueError("X width does not match the weights")
+    if X.dtype != weights.W_uvz.dtype:
+        raise ValueError("X and weights must share the io dtype")
+    if weights.relpos.numel() != 2 * C - 1:
+        raise ValueError("relpos must hold 2C-1 values")
+    if out is None:
+        out = torch.empty_like(X)
+    if workspace is None:
+        workspace = weights.new_workspace(B, T, C, causal, X.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(X.device)
+    sp = stream.cuda_stream
+    args = (_dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), B, T, C, int(bool(causal)),
+            weights.dtype, _dev_ptr(out, "out", X.dtype), _dev_ptr(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), sp)
+    if stage_events:
+        for ev in stage_events:  # torch creates the CUDA event on first record
+            if not ev.cuda_event:
+                ev.record(stream)
+        arr = (ctypes.c_void_p * len(stage_events))(*[ev.cuda_event for ev in stage_events])
+        st = lib().flash_gau_forward_timed(*args, arr, len(stage_events))
+    else:
+        st = lib().flash_gau_forward(*args)
+    _check(st)
+    return out
+
+
+def workspace_status(workspace, stream=None):
+    """Synchronises and returns (and clears) the kernels' status word."""
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return lib().flash_gau_workspace_status(_dev_ptr(workspace, "workspace"), stream.cuda_stream)

@@ -1,0 +1,270 @@
+// C ABI of libflashgau: argument validation, workspace layout and the stage
+// schedule of one forward pass.  Every launch happens on the caller's stream.
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "flash_gau_internal.h"
+
+using namespace flashgau;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+thread_local char g_cuda_msg[256] = "no CUDA error recorded";
+
+int record_cuda(cudaError_t err) {
+  snprintf(g_cuda_msg, sizeof(g_cuda_msg), "CUDA error %d: %s", (int)err,
+           cudaGetErrorString(err));
+  return FLASH_GAU_ECUDA;
+}
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Per-device facts looked up once: compute capability and SM count.
+struct DeviceInfo {
+  int checked = 0;
+  int ok = 0;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(int *num_sms) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return record_cuda(err);
+  if (dev < 0 || dev >= kMaxDevices) return FLASH_GAU_EDEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo &di = g_dev[dev];
+  if (!di.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return record_cuda(err);
+    di.ok = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    di.checked = 1;
+  }
+  if (!di.ok) return FLASH_GAU_EDEVICE;
+  *num_sms = di.num_sms;
+  return FLASH_GAU_OK;
+}
+
+int check_shape(int B, int T, int C, int d, int e, int s, int dtype) {
+  if (B <= 0 || T <= 0 || C <= 0 || d <= 0 || e <= 0 || s <= 0) return FLASH_GAU_EINVAL;
+  if (T % C != 0) return FLASH_GAU_EINVAL;
+  if (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16) return FLASH_GAU_EINVAL;
+  if ((long long)B * T > (1LL << 30) || d > (1 << 16) || e > (1 << 16) || s > (1 << 16))
+    return FLASH_GAU_ENOTSUP;
+  if (C > 4096) return FLASH_GAU_ENOTSUP;
+  if ((long long)B * (T / C) > 65535) return FLASH_GAU_ENOTSUP;
+  if (dtype == FLASH_GAU_FP32) {
+    if (s > 128) return FLASH_GAU_ENOTSUP;
+  } else {
+    if (d % 64 != 0 || e % 256 != 0 || s != 128 || C % 128 != 0) return FLASH_GAU_ENOTSUP;
+  }
+  return FLASH_GAU_OK;
+}
+
+int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
+           flash_gau_workspace_layout *L) {
+  int st = check_shape(B, T, C, d, e, s, dtype);
+  if (st != FLASH_GAU_OK) return st;
+  const size_t io = dtype == FLASH_GAU_BF16 ? 2 : 4;
+  const size_t M = (size_t)B * T, G = (size_t)(T / C);
+  size_t off = 0;
+  L->status = off;
+  off = align_up(off + sizeof(int));
+  L->U = off;
+  off = align_up(off + M * e * io);
+  L->V = off;
+  off = align_up(off + M * e * io);
+  L->heads = off;
+  off = align_up(off + 4 * M * s * io);
+  L->state = off;
+  off = align_up(off + (size_t)B * G * s * e * sizeof(float));
+  L->prefix = off;
+  off = align_up(off + (causal ? (size_t)B * G : (size_t)B) * s * e * io);
+  L->gated = off;
+  off = align_up(off + M * e * io);
+  L->total_bytes = off;
+  return FLASH_GAU_OK;
+}
+
+// ---- stage schedules ------------------------------------------------------
+const Stage kStagesF32[] = {
+    {"projection", simt_projection_f32},
+    {"chunk_state", simt_chunk_state_f32},
+    {"prefix_scan", simt_prefix_scan_f32},
+    {"chunk_attention", simt_chunk_attention_f32},
+    {"output", simt_output_f32},
+};
+const Stage kStagesBF16[] = {
+    {"projection", simt_projection_bf16},
+    {"chunk_state", simt_chunk_state_bf16},
+    {"prefix_scan", simt_prefix_scan_bf16},
+    {"chunk_attention", simt_chunk_attention_bf16},
+    {"output", simt_output_bf16},
+};
+
+const Stage *stages(int dtype, int /*causal*/, int *n) {
+  if (dtype == FLASH_GAU_FP32) {
+    *n = (int)(sizeof(kStagesF32) / sizeof(kStagesF32[0]));
+    return kStagesF32;
+  }
+  if (dtype == FLASH_GAU_BF16) {
+    *n = (int)(sizeof(kStagesBF16) / sizeof(kStagesBF16[0]));
+    return kStagesBF16;
+  }
+  *n = 0;
+  return nullptr;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const char *pa = (const char *)a, *pb = (const char *)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+int flash_gau_workspace_layout_query(int B, int T, int C, int d, int e, int s, int causal,
+                                     int dtype, flash_gau_workspace_layout *out) {
+  if (!out) return FLASH_GAU_EINVAL;
+  return layout(B, T, C, d, e, s, causal, dtype, out);
+}
+
+size_t flash_gau_workspace_bytes(int B, int T, int C, const flash_gau_weights *w, int causal,
+                                 int dtype) {
+  if (!w) return 0;
+  flash_gau_workspace_layout L;
+  if (layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L) != FLASH_GAU_OK) return 0;
+  return L.total_bytes;
+}
+
+int flash_gau_num_stages(int dtype, int causal) {
+  int n = 0;
+  stages(dtype, causal, &n);
+  return n;
+}
+
+const char *flash_gau_stage_name(int dtype, int causal, int k) {
+  int n = 0;
+  const Stage *st = stages(dtype, causal, &n);
+  if (!st || k < 0 || k >= n) return nullptr;
+  return st[k].name;
+}
+
+int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, int T, int C,
+                            int causal, int dtype, void *out, void *workspace,
+                            size_t workspace_bytes, void *stream, void *const *stage_events,
+                            int n_events) {
+  if (!X || !w || !out || !workspace || !w->W_uvz || !w->W_o || !w->gamma || !w->beta ||
+      !w->relpos)
+    return FLASH_GAU_EINVAL;
+  if (n_events < 0 || (n_events > 0 && !stage_events)) return FLASH_GAU_EINVAL;
+  causal = causal ? 1 : 0;
+  flash_gau_workspace_layout L;
+  int st = layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
+  if (st != FLASH_GAU_OK) return st;
+  if (workspace_bytes < L.total_bytes || ((uintptr_t)workspace % kAlign) != 0)
+    return FLASH_GAU_EWORKSPACE;
+  const size_t io = dtype == FLASH_GAU_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * T * w->d * io;
+  if (overlaps(out, nx, X, nx) || overlaps(out, nx, workspace, L.total_bytes))
+    return FLASH_GAU_EINVAL;
+  int num_sms = 0;
+  st = device_info(&num_sms);
+  if (st != FLASH_GAU_OK) return st;
+
+  Problem p;
+  p.B = B;
+  p.T = T;
+  p.C = C;
+  p.G = T / C;
+  p.d = w->d;
+  p.e = w->e;
+  p.s = w->s;
+  p.causal = causal;
+  p.dtype = dtype;
+  p.M = (long long)B * T;
+  p.lin_scale = w->lin_scale;
+  p.X = X;
+  p.W_uvz = w->W_uvz;
+  p.W_o = w->W_o;
+  p.gamma = w->gamma;
+  p.beta = w->beta;
+  p.relpos = w->relpos;
+  p.out = out;
+  char *ws = (char *)workspace;
+  p.status = (int *)(ws + L.status);
+  p.U = ws + L.U;
+  p.V = ws + L.V;
+  p.heads = ws + L.heads;
+  p.state = (float *)(ws + L.state);
+  p.prefix = ws + L.prefix;
+  p.gated = ws + L.gated;
+  p.stream = (cudaStream_t)stream;
+  p.num_sms = num_sms;
+
+  int n = 0;
+  const Stage *sched = stages(dtype, causal, &n);
+  cudaError_t err;
+  if (n_events > 0 &&
+      (err = cudaEventRecord((cudaEvent_t)stage_events[0], p.stream)) != cudaSuccess)
+    return record_cuda(err);
+  for (int k = 0; k < n; ++k) {
+    if ((err = sched[k].fn(p)) != cudaSuccess) return record_cuda(err);
+    if (k + 1 < n_events &&
+        (err = cudaEventRecord((cudaEvent_t)stage_events[k + 1], p.stream)) != cudaSuccess)
+      return record_cuda(err);
+  }
+  return FLASH_GAU_OK;
+}
+
+int flash_gau_forward(const void *X, const flash_gau_weights *w, int B, int T, int C, int causal,
+                      int dtype, void *out, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+  return flash_gau_forward_timed(X, w, B, T, C, causal, dtype, out, workspace, workspace_bytes,
+                                 stream, nullptr, 0);
+}
+
+int flash_gau_workspace_status(void *workspace, void *stream) {
+  if (!workspace) return FLASH_GAU_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  int word = 0;
+  cudaError_t err = cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return record_cuda(err);
+  if (word != 0) {
+    int zero = 0;
+    err = cudaMemcpyAsync(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return record_cuda(err);
+  }
+  return word;
+}
+
+const char *flash_gau_strerror(int status) {
+  switch (status) {
+    case FLASH_GAU_OK: return "success";
+    case FLASH_GAU_EINVAL: return "invalid argument (null pointer, non-positive size, T % C != 0, "
+                                  "unknown dtype or overlapping output)";
+    case FLASH_GAU_ENOTSUP: return "shape not supported for this dtype";
+    case FLASH_GAU_EWORKSPACE: return "workspace too small or not 256-byte aligned";
+    case FLASH_GAU_ECUDA: return g_cuda_msg;
+    case FLASH_GAU_EDEVICE: return "current CUDA device is not an sm_103 (GB300) GPU";
+    case FLASH_GAU_ETIMEOUT: return "a kernel gave up a bounded wait (pipeline stalled)";
+    default: return "unknown status";
+  }
+}
+
+int flash_gau_version(void) { return 100; }
+
+}  // extern "C"

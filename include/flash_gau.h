@@ -1,0 +1,161 @@
+/*
+ * flash_gau.h -- C ABI of libflashgau, the sm_103a (GB300) forward pass of
+ * the FLASH gated attention unit with mixed chunk attention.
+ *
+ * The operation ("Transformer Quality in Linear Time", Method, eq. 5, eq. 7,
+ * eq. 8 and the display after eq. 8; "FLASH: Possibly the Most Interesting
+ * Efficient Transformer Design in Recent Times", sections "Gated Attention",
+ * "Weak Attention" and "Mixed Chunking"):
+ *
+ *   [U | V | Z] = swish(X [W_u | W_v | W_z])               swish(x) = x*sigmoid(x)
+ *   Q_quad, K_quad, Q_lin, K_lin = Z * gamma_h + beta_h     (per-dimension heads)
+ *   for every chunk g of C consecutive tokens (G = T / C chunks):
+ *     Vq_g   = relu^2(Q_quad,g K_quad,g^T / C + b) V_g      b[i][j] = relpos[j-i+C-1]
+ *              (entries with j > i are zero when causal; diagonal kept)
+ *     P_g    = sum_{h<g} K_lin,h^T V_h   (causal, eq. 8; zero for g = 0)
+ *            = sum_{h}   K_lin,h^T V_h   (non-causal, eq. 7)
+ *     Vl_g   = lin_scale * Q_lin,g P_g
+ *     O_g    = [U_g * (Vq_g + Vl_g)] W_o
+ *
+ * Readings where the pages differ: scores are divided by C before the bias
+ * (flash_block pseudocode); the chunk states are summed plainly (eq. 7/8),
+ * lin_scale = 1 reproduces that, 1/C the appendix listing, 0 the LocalOnly
+ * ablation; the Toeplitz bias of appendix D Code 4 (2C-1 weights) is used for
+ * every C.  No projection biases, norm, RoPE or residual are applied.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device pointers on the current device;
+ *     the caller owns every buffer.  The library allocates no memory.
+ *   - All matrices are dense and row-major (last index fastest), without
+ *     padding between rows.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Calls are asynchronous: they return once the kernels are
+ *     queued, and the caller synchronises.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a negative status and enqueues nothing.  No C++
+ *     exception crosses this interface.
+ *   - Entry points are thread-safe with respect to one another, except that
+ *     concurrent forwards must not share a workspace.
+ */
+#ifndef FLASH_GAU_H
+#define FLASH_GAU_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define FLASH_GAU_OK 0
+#define FLASH_GAU_EINVAL (-1)     /* null pointer, bad size, T % C != 0, ... */
+#define FLASH_GAU_ENOTSUP (-2)    /* valid shape outside the supported set   */
+#define FLASH_GAU_EWORKSPACE (-3) /* workspace too small or misaligned       */
+#define FLASH_GAU_ECUDA (-4)      /* CUDA runtime/launch error (see strerror) */
+#define FLASH_GAU_EDEVICE (-5)    /* current device is not sm_103            */
+#define FLASH_GAU_ETIMEOUT (-6)   /* a kernel gave up a bounded wait         */
+
+/* ---- io data types ----------------------------------------------------- */
+/* FP32: X, weights, out and all intermediates in fp32, fp32 arithmetic.
+ * BF16: X, W_uvz, W_o and out in bf16; tensor-core products with fp32
+ *       accumulation; U, V, heads, prefix states and the gated product are
+ *       stored in bf16. gamma, beta and relpos are fp32 for both types.    */
+#define FLASH_GAU_FP32 0
+#define FLASH_GAU_BF16 1
+
+typedef struct flash_gau_weights {
+  const void *W_uvz;    /* device [d, 2e+s], io type: columns [0,e) W_u,
+                           [e,2e) W_v, [2e,2e+s) W_z                        */
+  const void *W_o;      /* device [e, d], io type                           */
+  const float *gamma;   /* device [4, s] fp32, rows Q_quad K_quad Q_lin K_lin */
+  const float *beta;    /* device [4, s] fp32, same row order               */
+  const float *relpos;  /* device [2C-1] fp32, b[i][j] = relpos[j-i+C-1]    */
+  int d;                /* model width                                      */
+  int e;                /* expansion width (U, V)                           */
+  int s;                /* shared head width (Z)                            */
+  float lin_scale;      /* factor on the global (linear) term               */
+} flash_gau_weights;
+
+/* Byte offsets of the intermediates inside a workspace (all from its start).
+ * io = the io type's size.  The offsets are 256-byte aligned.              */
+typedef struct flash_gau_workspace_layout {
+  size_t total_bytes;   /* bytes the workspace must hold                    */
+  size_t status;        /* int32 device status word (FLASH_GAU_ETIMEOUT...) */
+  size_t U;             /* [B*T, e] io: swish(X W_u)                        */
+  size_t V;             /* [B*T, e] io: swish(X W_v)                        */
+  size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
+  size_t state;         /* [B, G, s, e] fp32: K_lin,g^T V_g per chunk        */
+  size_t prefix;        /* causal [B, G, s, e], non-causal [B, s, e], io:
+                           lin_scale * (exclusive / total) chunk-state sum  */
+  size_t gated;         /* [B*T, e] io: U * (Vq + Vl)                       */
+} flash_gau_workspace_layout;
+
+/* Supported shapes.  All types: B, T, C, d, e, s > 0 and T % C == 0.
+ *   FP32: any such shape with s <= 128 and C <= 4096.
+ *   BF16: d % 64 == 0, e % 256 == 0, s == 128, C % 128 == 0, C <= 4096.
+ * Other shapes return FLASH_GAU_ENOTSUP.                                   */
+
+/* Fills *out for the given problem.  Returns FLASH_GAU_OK, FLASH_GAU_EINVAL
+ * (bad sizes or null out) or FLASH_GAU_ENOTSUP.                            */
+int flash_gau_workspace_layout_query(int B, int T, int C, int d, int e, int s,
+                                     int causal, int dtype,
+                                     flash_gau_workspace_layout *out);
+
+/* Workspace size in bytes for the given problem, or 0 if the arguments are
+ * invalid or unsupported.                                                  */
+size_t flash_gau_workspace_bytes(int B, int T, int C, const flash_gau_weights *w,
+                                 int causal, int dtype);
+
+/* The forward pass, O = FLASH-GAU(X).
+ *   X         device [B, T, d], io type
+ *   w         host pointer to the weight descriptor (read during the call)
+ *   B, T, C   batch, sequence length, chunk length (T % C == 0; C == T gives
+ *             FLASH-Quad, the quadratic GAU)
+ *   causal    nonzero: causal local mask and exclusive chunk prefix (eq. 8);
+ *             zero: full local attention and total chunk sum (eq. 7)
+ *   dtype     FLASH_GAU_FP32 or FLASH_GAU_BF16
+ *   out       device [B, T, d], io type; must not overlap X or the workspace
+ *   workspace device, >= flash_gau_workspace_bytes(...) bytes, 256-byte
+ *             aligned; its contents on return are the intermediates listed
+ *             in flash_gau_workspace_layout
+ *   stream    cudaStream_t
+ * Returns FLASH_GAU_OK once all kernels are queued, or a negative status.  A
+ * kernel that gives up a bounded wait records FLASH_GAU_ETIMEOUT in the
+ * workspace status word; read it with flash_gau_workspace_status().        */
+int flash_gau_forward(const void *X, const flash_gau_weights *w, int B, int T,
+                      int C, int causal, int dtype, void *out, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Same as flash_gau_forward, and additionally records stage_events[0] on the
+ * stream before the first kernel and stage_events[k+1] after stage k
+ * (k = 0 .. n_events-2).  stage_events are cudaEvent_t handles owned by the
+ * caller; n_events may be 0.  The stage count and names come from
+ * flash_gau_num_stages / flash_gau_stage_name.                              */
+int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B,
+                            int T, int C, int causal, int dtype, void *out,
+                            void *workspace, size_t workspace_bytes,
+                            void *stream, void *const *stage_events,
+                            int n_events);
+
+/* Number of kernel stages one forward launches for this dtype / causality,
+ * and a static name for stage k (NULL when out of range).                  */
+int flash_gau_num_stages(int dtype, int causal);
+const char *flash_gau_stage_name(int dtype, int causal, int k);
+
+/* Synchronises `stream`, returns the status word the kernels left in the
+ * workspace (FLASH_GAU_OK or FLASH_GAU_ETIMEOUT) and resets it to zero.
+ * Returns FLASH_GAU_ECUDA if the stream reported an error.                 */
+int flash_gau_workspace_status(void *workspace, void *stream);
+
+/* Static description of a status code.  For FLASH_GAU_ECUDA it includes the
+ * last CUDA error seen by this thread.                                     */
+const char *flash_gau_strerror(int status);
+
+/* Library version as major*10000 + minor*100 + patch.                      */
+int flash_gau_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASH_GAU_H */

@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+function include/flash_gau.h declares; layouts and argument validation work
+without a GPU (invalid calls return before touching CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from efficient_attention_transformer_gb300 import build as buildmod
+from efficient_attention_transformer_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    buildmod.build()
+    return bd.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "flash_gau.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flash_gau_\w+)\s*\(", text)))
+
+
+def test_header_declarations_are_exported(L):
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    assert sorted(bd.EXPORTED) == declared
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_version_and_strerror(L):
+    assert L.flash_gau_version() >= 100
+    for code in (bd.OK, bd.EINVAL, bd.ENOTSUP, bd.EWORKSPACE, bd.ECUDA, bd.EDEVICE, bd.ETIMEOUT):
+        assert bd.strerror(code)
+    assert bd.strerror(12345) == "unknown status"
+
+
+def test_layout_offsets_aligned_and_sized(L):
+    B, T, C, d, e, s = 2, 8192, 256, 768, 1536, 128
+    lay = bd.workspace_layout(B, T, C, d, e, s, True, bd.BF16)
+    order = ["status", "U", "V", "heads", "state", "prefix", "gated"]
+    offs = [lay[k] for k in order]
+    assert offs == sorted(offs)
+    assert all(o % 256 == 0 for o in offs)
+    M, G = B * T, T // C
+    assert lay["V"] - lay["U"] >= M * e * 2
+    assert lay["heads"] - lay["V"] >= M * e * 2
+    assert lay["state"] - lay["heads"] >= 4 * M * s * 2
+    assert lay["prefix"] - lay["state"] >= B * G * s * e * 4
+    assert lay["gated"] - lay["prefix"] >= B * G * s * e * 2
+    assert lay["total_bytes"] - lay["gated"] >= M * e * 2
+    nc = bd.workspace_layout(B, T, C, d, e, s, False, bd.BF16)
+    assert nc["gated"] - nc["prefix"] < lay["gated"] - lay["prefix"]  # [B,s,e] only
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 100, 64, 64, 128, 32, 1, bd.FP32), bd.EINVAL),     # T % C != 0
+    ((0, 128, 64, 64, 128, 32, 1, bd.FP32), bd.EINVAL),     # B == 0
+    ((1, 128, 64, 64, 128, 32, 1, 7), bd.EINVAL),           # unknown dtype
+    ((1, 256, 128, 768, 1000, 128, 1, bd.BF16), bd.ENOTSUP),  # e % 256
+    ((1, 256, 128, 768, 1536, 64, 1, bd.BF16), bd.ENOTSUP),   # s != 128
+    ((1, 192, 64, 768, 1536, 128, 1, bd.BF16), bd.ENOTSUP),   # C % 128
+    ((1, 256, 64, 64, 128, 256, 1, bd.FP32), bd.ENOTSUP),     # s > 128 (fp32)
+])
+def test_layout_rejects(L, args, code):
+    lay = bd.WorkspaceLayout()
+    assert L.flash_gau_workspace_layout_query(*args, ctypes.byref(lay)) == code
+
+
+def test_forward_rejects_before_any_launch(L):
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 32, 1.0)  # fake non-null pointers
+    ws = 1 << 20
+    # null X
+    assert L.flash_gau_forward(None, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 8, 256 * 64,
+                               ws, None) == bd.EINVAL
+    # null weights
+    assert L.flash_gau_forward(16, None, 1, 256, 64, 1, bd.FP32, 8, 256, ws, None) == bd.EINVAL
+    # ragged T
+    assert L.flash_gau_forward(16, ctypes.byref(w), 1, 250, 64, 1, bd.FP32, 1 << 40, 256,
+                               ws, None) == bd.EINVAL
+    # workspace too small
+    assert L.flash_gau_forward(16, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 1 << 40, 256,
+                               16, None) == bd.EWORKSPACE
+    # misaligned workspace
+    assert L.flash_gau_forward(16, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 1 << 40, 257,
+                               ws, None) == bd.EWORKSPACE
+    # output overlapping X
+    assert L.flash_gau_forward(1 << 30, ctypes.byref(w), 1, 256, 64, 1, bd.FP32,
+                               (1 << 30) + 64, 1 << 34, ws, None) == bd.EINVAL
+    # events requested but none given
+    assert L.flash_gau_forward_timed(16, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 1 << 40,
+                                     256, ws, None, None, 3) == bd.EINVAL
+
+
+def test_workspace_bytes_matches_layout(L):
+    w = bd.Weights(1, 2, 3, 4, 5, 768, 1536, 128, 1.0)
+    n = L.flash_gau_workspace_bytes(8, 1024, 256, ctypes.byref(w), 1, bd.BF16)
+    assert n == bd.workspace_layout(8, 1024, 256, 768, 1536, 128, True, bd.BF16)["total_bytes"]
+    assert L.flash_gau_workspace_bytes(8, 1000, 256, ctypes.byref(w), 1, bd.BF16) == 0
+
+
+def test_stage_names(L):
+    for dt in (bd.FP32, bd.BF16):
+        names = bd.stage_names(dt, True)
+        assert len(names) == bd.num_stages(dt, True) >= 1
+        assert L.flash_gau_stage_name(dt, 1, len(names)) is None
