@@ -105,11 +105,11 @@ const Stage kStagesF32[] = {
     {"output", simt_output_f32},
 };
 const Stage kStagesBF16[] = {
-    {"projection", simt_projection_bf16},
-    {"chunk_state", simt_chunk_state_bf16},
+    {"projection", tc_projection_bf16},
+    {"chunk_state", tc_chunk_state_bf16},
     {"prefix_scan", simt_prefix_scan_bf16},
     {"chunk_attention", simt_chunk_attention_bf16},
-    {"output", simt_output_bf16},
+    {"output", tc_output_bf16},
 };
 
 const Stage *stages(int dtype, int /*causal*/, int *n) {

@@ -47,7 +47,12 @@ cudaError_t simt_prefix_scan_f32(const Problem &p);
 cudaError_t simt_chunk_attention_f32(const Problem &p);
 cudaError_t simt_output_f32(const Problem &p);
 
-// bf16 stages
+// bf16 tensor-core stages (tc_gemm.cu)
+cudaError_t tc_projection_bf16(const Problem &p);
+cudaError_t tc_chunk_state_bf16(const Problem &p);
+cudaError_t tc_output_bf16(const Problem &p);
+
+// bf16 CUDA-core stages
 cudaError_t simt_projection_bf16(const Problem &p);
 cudaError_t simt_chunk_state_bf16(const Problem &p);
 cudaError_t simt_prefix_scan_bf16(const Problem &p);

@@ -1,0 +1,393 @@
+// Persistent tcgen05 GEMM with fused epilogues, the dense contractions of the
+// FLASH GAU forward in bf16 with fp32 accumulation in TMEM:
+//   projection   [U|V|Z] = swish(X W_uvz); the Z tile's epilogue writes the
+//                four scale/offset heads Z*gamma_h + beta_h
+//                ("Transformer Quality in Linear Time", Method, eq. 5 and
+//                 the four heads of mixed chunk attention)
+//   output       O = gated W_o                   (display after eq. 8)
+//   chunk state  State_g = K_lin,g^T V_g, batched over chunks (eq. 7/8)
+//
+// One CTA per SM loops over 128 x 256 output tiles.  Warp 0 streams A and B
+// k-blocks (64 deep) into a 4-stage shared-memory ring with TMA; one thread
+// of warp 1 issues tcgen05.mma into one of two TMEM accumulators; warps 2-5
+// drain the other accumulator through tcgen05.ld, apply the epilogue in
+// registers and store.  All operand tiles use the 128-byte swizzled layout;
+// A is K-major (or M-major for the chunk state), B is N-major (row-major
+// weights / values).
+#include <cuda_bf16.h>
+
+#include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace flashgau {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;  // one 64-wide N block of a k-block: 8 KB
+constexpr int B_BYTES = BN * BK * 2;      // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int NUM_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_STATE = 2 };
+
+struct GemmParams {
+  int N, K;             // output columns, contraction depth (per batch)
+  int m_tiles, n_tiles; // per batch
+  int total_tiles;      // batches * m_tiles * n_tiles
+  int k_rows_per_batch; // row offset of a batch along K in the K-indexed maps
+  // projection epilogue
+  __nv_bfloat16 *U, *V, *heads;
+  const float *gamma, *beta;
+  long long M_tokens;
+  int e, s;
+  // plain store epilogue
+  __nv_bfloat16 *out;
+  int ld_out;
+  // chunk-state epilogue
+  float *state;
+  int *status;
+};
+
+struct Smem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ void raise_timeout(Smem *sm, int *status) {
+  sm->abort_flag = 1;
+  atomicExch(status, FLASH_GAU_ETIMEOUT);
+}
+
+__device__ __forceinline__ float swish_fast(float x) { return x / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, int batch, long long row,
+                                               int n0, int c0, const uint32_t (&r)[32]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if constexpr (EPI == EPI_PROJ) {
+    const int n = n0 + c0;
+    if (n < 2 * p.e) {
+      __nv_bfloat16 *dst = (n < p.e ? p.U : p.V) + row * p.e + (n < p.e ? n : n - p.e);
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16(swish_fast(v[8 * q + 0]), swish_fast(v[8 * q + 1]));
+        w.y = pack_bf16(swish_fast(v[8 * q + 2]), swish_fast(v[8 * q + 3]));
+        w.z = pack_bf16(swish_fast(v[8 * q + 4]), swish_fast(v[8 * q + 5]));
+        w.w = pack_bf16(swish_fast(v[8 * q + 6]), swish_fast(v[8 * q + 7]));
+        d4[q] = w;
+      }
+    } else {
+      const int c = n - 2 * p.e;  // column inside Z
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = swish_fast(v[j]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float *g = p.gamma + h * p.s + c;
+        const float *b = p.beta + h * p.s + c;
+        uint4 *d4 = reinterpret_cast<uint4 *>(p.heads + (long long)h * p.M_tokens * p.s +
+                                              row * p.s + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16(fmaf(v[8 * q + 0], g[8 * q + 0], b[8 * q + 0]),
+                          fmaf(v[8 * q + 1], g[8 * q + 1], b[8 * q + 1]));
+          w.y = pack_bf16(fmaf(v[8 * q + 2], g[8 * q + 2], b[8 * q + 2]),
+                          fmaf(v[8 * q + 3], g[8 * q + 3], b[8 * q + 3]));
+          w.z = pack_bf16(fmaf(v[8 * q + 4], g[8 * q + 4], b[8 * q + 4]),
+                          fmaf(v[8 * q + 5], g[8 * q + 5], b[8 * q + 5]));
+          w.w = pack_bf16(fmaf(v[8 * q + 6], g[8 * q + 6], b[8 * q + 6]),
+                          fmaf(v[8 * q + 7], g[8 * q + 7], b[8 * q + 7]));
+          d4[q] = w;
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_STORE) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(p.out + row * p.ld_out + n0 + c0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+      d4[q] = w;
+    }
+  } else {  // EPI_STATE: row is the s-index inside the chunk state
+    float4 *d4 = reinterpret_cast<float4 *>(p.state + ((long long)batch * p.s + row) * p.N + n0 +
+                                            c0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      d4[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+// A_MN: A is stored M-contiguous (K_lin^T of the chunk state); otherwise
+// K-contiguous.
+template <int EPI, bool A_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem *sm = reinterpret_cast<Smem *>(tiles + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&sm->full[i]), 1);
+      mbar_init(smem_u32(&sm->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm->acc_full[i]), 1);
+      mbar_init(smem_u32(&sm->acc_empty[i]), 128);
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    sm->abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm->tmem_base;
+  const int kblocks = p.K / BK;
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x) {
+        const int batch = t / tiles_per_batch, rem = t % tiles_per_batch;
+        const int mt = rem / p.n_tiles, nt = rem % p.n_tiles;
+        const int n0 = nt * BN, nboxes = min(BN, p.N - n0) / 64;
+        const int krow0 = batch * p.k_rows_per_batch;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1)) {
+            raise_timeout(sm, p.status);
+            break;
+          }
+          const uint32_t full = smem_u32(&sm->full[stage]);
+          uint8_t *sA = tiles + stage * STAGE_BYTES;
+          uint8_t *sB = sA + A_BYTES;
+          mbar_arrive_expect_tx(full, A_BYTES + nboxes * B_BOX_BYTES);
+          if (A_MN) {
+            // two 64-wide M blocks of K_lin (columns of the head), 64 tokens deep
+            tma_load_2d(smem_u32(sA), &tmA, full, 0, krow0 + kb * BK);
+            tma_load_2d(smem_u32(sA + A_BYTES / 2), &tmA, full, 64, krow0 + kb * BK);
+          } else {
+            tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, mt * BM);
+          }
+          for (int j = 0; j < nboxes; ++j)
+            tma_load_2d(smem_u32(sB + j * B_BOX_BYTES), &tmB, full, n0 + j * 64,
+                        krow0 + kb * BK);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x, ++local) {
+        const int rem = t % tiles_per_batch;
+        const int nt = rem % p.n_tiles;
+        const int nsz = min(BN, p.N - nt * BN);
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1)) {
+          raise_timeout(sm, p.status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        const uint32_t idesc = idesc_bf16_f32(BM, nsz, A_MN ? 1 : 0, 1);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase)) {
+            raise_timeout(sm, p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // A: K-major advances 16 elements (32 B) inside the swizzle atom;
+            //    M-major advances 16 rows of 128 B.  B advances 16 rows.
+            const uint64_t adesc = A_MN ? sw128_desc(sA + k * 2048, A_BYTES / 2, 1024)
+                                        : sw128_desc(sA + k * 32, 16, 1024);
+            const uint64_t bdesc = sw128_desc(sB + k * 2048, B_BOX_BYTES, 1024);
+            mma_f16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+          }
+          mma_commit(smem_u32(&sm->empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&sm->acc_full[acc]));
+      }
+      // every MMA this thread issued has completed once `drain` flips
+      mma_commit(smem_u32(&sm->drain));
+      if (!mbar_wait(smem_u32(&sm->drain), 0)) raise_timeout(sm, p.status);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    int local = 0;
+    for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x, ++local) {
+      const int batch = t / tiles_per_batch, rem = t % tiles_per_batch;
+      const int mt = rem / p.n_tiles, nt = rem % p.n_tiles;
+      const int n0 = nt * BN, nsz = min(BN, p.N - n0);
+      const int acc = local & 1;
+      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1)) {
+        raise_timeout(sm, p.status);
+        break;
+      }
+      tc_fence_after();
+      const long long row = (long long)mt * BM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+      for (int c0 = 0; c0 < nsz; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        tmem_ld_wait();
+        epilogue_chunk<EPI>(p, batch, row, n0, c0, r);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI, bool A_MN>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+                   const Problem &pr) {
+  static unsigned long long configured = 0;  // one bit per device ordinal
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !(configured & (1ull << dev))) {
+    err = cudaFuncSetAttribute(tc_gemm_kernel<EPI, A_MN>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    configured |= 1ull << dev;
+  }
+  const int grid = p.total_tiles < pr.num_sms ? p.total_tiles : pr.num_sms;
+  tc_gemm_kernel<EPI, A_MN><<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+GemmParams base_params(const Problem &pr) {
+  GemmParams p = {};
+  p.status = pr.status;
+  p.M_tokens = pr.M;
+  p.e = pr.e;
+  p.s = pr.s;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t tc_projection_bf16(const Problem &pr) {
+  const int N = 2 * pr.e + pr.s;
+  CUtensorMap tmA, tmB;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
+  GemmParams p = base_params(pr);
+  p.N = N;
+  p.K = pr.d;
+  p.m_tiles = (int)(pr.M / BM);
+  p.n_tiles = (N + BN - 1) / BN;
+  p.total_tiles = p.m_tiles * p.n_tiles;
+  p.U = (__nv_bfloat16 *)pr.U;
+  p.V = (__nv_bfloat16 *)pr.V;
+  p.heads = (__nv_bfloat16 *)pr.heads;
+  p.gamma = pr.gamma;
+  p.beta = pr.beta;
+  return launch<EPI_PROJ, false>(tmA, tmB, p, pr);
+}
+
+cudaError_t tc_output_bf16(const Problem &pr) {
+  CUtensorMap tmA, tmB;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, pr.gated, pr.M, pr.e, pr.e, BM, 64)) != cudaSuccess)
+    return err;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
+    return err;
+  GemmParams p = base_params(pr);
+  p.N = pr.d;
+  p.K = pr.e;
+  p.m_tiles = (int)(pr.M / BM);
+  p.n_tiles = (pr.d + BN - 1) / BN;
+  p.total_tiles = p.m_tiles * p.n_tiles;
+  p.out = (__nv_bfloat16 *)pr.out;
+  p.ld_out = pr.d;
+  return launch<EPI_STORE, false>(tmA, tmB, p, pr);
+}
+
+cudaError_t tc_chunk_state_bf16(const Problem &pr) {
+  // batch = chunk (b*G + g): State[chunk] = K_lin[chunk rows]^T V[chunk rows]
+  const __nv_bfloat16 *Kl = (const __nv_bfloat16 *)pr.heads + 3 * pr.M * pr.s;
+  CUtensorMap tmA, tmB;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, Kl, pr.M, pr.s, pr.s, BK, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.V, pr.M, pr.e, pr.e, BK, 64)) != cudaSuccess) return err;
+  GemmParams p = base_params(pr);
+  p.N = pr.e;
+  p.K = pr.C;
+  p.m_tiles = 1;  // s == 128 rows
+  p.n_tiles = (pr.e + BN - 1) / BN;
+  p.total_tiles = pr.B * pr.G * p.n_tiles;
+  p.k_rows_per_batch = pr.C;
+  p.state = pr.state;
+  return launch<EPI_STATE, true>(tmA, tmB, p, pr);
+}
+
+}  // namespace flashgau
