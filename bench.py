@@ -1,0 +1,413 @@
+"""Benchmark of the FLASH GAU layer forward (mixed chunk attention) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the float64 CPU oracle arm
+
+One step = one full forward (projection, chunk states, prefix scan, chunk
+attention, output projection) over one batch of seeded synthetic input that
+is resident in HBM.  L2 is flushed (a 512 MiB write) before every timed
+step.  Per-stage device times come from CUDA events the library records on
+the launching stream between its kernels.  Prints one JSON line (rank 0).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FLASH GAU layer forward tokens/sec at T=8192 causal; % of bf16 TC roofline"
+DEFAULT_WORKLOAD = "long_causal_B2_T8192"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return dict(hbm_gbs=float(m["hbm_gbs"]), bf16_tflops=float(m["bf16_tflops"]),
+                    bf16_tflops_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                    source="fallback")
+
+
+def stage_work(w):
+    """Algorithmic work per launch of each stage: (flops, bytes)."""
+    B, T, d, e, s, C = w["B"], w["T"], w["d"], w["e"], w["s"], w["C"]
+    causal = w["causal"]
+    io = 2 if w["dtype"] == "bf16" else 4
+    M, G = B * T, T // C
+    cbar = (C + 1) / 2.0 if causal else float(C)
+    pre_rows = B * G if causal else B
+    return {
+        "projection": (2.0 * M * d * (2 * e + s),
+                       io * (M * d + d * (2 * e + s) + 2 * M * e + 4 * M * s)),
+        "chunk_state": (2.0 * M * s * e, io * (M * s + M * e) + 4.0 * B * G * s * e),
+        "prefix_scan": (float(B * G * s * e), 4.0 * B * G * s * e + io * pre_rows * s * e),
+        "chunk_attention": (2.0 * M * (cbar * s + cbar * e + s * e),
+                            io * (2 * M * e + 3 * M * s + pre_rows * s * e + M * e)),
+        "output": (2.0 * M * e * d, io * (M * e + e * d + M * d)),
+    }
+
+
+def traffic_record(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of that kernel (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) < 4 or line.startswith("#"):
+            continue
+        k, src, sha, nbytes = parts[0], parts[1], parts[2], parts[3]
+        wl = parts[4] if len(parts) > 4 else ""
+        if k != kernel or wl != workload:
+            continue
+        try:
+            cur = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        return float(nbytes) if cur == sha else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import efficient_attention_transformer_gb300 as fg
+    from efficient_attention_transformer_gb300 import binding as bd
+    from efficient_attention_transformer_gb300.build import build
+    from efficient_attention_transformer_gb300.synthetic import WORKLOADS, make_inputs
+
+    build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = dict(WORKLOADS[args.workload])
+    B, T, d, e, s, C, causal = w["B"], w["T"], w["d"], w["e"], w["s"], w["C"], w["causal"]
+    tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    inp = make_inputs(**w)
+    W_uvz = np.concatenate([inp["W_u"], inp["W_v"], inp["W_z"]], axis=1)
+    weights = fg.GauWeights(torch.tensor(W_uvz, dtype=tdt, device=dev),
+                            torch.tensor(inp["W_o"], dtype=tdt, device=dev),
+                            torch.tensor(inp["gamma"], dtype=torch.float32, device=dev),
+                            torch.tensor(inp["beta"], dtype=torch.float32, device=dev),
+                            torch.tensor(inp["relpos"], dtype=torch.float32, device=dev),
+                            d, e, s)
+    X = torch.tensor(inp["X"], dtype=tdt, device=dev)
+    out = torch.empty_like(X)
+    ws = weights.new_workspace(B, T, C, causal, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = bd.stage_names(weights.dtype, causal)
+    nst = len(names)
+
+    def step(evs):
+        bd.forward(X, weights, C, causal, out=out, workspace=ws, stream=stream, stage_events=evs)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step(None)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+           for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(1.0)
+        step(evs[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    st = bd.workspace_status(ws)
+    if st != 0:
+        raise RuntimeError("kernel status %d after the timed region" % st)
+
+    per_stage = np.zeros(nst)
+    total_ms = 0.0
+    for k in range(args.steps):
+        for j in range(nst):
+            per_stage[j] += evs[k][j].elapsed_time(evs[k][j + 1])
+        total_ms += evs[k][0].elapsed_time(evs[k][nst])
+    per_stage /= args.steps
+    step_ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms, wall], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms, wall = float(t[0]), float(t[1])
+
+    # ---- end to end: pinned host X -> device, forward, O -> pinned host
+    Xh = X.cpu().pin_memory()
+    Oh = torch.empty_like(Xh).pin_memory()
+    for _ in range(max(1, args.warmup // 2)):
+        X.copy_(Xh, non_blocking=True)
+        step(None)
+        Oh.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 200))
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        X.copy_(Xh, non_blocking=True)
+        step(None)
+        Oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    if rank != 0:
+        return None
+    peaks = _peaks()
+    work = stage_work(w)
+    tokens = B * T * world
+    total_flops = sum(f for f, _ in work.values())
+    stages = {}
+    for j, n in enumerate(names):
+        f, b = work[n]
+        ms = float(per_stage[j])
+        stages[n] = {"ms": round(ms, 5), "share": round(ms / per_stage.sum(), 4),
+                     "bound": "tensor" if f / (peaks["bf16_tflops"] * 1e12) >=
+                              b / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                     "tflops": round(f / (ms * 1e-3) / 1e12, 1),
+                     "gbs": round(b / (ms * 1e-3) / 1e9, 1)}
+    dom = names[int(np.argmax(per_stage))]
+    f, b = work[dom]
+    dom_ms = float(per_stage[names.index(dom)])
+    # roofline: the bound is whichever of compute time and memory time at
+    # peak is larger for the kernel's algorithmic work
+    tensor_bound = f / (peaks["bf16_tflops"] * 1e12) >= b / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        achieved = f / (dom_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = b / (dom_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    layer_tflops = total_flops / (step_ms * 1e-3) / 1e12
+    res = {
+        "metric": METRIC,
+        "value": round(tokens / (step_ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w["dtype"],
+        "data": "synthetic (seeded numpy normal draws; no dataset)",
+        "config": {"workload": "%s: FLASH GAU forward B=%d T=%d d=%d e=%d s=%d C=%d %s %s"
+                               % (args.workload, B, T, d, e, s, C,
+                                  "causal" if causal else "non-causal", w["dtype"]),
+                   "B": B, "T": T, "d": d, "e": e, "s": s, "C": C, "causal": causal,
+                   "l2": "flushed before every timed step (512 MiB write)",
+                   "parallelism": "replicas (one independent problem per GPU)"},
+        "layer_tflops": round(layer_tflops, 1),
+        "layer_frac_of_bf16_peak": round(layer_tflops / peaks["bf16_tflops"], 4),
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "kernel": dom,
+                     "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": peaks["source"] + " (burst)",
+                     "traffic": traffic_record(dom, args.workload)},
+        "stages": stages,
+        "gpu_launches": nst * args.steps,
+        "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(X.numel() * X.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "ms_per_step": round(e2e_ms, 5)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return res
+
+
+def _oracle_sample(w, tokens):
+    """Oracle on a causal prefix of one sequence of the workload (a multiple
+    of C tokens), returns (seconds, tokens)."""
+    from efficient_attention_transformer_gb300.synthetic import make_inputs
+    from oracle import flash_gau
+    T = max(w["C"], min(w["T"], (tokens // w["C"]) * w["C"]))
+    inp = make_inputs(1, T, w["d"], w["e"], w["s"], w["C"], w["dtype"], w["seed"])
+    t0 = time.perf_counter()
+    flash_gau(inp["X"], inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"], inp["gamma"],
+              inp["beta"], inp["relpos"], w["C"], w["causal"])
+    return time.perf_counter() - t0, T
+
+
+def _threads():
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The oracle as it stands on the host cores, on whole sequences of the
+    workload repeated until about budget_s seconds of CPU work."""
+    secs, toks, reps = 0.0, 0, 0
+    while secs < budget_s and reps < 16:
+        dt, T = _oracle_sample(w, w["T"])
+        secs += dt
+        toks += T
+        reps += 1
+    return {"value": round(toks / secs, 1), "unit": "tokens/s", "cores": _threads(),
+            "kind": "oracle",
+            "sample": "%d x one full sequence (B=1, T=%d) of the workload, float64 numpy oracle, "
+                      "%.1f s" % (reps, w["T"], secs)}
+
+
+def run_reference(args):
+    """The oracle arm: each step runs the oracle on a causal prefix of one
+    sequence, sized so that warmup + steps stay within a few minutes."""
+    from efficient_attention_transformer_gb300.synthetic import WORKLOADS
+    w = dict(WORKLOADS[args.workload])
+    probe, T0 = _oracle_sample(w, w["C"])
+    per_tok = probe / T0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(budget / per_tok)
+    for _ in range(args.warmup):
+        _oracle_sample(w, tokens)
+    secs, toks = 0.0, 0
+    for _ in range(args.steps):
+        dt, T = _oracle_sample(w, tokens)
+        secs += dt
+        toks += T
+    v = toks / secs
+    sample = ("causal prefix of one sequence, %d tokens per step, float64 numpy oracle"
+              % (toks // max(1, args.steps)))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s (oracle on a bounded sample)" % args.workload},
+        "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s", "cores": _threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

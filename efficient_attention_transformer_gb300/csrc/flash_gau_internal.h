@@ -52,6 +52,9 @@ cudaError_t tc_projection_bf16(const Problem &p);
 cudaError_t tc_chunk_state_bf16(const Problem &p);
 cudaError_t tc_output_bf16(const Problem &p);
 
+// bf16 tensor-core chunk attention (chunk_attention.cu)
+cudaError_t tc_chunk_attention_bf16(const Problem &p);
+
 // bf16 CUDA-core stages
 cudaError_t simt_projection_bf16(const Problem &p);
 cudaError_t simt_chunk_state_bf16(const Problem &p);

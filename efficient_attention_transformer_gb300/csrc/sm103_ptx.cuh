@@ -68,13 +68,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false if
-// it has not completed within kWaitLimitNs (the caller then aborts).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// it has not completed within kWaitLimitNs, or as soon as *abort (a flag in
+// shared memory that another role of the CTA sets when it gives up) is
+// nonzero; the caller then aborts too.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int *abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((n & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
   }
 }
 

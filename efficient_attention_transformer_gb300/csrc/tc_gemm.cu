@@ -194,7 +194,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int n0 = nt * BN, nboxes = min(BN, p.N - n0) / 64;
         const int krow0 = batch * p.k_rows_per_batch;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1)) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
             break;
           }
@@ -231,7 +231,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int nsz = min(BN, p.N - nt * BN);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1)) {
+        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), acc_phase ^ 1, &sm->abort_flag)) {
           raise_timeout(sm, p.status);
           break;
         }
@@ -240,7 +240,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint32_t idesc = idesc_bf16_f32(BM, nsz, A_MN ? 1 : 0, 1);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&sm->full[stage]), phase)) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
             ok = false;
             break;
@@ -279,7 +279,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int mt = rem / p.n_tiles, nt = rem % p.n_tiles;
       const int n0 = nt * BN, nsz = min(BN, p.N - n0);
       const int acc = local & 1;
-      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1)) {
+      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
         raise_timeout(sm, p.status);
         break;
       }
