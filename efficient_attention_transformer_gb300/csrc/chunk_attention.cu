@@ -58,7 +58,7 @@ struct Bars {
   uint64_t b_full[2], b_empty[2];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_free[2];
-  uint64_t acc_full, drain;
+  uint64_t acc_full, drain, u_full;
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -69,8 +69,6 @@ struct AttnParams {
   int pre_rows_per_batch;  // causal: prefix row block per chunk; else per batch
   float inv_c;
   const float *relpos;
-  const __nv_bfloat16 *U;
-  __nv_bfloat16 *gated;
   int *status;
 };
 
@@ -103,7 +101,9 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                        const __grid_constant__ CUtensorMap tmKq,
                        const __grid_constant__ CUtensorMap tmQl,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmPre, const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tmPre,
+                       const __grid_constant__ CUtensorMap tmU,
+                       const __grid_constant__ CUtensorMap tmG, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -133,6 +133,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     }
     mbar_init(smem_u32(&bar->acc_full), 1);
     mbar_init(smem_u32(&bar->drain), 1);
+    mbar_init(smem_u32(&bar->u_full), 1);
     bar->abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -191,6 +192,20 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         if (kb + 1 < nkb) ok = load_k(kb + 1);
         const int vrow = (int)(tok0 + kb * KB);
         ok = ok && load_b(&tmV, vrow) && load_b(&tmV, vrow + 64);
+      }
+      // the U tile of the epilogue goes into the K_quad ring once the last
+      // S product has read it: 4 row quarters x 4 column boxes of 32 x 64
+      for (int i = 0; ok && i < 2; ++i) {
+        ok = mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, &bar->abort_flag);
+        kr.next();
+      }
+      if (ok) {
+        const uint32_t f = smem_u32(&bar->u_full);
+        mbar_arrive_expect_tx(f, QT * ET * 2);
+        for (int q = 0; q < 4; ++q)
+          for (int j = 0; j < ET / 64; ++j)
+            tma_load_2d(smem_u32(tiles + OFF_K + (q * 4 + j) * 4096), &tmU, f, et * ET + j * 64,
+                        qrow + q * 32);
       }
       if (!ok) raise_timeout(bar, p.status);
     }
@@ -309,33 +324,46 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       mbar_arrive(smem_u32(&bar->s_free[sb]));
       mbar_arrive(smem_u32(&bar->p_full[sb]));
     }
-    if (ok && mbar_wait(smem_u32(&bar->acc_full), 0, &bar->abort_flag)) {
+    if (ok && mbar_wait(smem_u32(&bar->acc_full), 0, &bar->abort_flag) &&
+        mbar_wait(smem_u32(&bar->u_full), 0, &bar->abort_flag)) {
       tc_fence_after();
-      const long long row = tok0 + i;
-      const __nv_bfloat16 *urow = p.U + row * p.e + et * ET;
-      __nv_bfloat16 *grow = p.gated + row * p.e + et * ET;
-#pragma unroll 1
-      for (int c0 = 0; c0 < ET; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + TM_ACC + c0, v);
-        uint4 u4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) u4[q] = __ldg(reinterpret_cast<const uint4 *>(urow + c0) + q);
+      // U boxes sit in the K ring, the gated boxes are staged in the B ring
+      // (free once every MMA has completed); both 32 rows x 128 bytes,
+      // swizzled, one per (row quarter, 64-column block).
+      for (int j = 0; j < ET / 64; ++j) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tmem + lane_off + TM_ACC + j * 64, va);
+        tmem_ld32(tmem + lane_off + TM_ACC + j * 64 + 32, vb);
         tmem_ld_wait();
+        const uint8_t *ubox = tiles + OFF_K + (quarter * 4 + j) * 4096;
+        uint8_t *gbox = tiles + OFF_B + (quarter * 4 + j) * 4096;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const __nv_bfloat162 *uh = reinterpret_cast<const __nv_bfloat162 *>(&u4[q]);
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u4 = *reinterpret_cast<const uint4 *>(ubox + sw128_offset(lane, c));
+          const __nv_bfloat162 *uh = reinterpret_cast<const __nv_bfloat162 *>(&u4);
+          const uint32_t *src = c < 4 ? &va[8 * c] : &vb[8 * (c - 4)];
           uint4 w;
           uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            float2 uf = __bfloat1622float2(uh[h]);
-            wp[h] = pack_bf16(uf.x * __uint_as_float(v[8 * q + 2 * h]),
-                              uf.y * __uint_as_float(v[8 * q + 2 * h + 1]));
+            const float2 uf = __bfloat1622float2(uh[h]);
+            wp[h] = pack_bf16(uf.x * __uint_as_float(src[2 * h]),
+                              uf.y * __uint_as_float(src[2 * h + 1]));
           }
-          reinterpret_cast<uint4 *>(grow + c0)[q] = w;
+          *reinterpret_cast<uint4 *>(gbox + sw128_offset(lane, c)) = w;
         }
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int grow = (int)(tok0 + qt * QT + quarter * 32);
+        for (int j = 0; j < ET / 64; ++j)
+          tma_store_2d(&tmG, smem_u32(tiles + OFF_B + (quarter * 4 + j) * 4096), et * ET + j * 64,
+                       grow);
+        tma_store_commit();
+        tma_store_wait<0>();
+      }
+      __syncwarp();
     } else {
       raise_timeout(bar, p.status);
     }
@@ -362,6 +390,9 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   if ((err = make_tmap_bf16_2d(&tQl, heads + 2 * Ms, pr.M, pr.s, pr.s, QT, 64)) != cudaSuccess)
     return err;
   if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 64, 64)) != cudaSuccess) return err;
+  CUtensorMap tU, tG;
+  if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tG, pr.gated, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   const long long pre_rows = (long long)(pr.causal ? pr.B * pr.G : pr.B) * pr.s;
   if ((err = make_tmap_bf16_2d(&tPre, pr.prefix, pre_rows, pr.e, pr.e, 64, 64)) != cudaSuccess)
     return err;
@@ -384,11 +415,10 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.pre_rows_per_batch = pr.s;
   p.inv_c = 1.0f / (float)pr.C;
   p.relpos = pr.relpos;
-  p.U = (const __nv_bfloat16 *)pr.U;
-  p.gated = (__nv_bfloat16 *)pr.gated;
   p.status = pr.status;
   dim3 grid(pr.e / ET, pr.C / QT, pr.B * pr.G);
-  chunk_attention_kernel<<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tQq, tKq, tQl, tV, tPre, p);
+  chunk_attention_kernel<<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tQq, tKq, tQl, tV, tPre,
+                                                                       tU, tG, p);
   return cudaGetLastError();
 }
 

@@ -100,6 +100,48 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
+// 2-D tiled store of one box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed store groups of this thread still read smem.
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N committed store groups of this thread are incomplete.
+template <int N>
+__device__ __forceinline__ void tma_store_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Hardware tanh approximation (one MUFU operation).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// swish(x) = x * sigmoid(x) = (x/2) * (1 + tanh(x/2)).
+__device__ __forceinline__ float swish_tanh(float x) {
+  const float h = 0.5f * x;
+  return fmaf(h, tanh_approx(h), h);
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` inside a 128-byte-swizzled
+// tile whose rows are 128 bytes (the layout TMA writes and reads with
+// CU_TENSOR_MAP_SWIZZLE_128B on a 1024-byte-aligned buffer).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
 // ----------------------------------------------------------------- tcgen05
 // TMEM allocation is warp-wide; the base address is written to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -26,32 +26,29 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int A_BYTES = BM * BK * 2;      // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;  // one 64-wide N block of a k-block: 8 KB
 constexpr int B_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int STG_BYTES = 32 * 128;                  // one 32-row x 128-byte store box
+constexpr int STG_OFF = STAGES * STAGE_BYTES;        // 2 staging boxes per epilogue warp
+constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
+constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_STATE = 2 };
 
 struct GemmParams {
-  int N, K;             // output columns, contraction depth (per batch)
-  int m_tiles, n_tiles; // per batch
-  int total_tiles;      // batches * m_tiles * n_tiles
-  int k_rows_per_batch; // row offset of a batch along K in the K-indexed maps
+  int N, K;              // output columns, contraction depth (per batch)
+  int m_tiles, n_tiles;  // per batch
+  int total_tiles;       // batches * m_tiles * n_tiles
+  int k_rows_per_batch;  // row offset of a batch along K in the K-indexed maps
   // projection epilogue
-  __nv_bfloat16 *U, *V, *heads;
   const float *gamma, *beta;
-  long long M_tokens;
+  int M_tokens;
   int e, s;
-  // plain store epilogue
-  __nv_bfloat16 *out;
-  int ld_out;
-  // chunk-state epilogue
-  float *state;
   int *status;
 };
 
@@ -70,88 +67,71 @@ __device__ __forceinline__ void raise_timeout(Smem *sm, int *status) {
   atomicExch(status, FLASH_GAU_ETIMEOUT);
 }
 
-__device__ __forceinline__ float swish_fast(float x) { return x / (1.0f + __expf(-x)); }
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int EPI>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams &p, int batch, long long row,
-                                               int n0, int c0, const uint32_t (&r)[32]) {
-  float v[32];
+// Per-warp staged TMA store: the warp writes one 32-row x 128-byte box into
+// one of its two staging buffers (row = lane, swizzled), then lane 0 stores
+// it.  A buffer is rewritten only after the store issued from it two boxes
+// earlier has finished reading shared memory.
+struct Stager {
+  uint8_t *buf;  // this warp's 2 x 4 KB
+  int lane;
+  int count = 0;
+  __device__ uint8_t *begin() {
+    if (lane == 0) tma_store_wait_read<1>();
+    __syncwarp();
+    return buf + (count & 1) * STG_BYTES;
+  }
+  // row data: 8 x 16 bytes
+  __device__ void put(uint8_t *b, const uint4 (&w)[8]) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if constexpr (EPI == EPI_PROJ) {
-    const int n = n0 + c0;
-    if (n < 2 * p.e) {
-      __nv_bfloat16 *dst = (n < p.e ? p.U : p.V) + row * p.e + (n < p.e ? n : n - p.e);
-      uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        w.x = pack_bf16(swish_fast(v[8 * q + 0]), swish_fast(v[8 * q + 1]));
-        w.y = pack_bf16(swish_fast(v[8 * q + 2]), swish_fast(v[8 * q + 3]));
-        w.z = pack_bf16(swish_fast(v[8 * q + 4]), swish_fast(v[8 * q + 5]));
-        w.w = pack_bf16(swish_fast(v[8 * q + 6]), swish_fast(v[8 * q + 7]));
-        d4[q] = w;
-      }
-    } else {
-      const int c = n - 2 * p.e;  // column inside Z
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = swish_fast(v[j]);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float *g = p.gamma + h * p.s + c;
-        const float *b = p.beta + h * p.s + c;
-        uint4 *d4 = reinterpret_cast<uint4 *>(p.heads + (long long)h * p.M_tokens * p.s +
-                                              row * p.s + c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16(fmaf(v[8 * q + 0], g[8 * q + 0], b[8 * q + 0]),
-                          fmaf(v[8 * q + 1], g[8 * q + 1], b[8 * q + 1]));
-          w.y = pack_bf16(fmaf(v[8 * q + 2], g[8 * q + 2], b[8 * q + 2]),
-                          fmaf(v[8 * q + 3], g[8 * q + 3], b[8 * q + 3]));
-          w.z = pack_bf16(fmaf(v[8 * q + 4], g[8 * q + 4], b[8 * q + 4]),
-                          fmaf(v[8 * q + 5], g[8 * q + 5], b[8 * q + 5]));
-          w.w = pack_bf16(fmaf(v[8 * q + 6], g[8 * q + 6], b[8 * q + 6]),
-                          fmaf(v[8 * q + 7], g[8 * q + 7], b[8 * q + 7]));
-          d4[q] = w;
-        }
-      }
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(b + sw128_offset(lane, c)) = w[c];
+  }
+  __device__ void finish(uint8_t *b, const CUtensorMap *tm, int x, int y) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, smem_u32(b), x, y);
+      tma_store_commit();
     }
-  } else if constexpr (EPI == EPI_STORE) {
-    uint4 *d4 = reinterpret_cast<uint4 *>(p.out + row * p.ld_out + n0 + c0);
+    ++count;
+  }
+  __device__ void drain() {
+    if (lane == 0) tma_store_wait<0>();
+    __syncwarp();
+  }
+};
+
+// 64 accumulator columns of this thread's row -> 8 x 16 bytes of bf16
+template <typename F>
+__device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (&b)[32], F f,
+                                       uint4 (&w)[8]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-      w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-      w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-      w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-      d4[q] = w;
-    }
-  } else {  // EPI_STATE: row is the s-index inside the chunk state
-    float4 *d4 = reinterpret_cast<float4 *>(p.state + ((long long)batch * p.s + row) * p.N + n0 +
-                                            c0);
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      d4[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t *src = c < 4 ? &a[8 * c] : &b[8 * (c - 4)];
+    const int col = 8 * c;
+    w[c].x = pack_bf16(f(__uint_as_float(src[0]), col + 0), f(__uint_as_float(src[1]), col + 1));
+    w[c].y = pack_bf16(f(__uint_as_float(src[2]), col + 2), f(__uint_as_float(src[3]), col + 3));
+    w[c].z = pack_bf16(f(__uint_as_float(src[4]), col + 4), f(__uint_as_float(src[5]), col + 5));
+    w[c].w = pack_bf16(f(__uint_as_float(src[6]), col + 6), f(__uint_as_float(src[7]), col + 7));
   }
 }
 
 // A_MN: A is stored M-contiguous (K_lin^T of the chunk state); otherwise
-// K-contiguous.
+// K-contiguous.  tmC0..2 are the output maps of the epilogue (U, V, heads
+// for the projection; the output for the plain store; the state).
 template <int EPI, bool A_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+               const __grid_constant__ CUtensorMap tmC2, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem *sm = reinterpret_cast<Smem *>(tiles + STAGES * STAGE_BYTES);
+  Smem *sm = reinterpret_cast<Smem *>(tiles + TILE_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -273,6 +253,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    Stager st{tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES, lane};
     int local = 0;
     for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x, ++local) {
       const int batch = t / tiles_per_batch, rem = t % tiles_per_batch;
@@ -284,17 +265,73 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         break;
       }
       tc_fence_after();
-      const long long row = (long long)mt * BM + quarter * 32 + lane;
+      const int row0 = mt * BM + quarter * 32;  // first row of this warp's box
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
-      for (int c0 = 0; c0 < nsz; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c0, r);
-        tmem_ld_wait();
-        epilogue_chunk<EPI>(p, batch, row, n0, c0, r);
+      if constexpr (EPI == EPI_STATE) {
+        // fp32: 32 columns (128 bytes) per box
+        for (int c0 = 0; c0 < nsz; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c0, r);
+          tmem_ld_wait();
+          if (c0 + 32 >= nsz) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+          }
+          uint4 w[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) w[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+          uint8_t *b = st.begin();
+          st.put(b, w);
+          st.finish(b, &tmC0, n0 + c0, batch * p.s + row0);
+        }
+      } else {
+        for (int c0 = 0; c0 < nsz; c0 += 64) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + c0, ra);
+          tmem_ld32(taddr + c0 + 32, rb);
+          tmem_ld_wait();
+          if (c0 + 64 >= nsz) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+          }
+          if constexpr (EPI == EPI_STORE) {
+            uint4 w[8];
+            pack64(ra, rb, [](float x, int) { return x; }, w);
+            uint8_t *b = st.begin();
+            st.put(b, w);
+            st.finish(b, &tmC0, n0 + c0, row0);
+          } else {
+            const int n = n0 + c0;
+            if (n < 2 * p.e) {
+              uint4 w[8];
+              pack64(ra, rb, [](float x, int) { return swish_tanh(x); }, w);
+              uint8_t *b = st.begin();
+              st.put(b, w);
+              if (n < p.e) st.finish(b, &tmC0, n, row0);
+              else st.finish(b, &tmC1, n - p.e, row0);
+            } else {
+              const int c = n - 2 * p.e;  // column inside Z
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                ra[j] = __float_as_uint(swish_tanh(__uint_as_float(ra[j])));
+                rb[j] = __float_as_uint(swish_tanh(__uint_as_float(rb[j])));
+              }
+#pragma unroll 1
+              for (int h = 0; h < 4; ++h) {
+                const float *g = p.gamma + h * p.s + c;
+                const float *be = p.beta + h * p.s + c;
+                uint4 w[8];
+                pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); }, w);
+                uint8_t *b = st.begin();
+                st.put(b, w);
+                st.finish(b, &tmC2, c, h * p.M_tokens + row0);
+              }
+            }
+          }
+        }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm->acc_empty[acc]));
     }
+    st.drain();
   }
 
   tc_fence_before();
@@ -306,7 +343,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 template <int EPI, bool A_MN>
-cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p,
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &c0,
+                   const CUtensorMap &c1, const CUtensorMap &c2, const GemmParams &p,
                    const Problem &pr) {
   static unsigned long long configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -319,14 +357,14 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmPar
     configured |= 1ull << dev;
   }
   const int grid = p.total_tiles < pr.num_sms ? p.total_tiles : pr.num_sms;
-  tc_gemm_kernel<EPI, A_MN><<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tmA, tmB, p);
+  tc_gemm_kernel<EPI, A_MN><<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tmA, tmB, c0, c1, c2, p);
   return cudaGetLastError();
 }
 
 GemmParams base_params(const Problem &pr) {
   GemmParams p = {};
   p.status = pr.status;
-  p.M_tokens = pr.M;
+  p.M_tokens = (int)pr.M;
   p.e = pr.e;
   p.s = pr.s;
   return p;
@@ -336,49 +374,52 @@ GemmParams base_params(const Problem &pr) {
 
 cudaError_t tc_projection_bf16(const Problem &pr) {
   const int N = 2 * pr.e + pr.s;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tU, tV, tH;
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tH, pr.heads, 4 * pr.M, pr.s, pr.s, 32, 64)) != cudaSuccess)
+    return err;
   GemmParams p = base_params(pr);
   p.N = N;
   p.K = pr.d;
   p.m_tiles = (int)(pr.M / BM);
   p.n_tiles = (N + BN - 1) / BN;
   p.total_tiles = p.m_tiles * p.n_tiles;
-  p.U = (__nv_bfloat16 *)pr.U;
-  p.V = (__nv_bfloat16 *)pr.V;
-  p.heads = (__nv_bfloat16 *)pr.heads;
   p.gamma = pr.gamma;
   p.beta = pr.beta;
-  return launch<EPI_PROJ, false>(tmA, tmB, p, pr);
+  return launch<EPI_PROJ, false>(tmA, tmB, tU, tV, tH, p, pr);
 }
 
 cudaError_t tc_output_bf16(const Problem &pr) {
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tO;
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tmA, pr.gated, pr.M, pr.e, pr.e, BM, 64)) != cudaSuccess)
     return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
     return err;
+  if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
   GemmParams p = base_params(pr);
   p.N = pr.d;
   p.K = pr.e;
   p.m_tiles = (int)(pr.M / BM);
   p.n_tiles = (pr.d + BN - 1) / BN;
   p.total_tiles = p.m_tiles * p.n_tiles;
-  p.out = (__nv_bfloat16 *)pr.out;
-  p.ld_out = pr.d;
-  return launch<EPI_STORE, false>(tmA, tmB, p, pr);
+  return launch<EPI_STORE, false>(tmA, tmB, tO, tO, tO, p, pr);
 }
 
 cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   // batch = chunk (b*G + g): State[chunk] = K_lin[chunk rows]^T V[chunk rows]
   const __nv_bfloat16 *Kl = (const __nv_bfloat16 *)pr.heads + 3 * pr.M * pr.s;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tS;
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tmA, Kl, pr.M, pr.s, pr.s, BK, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.V, pr.M, pr.e, pr.e, BK, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_f32_2d(&tS, pr.state, (long long)pr.B * pr.G * pr.s, pr.e, pr.e, 32, 32)) !=
+      cudaSuccess)
+    return err;
   GemmParams p = base_params(pr);
   p.N = pr.e;
   p.K = pr.C;
@@ -386,8 +427,7 @@ cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   p.n_tiles = (pr.e + BN - 1) / BN;
   p.total_tiles = pr.B * pr.G * p.n_tiles;
   p.k_rows_per_batch = pr.C;
-  p.state = pr.state;
-  return launch<EPI_STATE, true>(tmA, tmB, p, pr);
+  return launch<EPI_STATE, true>(tmA, tmB, tS, tS, tS, p, pr);
 }
 
 }  // namespace flashgau

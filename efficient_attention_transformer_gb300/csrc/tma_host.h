@@ -15,4 +15,8 @@ namespace flashgau {
 cudaError_t make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                               uint64_t ld, uint32_t box_rows, uint32_t box_cols);
 
+// Same for fp32 elements (box_cols * 4 must be 128).
+cudaError_t make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                             uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
 }  // namespace flashgau
