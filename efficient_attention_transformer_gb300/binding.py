@@ -35,7 +35,11 @@ EXPORTED = (
     "flash_gau_workspace_status",
     "flash_gau_strerror",
     "flash_gau_version",
+    "flash_gau_forward_noalloc",
 )
+
+# Capacity of the static scratch behind flash_gau_forward_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
 class Weights(ctypes.Structure):
@@ -96,6 +100,8 @@ def lib():
         L.flash_gau_strerror.restype = ctypes.c_char_p
         L.flash_gau_version.argtypes = []
         L.flash_gau_version.restype = i
+        L.flash_gau_forward_noalloc.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p]
+        L.flash_gau_forward_noalloc.restype = i
         _lib = L
     return _lib
 
@@ -207,6 +213,25 @@ def forward(X, weights, C, causal, out=None, workspace=None, stream=None,
     else:
         st = lib().flash_gau_forward(*args)
     _check(st)
+    return out
+
+
+def forward_noalloc(X, weights, C, causal, out=None, stream=None):
+    """O = FLASH-GAU(X) through flash_gau_forward_noalloc: no workspace, the
+    intermediates live in the library's static 32 MiB device scratch (shared
+    by every call on the device; calls must not overlap on the GPU)."""
+    if X.dim() != 3:
+        raise ValueError("X must be [B, T, d]")
+    B, T, d = X.shape
+    if d != weights.d or X.dtype != weights.W_uvz.dtype:
+        raise ValueError("X does not match the weights")
+    if out is None:
+        out = torch.empty_like(X)
+    if stream is None:
+        stream = torch.cuda.current_stream(X.device)
+    _check(lib().flash_gau_forward_noalloc(
+        _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), B, T, C, int(bool(causal)),
+        weights.dtype, _dev_ptr(out, "out", X.dtype), stream.cuda_stream))
     return out
 
 

@@ -1,0 +1,53 @@
+// flash_gau_forward_noalloc: the forward pass with its workspace in a static
+// device array instead of caller memory, for callers that cannot allocate
+// device memory where they run the layer.  It runs the unchanged
+// flash_gau_forward on that array.
+#include <mutex>
+
+#include "flash_gau_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// The scratch itself.  In host code this name is only a stand-in for the
+// symbol: its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FLASH_GAU_NOALLOC_SCRATCH_BYTES];
+
+void *g_scratch_addr[kMaxDevices];  // device address per device ordinal
+std::mutex g_scratch_mu;
+
+}  // namespace
+
+extern "C" int flash_gau_forward_noalloc(const void *X, const flash_gau_weights *w, int B, int T,
+                                         int C, int causal, int dtype, void *out, void *stream) {
+  if (!X || !w || !out) return FLASH_GAU_EINVAL;
+  causal = causal ? 1 : 0;
+  flash_gau_workspace_layout L;
+  int st = flash_gau_workspace_layout_query(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
+  if (st != FLASH_GAU_OK) return st;
+  if (L.total_bytes > FLASH_GAU_NOALLOC_SCRATCH_BYTES) return FLASH_GAU_EWORKSPACE;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLASH_GAU_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FLASH_GAU_EDEVICE;
+  void *scratch = nullptr;
+  {
+    // once per device, with that device current
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+        return FLASH_GAU_ECUDA;
+      g_scratch_addr[dev] = ptr;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  // The status word is the only part of the workspace that must start at
+  // zero; every intermediate is fully rewritten by the kernels.
+  if (cudaMemsetAsync(static_cast<char *>(scratch) + L.status, 0, sizeof(int),
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLASH_GAU_ECUDA;
+  return flash_gau_forward(X, w, B, T, C, causal, dtype, out, scratch,
+                           FLASH_GAU_NOALLOC_SCRATCH_BYTES, stream);
+}

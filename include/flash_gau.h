@@ -154,6 +154,45 @@ const char *flash_gau_strerror(int status);
 /* Library version as major*10000 + minor*100 + patch.                      */
 int flash_gau_version(void);
 
+/* ---- allocation-free variant ------------------------------------------- */
+/* No counterpart on the pages: this entry point exists for deployment, not
+ * for the method.
+ *
+ * Some callers cannot allocate device memory at the point where they run
+ * the layer: a plugin whose host framework owns every byte of the device
+ * through its own pool and forbids raw allocations, a callback that runs
+ * while such a pool is locked, or a latency-critical path that must not
+ * take the implicit device synchronisation of cudaMalloc/cudaFree.  For
+ * them, flash_gau_forward_noalloc computes exactly what flash_gau_forward
+ * computes, but keeps its intermediates in a scratch array that is part of
+ * the library image instead of a caller-supplied workspace.
+ *
+ *   - The scratch is a file-scope static __device__ array of
+ *     FLASH_GAU_NOALLOC_SCRATCH_BYTES (32 MiB).  Every GPU on which the
+ *     library's device code is loaded holds these 32 MiB until the process
+ *     exits.
+ *   - Problems whose workspace (flash_gau_workspace_bytes) is larger than
+ *     the scratch are rejected with FLASH_GAU_EWORKSPACE before anything is
+ *     launched; other argument errors return the same codes as
+ *     flash_gau_forward.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make
+ *     that first call before any stream capture on that device.
+ *   - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine.  It enqueues a 4-byte cudaMemsetAsync that clears
+ *     the status word, then the same kernels as flash_gau_forward, on
+ *     `stream`, and returns without synchronising.
+ *   - All calls on a device share the one array, which keeps the previous
+ *     call's intermediates.  Calls whose kernels overlap on the GPU (other
+ *     streams, other host threads) race on it: the caller must order them,
+ *     e.g. by issuing them on one stream.
+ *   - A bounded-wait timeout of these kernels is recorded in the shared
+ *     status word only and is not reported to the caller.
+ * Arguments as for flash_gau_forward, without the workspace.               */
+#define FLASH_GAU_NOALLOC_SCRATCH_BYTES ((size_t)32 * 1024 * 1024)
+int flash_gau_forward_noalloc(const void *X, const flash_gau_weights *w, int B, int T,
+                              int C, int causal, int dtype, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
