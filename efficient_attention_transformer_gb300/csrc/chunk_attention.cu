@@ -145,6 +145,9 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // setup above overlaps the previous kernel's tail; its outputs are read below
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = bar->tmem_base;
 
   if (warp == 0) {
@@ -417,9 +420,8 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.relpos = pr.relpos;
   p.status = pr.status;
   dim3 grid(pr.e / ET, pr.C / QT, pr.B * pr.G);
-  chunk_attention_kernel<<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tQq, tKq, tQl, tV, tPre,
-                                                                       tU, tG, p);
-  return cudaGetLastError();
+  return launch_pdl(chunk_attention_kernel, grid, dim3(NUM_THREADS), SMEM_BYTES, pr.stream, tQq,
+                    tKq, tQl, tV, tPre, tU, tG, p);
 }
 
 }  // namespace flashgau

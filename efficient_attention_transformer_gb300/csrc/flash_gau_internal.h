@@ -35,6 +35,26 @@ struct Problem {
 
 using StageFn = cudaError_t (*)(const Problem &);
 
+// Launches `kernel` on the problem's stream with programmatic stream
+// serialisation, so that it may start while the previous kernel drains; the
+// kernel itself waits (griddepcontrol.wait) before touching data that the
+// previous kernels produce or consume.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct Stage {
   const char *name;
   StageFn fn;

@@ -11,8 +11,11 @@
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace flashgau {
+using ptx::griddep_launch_dependents;
+using ptx::griddep_wait;
 namespace {
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -126,6 +129,8 @@ struct StoreEpi {
 template <typename T>
 __global__ void simt_prefix_scan(const float *__restrict__ state, T *__restrict__ prefix,
                                  int B, int G, long long se, int causal, float lin_scale) {
+  griddep_wait();
+  griddep_launch_dependents();
   long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= B * se) return;
   long long b = idx / se, r = idx % se;
@@ -276,9 +281,8 @@ cudaError_t chunk_state(const Problem &p) {
 template <typename T>
 cudaError_t prefix_scan(const Problem &p) {
   long long se = (long long)p.s * p.e;
-  simt_prefix_scan<T><<<cdiv(p.B * se, 256), 256, 0, p.stream>>>(
-      p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
-  return cudaGetLastError();
+  return launch_pdl(simt_prefix_scan<T>, dim3(cdiv(p.B * se, 256)), dim3(256), 0, p.stream,
+                    p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
 }
 
 template <typename T>

@@ -84,6 +84,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------ programmatic dependent launch
+// Blocks until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic stream serialisation) have
+// completed and their memory is visible.  A no-op for ordinary launches.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream be scheduled before this one ends (it
+// still waits in griddep_wait for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

@@ -159,6 +159,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // setup above overlaps the previous kernel's tail; its outputs are read below
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
@@ -357,8 +360,8 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
     configured |= 1ull << dev;
   }
   const int grid = p.total_tiles < pr.num_sms ? p.total_tiles : pr.num_sms;
-  tc_gemm_kernel<EPI, A_MN><<<grid, NUM_THREADS, SMEM_BYTES, pr.stream>>>(tmA, tmB, c0, c1, c2, p);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<EPI, A_MN>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES,
+                    pr.stream, tmA, tmB, c0, c1, c2, p);
 }
 
 GemmParams base_params(const Problem &pr) {
