@@ -66,7 +66,7 @@ int check_shape(int B, int T, int C, int d, int e, int s, int dtype) {
   if (dtype == FLASH_GAU_FP32) {
     if (s > 128) return FLASH_GAU_ENOTSUP;
   } else {
-    if (d % 64 != 0 || e % 256 != 0 || s != 128 || C % 128 != 0) return FLASH_GAU_ENOTSUP;
+    if (d % 128 != 0 || e % 256 != 0 || s != 128 || C % 128 != 0) return FLASH_GAU_ENOTSUP;
   }
   return FLASH_GAU_OK;
 }

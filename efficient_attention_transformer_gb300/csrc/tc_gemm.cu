@@ -375,44 +375,6 @@ GemmParams base_params(const Problem &pr) {
 
 }  // namespace
 
-cudaError_t tc_projection_bf16(const Problem &pr) {
-  const int N = 2 * pr.e + pr.s;
-  CUtensorMap tmA, tmB, tU, tV, tH;
-  cudaError_t err;
-  if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tH, pr.heads, 4 * pr.M, pr.s, pr.s, 32, 64)) != cudaSuccess)
-    return err;
-  GemmParams p = base_params(pr);
-  p.N = N;
-  p.K = pr.d;
-  p.m_tiles = (int)(pr.M / BM);
-  p.n_tiles = (N + BN - 1) / BN;
-  p.total_tiles = p.m_tiles * p.n_tiles;
-  p.gamma = pr.gamma;
-  p.beta = pr.beta;
-  return launch<EPI_PROJ, false>(tmA, tmB, tU, tV, tH, p, pr);
-}
-
-cudaError_t tc_output_bf16(const Problem &pr) {
-  CUtensorMap tmA, tmB, tO;
-  cudaError_t err;
-  if ((err = make_tmap_bf16_2d(&tmA, pr.gated, pr.M, pr.e, pr.e, BM, 64)) != cudaSuccess)
-    return err;
-  if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
-    return err;
-  if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
-  GemmParams p = base_params(pr);
-  p.N = pr.d;
-  p.K = pr.e;
-  p.m_tiles = (int)(pr.M / BM);
-  p.n_tiles = (pr.d + BN - 1) / BN;
-  p.total_tiles = p.m_tiles * p.n_tiles;
-  return launch<EPI_STORE, false>(tmA, tmB, tO, tO, tO, p, pr);
-}
-
 cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   // batch = chunk (b*G + g): State[chunk] = K_lin[chunk rows]^T V[chunk rows]
   const __nv_bfloat16 *Kl = (const __nv_bfloat16 *)pr.heads + 3 * pr.M * pr.s;

@@ -1,0 +1,412 @@
+// Pair (2-SM) tcgen05 GEMM with fused epilogues for the two large dense
+// contractions of the FLASH GAU forward, bf16 in, fp32 accumulation:
+//   projection   [U|V|Z] = swish(X W_uvz); the Z tile's epilogue writes the
+//                four scale/offset heads Z*gamma_h + beta_h
+//                ("Transformer Quality in Linear Time", Method, eq. 5 and
+//                 the four heads of mixed chunk attention)
+//   output       O = gated W_o                   (display after eq. 8)
+//
+// A cluster of two CTAs on neighbouring SMs computes 256 x 256 output tiles
+// with tcgen05.mma.cta_group::2 (M = 256): each CTA holds its own 128 rows
+// of A and half of the B columns of every 64-deep k-block (32 KB per stage,
+// 6 stages), so each SM moves two thirds of the operand bytes a single-SM
+// 128 x 256 tile needs.  The leader CTA's warp 1 issues the MMAs; both CTAs'
+// TMA loads complete on the leader's stage barrier; the leader's commits
+// release the stage, and announce a finished accumulator, in both CTAs.
+// Each CTA's TMEM holds its own 128 rows (two 256-column accumulators); its
+// warps 2-5 drain them through tcgen05.ld into swizzled staging and TMA
+// stores, and report the accumulator free to the leader.
+#include <cuda_bf16.h>
+
+#include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace flashgau {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;                          // rows per CTA (256 per pair)
+constexpr int BN = 256;                          // columns per pair tile
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;         // 8 KB: 64 columns x 64 k-rows
+constexpr int STAGE_BYTES = A_BYTES + BN / 2 * BK * 2;  // 32 KB
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int NUM_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int STG_BYTES = 32 * 128;                    // one 32-row x 128-byte store box
+constexpr int STG_OFF = STAGES * STAGE_BYTES;          // 2 staging boxes per epilogue warp
+constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
+constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint16_t kPair = 0x3, kLeader = 0x1;
+
+enum Epi { EPI_PROJ = 0, EPI_STORE = 1 };
+
+struct Params {
+  int N, K;        // output columns, contraction depth
+  int m_tiles;     // 128-row tiles of the output
+  int n_tiles;     // 256-column pair tiles
+  int total;       // ceil(m_tiles / 2) * n_tiles pair tiles
+  const float *gamma, *beta;
+  int M_tokens;
+  int e, s;
+  int *status;
+};
+
+struct Smem {
+  uint64_t full[STAGES];   // leader: both CTAs' loads of a stage landed
+  uint64_t empty[STAGES];  // both: the pair MMAs have read the stage
+  uint64_t acc_full[2];    // both: an accumulator is ready
+  uint64_t acc_empty[2];   // leader: both CTAs drained an accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ void raise_timeout(Smem *sm, int *status) {
+  sm->abort_flag = 1;
+  atomicExch(status, FLASH_GAU_ETIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Per-warp staged TMA store: the warp writes one 32-row x 128-byte box into
+// one of its two staging buffers (row = lane, swizzled), then lane 0 stores
+// it.  A buffer is rewritten only after the store issued from it two boxes
+// earlier has finished reading shared memory.
+struct Stager {
+  uint8_t *buf;  // this warp's 2 x 4 KB
+  int lane;
+  int count = 0;
+  __device__ uint8_t *begin() {
+    if (lane == 0) tma_store_wait_read<1>();
+    __syncwarp();
+    return buf + (count & 1) * STG_BYTES;
+  }
+  // row data: 8 x 16 bytes
+  __device__ void put(uint8_t *b, const uint4 (&w)[8]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(b + sw128_offset(lane, c)) = w[c];
+  }
+  __device__ void finish(uint8_t *b, const CUtensorMap *tm, int x, int y) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, smem_u32(b), x, y);
+      tma_store_commit();
+    }
+    ++count;
+  }
+  __device__ void drain() {
+    if (lane == 0) tma_store_wait<0>();
+    __syncwarp();
+  }
+};
+
+// 64 accumulator columns of this thread's row -> 8 x 16 bytes of bf16
+template <typename F>
+__device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (&b)[32], F f,
+                                       uint4 (&w)[8]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t *src = c < 4 ? &a[8 * c] : &b[8 * (c - 4)];
+    const int col = 8 * c;
+    w[c].x = pack_bf16(f(__uint_as_float(src[0]), col + 0), f(__uint_as_float(src[1]), col + 1));
+    w[c].y = pack_bf16(f(__uint_as_float(src[2]), col + 2), f(__uint_as_float(src[3]), col + 3));
+    w[c].z = pack_bf16(f(__uint_as_float(src[4]), col + 4), f(__uint_as_float(src[5]), col + 5));
+    w[c].w = pack_bf16(f(__uint_as_float(src[6]), col + 6), f(__uint_as_float(src[7]), col + 7));
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC0,
+                    const __grid_constant__ CUtensorMap tmC1,
+                    const __grid_constant__ CUtensorMap tmC2, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem *sm = reinterpret_cast<Smem *>(tiles + TILE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = (int)cluster_ctarank();  // 0 = leader of the pair
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&sm->full[i]), 1);
+      mbar_init(smem_u32(&sm->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm->acc_full[i]), 1);
+      mbar_init(smem_u32(&sm->acc_empty[i]), 8);  // 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    sm->abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any remote access
+  tc_fence_after();
+  // setup above overlaps the previous kernel's tail; its outputs are read below
+  griddep_wait();
+  griddep_launch_dependents();
+  const uint32_t tmem_base = sm->tmem_base;
+  const int kblocks = p.K / BK;
+  const int first = blockIdx.x / 2, step = gridDim.x / 2;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both)
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = first; t < p.total && !sm->abort_flag; t += step) {
+        const int mt = (t / p.n_tiles) * 2 + rank, nt = t % p.n_tiles;
+        // an overhanging CTA of the last pair re-reads the last valid rows
+        // (its results are discarded) so every box is in bounds
+        const int arow = min(mt, p.m_tiles - 1) * BM;
+        const int n0 = nt * BN, half = min(BN, p.N - n0) / 2, hboxes = half / 64;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
+            raise_timeout(sm, p.status);
+            break;
+          }
+          const uint32_t full_own = smem_u32(&sm->full[stage]);
+          const uint32_t full_leader = mapa_shared(full_own, 0);
+          uint8_t *sA = tiles + stage * STAGE_BYTES;
+          uint8_t *sB = sA + A_BYTES;
+          if (leader) mbar_arrive_expect_tx(full_own, 2 * (A_BYTES + hboxes * B_BOX_BYTES));
+          tma_load_2d_pair(smem_u32(sA), &tmA, full_leader, kb * BK, arow);
+          for (int j = 0; j < hboxes; ++j)
+            tma_load_2d_pair(smem_u32(sB + j * B_BOX_BYTES), &tmB, full_leader,
+                             n0 + rank * half + j * 64, kb * BK);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (leader)
+    if (leader && elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
+        const int nt = t % p.n_tiles;
+        const int nsz = min(BN, p.N - nt * BN);
+        const int acc = local & 1;
+        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), ((local >> 1) & 1) ^ 1, &sm->abort_flag)) {
+          raise_timeout(sm, p.status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        const uint32_t idesc = idesc_bf16_f32(2 * BM, nsz, 0, 1);
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, &sm->abort_flag)) {
+            raise_timeout(sm, p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sB = sA + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // A: K-major, 16 elements (32 B) per step inside the swizzle atom;
+            // B: N-major, 16 rows of 128 B per step, 64-column boxes 8 KB apart
+            mma_f16_ss_pair(d_tmem, sw128_desc(sA + k * 32, 16, 1024),
+                            sw128_desc(sB + k * 2048, B_BOX_BYTES, 1024), idesc, (kb | k) != 0);
+          }
+          mma_commit_pair_mc(smem_u32(&sm->empty[stage]), kPair);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(smem_u32(&sm->acc_full[acc]), kPair);
+      }
+      // every MMA this thread issued has completed once `drain` flips
+      mma_commit_pair_mc(smem_u32(&sm->drain), kLeader);
+      if (!mbar_wait(smem_u32(&sm->drain), 0)) raise_timeout(sm, p.status);
+    }
+  } else {
+    // -------------------------------------------------- epilogue (both)
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    Stager st{tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES, lane};
+    int local = 0;
+    for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
+      const int mt = (t / p.n_tiles) * 2 + rank, nt = t % p.n_tiles;
+      const bool valid = mt < p.m_tiles;
+      const int n0 = nt * BN, nsz = min(BN, p.N - n0);
+      const int acc = local & 1;
+      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
+        raise_timeout(sm, p.status);
+        break;
+      }
+      tc_fence_after();
+      const int row0 = mt * BM + quarter * 32;  // first row of this warp's box
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+      for (int c0 = 0; c0 < nsz; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c0 + 32, rb);
+        tmem_ld_wait();
+        if (c0 + 64 >= nsz) {
+          // the accumulator is drained: tell the leader (one arrival per warp)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm->acc_empty[acc]), 0));
+        }
+        if (!valid) continue;
+        if constexpr (EPI == EPI_STORE) {
+          uint4 w[8];
+          pack64(ra, rb, [](float x, int) { return x; }, w);
+          uint8_t *b = st.begin();
+          st.put(b, w);
+          st.finish(b, &tmC0, n0 + c0, row0);
+        } else {
+          const int n = n0 + c0;
+          if (n < 2 * p.e) {
+            uint4 w[8];
+            pack64(ra, rb, [](float x, int) { return swish_tanh(x); }, w);
+            uint8_t *b = st.begin();
+            st.put(b, w);
+            if (n < p.e) st.finish(b, &tmC0, n, row0);
+            else st.finish(b, &tmC1, n - p.e, row0);
+          } else {
+            const int c = n - 2 * p.e;  // column inside Z
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              ra[j] = __float_as_uint(swish_tanh(__uint_as_float(ra[j])));
+              rb[j] = __float_as_uint(swish_tanh(__uint_as_float(rb[j])));
+            }
+#pragma unroll 1
+            for (int h = 0; h < 4; ++h) {
+              const float *g = p.gamma + h * p.s + c;
+              const float *be = p.beta + h * p.s + c;
+              uint4 w[8];
+              pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); },
+                     w);
+              uint8_t *b = st.begin();
+              st.put(b, w);
+              st.finish(b, &tmC2, c, h * p.M_tokens + row0);
+            }
+          }
+        }
+      }
+    }
+    st.drain();
+  }
+
+  tc_fence_before();
+  // neither CTA exits while its peer may still signal its barriers
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &c0,
+                   const CUtensorMap &c1, const CUtensorMap &c2, const Params &p,
+                   const Problem &pr) {
+  // per device: shared-memory attribute set, and how many pairs fit at once
+  static int max_pairs[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kernel = tc_gemm_pair_kernel<EPI>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = pr.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (max_pairs[dev] == 0) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    int n = 0;
+    cfg.gridDim = dim3(2 * (pr.num_sms / 2));
+    err = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (err != cudaSuccess) return err;
+    max_pairs[dev] = n > 0 ? n : 1;
+  }
+  const int pairs = p.total < max_pairs[dev] ? p.total : max_pairs[dev];
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, c0, c1, c2, p);
+}
+
+Params base_params(const Problem &pr, int N, int K) {
+  Params p = {};
+  p.N = N;
+  p.K = K;
+  p.m_tiles = (int)(pr.M / BM);
+  p.n_tiles = (N + BN - 1) / BN;
+  p.total = (p.m_tiles + 1) / 2 * p.n_tiles;
+  p.status = pr.status;
+  p.M_tokens = (int)pr.M;
+  p.e = pr.e;
+  p.s = pr.s;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t tc_projection_bf16(const Problem &pr) {
+  const int N = 2 * pr.e + pr.s;
+  CUtensorMap tmA, tmB, tU, tV, tH;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tH, pr.heads, 4 * pr.M, pr.s, pr.s, 32, 64)) != cudaSuccess)
+    return err;
+  Params p = base_params(pr, N, pr.d);
+  p.gamma = pr.gamma;
+  p.beta = pr.beta;
+  return launch<EPI_PROJ>(tmA, tmB, tU, tV, tH, p, pr);
+}
+
+cudaError_t tc_output_bf16(const Problem &pr) {
+  CUtensorMap tmA, tmB, tO;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, pr.gated, pr.M, pr.e, pr.e, BM, 64)) != cudaSuccess)
+    return err;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
+    return err;
+  if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
+  Params p = base_params(pr, pr.d, pr.e);
+  return launch<EPI_STORE>(tmA, tmB, tO, tO, tO, p, pr);
+}
+
+}  // namespace flashgau

@@ -92,7 +92,7 @@ typedef struct flash_gau_workspace_layout {
 
 /* Supported shapes.  All types: B, T, C, d, e, s > 0 and T % C == 0.
  *   FP32: any such shape with s <= 128 and C <= 4096.
- *   BF16: d % 64 == 0, e % 256 == 0, s == 128, C % 128 == 0, C <= 4096.
+ *   BF16: d % 128 == 0, e % 256 == 0, s == 128, C % 128 == 0, C <= 4096.
  * Other shapes return FLASH_GAU_ENOTSUP.                                   */
 
 /* Fills *out for the given problem.  Returns FLASH_GAU_OK, FLASH_GAU_EINVAL

@@ -64,6 +64,7 @@ def test_layout_offsets_aligned_and_sized(L):
     ((0, 128, 64, 64, 128, 32, 1, bd.FP32), bd.EINVAL),     # B == 0
     ((1, 128, 64, 64, 128, 32, 1, 7), bd.EINVAL),           # unknown dtype
     ((1, 256, 128, 768, 1000, 128, 1, bd.BF16), bd.ENOTSUP),  # e % 256
+    ((1, 256, 128, 192, 1536, 128, 1, bd.BF16), bd.ENOTSUP),  # d % 128
     ((1, 256, 128, 768, 1536, 64, 1, bd.BF16), bd.ENOTSUP),   # s != 128
     ((1, 192, 64, 768, 1536, 128, 1, bd.BF16), bd.ENOTSUP),   # C % 128
     ((1, 256, 64, 64, 128, 256, 1, bd.FP32), bd.ENOTSUP),     # s > 128 (fp32)

@@ -79,8 +79,8 @@ EDGE = [
     ("fp32_one_chunk_quad", 2, 160, 32, 64, 16, 160, True, "fp32"),
     ("bf16_one_chunk_causal", 1, 256, 128, 256, 128, 256, True, "bf16"),
     ("bf16_one_chunk_noncausal", 1, 256, 128, 256, 128, 256, False, "bf16"),
-    ("bf16_single_tile", 3, 128, 64, 256, 128, 128, True, "bf16"),
-    ("bf16_many_chunks_noncausal", 2, 2048, 192, 512, 128, 128, False, "bf16"),
+    ("bf16_single_tile", 3, 128, 128, 256, 128, 128, True, "bf16"),
+    ("bf16_many_chunks_noncausal", 2, 2048, 384, 512, 128, 128, False, "bf16"),
     ("bf16_c1024_causal", 1, 2048, 256, 512, 128, 1024, True, "bf16"),
     ("bf16_max_chunk", 1, 4096, 128, 256, 128, 4096, True, "bf16"),
 ]
