@@ -2,23 +2,35 @@
 // fp32 accumulation ("Transformer Quality in Linear Time", Method: local
 // part, eq. 7/8 global part, display after eq. 8; flash_block pseudocode):
 //
-//   acc   = Q_lin Prefix_g                               (global term)
-//   acc  += sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]   (local term)
+//   acc   = Q_lin Prefix_g                                      (global term)
+//   acc  += sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]    (local term)
 //   gated = U * acc
 //
-// One CTA per (chunk, 128-query tile, 256-column value tile).  Key blocks of
-// 128 are visited in order (only those at or below the diagonal when
-// causal).  S = Q_quad K_quad^T of a key block lands in one of two TMEM
-// buffers; four warps turn it into P = relu^2(S/C + b) (masked) in
-// registers and write P as bf16 to shared memory in the 128-byte swizzled
-// K-major layout, where it is the A operand of the next MMA.  The C x C
-// score matrix never leaves the SM.  Because relu^2 has no row
-// normalisation, the products of successive key blocks simply add.
+// Work unit: (chunk, 128-query tile, 256-column value tile), value tile
+// fastest; one persistent CTA per SM walks its units round-robin.  Key
+// blocks of 128 are visited in order, only those at or below the diagonal
+// when causal.  Because relu^2 has no row normalisation, the products of
+// successive key blocks simply add into one accumulator.
 //
-// Shared memory (224 KB): Q_quad tile 32 KB; P slots 4 x 16 KB (Q_lin first
-// occupies slots 0-1); K_quad ring 2 x 32 KB; B-operand ring 2 x 32 KB (the
-// prefix state rows, then V rows, 64 rows x 256 columns per stage).
-// TMEM: accumulator columns 0-255, S buffers 256-383 and 384-511.
+// Roles (320 threads):
+//   warp 0     TMA producer: Q_quad, Q_lin, the K_quad ring, and a ring of
+//              64-row x 256-column B operands (prefix state rows, then V
+//              rows);
+//   warp 1     MMA issuer: S = Q_quad K_quad^T into a 128-column TMEM
+//              buffer (two buffers), acc = Q_lin Prefix (smem A), acc += P V
+//              with P read from TMEM;
+//   warps 2-5  relu^2: read S with tcgen05.ld, compute relu^2(S/C + b) with
+//              the causal mask in registers, write P as packed bf16 over the
+//              same TMEM buffer with tcgen05.st (the C x C scores never
+//              leave TMEM and registers);
+//   warps 6-9  epilogue: gated = U * acc, U boxes TMA-loaded into per-warp
+//              double buffers, the product written in place and TMA-stored.
+// While the epilogue warps drain one unit's accumulator, the producer, the
+// S products and the relu^2 warps already work on the next unit.
+//
+// Shared memory (224 KB): Q_quad 32 KB, Q_lin 32 KB, K ring 2 x 32 KB,
+// B ring 2 x 32 KB, epilogue boxes 4 warps x 2 x 4 KB.  TMEM: accumulator
+// columns 0-255, S/P buffers 256-383 and 384-511.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -30,47 +42,64 @@ namespace {
 
 using namespace ptx;
 
-constexpr int QT = 128;     // query rows per CTA
-constexpr int KB = 128;     // keys per block
-constexpr int ET = 256;     // value columns per CTA
-constexpr int SD = 128;     // head width s
-constexpr int NUM_THREADS = 192;
+constexpr int QT = 128;  // query rows per unit
+constexpr int KB = 128;  // keys per block
+constexpr int ET = 256;  // value columns per unit
+constexpr int SD = 128;  // head width s
+constexpr int NUM_THREADS = 320;
 
-constexpr int Q_BYTES = QT * SD * 2;          // 32 KB (two 64-wide atoms)
-constexpr int ATOM_BYTES = 128 * 64 * 2;      // 16 KB: 128 rows x 64 bf16
-constexpr int P_SLOT_BYTES = ATOM_BYTES;      // 128 rows x 64 keys
-constexpr int K_STAGE_BYTES = KB * SD * 2;    // 32 KB
-constexpr int B_BOX_BYTES = 64 * 64 * 2;      // 64 rows x 64 columns: 8 KB
-constexpr int B_STAGE_BYTES = 64 * ET * 2;    // 32 KB
+constexpr int ATOM_BYTES = 128 * 64 * 2;        // 128 rows x 64 bf16: 16 KB
+constexpr int Q_BYTES = 2 * ATOM_BYTES;         // 32 KB
+constexpr int K_STAGE_BYTES = 2 * ATOM_BYTES;   // 128 keys x 128: 32 KB
+constexpr int B_BOX_BYTES = 64 * 64 * 2;        // 64 rows x 64 columns: 8 KB
+constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;  // 64 rows x 256 columns: 32 KB
+constexpr int E_BOX_BYTES = 32 * 128;           // 32 rows x 64 bf16: 4 KB
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_P = OFF_Q + Q_BYTES;                 // 4 slots
-constexpr int OFF_K = OFF_P + 4 * P_SLOT_BYTES;        // 2 stages
-constexpr int OFF_B = OFF_K + 2 * K_STAGE_BYTES;       // 2 stages
-constexpr int TILE_BYTES = OFF_B + 2 * B_STAGE_BYTES;  // 224 KB
+constexpr int OFF_QQ = 0;
+constexpr int OFF_QL = OFF_QQ + Q_BYTES;
+constexpr int OFF_K = OFF_QL + Q_BYTES;
+constexpr int OFF_B = OFF_K + 2 * K_STAGE_BYTES;
+constexpr int OFF_E = OFF_B + 2 * B_STAGE_BYTES;
+constexpr int TILE_BYTES = OFF_E + 4 * 2 * E_BOX_BYTES;  // 224 KB
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 512;
 
-constexpr uint32_t TM_ACC = 0, TM_S0 = 256;
+constexpr uint32_t TM_ACC = 0, TM_S = 256;
 
 struct Bars {
-  uint64_t q_full, ql_full;
+  uint64_t q_full, q_empty, ql_full, ql_empty;
   uint64_t k_full[2], k_empty[2];
   uint64_t b_full[2], b_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], p_free[2];
-  uint64_t acc_full, drain, u_full;
+  uint64_t s_full[2], p_full[2], sb_free[2];
+  uint64_t acc_full, acc_empty;
+  uint64_t u_full[4][2];
+  uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
 };
 
 struct AttnParams {
-  int C, G, e, causal;
-  long long M;
-  int pre_rows_per_batch;  // causal: prefix row block per chunk; else per batch
+  int C, G, causal;
+  int n_et, n_qt, total;  // units (chunk, query tile, value tile), value tile fastest
   float inv_c;
   const float *relpos;
   int *status;
 };
+
+struct Unit {
+  int chunk, b, qt, et, nkb;
+  long long tok0;  // first token of the chunk
+};
+
+__device__ __forceinline__ Unit unit_of(const AttnParams &p, int u) {
+  Unit x;
+  x.et = u % p.n_et;
+  x.qt = (u / p.n_et) % p.n_qt;
+  x.chunk = u / (p.n_et * p.n_qt);
+  x.b = x.chunk / p.G;
+  x.tok0 = (long long)x.chunk * p.C;
+  x.nkb = p.causal ? x.qt + 1 : p.C / KB;
+  return x;
+}
 
 __device__ __forceinline__ void raise_timeout(Bars *b, int *status) {
   b->abort_flag = 1;
@@ -82,7 +111,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Ring position helper: stage index and the parity of its current phase.
+// Ring position: stage index and the parity of its current phase.
 struct Ring {
   int stage = 0;
   uint32_t phase = 0;
@@ -109,31 +138,26 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars *bar = reinterpret_cast<Bars *>(tiles + TILE_BYTES);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  const int et = blockIdx.x;                 // value column tile
-  const int qt = blockIdx.y;                 // query tile inside the chunk
-  const int chunk = blockIdx.z;              // b * G + g
-  const int b = chunk / p.G;
-  const long long tok0 = (long long)chunk * p.C;  // first token of the chunk
-  const int nkb = p.causal ? qt + 1 : p.C / KB;
-  const int pre_row0 = p.causal ? chunk * SD : b * SD;
+  const volatile int *abort = &bar->abort_flag;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar->q_full), 1);
+    mbar_init(smem_u32(&bar->q_empty), 1);
     mbar_init(smem_u32(&bar->ql_full), 1);
+    mbar_init(smem_u32(&bar->ql_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar->k_full[i]), 1);
       mbar_init(smem_u32(&bar->k_empty[i]), 1);
       mbar_init(smem_u32(&bar->b_full[i]), 1);
       mbar_init(smem_u32(&bar->b_empty[i]), 1);
       mbar_init(smem_u32(&bar->s_full[i]), 1);
-      mbar_init(smem_u32(&bar->s_free[i]), 128);
       mbar_init(smem_u32(&bar->p_full[i]), 128);
-      mbar_init(smem_u32(&bar->p_free[i]), 1);
+      mbar_init(smem_u32(&bar->sb_free[i]), 1);
+      for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bar->u_full[w][i]), 1);
     }
     mbar_init(smem_u32(&bar->acc_full), 1);
+    mbar_init(smem_u32(&bar->acc_empty), 128);
     mbar_init(smem_u32(&bar->drain), 1);
-    mbar_init(smem_u32(&bar->u_full), 1);
     bar->abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -153,62 +177,52 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (elect_one()) {
-      const int qrow = (int)(tok0 + qt * QT);
-      uint32_t fb = smem_u32(&bar->q_full);
-      mbar_arrive_expect_tx(fb, Q_BYTES);
-      tma_load_2d(smem_u32(tiles + OFF_Q), &tmQq, fb, 0, qrow);
-      tma_load_2d(smem_u32(tiles + OFF_Q + ATOM_BYTES), &tmQq, fb, 64, qrow);
       Ring kr(2), br(2);
       bool ok = true;
-      // K_quad block 0
-      auto load_k = [&](int kb) -> bool {
-        if (!mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, &bar->abort_flag)) return false;
+      auto load_k = [&](long long krow) -> bool {
+        if (!mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, abort)) return false;
         const uint32_t f = smem_u32(&bar->k_full[kr.stage]);
         uint8_t *dst = tiles + OFF_K + kr.stage * K_STAGE_BYTES;
         mbar_arrive_expect_tx(f, K_STAGE_BYTES);
-        const int krow = (int)(tok0 + kb * KB);
-        tma_load_2d(smem_u32(dst), &tmKq, f, 0, krow);
-        tma_load_2d(smem_u32(dst + ATOM_BYTES), &tmKq, f, 64, krow);
+        tma_load_2d(smem_u32(dst), &tmKq, f, 0, (int)krow);
+        tma_load_2d(smem_u32(dst + ATOM_BYTES), &tmKq, f, 64, (int)krow);
         kr.next();
         return true;
       };
-      auto load_b = [&](const CUtensorMap *tm, int row) -> bool {
-        if (!mbar_wait(smem_u32(&bar->b_empty[br.stage]), br.phase ^ 1, &bar->abort_flag)) return false;
+      auto load_b = [&](const CUtensorMap *tm, int col0, long long row) -> bool {
+        if (!mbar_wait(smem_u32(&bar->b_empty[br.stage]), br.phase ^ 1, abort)) return false;
         const uint32_t f = smem_u32(&bar->b_full[br.stage]);
         uint8_t *dst = tiles + OFF_B + br.stage * B_STAGE_BYTES;
         mbar_arrive_expect_tx(f, B_STAGE_BYTES);
 #pragma unroll
         for (int j = 0; j < ET / 64; ++j)
-          tma_load_2d(smem_u32(dst + j * B_BOX_BYTES), tm, f, et * ET + j * 64, row);
+          tma_load_2d(smem_u32(dst + j * B_BOX_BYTES), tm, f, col0 + j * 64, (int)row);
         br.next();
         return true;
       };
-      ok = load_k(0);
-      if (ok) {
-        fb = smem_u32(&bar->ql_full);
-        mbar_arrive_expect_tx(fb, Q_BYTES);
-        tma_load_2d(smem_u32(tiles + OFF_P), &tmQl, fb, 0, qrow);
-        tma_load_2d(smem_u32(tiles + OFF_P + P_SLOT_BYTES), &tmQl, fb, 64, qrow);
-        ok = load_b(&tmPre, pre_row0) && load_b(&tmPre, pre_row0 + 64);
-      }
-      for (int kb = 0; ok && kb < nkb && !bar->abort_flag; ++kb) {
-        if (kb + 1 < nkb) ok = load_k(kb + 1);
-        const int vrow = (int)(tok0 + kb * KB);
-        ok = ok && load_b(&tmV, vrow) && load_b(&tmV, vrow + 64);
-      }
-      // the U tile of the epilogue goes into the K_quad ring once the last
-      // S product has read it: 4 row quarters x 4 column boxes of 32 x 64
-      for (int i = 0; ok && i < 2; ++i) {
-        ok = mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, &bar->abort_flag);
-        kr.next();
-      }
-      if (ok) {
-        const uint32_t f = smem_u32(&bar->u_full);
-        mbar_arrive_expect_tx(f, QT * ET * 2);
-        for (int q = 0; q < 4; ++q)
-          for (int j = 0; j < ET / 64; ++j)
-            tma_load_2d(smem_u32(tiles + OFF_K + (q * 4 + j) * 4096), &tmU, f, et * ET + j * 64,
-                        qrow + q * 32);
+      int i = 0;
+      for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
+        const Unit x = unit_of(p, u);
+        const long long qrow = x.tok0 + x.qt * QT;
+        const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
+        ok = mbar_wait(smem_u32(&bar->q_empty), (i & 1) ^ 1, abort);
+        if (!ok) break;
+        uint32_t f = smem_u32(&bar->q_full);
+        mbar_arrive_expect_tx(f, Q_BYTES);
+        tma_load_2d(smem_u32(tiles + OFF_QQ), &tmQq, f, 0, (int)qrow);
+        tma_load_2d(smem_u32(tiles + OFF_QQ + ATOM_BYTES), &tmQq, f, 64, (int)qrow);
+        ok = load_k(x.tok0) && mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
+        if (!ok) break;
+        f = smem_u32(&bar->ql_full);
+        mbar_arrive_expect_tx(f, Q_BYTES);
+        tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
+        tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
+        ok = load_b(&tmPre, x.et * ET, pre_row0) && load_b(&tmPre, x.et * ET, pre_row0 + 64);
+        for (int kb = 0; ok && kb < x.nkb; ++kb) {
+          if (kb + 1 < x.nkb) ok = load_k(x.tok0 + (kb + 1) * KB);
+          ok = ok && load_b(&tmV, x.et * ET, x.tok0 + kb * KB) &&
+               load_b(&tmV, x.et * ET, x.tok0 + kb * KB + 64);
+        }
       }
       if (!ok) raise_timeout(bar, p.status);
     }
@@ -217,33 +231,36 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     if (elect_one()) {
       const uint32_t idesc_s = idesc_bf16_f32(128, KB, 0, 0);
       const uint32_t idesc_v = idesc_bf16_f32(128, ET, 0, 1);
-      const uint32_t sQ = smem_u32(tiles + OFF_Q);
-      const uint32_t sP = smem_u32(tiles + OFF_P);
+      const uint32_t sQ = smem_u32(tiles + OFF_QQ);
+      const uint32_t sQL = smem_u32(tiles + OFF_QL);
       const uint32_t sK = smem_u32(tiles + OFF_K);
       const uint32_t sB = smem_u32(tiles + OFF_B);
       Ring kr(2), br(2);
+      int n = 0;  // S blocks issued so far (all units): buffer n & 1
       bool ok = true;
-      // S[kb] = Q_quad K_quad[kb]^T into TMEM buffer kb % 2
-      auto issue_s = [&](int kb) -> bool {
-        const int sb = kb & 1;
-        if (kb >= 2 && !mbar_wait(smem_u32(&bar->s_free[sb]), ((kb >> 1) - 1) & 1, &bar->abort_flag)) return false;
-        if (!mbar_wait(smem_u32(&bar->k_full[kr.stage]), kr.phase, &bar->abort_flag)) return false;
+      // S[n] = Q_quad K_quad^T into TMEM buffer n & 1
+      auto issue_s = [&]() -> bool {
+        const int sb = n & 1;
+        if (n >= 2 && !mbar_wait(smem_u32(&bar->sb_free[sb]), ((n >> 1) - 1) & 1, abort))
+          return false;
+        if (!mbar_wait(smem_u32(&bar->k_full[kr.stage]), kr.phase, abort)) return false;
         tc_fence_after();
         const uint32_t kst = sK + kr.stage * K_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < SD / 16; ++k) {
           const uint32_t off = (k >> 2) * ATOM_BYTES + (k & 3) * 32;
-          mma_f16_ss(tmem + TM_S0 + sb * KB, sw128_desc(sQ + off, 16, 1024),
+          mma_f16_ss(tmem + TM_S + sb * KB, sw128_desc(sQ + off, 16, 1024),
                      sw128_desc(kst + off, 16, 1024), idesc_s, k != 0);
         }
         mma_commit(smem_u32(&bar->k_empty[kr.stage]));
         mma_commit(smem_u32(&bar->s_full[sb]));
         kr.next();
+        ++n;
         return true;
       };
-      // acc (+)= A[two or four 16-row K steps per stage] * B stage
-      auto issue_b = [&](uint32_t a_atom, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, &bar->abort_flag)) return false;
+      // acc (+)= A * B stage, A a 64-wide K-major atom in shared memory
+      auto issue_b_smem = [&](uint32_t a_atom, bool first) -> bool {
+        if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
         tc_fence_after();
         const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
 #pragma unroll
@@ -254,122 +271,174 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         br.next();
         return true;
       };
-      ok = mbar_wait(smem_u32(&bar->q_full), 0, &bar->abort_flag);
-      ok = ok && issue_s(0);
-      // global term first: acc = Q_lin Prefix (Q_lin sits in P slots 0-1)
-      ok = ok && mbar_wait(smem_u32(&bar->ql_full), 0, &bar->abort_flag);
-      ok = ok && issue_b(sP, true) && issue_b(sP + P_SLOT_BYTES, false);
-      if (ok) mma_commit(smem_u32(&bar->p_free[0]));
-      for (int kb = 0; ok && kb < nkb && !bar->abort_flag; ++kb) {
-        if (kb + 1 < nkb) ok = issue_s(kb + 1);
-        const int pp = kb & 1;
-        ok = ok && mbar_wait(smem_u32(&bar->p_full[pp]), (kb >> 1) & 1, &bar->abort_flag);
+      // acc += P * B stage, P: 64 keys = 32 packed columns of TMEM at a_col
+      auto issue_b_tmem = [&](uint32_t a_col) -> bool {
+        if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
+        tc_fence_after();
+        const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16_ts(tmem + TM_ACC, tmem + a_col + k * 8,
+                     sw128_desc(bst + k * 2048, B_BOX_BYTES, 1024), idesc_v, 1);
+        mma_commit(smem_u32(&bar->b_empty[br.stage]));
+        br.next();
+        return true;
+      };
+      int i = 0;
+      for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
+        const Unit x = unit_of(p, u);
+        const int n0 = n;
+        ok = mbar_wait(smem_u32(&bar->q_full), i & 1, abort) && issue_s();
+        if (ok && x.nkb == 1) mma_commit(smem_u32(&bar->q_empty));
+        // the accumulator must have been drained by the previous unit's epilogue
+        ok = ok && mbar_wait(smem_u32(&bar->acc_empty), (i & 1) ^ 1, abort) &&
+             mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t pslot = sP + pp * 2 * P_SLOT_BYTES;
-        ok = issue_b(pslot, false) && issue_b(pslot + P_SLOT_BYTES, false);
-        if (ok) mma_commit(smem_u32(&bar->p_free[pp]));
+        ok = issue_b_smem(sQL, true) && issue_b_smem(sQL + ATOM_BYTES, false);
+        if (ok) mma_commit(smem_u32(&bar->ql_empty));
+        for (int kb = 0; ok && kb < x.nkb; ++kb) {
+          if (kb + 1 < x.nkb) {
+            ok = issue_s();
+            if (ok && kb + 2 == x.nkb) mma_commit(smem_u32(&bar->q_empty));
+          }
+          const int si = n0 + kb, sb = si & 1;
+          ok = ok && mbar_wait(smem_u32(&bar->p_full[sb]), (si >> 1) & 1, abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pcol = TM_S + sb * KB;
+          ok = issue_b_tmem(pcol) && issue_b_tmem(pcol + 32);
+          if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
+        }
+        if (ok) mma_commit(smem_u32(&bar->acc_full));
       }
-      if (ok) mma_commit(smem_u32(&bar->acc_full));
-      else raise_timeout(bar, p.status);
+      if (!ok) raise_timeout(bar, p.status);
       mma_commit(smem_u32(&bar->drain));
       if (!mbar_wait(smem_u32(&bar->drain), 0)) raise_timeout(bar, p.status);
     }
-  } else {
-    // ------------------------------------- relu^2 warps, then the epilogue
+  } else if (warp < 6) {
+    // -------------------------------------------------- relu^2 warps
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;   // row inside the query tile
-    const int i = qt * QT + r;           // row inside the chunk
+    const int r = quarter * 32 + lane;  // row inside the query tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint8_t *sP = tiles + OFF_P;
+    int n = 0;
     bool ok = true;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int sb = kb & 1;
-      if (!mbar_wait(smem_u32(&bar->s_full[sb]), (kb >> 1) & 1, &bar->abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      // P slot pair kb&1 must be free (slot pair 0 first held Q_lin)
-      const uint32_t pf_parity = (sb == 0) ? ((kb >> 1) & 1) : (((kb >> 1) & 1) ^ 1);
-      if (!mbar_wait(smem_u32(&bar->p_free[sb]), pf_parity, &bar->abort_flag)) { ok = false; break; }
-      const bool diag = p.causal && kb == qt;
-      const float *bias_row = p.relpos + (kb * KB - i + p.C - 1);  // + key index j
+    for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x) {
+      const Unit x = unit_of(p, u);
+      const int i = x.qt * QT + r;  // row inside the chunk
+      for (int kb = 0; kb < x.nkb; ++kb, ++n) {
+        const int sb = n & 1;
+        if (!mbar_wait(smem_u32(&bar->s_full[sb]), (n >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool diag = p.causal && kb == x.qt;
+        const float *bias_row = p.relpos + (kb * KB - i + p.C - 1);  // + key index j
+        const uint32_t sbuf = tmem + lane_off + TM_S + sb * KB;
 #pragma unroll 1
-      for (int c0 = 0; c0 < KB; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + TM_S0 + sb * KB + c0, v);
-        tmem_ld_wait();
-        uint32_t packed[16];
+        for (int c0 = 0; c0 < KB; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(sbuf + c0, v);
+          tmem_ld_wait();
+          uint32_t packed[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float x0 = fmaf(__uint_as_float(v[j]), p.inv_c, __ldg(bias_row + c0 + j));
-          float x1 = fmaf(__uint_as_float(v[j + 1]), p.inv_c, __ldg(bias_row + c0 + j + 1));
-          x0 = fmaxf(x0, 0.f);
-          x1 = fmaxf(x1, 0.f);
-          x0 *= x0;
-          x1 *= x1;
-          if (diag) {
-            if (c0 + j > r) x0 = 0.f;
-            if (c0 + j + 1 > r) x1 = 0.f;
+          for (int j = 0; j < 32; j += 2) {
+            float x0 = fmaf(__uint_as_float(v[j]), p.inv_c, __ldg(bias_row + c0 + j));
+            float x1 = fmaf(__uint_as_float(v[j + 1]), p.inv_c, __ldg(bias_row + c0 + j + 1));
+            x0 = fmaxf(x0, 0.f);
+            x1 = fmaxf(x1, 0.f);
+            x0 *= x0;
+            x1 *= x1;
+            if (diag) {
+              if (c0 + j > r) x0 = 0.f;
+              if (c0 + j + 1 > r) x1 = 0.f;
+            }
+            packed[j / 2] = pack_bf16(x0, x1);
           }
-          packed[j / 2] = pack_bf16(x0, x1);
+          // keys c0..c0+31 -> packed columns c0/2 .. c0/2+15 (S columns
+          // below c0 + 32 have all been read already)
+          tmem_st16(sbuf + c0 / 2, packed);
         }
-        // keys c0..c0+31 -> slot (c0 / 64), 16-byte chunks (c0 % 64)/8 .. +3
-        uint8_t *slot = sP + (sb * 2 + (c0 >> 6)) * P_SLOT_BYTES + r * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk16 = ((c0 & 63) >> 3) + q;
-          uint4 w = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
-                               packed[4 * q + 3]);
-          *reinterpret_cast<uint4 *>(slot + ((chunk16 ^ (r & 7)) << 4)) = w;
-        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar->p_full[sb]));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar->s_free[sb]));
-      mbar_arrive(smem_u32(&bar->p_full[sb]));
     }
-    if (ok && mbar_wait(smem_u32(&bar->acc_full), 0, &bar->abort_flag) &&
-        mbar_wait(smem_u32(&bar->u_full), 0, &bar->abort_flag)) {
+    if (!ok) raise_timeout(bar, p.status);
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int quarter = warp & 3, w = warp - 6;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint8_t *ebuf = tiles + OFF_E + w * 2 * E_BOX_BYTES;
+    // chunk c of this CTA = 64 value columns of unit (c / 4), part c % 4
+    auto load_u = [&](int c) {
+      const int u = blockIdx.x + (c >> 2) * gridDim.x;
+      if (lane != 0 || u >= p.total) return;
+      const Unit x = unit_of(p, u);
+      const int b = c & 1;
+      const uint32_t f = smem_u32(&bar->u_full[w][b]);
+      mbar_arrive_expect_tx(f, E_BOX_BYTES);
+      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + (c & 3) * 64,
+                  (int)(x.tok0 + x.qt * QT + quarter * 32));
+    };
+    load_u(0);
+    load_u(1);
+    int c = 0, i = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
+      const Unit x = unit_of(p, u);
+      if (!mbar_wait(smem_u32(&bar->acc_full), i & 1, abort)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      // U boxes sit in the K ring, the gated boxes are staged in the B ring
-      // (free once every MMA has completed); both 32 rows x 128 bytes,
-      // swizzled, one per (row quarter, 64-column block).
-      for (int j = 0; j < ET / 64; ++j) {
+      const int grow = (int)(x.tok0 + x.qt * QT + quarter * 32);
+      for (int j = 0; j < ET / 64; ++j, ++c) {
+        const int b = c & 1;
+        if (!mbar_wait(smem_u32(&bar->u_full[w][b]), (c >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
         uint32_t va[32], vb[32];
         tmem_ld32(tmem + lane_off + TM_ACC + j * 64, va);
         tmem_ld32(tmem + lane_off + TM_ACC + j * 64 + 32, vb);
         tmem_ld_wait();
-        const uint8_t *ubox = tiles + OFF_K + (quarter * 4 + j) * 4096;
-        uint8_t *gbox = tiles + OFF_B + (quarter * 4 + j) * 4096;
+        if (j == ET / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar->acc_empty));
+        }
+        uint8_t *box = ebuf + b * E_BOX_BYTES;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 u4 = *reinterpret_cast<const uint4 *>(ubox + sw128_offset(lane, c));
+        for (int q = 0; q < 8; ++q) {
+          uint4 *slot = reinterpret_cast<uint4 *>(box + sw128_offset(lane, q));
+          const uint4 u4 = *slot;
           const __nv_bfloat162 *uh = reinterpret_cast<const __nv_bfloat162 *>(&u4);
-          const uint32_t *src = c < 4 ? &va[8 * c] : &vb[8 * (c - 4)];
-          uint4 w;
-          uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
+          const uint32_t *src = q < 4 ? &va[8 * q] : &vb[8 * (q - 4)];
+          uint4 g4;
+          uint32_t *gp = reinterpret_cast<uint32_t *>(&g4);
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const float2 uf = __bfloat1622float2(uh[h]);
-            wp[h] = pack_bf16(uf.x * __uint_as_float(src[2 * h]),
+            gp[h] = pack_bf16(uf.x * __uint_as_float(src[2 * h]),
                               uf.y * __uint_as_float(src[2 * h + 1]));
           }
-          *reinterpret_cast<uint4 *>(gbox + sw128_offset(lane, c)) = w;
+          *slot = g4;
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmG, smem_u32(box), x.et * ET + j * 64, grow);
+          tma_store_commit();
+          tma_store_wait_read<0>();  // the box is refilled next
+        }
+        __syncwarp();
+        load_u(c + 2);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int grow = (int)(tok0 + qt * QT + quarter * 32);
-        for (int j = 0; j < ET / 64; ++j)
-          tma_store_2d(&tmG, smem_u32(tiles + OFF_B + (quarter * 4 + j) * 4096), et * ET + j * 64,
-                       grow);
-        tma_store_commit();
-        tma_store_wait<0>();
-      }
-      __syncwarp();
-    } else {
-      raise_timeout(bar, p.status);
     }
+    if (lane == 0) tma_store_wait<0>();
+    __syncwarp();
+    if (!ok) raise_timeout(bar, p.status);
   }
 
   tc_fence_before();
@@ -385,7 +454,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
 cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   const __nv_bfloat16 *heads = (const __nv_bfloat16 *)pr.heads;
   const long long Ms = pr.M * pr.s;
-  CUtensorMap tQq, tKq, tQl, tV, tPre;
+  CUtensorMap tQq, tKq, tQl, tV, tPre, tU, tG;
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tQq, heads, pr.M, pr.s, pr.s, QT, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tKq, heads + Ms, pr.M, pr.s, pr.s, KB, 64)) != cudaSuccess)
@@ -393,7 +462,6 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   if ((err = make_tmap_bf16_2d(&tQl, heads + 2 * Ms, pr.M, pr.s, pr.s, QT, 64)) != cudaSuccess)
     return err;
   if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 64, 64)) != cudaSuccess) return err;
-  CUtensorMap tU, tG;
   if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tG, pr.gated, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   const long long pre_rows = (long long)(pr.causal ? pr.B * pr.G : pr.B) * pr.s;
@@ -412,16 +480,16 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   AttnParams p;
   p.C = pr.C;
   p.G = pr.G;
-  p.e = pr.e;
   p.causal = pr.causal;
-  p.M = pr.M;
-  p.pre_rows_per_batch = pr.s;
+  p.n_et = pr.e / ET;
+  p.n_qt = pr.C / QT;
+  p.total = pr.B * pr.G * p.n_qt * p.n_et;
   p.inv_c = 1.0f / (float)pr.C;
   p.relpos = pr.relpos;
   p.status = pr.status;
-  dim3 grid(pr.e / ET, pr.C / QT, pr.B * pr.G);
-  return launch_pdl(chunk_attention_kernel, grid, dim3(NUM_THREADS), SMEM_BYTES, pr.stream, tQq,
-                    tKq, tQl, tV, tPre, tU, tG, p);
+  const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;
+  return launch_pdl(chunk_attention_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
+                    tQq, tKq, tQl, tV, tPre, tU, tG, p);
 }
 
 }  // namespace flashgau
