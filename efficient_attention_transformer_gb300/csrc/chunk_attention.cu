@@ -6,7 +6,7 @@
 //   acc  += sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]    (local term)
 //   gated = U * acc
 //
-// Work unit: (chunk, 128-query tile, 256-column value tile), value tile
+// Work unit: (chunk, 128-query tile, 128-column value tile), value tile
 // fastest; one persistent CTA per SM walks its units round-robin.  Key
 // blocks of 128 are visited in order, only those at or below the diagonal
 // when causal.  Because relu^2 has no row normalisation, the products of
@@ -14,7 +14,7 @@
 //
 // Roles (320 threads):
 //   warp 0     TMA producer: Q_quad, Q_lin, the K_quad ring, and a ring of
-//              64-row x 256-column B operands (prefix state rows, then V
+//              64-row x 128-column B operands (prefix state rows, then V
 //              rows);
 //   warp 1     MMA issuer: S = Q_quad K_quad^T into a 128-column TMEM
 //              buffer (two buffers), acc = Q_lin Prefix (smem A), acc += P V
@@ -25,12 +25,12 @@
 //              leave TMEM and registers);
 //   warps 6-9  epilogue: gated = U * acc, U boxes TMA-loaded into per-warp
 //              double buffers, the product written in place and TMA-stored.
-// While the epilogue warps drain one unit's accumulator, the producer, the
-// S products and the relu^2 warps already work on the next unit.
+// Two accumulators alternate between units, so while the epilogue warps
+// drain one, the MMAs of the next unit already fill the other.
 //
 // Shared memory (224 KB): Q_quad 32 KB, Q_lin 32 KB, K ring 2 x 32 KB,
-// B ring 2 x 32 KB, epilogue boxes 4 warps x 2 x 4 KB.  TMEM: accumulator
-// columns 0-255, S/P buffers 256-383 and 384-511.
+// B ring 4 x 16 KB, epilogue boxes 4 warps x 2 x 4 KB.  TMEM: accumulators
+// at columns 0 and 128, S/P buffers at 256 and 384 (128 columns each).
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -44,7 +44,7 @@ using namespace ptx;
 
 constexpr int QT = 128;  // query rows per unit
 constexpr int KB = 128;  // keys per block
-constexpr int ET = 256;  // value columns per unit
+constexpr int ET = 128;  // value columns per unit
 constexpr int SD = 128;  // head width s
 constexpr int NUM_THREADS = 320;
 
@@ -52,14 +52,15 @@ constexpr int ATOM_BYTES = 128 * 64 * 2;        // 128 rows x 64 bf16: 16 KB
 constexpr int Q_BYTES = 2 * ATOM_BYTES;         // 32 KB
 constexpr int K_STAGE_BYTES = 2 * ATOM_BYTES;   // 128 keys x 128: 32 KB
 constexpr int B_BOX_BYTES = 64 * 64 * 2;        // 64 rows x 64 columns: 8 KB
-constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;  // 64 rows x 256 columns: 32 KB
+constexpr int B_STAGES = 4;
+constexpr int B_STAGE_BYTES = 2 * B_BOX_BYTES;  // 64 rows x 128 columns: 16 KB
 constexpr int E_BOX_BYTES = 32 * 128;           // 32 rows x 64 bf16: 4 KB
 
 constexpr int OFF_QQ = 0;
 constexpr int OFF_QL = OFF_QQ + Q_BYTES;
 constexpr int OFF_K = OFF_QL + Q_BYTES;
 constexpr int OFF_B = OFF_K + 2 * K_STAGE_BYTES;
-constexpr int OFF_E = OFF_B + 2 * B_STAGE_BYTES;
+constexpr int OFF_E = OFF_B + B_STAGES * B_STAGE_BYTES;
 constexpr int TILE_BYTES = OFF_E + 4 * 2 * E_BOX_BYTES;  // 224 KB
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 512;
 
@@ -68,9 +69,9 @@ constexpr uint32_t TM_ACC = 0, TM_S = 256;
 struct Bars {
   uint64_t q_full, q_empty, ql_full, ql_empty;
   uint64_t k_full[2], k_empty[2];
-  uint64_t b_full[2], b_empty[2];
+  uint64_t b_full[B_STAGES], b_empty[B_STAGES];
   uint64_t s_full[2], p_full[2], sb_free[2];
-  uint64_t acc_full, acc_empty;
+  uint64_t acc_full[2], acc_empty[2];
   uint64_t u_full[4][2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -148,15 +149,17 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar->k_full[i]), 1);
       mbar_init(smem_u32(&bar->k_empty[i]), 1);
-      mbar_init(smem_u32(&bar->b_full[i]), 1);
-      mbar_init(smem_u32(&bar->b_empty[i]), 1);
+      mbar_init(smem_u32(&bar->acc_full[i]), 1);
+      mbar_init(smem_u32(&bar->acc_empty[i]), 128);
       mbar_init(smem_u32(&bar->s_full[i]), 1);
       mbar_init(smem_u32(&bar->p_full[i]), 128);
       mbar_init(smem_u32(&bar->sb_free[i]), 1);
       for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bar->u_full[w][i]), 1);
     }
-    mbar_init(smem_u32(&bar->acc_full), 1);
-    mbar_init(smem_u32(&bar->acc_empty), 128);
+    for (int i = 0; i < B_STAGES; ++i) {
+      mbar_init(smem_u32(&bar->b_full[i]), 1);
+      mbar_init(smem_u32(&bar->b_empty[i]), 1);
+    }
     mbar_init(smem_u32(&bar->drain), 1);
     bar->abort_flag = 0;
     fence_mbar_init();
@@ -177,7 +180,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (elect_one()) {
-      Ring kr(2), br(2);
+      Ring kr(2), br(B_STAGES);
       bool ok = true;
       auto load_k = [&](long long krow) -> bool {
         if (!mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, abort)) return false;
@@ -235,8 +238,9 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       const uint32_t sQL = smem_u32(tiles + OFF_QL);
       const uint32_t sK = smem_u32(tiles + OFF_K);
       const uint32_t sB = smem_u32(tiles + OFF_B);
-      Ring kr(2), br(2);
+      Ring kr(2), br(B_STAGES);
       int n = 0;  // S blocks issued so far (all units): buffer n & 1
+      uint32_t acc_col = TM_ACC;  // accumulator of the current unit
       bool ok = true;
       // S[n] = Q_quad K_quad^T into TMEM buffer n & 1
       auto issue_s = [&]() -> bool {
@@ -265,7 +269,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ss(tmem + TM_ACC, sw128_desc(a_atom + k * 32, 16, 1024),
+          mma_f16_ss(tmem + acc_col, sw128_desc(a_atom + k * 32, 16, 1024),
                      sw128_desc(bst + k * 2048, B_BOX_BYTES, 1024), idesc_v, !(first && k == 0));
         mma_commit(smem_u32(&bar->b_empty[br.stage]));
         br.next();
@@ -278,7 +282,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ts(tmem + TM_ACC, tmem + a_col + k * 8,
+          mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8,
                      sw128_desc(bst + k * 2048, B_BOX_BYTES, 1024), idesc_v, 1);
         mma_commit(smem_u32(&bar->b_empty[br.stage]));
         br.next();
@@ -290,8 +294,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const int n0 = n;
         ok = mbar_wait(smem_u32(&bar->q_full), i & 1, abort) && issue_s();
         if (ok && x.nkb == 1) mma_commit(smem_u32(&bar->q_empty));
-        // the accumulator must have been drained by the previous unit's epilogue
-        ok = ok && mbar_wait(smem_u32(&bar->acc_empty), (i & 1) ^ 1, abort) &&
+        // this unit's accumulator must have been drained by the epilogue of
+        // the unit two before
+        acc_col = TM_ACC + (i & 1) * ET;
+        ok = ok && mbar_wait(smem_u32(&bar->acc_empty[i & 1]), ((i >> 1) & 1) ^ 1, abort) &&
              mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
         if (!ok) break;
         tc_fence_after();
@@ -310,7 +316,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           ok = issue_b_tmem(pcol) && issue_b_tmem(pcol + 32);
           if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
         }
-        if (ok) mma_commit(smem_u32(&bar->acc_full));
+        if (ok) mma_commit(smem_u32(&bar->acc_full[i & 1]));
       }
       if (!ok) raise_timeout(bar, p.status);
       mma_commit(smem_u32(&bar->drain));
@@ -371,15 +377,15 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     const int quarter = warp & 3, w = warp - 6;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t *ebuf = tiles + OFF_E + w * 2 * E_BOX_BYTES;
-    // chunk c of this CTA = 64 value columns of unit (c / 4), part c % 4
+    // chunk c of this CTA = 64 value columns of unit (c / 2), part c % 2
     auto load_u = [&](int c) {
-      const int u = blockIdx.x + (c >> 2) * gridDim.x;
+      const int u = blockIdx.x + (c >> 1) * gridDim.x;
       if (lane != 0 || u >= p.total) return;
       const Unit x = unit_of(p, u);
       const int b = c & 1;
       const uint32_t f = smem_u32(&bar->u_full[w][b]);
       mbar_arrive_expect_tx(f, E_BOX_BYTES);
-      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + (c & 3) * 64,
+      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + (c & 1) * 64,
                   (int)(x.tok0 + x.qt * QT + quarter * 32));
     };
     load_u(0);
@@ -388,7 +394,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
       const Unit x = unit_of(p, u);
-      if (!mbar_wait(smem_u32(&bar->acc_full), i & 1, abort)) {
+      if (!mbar_wait(smem_u32(&bar->acc_full[i & 1]), (i >> 1) & 1, abort)) {
         ok = false;
         break;
       }
@@ -401,12 +407,13 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           break;
         }
         uint32_t va[32], vb[32];
-        tmem_ld32(tmem + lane_off + TM_ACC + j * 64, va);
-        tmem_ld32(tmem + lane_off + TM_ACC + j * 64 + 32, vb);
+        const uint32_t acc = tmem + lane_off + TM_ACC + (i & 1) * ET + j * 64;
+        tmem_ld32(acc, va);
+        tmem_ld32(acc + 32, vb);
         tmem_ld_wait();
         if (j == ET / 64 - 1) {
           tc_fence_before();
-          mbar_arrive(smem_u32(&bar->acc_empty));
+          mbar_arrive(smem_u32(&bar->acc_empty[i & 1]));
         }
         uint8_t *box = ebuf + b * E_BOX_BYTES;
 #pragma unroll
