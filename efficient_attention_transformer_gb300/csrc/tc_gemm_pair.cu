@@ -14,7 +14,8 @@
 // TMA loads complete on the leader's stage barrier; the leader's commits
 // release the stage, and announce a finished accumulator, in both CTAs.
 // Each CTA's TMEM holds its own 128 rows (two 256-column accumulators); its
-// warps 2-5 drain them through tcgen05.ld into swizzled staging and TMA
+// eight epilogue warps (two per TMEM lane quarter, each half of the
+// columns) drain them through tcgen05.ld into swizzled staging and TMA
 // stores, and report the accumulator free to the leader.
 #include <cuda_bf16.h>
 
@@ -36,10 +37,11 @@ constexpr int B_BOX_BYTES = 64 * BK * 2;         // 8 KB: 64 columns x 64 k-rows
 constexpr int STAGE_BYTES = A_BYTES + BN / 2 * BK * 2;  // 32 KB
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
-constexpr int NUM_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
-constexpr int STG_BYTES = 32 * 128;                    // one 32-row x 128-byte store box
-constexpr int STG_OFF = STAGES * STAGE_BYTES;          // 2 staging boxes per epilogue warp
-constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);  // producer, MMA issuer, epilogue
+constexpr int STG_BYTES = 32 * 128;                // one 32-row x 128-byte store box
+constexpr int STG_OFF = STAGES * STAGE_BYTES;      // one staging box per epilogue warp
+constexpr int TILE_BYTES = STG_OFF + EPI_WARPS * STG_BYTES;
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint16_t kPair = 0x3, kLeader = 0x1;
 
@@ -77,17 +79,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // Per-warp staged TMA store: the warp writes one 32-row x 128-byte box into
-// one of its two staging buffers (row = lane, swizzled), then lane 0 stores
-// it.  A buffer is rewritten only after the store issued from it two boxes
-// earlier has finished reading shared memory.
+// its staging buffer (row = lane, swizzled), then lane 0 stores it.  The
+// buffer is rewritten only after the previous store has finished reading
+// shared memory.
 struct Stager {
-  uint8_t *buf;  // this warp's 2 x 4 KB
+  uint8_t *buf;  // this warp's 4 KB
   int lane;
   int count = 0;
   __device__ uint8_t *begin() {
-    if (lane == 0) tma_store_wait_read<1>();
+    if (lane == 0) tma_store_wait_read<0>();
     __syncwarp();
-    return buf + (count & 1) * STG_BYTES;
+    return buf;
   }
   // row data: 8 x 16 bytes
   __device__ void put(uint8_t *b, const uint4 (&w)[8]) {
@@ -145,7 +147,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm->acc_full[i]), 1);
-      mbar_init(smem_u32(&sm->acc_empty[i]), 8);  // 4 epilogue warps x 2 CTAs
+      mbar_init(smem_u32(&sm->acc_empty[i]), 2 * EPI_WARPS);  // all epilogue warps, 2 CTAs
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort_flag = 0;
@@ -251,8 +253,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
   } else {
     // -------------------------------------------------- epilogue (both)
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    Stager st{tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES, lane};
+    const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31
+    const int half = (warp - 2) >> 2;   // which half of the tile's columns
+    Stager st{tiles + STG_OFF + (warp - 2) * STG_BYTES, lane};
     int local = 0;
     for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
       const int mt = (t / p.n_tiles) * 2 + rank, nt = t % p.n_tiles;
@@ -266,12 +269,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       tc_fence_after();
       const int row0 = mt * BM + quarter * 32;  // first row of this warp's box
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
-      for (int c0 = 0; c0 < nsz; c0 += 64) {
+      const int cend = (half + 1) * (nsz / 2);
+      for (int c0 = half * (nsz / 2); c0 < cend; c0 += 64) {
         uint32_t ra[32], rb[32];
         tmem_ld32(taddr + c0, ra);
         tmem_ld32(taddr + c0 + 32, rb);
         tmem_ld_wait();
-        if (c0 + 64 >= nsz) {
+        if (c0 + 64 >= cend) {
           // the accumulator is drained: tell the leader (one arrival per warp)
           tc_fence_before();
           __syncwarp();
