@@ -87,7 +87,7 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   L->heads = off;
   off = align_up(off + 4 * M * s * io);
   L->state = off;
-  off = align_up(off + (size_t)B * G * s * e * sizeof(float));
+  off = align_up(off + (size_t)B * G * s * e * io);
   L->prefix = off;
   off = align_up(off + (causal ? (size_t)B * G : (size_t)B) * s * e * io);
   L->gated = off;
@@ -207,7 +207,7 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, in
   p.U = ws + L.U;
   p.V = ws + L.V;
   p.heads = ws + L.heads;
-  p.state = (float *)(ws + L.state);
+  p.state = ws + L.state;
   p.prefix = ws + L.prefix;
   p.gated = ws + L.gated;
   p.stream = (cudaStream_t)stream;

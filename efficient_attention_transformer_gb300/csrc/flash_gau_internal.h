@@ -26,7 +26,7 @@ struct Problem {
   void *U;
   void *V;
   void *heads;  // [4][M][s]
-  float *state;
+  void *state;  // [B, G, s, e] io type
   void *prefix;
   void *gated;
   cudaStream_t stream;

@@ -107,11 +107,12 @@ struct ProjEpi {
   }
 };
 
+template <typename T>
 struct StateEpi {  // batch = b*G + g; State_g[si, ej]
-  float *state;
+  T *state;
   int s, e;
   __device__ void operator()(int batch, int m, int n, float acc) const {
-    state[((long long)batch * s + m) * e + n] = acc;
+    state[((long long)batch * s + m) * e + n] = from_f<T>(acc);
   }
 };
 
@@ -127,25 +128,71 @@ struct StoreEpi {
 // ---------------------------------------------------------- prefix scan ----
 // One thread per (b, s*e element): the G-step running sum of chunk states.
 template <typename T>
-__global__ void simt_prefix_scan(const float *__restrict__ state, T *__restrict__ prefix,
+__global__ void simt_prefix_scan(const T *__restrict__ state, T *__restrict__ prefix,
                                  int B, int G, long long se, int causal, float lin_scale) {
   griddep_wait();
   griddep_launch_dependents();
   long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= B * se) return;
   long long b = idx / se, r = idx % se;
-  const float *st = state + b * G * se + r;
+  const T *st = state + b * G * se + r;
   float run = 0.f;
   if (causal) {
     T *pre = prefix + b * G * se + r;
     for (int g = 0; g < G; ++g) {
       pre[g * se] = from_f<T>(lin_scale * run);
-      run += st[g * se];
+      run += to_f(st[g * se]);
     }
   } else {
-    for (int g = 0; g < G; ++g) run += st[g * se];
+    for (int g = 0; g < G; ++g) run += to_f(st[g * se]);
     prefix[b * se + r] = from_f<T>(lin_scale * run);
   }
+}
+
+// bf16 states: one thread per 8 consecutive state elements (16-byte loads
+// and stores), fp32 running sums, chunk states fetched 8 chunks ahead.
+__device__ __forceinline__ void add8(float (&run)[8], const uint4 &v) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    run[2 * k] += f.x;
+    run[2 * k + 1] += f.y;
+  }
+}
+__device__ __forceinline__ uint4 scaled8(const float (&run)[8], float scale) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(scale * run[2 * k], scale * run[2 * k + 1]);
+  return w;
+}
+
+__global__ void prefix_scan_bf16x8(const uint4 *__restrict__ state, uint4 *__restrict__ prefix,
+                                   int B, int G, long long se8, int causal, float lin_scale) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= B * se8) return;
+  const long long b = idx / se8, r = idx % se8;
+  const uint4 *st = state + b * G * se8 + r;
+  uint4 *pre = prefix + (causal ? b * G * se8 : b * se8) + r;
+  float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int g0 = 0; g0 < G; g0 += 8) {
+    const int n = min(8, G - g0);
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < n) v[k] = __ldg(st + (long long)(g0 + k) * se8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < n) {
+        if (causal) pre[(long long)(g0 + k) * se8] = scaled8(run, lin_scale);
+        add8(run, v[k]);
+      }
+    }
+  }
+  if (!causal) *pre = scaled8(run, lin_scale);
 }
 
 // ------------------------------------------------------ chunk attention ----
@@ -272,7 +319,7 @@ cudaError_t chunk_state(const Problem &p) {
   // batch = b*G+g; A(m = si, k = t) = K_lin[t, si]; B(k = t, n) = V[t, n]
   const T *Kl = (const T *)p.heads + 3 * p.M * p.s;
   dim3 grid(cdiv(p.e, kTile), cdiv(p.s, kTile), p.B * p.G);
-  StateEpi epi{p.state, p.s, p.e};
+  StateEpi<T> epi{(T *)p.state, p.s, p.e};
   simt_gemm<T><<<grid, 256, 0, p.stream>>>(p.s, p.e, p.C, Kl, 1, p.s, (long long)p.C * p.s,
                                            (const T *)p.V, p.e, 1, (long long)p.C * p.e, epi);
   return cudaGetLastError();
@@ -281,8 +328,14 @@ cudaError_t chunk_state(const Problem &p) {
 template <typename T>
 cudaError_t prefix_scan(const Problem &p) {
   long long se = (long long)p.s * p.e;
+  if (sizeof(T) == 2 && se % 8 == 0) {
+    const long long se8 = se / 8;
+    return launch_pdl(prefix_scan_bf16x8, dim3(cdiv(p.B * se8, 256)), dim3(256), 0, p.stream,
+                      (const uint4 *)p.state, (uint4 *)p.prefix, p.B, p.G, se8, p.causal,
+                      p.lin_scale);
+  }
   return launch_pdl(simt_prefix_scan<T>, dim3(cdiv(p.B * se, 256)), dim3(256), 0, p.stream,
-                    p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
+                    (const T *)p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
 }
 
 template <typename T>

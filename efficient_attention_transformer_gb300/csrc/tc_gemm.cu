@@ -1,19 +1,15 @@
-// Persistent tcgen05 GEMM with fused epilogues, the dense contractions of the
-// FLASH GAU forward in bf16 with fp32 accumulation in TMEM:
-//   projection   [U|V|Z] = swish(X W_uvz); the Z tile's epilogue writes the
-//                four scale/offset heads Z*gamma_h + beta_h
-//                ("Transformer Quality in Linear Time", Method, eq. 5 and
-//                 the four heads of mixed chunk attention)
-//   output       O = gated W_o                   (display after eq. 8)
-//   chunk state  State_g = K_lin,g^T V_g, batched over chunks (eq. 7/8)
+// Chunk states of mixed chunk attention on tcgen05 tensor cores:
+//   State_g = K_lin,g^T V_g   for every chunk g of C tokens
+// ("Transformer Quality in Linear Time", eq. 7 and eq. 8, the summands of
+// the global term), bf16 operands, fp32 accumulation in TMEM, bf16 result.
 //
-// One CTA per SM loops over 128 x 256 output tiles.  Warp 0 streams A and B
-// k-blocks (64 deep) into a 4-stage shared-memory ring with TMA; one thread
-// of warp 1 issues tcgen05.mma into one of two TMEM accumulators; warps 2-5
-// drain the other accumulator through tcgen05.ld, apply the epilogue in
-// registers and store.  All operand tiles use the 128-byte swizzled layout;
-// A is K-major (or M-major for the chunk state), B is N-major (row-major
-// weights / values).
+// A batched GEMM (one batch per chunk: M = s = 128, N = e, K = C) run by a
+// persistent CTA per SM over 128 x 256 output tiles.  Warp 0 streams
+// k-blocks (64 tokens deep) into a 4-stage 128-byte-swizzled ring with TMA:
+// A = K_lin^T read M-major straight from the heads buffer, B = V rows
+// N-major.  One thread of warp 1 issues tcgen05.mma into one of two TMEM
+// accumulators; warps 2-5 drain the other through tcgen05.ld into swizzled
+// staging and TMA stores.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -38,17 +34,13 @@ constexpr int STG_OFF = STAGES * STAGE_BYTES;        // 2 staging boxes per epil
 constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_STATE = 2 };
 
 struct GemmParams {
   int N, K;              // output columns, contraction depth (per batch)
   int m_tiles, n_tiles;  // per batch
   int total_tiles;       // batches * m_tiles * n_tiles
   int k_rows_per_batch;  // row offset of a batch along K in the K-indexed maps
-  // projection epilogue
-  const float *gamma, *beta;
-  int M_tokens;
-  int e, s;
+  int s;  // rows of one chunk state
   int *status;
 };
 
@@ -120,14 +112,12 @@ __device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (
   }
 }
 
-// A_MN: A is stored M-contiguous (K_lin^T of the chunk state); otherwise
-// K-contiguous.  tmC0..2 are the output maps of the epilogue (U, V, heads
-// for the projection; the output for the plain store; the state).
-template <int EPI, bool A_MN>
+// A_MN: A is stored M-contiguous (K_lin^T); otherwise K-contiguous.  tmC
+// is the output map (bf16 [B*G*s, e], 32-row x 64-column boxes).
+template <bool A_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
-               const __grid_constant__ CUtensorMap tmC2, const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -270,68 +260,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_after();
       const int row0 = mt * BM + quarter * 32;  // first row of this warp's box
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
-      if constexpr (EPI == EPI_STATE) {
-        // fp32: 32 columns (128 bytes) per box
-        for (int c0 = 0; c0 < nsz; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c0, r);
-          tmem_ld_wait();
-          if (c0 + 32 >= nsz) {
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sm->acc_empty[acc]));
-          }
-          uint4 w[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) w[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-          uint8_t *b = st.begin();
-          st.put(b, w);
-          st.finish(b, &tmC0, n0 + c0, batch * p.s + row0);
+      for (int c0 = 0; c0 < nsz; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c0 + 32, rb);
+        tmem_ld_wait();
+        if (c0 + 64 >= nsz) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm->acc_empty[acc]));
         }
-      } else {
-        for (int c0 = 0; c0 < nsz; c0 += 64) {
-          uint32_t ra[32], rb[32];
-          tmem_ld32(taddr + c0, ra);
-          tmem_ld32(taddr + c0 + 32, rb);
-          tmem_ld_wait();
-          if (c0 + 64 >= nsz) {
-            tc_fence_before();
-            mbar_arrive(smem_u32(&sm->acc_empty[acc]));
-          }
-          if constexpr (EPI == EPI_STORE) {
-            uint4 w[8];
-            pack64(ra, rb, [](float x, int) { return x; }, w);
-            uint8_t *b = st.begin();
-            st.put(b, w);
-            st.finish(b, &tmC0, n0 + c0, row0);
-          } else {
-            const int n = n0 + c0;
-            if (n < 2 * p.e) {
-              uint4 w[8];
-              pack64(ra, rb, [](float x, int) { return swish_tanh(x); }, w);
-              uint8_t *b = st.begin();
-              st.put(b, w);
-              if (n < p.e) st.finish(b, &tmC0, n, row0);
-              else st.finish(b, &tmC1, n - p.e, row0);
-            } else {
-              const int c = n - 2 * p.e;  // column inside Z
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                ra[j] = __float_as_uint(swish_tanh(__uint_as_float(ra[j])));
-                rb[j] = __float_as_uint(swish_tanh(__uint_as_float(rb[j])));
-              }
-#pragma unroll 1
-              for (int h = 0; h < 4; ++h) {
-                const float *g = p.gamma + h * p.s + c;
-                const float *be = p.beta + h * p.s + c;
-                uint4 w[8];
-                pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); }, w);
-                uint8_t *b = st.begin();
-                st.put(b, w);
-                st.finish(b, &tmC2, c, h * p.M_tokens + row0);
-              }
-            }
-          }
-        }
+        uint4 w[8];
+        pack64(ra, rb, [](float x, int) { return x; }, w);
+        uint8_t *b = st.begin();
+        st.put(b, w);
+        st.finish(b, &tmC, n0 + c0, batch * p.s + row0);
       }
     }
     st.drain();
@@ -345,30 +287,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int EPI, bool A_MN>
-cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &c0,
-                   const CUtensorMap &c1, const CUtensorMap &c2, const GemmParams &p,
-                   const Problem &pr) {
+template <bool A_MN>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                   const GemmParams &p, const Problem &pr) {
   static unsigned long long configured = 0;  // one bit per device ordinal
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 64 && !(configured & (1ull << dev))) {
-    err = cudaFuncSetAttribute(tc_gemm_kernel<EPI, A_MN>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(tc_gemm_kernel<A_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
     if (err != cudaSuccess) return err;
     configured |= 1ull << dev;
   }
   const int grid = p.total_tiles < pr.num_sms ? p.total_tiles : pr.num_sms;
-  return launch_pdl(tc_gemm_kernel<EPI, A_MN>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES,
-                    pr.stream, tmA, tmB, c0, c1, c2, p);
+  return launch_pdl(tc_gemm_kernel<A_MN>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
+                    tmA, tmB, tmC, p);
 }
 
 GemmParams base_params(const Problem &pr) {
   GemmParams p = {};
   p.status = pr.status;
-  p.M_tokens = (int)pr.M;
-  p.e = pr.e;
   p.s = pr.s;
   return p;
 }
@@ -382,7 +321,7 @@ cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tmA, Kl, pr.M, pr.s, pr.s, BK, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.V, pr.M, pr.e, pr.e, BK, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_f32_2d(&tS, pr.state, (long long)pr.B * pr.G * pr.s, pr.e, pr.e, 32, 32)) !=
+  if ((err = make_tmap_bf16_2d(&tS, pr.state, (long long)pr.B * pr.G * pr.s, pr.e, pr.e, 32, 64)) !=
       cudaSuccess)
     return err;
   GemmParams p = base_params(pr);
@@ -392,7 +331,7 @@ cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   p.n_tiles = (pr.e + BN - 1) / BN;
   p.total_tiles = pr.B * pr.G * p.n_tiles;
   p.k_rows_per_batch = pr.C;
-  return launch<EPI_STATE, true>(tmA, tmB, tS, tS, tS, p, pr);
+  return launch<true>(tmA, tmB, tS, p, pr);
 }
 
 }  // namespace flashgau

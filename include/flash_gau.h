@@ -58,8 +58,9 @@ extern "C" {
 /* ---- io data types ----------------------------------------------------- */
 /* FP32: X, weights, out and all intermediates in fp32, fp32 arithmetic.
  * BF16: X, W_uvz, W_o and out in bf16; tensor-core products with fp32
- *       accumulation; U, V, heads, prefix states and the gated product are
- *       stored in bf16. gamma, beta and relpos are fp32 for both types.    */
+ *       accumulation; U, V, heads, chunk states, prefix states and the gated
+ *       product are stored in bf16 (prefix sums accumulate in fp32).
+ *       gamma, beta and relpos are fp32 for both types.                     */
 #define FLASH_GAU_FP32 0
 #define FLASH_GAU_BF16 1
 
@@ -84,7 +85,7 @@ typedef struct flash_gau_workspace_layout {
   size_t U;             /* [B*T, e] io: swish(X W_u)                        */
   size_t V;             /* [B*T, e] io: swish(X W_v)                        */
   size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
-  size_t state;         /* [B, G, s, e] fp32: K_lin,g^T V_g per chunk        */
+  size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk          */
   size_t prefix;        /* causal [B, G, s, e], non-causal [B, s, e], io:
                            lin_scale * (exclusive / total) chunk-state sum  */
   size_t gated;         /* [B*T, e] io: U * (Vq + Vl)                       */

@@ -60,7 +60,7 @@ class Case:
         B, T, e, s, M = self.B, self.T, self.e, self.s, self.B * self.T
         G = T // self.C
         shapes = {"U": (M, e), "V": (M, e), "heads": (4, M, s), "gated": (M, e),
-                  "prefix": (B * G if self.causal else B, s, e)}
+                  "state": (B * G, s, e), "prefix": (B * G if self.causal else B, s, e)}
         shape = shapes[name]
         n = int(np.prod(shape))
         raw = self.workspace[self.layout[name]:]

@@ -52,7 +52,7 @@ def test_layout_offsets_aligned_and_sized(L):
     assert lay["V"] - lay["U"] >= M * e * 2
     assert lay["heads"] - lay["V"] >= M * e * 2
     assert lay["state"] - lay["heads"] >= 4 * M * s * 2
-    assert lay["prefix"] - lay["state"] >= B * G * s * e * 4
+    assert lay["prefix"] - lay["state"] >= B * G * s * e * 2
     assert lay["gated"] - lay["prefix"] >= B * G * s * e * 2
     assert lay["total_bytes"] - lay["gated"] >= M * e * 2
     nc = bd.workspace_layout(B, T, C, d, e, s, False, bd.BF16)

@@ -3,9 +3,10 @@ the same seeded inputs, element by element.
 
 Bar: max|O_gpu - O_oracle| <= tol * max|O_oracle| with tol = 1e-4 for fp32
 io and 2e-2 for bf16 io.  Every intermediate the workspace holds (U, V, the
-four heads, the prefix states, the gated product) is checked against the
-oracle's own intermediate, relative to that tensor's maximum, because the
-global term dominates |O| and would hide a broken local term."""
+four heads, the chunk states, the prefix states, the gated product) is
+checked against the oracle's own intermediate, relative to that tensor's
+maximum, because the global term dominates |O| and would hide a broken
+local term."""
 
 import numpy as np
 import pytest
@@ -32,6 +33,7 @@ def _check_all(case, O, ref, inter):
     errs["U"] = rel_err(case.intermediate("U"), inter["U"].reshape(M, -1))
     errs["V"] = rel_err(case.intermediate("V"), inter["V"].reshape(M, -1))
     errs["heads"] = rel_err(case.intermediate("heads"), inter["heads"].reshape(4, M, -1))
+    errs["state"] = rel_err(case.intermediate("state"), inter["state"].reshape(-1, case.s, case.e))
     pre = inter["prefix"] * case.lin_scale
     if not case.causal:
         pre = pre[:, 0]
