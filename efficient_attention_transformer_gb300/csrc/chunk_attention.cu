@@ -12,18 +12,20 @@
 // when causal.  Because relu^2 has no row normalisation, the products of
 // successive key blocks simply add into one accumulator.
 //
-// Roles (320 threads):
+// Roles (448 threads):
 //   warp 0     TMA producer: Q_quad, Q_lin, the K_quad ring, and a ring of
 //              64-row x 128-column B operands (prefix state rows, then V
 //              rows);
 //   warp 1     MMA issuer: S = Q_quad K_quad^T into a 128-column TMEM
 //              buffer (two buffers), acc = Q_lin Prefix (smem A), acc += P V
 //              with P read from TMEM;
-//   warps 2-5  relu^2: read S with tcgen05.ld, compute relu^2(S/C + b) with
-//              the causal mask in registers, write P as packed bf16 over the
-//              same TMEM buffer with tcgen05.st (the C x C scores never
-//              leave TMEM and registers);
-//   warps 6-9  epilogue: gated = U * acc, U boxes TMA-loaded into per-warp
+//   warps 2-9  relu^2, two per TMEM lane quarter, each for 64 of a block's
+//              128 keys: read S with tcgen05.ld, compute relu^2(S/C + b)
+//              with the causal mask in registers, write P as packed bf16
+//              over the start of the same S columns with tcgen05.st (keys
+//              0-63 at packed columns 0-31, keys 64-127 at 64-95); the
+//              C x C scores never leave TMEM and registers;
+//   warps 10-13 epilogue: gated = U * acc, U boxes TMA-loaded into per-warp
 //              double buffers, the product written in place and TMA-stored.
 // Two accumulators alternate between units, so while the epilogue warps
 // drain one, the MMAs of the next unit already fill the other.
@@ -46,7 +48,8 @@ constexpr int QT = 128;  // query rows per unit
 constexpr int KB = 128;  // keys per block
 constexpr int ET = 128;  // value columns per unit
 constexpr int SD = 128;  // head width s
-constexpr int NUM_THREADS = 320;
+constexpr int RELU_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (2 + RELU_WARPS + 4);
 
 constexpr int ATOM_BYTES = 128 * 64 * 2;        // 128 rows x 64 bf16: 16 KB
 constexpr int Q_BYTES = 2 * ATOM_BYTES;         // 32 KB
@@ -126,6 +129,43 @@ struct Ring {
   }
 };
 
+// Half `half` (64 keys) of one 128-key block of the local term, for this
+// thread's query row r (row i = qt*128 + r of the chunk): reads the 64 S
+// columns (fp32) at sbuf + 64*half, writes P = relu^2(S/C + b), masked, as
+// 32 packed bf16 columns over the start of those same columns.  All 64 S
+// values are in registers before the first store lands.
+__device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, int kb, int qt,
+                                           int r, int half) {
+  const int i = qt * QT + r;
+  const bool diag = p.causal && kb == qt;
+  const int c0 = half * 64;
+  const float *bias_row = p.relpos + (kb * KB + c0 - i + p.C - 1);  // + key index j
+  uint32_t va[32], vb[32];
+  tmem_ld32(sbuf + c0, va);
+  tmem_ld32(sbuf + c0 + 32, vb);
+  tmem_ld_wait();
+  uint32_t lo[16], hi[16];
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const uint32_t s0 = j < 32 ? va[j] : vb[j - 32];
+    const uint32_t s1 = j < 32 ? va[j + 1] : vb[j - 31];
+    float x0 = fmaf(__uint_as_float(s0), p.inv_c, __ldg(bias_row + j));
+    float x1 = fmaf(__uint_as_float(s1), p.inv_c, __ldg(bias_row + j + 1));
+    x0 = fmaxf(x0, 0.f);
+    x1 = fmaxf(x1, 0.f);
+    x0 *= x0;
+    x1 *= x1;
+    if (diag) {
+      if (c0 + j > r) x0 = 0.f;
+      if (c0 + j + 1 > r) x1 = 0.f;
+    }
+    if (j < 32) lo[j / 2] = pack_bf16(x0, x1);
+    else hi[(j - 32) / 2] = pack_bf16(x0, x1);
+  }
+  tmem_st16(sbuf + c0, lo);
+  tmem_st16(sbuf + c0 + 16, hi);
+}
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                        const __grid_constant__ CUtensorMap tmKq,
@@ -152,7 +192,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       mbar_init(smem_u32(&bar->acc_full[i]), 1);
       mbar_init(smem_u32(&bar->acc_empty[i]), 128);
       mbar_init(smem_u32(&bar->s_full[i]), 1);
-      mbar_init(smem_u32(&bar->p_full[i]), 128);
+      mbar_init(smem_u32(&bar->p_full[i]), 32 * RELU_WARPS);
       mbar_init(smem_u32(&bar->sb_free[i]), 1);
       for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bar->u_full[w][i]), 1);
     }
@@ -234,7 +274,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     if (elect_one()) {
       const uint32_t idesc_s = idesc_bf16_f32(128, KB, 0, 0);
       const uint32_t idesc_v = idesc_bf16_f32(128, ET, 0, 1);
-      const uint32_t sQ = smem_u32(tiles + OFF_QQ);
+      const uint64_t dq = sw128_desc(smem_u32(tiles + OFF_QQ), 16, 1024);
       const uint32_t sQL = smem_u32(tiles + OFF_QL);
       const uint32_t sK = smem_u32(tiles + OFF_K);
       const uint32_t sB = smem_u32(tiles + OFF_B);
@@ -249,12 +289,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           return false;
         if (!mbar_wait(smem_u32(&bar->k_full[kr.stage]), kr.phase, abort)) return false;
         tc_fence_after();
-        const uint32_t kst = sK + kr.stage * K_STAGE_BYTES;
+        const uint64_t dk = sw128_desc(sK + kr.stage * K_STAGE_BYTES, 16, 1024);
 #pragma unroll
         for (int k = 0; k < SD / 16; ++k) {
           const uint32_t off = (k >> 2) * ATOM_BYTES + (k & 3) * 32;
-          mma_f16_ss(tmem + TM_S + sb * KB, sw128_desc(sQ + off, 16, 1024),
-                     sw128_desc(kst + off, 16, 1024), idesc_s, k != 0);
+          mma_f16_ss(tmem + TM_S + sb * KB, desc_advance(dq, off), desc_advance(dk, off), idesc_s,
+                     k != 0);
         }
         mma_commit(smem_u32(&bar->k_empty[kr.stage]));
         mma_commit(smem_u32(&bar->s_full[sb]));
@@ -266,11 +306,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       auto issue_b_smem = [&](uint32_t a_atom, bool first) -> bool {
         if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
         tc_fence_after();
-        const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
+        const uint64_t da = sw128_desc(a_atom, 16, 1024);
+        const uint64_t db = sw128_desc(sB + br.stage * B_STAGE_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ss(tmem + acc_col, sw128_desc(a_atom + k * 32, 16, 1024),
-                     sw128_desc(bst + k * 2048, B_BOX_BYTES, 1024), idesc_v, !(first && k == 0));
+          mma_f16_ss(tmem + acc_col, desc_advance(da, k * 32), desc_advance(db, k * 2048), idesc_v,
+                     !(first && k == 0));
         mma_commit(smem_u32(&bar->b_empty[br.stage]));
         br.next();
         return true;
@@ -279,11 +320,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       auto issue_b_tmem = [&](uint32_t a_col) -> bool {
         if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
         tc_fence_after();
-        const uint32_t bst = sB + br.stage * B_STAGE_BYTES;
+        const uint64_t db = sw128_desc(sB + br.stage * B_STAGE_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8,
-                     sw128_desc(bst + k * 2048, B_BOX_BYTES, 1024), idesc_v, 1);
+          mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8, desc_advance(db, k * 2048), idesc_v, 1);
         mma_commit(smem_u32(&bar->b_empty[br.stage]));
         br.next();
         return true;
@@ -313,7 +353,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           if (!ok) break;
           tc_fence_after();
           const uint32_t pcol = TM_S + sb * KB;
-          ok = issue_b_tmem(pcol) && issue_b_tmem(pcol + 32);
+          ok = issue_b_tmem(pcol) && issue_b_tmem(pcol + 64);
           if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
         }
         if (ok) mma_commit(smem_u32(&bar->acc_full[i & 1]));
@@ -322,16 +362,15 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       mma_commit(smem_u32(&bar->drain));
       if (!mbar_wait(smem_u32(&bar->drain), 0)) raise_timeout(bar, p.status);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + RELU_WARPS) {
     // -------------------------------------------------- relu^2 warps
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // row inside the query tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     int n = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x) {
       const Unit x = unit_of(p, u);
-      const int i = x.qt * QT + r;  // row inside the chunk
       for (int kb = 0; kb < x.nkb; ++kb, ++n) {
         const int sb = n & 1;
         if (!mbar_wait(smem_u32(&bar->s_full[sb]), (n >> 1) & 1, abort)) {
@@ -339,33 +378,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           break;
         }
         tc_fence_after();
-        const bool diag = p.causal && kb == x.qt;
-        const float *bias_row = p.relpos + (kb * KB - i + p.C - 1);  // + key index j
-        const uint32_t sbuf = tmem + lane_off + TM_S + sb * KB;
-#pragma unroll 1
-        for (int c0 = 0; c0 < KB; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(sbuf + c0, v);
-          tmem_ld_wait();
-          uint32_t packed[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float x0 = fmaf(__uint_as_float(v[j]), p.inv_c, __ldg(bias_row + c0 + j));
-            float x1 = fmaf(__uint_as_float(v[j + 1]), p.inv_c, __ldg(bias_row + c0 + j + 1));
-            x0 = fmaxf(x0, 0.f);
-            x1 = fmaxf(x1, 0.f);
-            x0 *= x0;
-            x1 *= x1;
-            if (diag) {
-              if (c0 + j > r) x0 = 0.f;
-              if (c0 + j + 1 > r) x1 = 0.f;
-            }
-            packed[j / 2] = pack_bf16(x0, x1);
-          }
-          // keys c0..c0+31 -> packed columns c0/2 .. c0/2+15 (S columns
-          // below c0 + 32 have all been read already)
-          tmem_st16(sbuf + c0 / 2, packed);
-        }
+        relu2_half(tmem + lane_off + TM_S + sb * KB, p, kb, x.qt, r, half);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar->p_full[sb]));
@@ -374,7 +387,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     if (!ok) raise_timeout(bar, p.status);
   } else {
     // ------------------------------------------------------- epilogue
-    const int quarter = warp & 3, w = warp - 6;
+    const int quarter = warp & 3, w = warp - (2 + RELU_WARPS);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t *ebuf = tiles + OFF_E + w * 2 * E_BOX_BYTES;
     // chunk c of this CTA = 64 value columns of unit (c / 2), part c % 2

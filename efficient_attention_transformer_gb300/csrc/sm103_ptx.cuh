@@ -353,6 +353,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple
+// of 16 that keeps the address inside the 18-bit shared window): only the
+// low 14-bit address field changes.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D:
 //   bits 4-5 D type (1 = f32), 7-9 A type (1 = bf16), 10-12 B type (1 =
 //   bf16), 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N >> 3,

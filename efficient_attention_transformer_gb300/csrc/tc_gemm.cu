@@ -220,16 +220,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
-          const uint32_t sB = sA + A_BYTES;
+          // A: K-major advances 16 elements (32 B) inside the swizzle atom;
+          //    M-major advances 16 rows of 128 B.  B advances 16 rows.
+          const uint64_t da = A_MN ? sw128_desc(sA, A_BYTES / 2, 1024) : sw128_desc(sA, 16, 1024);
+          const uint64_t db = sw128_desc(sA + A_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // A: K-major advances 16 elements (32 B) inside the swizzle atom;
-            //    M-major advances 16 rows of 128 B.  B advances 16 rows.
-            const uint64_t adesc = A_MN ? sw128_desc(sA + k * 2048, A_BYTES / 2, 1024)
-                                        : sw128_desc(sA + k * 32, 16, 1024);
-            const uint64_t bdesc = sw128_desc(sB + k * 2048, B_BOX_BYTES, 1024);
-            mma_f16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss(d_tmem, desc_advance(da, A_MN ? k * 2048 : k * 32), desc_advance(db, k * 2048),
+                       idesc, (kb | k) != 0);
           mma_commit(smem_u32(&sm->empty[stage]));
           if (++stage == STAGES) {
             stage = 0;

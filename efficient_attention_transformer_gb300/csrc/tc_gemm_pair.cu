@@ -230,14 +230,14 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
-          const uint32_t sB = sA + A_BYTES;
+          // A: K-major, 16 elements (32 B) per step inside the swizzle atom;
+          // B: N-major, 16 rows of 128 B per step, 64-column boxes 8 KB apart
+          const uint64_t da = sw128_desc(sA, 16, 1024);
+          const uint64_t db = sw128_desc(sA + A_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // A: K-major, 16 elements (32 B) per step inside the swizzle atom;
-            // B: N-major, 16 rows of 128 B per step, 64-column boxes 8 KB apart
-            mma_f16_ss_pair(d_tmem, sw128_desc(sA + k * 32, 16, 1024),
-                            sw128_desc(sB + k * 2048, B_BOX_BYTES, 1024), idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss_pair(d_tmem, desc_advance(da, k * 32), desc_advance(db, k * 2048), idesc,
+                            (kb | k) != 0);
           mma_commit_pair_mc(smem_u32(&sm->empty[stage]), kPair);
           if (++stage == STAGES) {
             stage = 0;
