@@ -345,7 +345,7 @@ def cpu_baseline(w, budget_s=20.0):
     """The oracle as it stands on the host cores, on whole sequences of the
     workload repeated until about budget_s seconds of CPU work."""
     secs, toks, reps = 0.0, 0, 0
-    while secs < budget_s and reps < 16:
+    while secs < budget_s and reps < 256:
         dt, T = _oracle_sample(w, w["T"])
         secs += dt
         toks += T
