@@ -6,8 +6,12 @@
 //   acc  += sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]    (local term)
 //   gated = U * acc
 //
-// Work unit: (chunk, 128-query tile, 128-column value tile), value tile
-// fastest; one persistent CTA per SM walks its units round-robin.  Key
+// Work unit: (chunk, 128-query tile, 128-column value tile).  One
+// persistent CTA per SM; the producer takes units from a global atomic
+// counter (dynamic scheduling: per chunk the query tiles with more key
+// blocks first, value tile fastest, so the cheapest units come last and
+// units sharing Q/K run on neighbouring SMs at the same time) and hands
+// their indices to the other roles through a 4-entry queue.  Key
 // blocks of 128 are visited in order, only those at or below the diagonal
 // when causal.  Because relu^2 has no row normalisation, the products of
 // successive key blocks simply add into one accumulator.
@@ -76,6 +80,8 @@ struct Bars {
   uint64_t s_full[2], p_full[2], sb_free[2];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t u_full[4][2];
+  uint64_t uq_full[4], uq_empty[4];  // unit-index queue
+  volatile int unit_q[4];
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -87,7 +93,12 @@ struct AttnParams {
   float inv_c;
   const float *relpos;
   int *status;
+  int *next_unit;  // work counter, zeroed by the chunk-state kernel
 };
+
+// Agents that consume each queued unit index: the MMA thread, the relu^2
+// warps and the epilogue warps (one arrival per warp).
+constexpr int QUEUE_AGENTS = 1 + 8 + 4;
 
 struct Unit {
   int chunk, b, qt, et, nkb;
@@ -97,7 +108,7 @@ struct Unit {
 __device__ __forceinline__ Unit unit_of(const AttnParams &p, int u) {
   Unit x;
   x.et = u % p.n_et;
-  x.qt = (u / p.n_et) % p.n_qt;
+  x.qt = p.n_qt - 1 - (u / p.n_et) % p.n_qt;  // more key blocks first
   x.chunk = u / (p.n_et * p.n_qt);
   x.b = x.chunk / p.G;
   x.tok0 = (long long)x.chunk * p.C;
@@ -200,6 +211,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       mbar_init(smem_u32(&bar->b_full[i]), 1);
       mbar_init(smem_u32(&bar->b_empty[i]), 1);
     }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(smem_u32(&bar->uq_full[q]), 1);
+      mbar_init(smem_u32(&bar->uq_empty[q]), QUEUE_AGENTS);
+    }
     mbar_init(smem_u32(&bar->drain), 1);
     bar->abort_flag = 0;
     fence_mbar_init();
@@ -212,10 +227,19 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // setup above overlaps the previous kernel's tail; its outputs are read below
-  griddep_wait();
+  // This kernel runs concurrently with the prefix scan launched before it:
+  // everything except the prefix states (U, V, the heads) was written by
+  // kernels that completed before the scan started, and the producer waits
+  // for the scan itself (griddepcontrol.wait) just before its first prefix
+  // load.  The work counter was zeroed by the chunk-state kernel.
   griddep_launch_dependents();
   const uint32_t tmem = bar->tmem_base;
+  // unit queue: entry q of this CTA's sequence sits in slot q & 3
+  auto pop = [&](int q) -> int {  // unit index, -1 when done, -2 on timeout
+    if (!mbar_wait(smem_u32(&bar->uq_full[q & 3]), (q >> 2) & 1, abort)) return -2;
+    return bar->unit_q[q & 3];
+  };
+  auto release = [&](int q) { mbar_arrive(smem_u32(&bar->uq_empty[q & 3])); };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -243,8 +267,20 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         br.next();
         return true;
       };
+      // next unit: from the global counter, announced through the queue
+      auto push = [&](int q, int u) -> bool {
+        if (!mbar_wait(smem_u32(&bar->uq_empty[q & 3]), ((q >> 2) & 1) ^ 1, abort)) return false;
+        bar->unit_q[q & 3] = u;
+        mbar_arrive(smem_u32(&bar->uq_full[q & 3]));
+        return true;
+      };
+      bool prefix_ready = false;
       int i = 0;
-      for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
+      for (;; ++i) {
+        int u = atomicAdd(p.next_unit, 1);
+        if (u >= p.total) u = -1;
+        ok = push(i, u);
+        if (!ok || u < 0) break;
         const Unit x = unit_of(p, u);
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
@@ -254,18 +290,25 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         mbar_arrive_expect_tx(f, Q_BYTES);
         tma_load_2d(smem_u32(tiles + OFF_QQ), &tmQq, f, 0, (int)qrow);
         tma_load_2d(smem_u32(tiles + OFF_QQ + ATOM_BYTES), &tmQq, f, 64, (int)qrow);
-        ok = load_k(x.tok0) && mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
+        ok = load_k(x.tok0);
+        for (int kb = 0; ok && kb < x.nkb; ++kb) {
+          if (kb + 1 < x.nkb) ok = load_k(x.tok0 + (kb + 1) * KB);
+          ok = ok && load_b(&tmV, x.et * ET, x.tok0 + kb * KB) &&
+               load_b(&tmV, x.et * ET, x.tok0 + kb * KB + 64);
+        }
+        // the global term last: the prefix states come from the kernel
+        // launched just before this one, which may still be running
+        if (ok && !prefix_ready) {
+          griddep_wait();
+          prefix_ready = true;
+        }
+        ok = ok && mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
         if (!ok) break;
         f = smem_u32(&bar->ql_full);
         mbar_arrive_expect_tx(f, Q_BYTES);
         tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
         tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
         ok = load_b(&tmPre, x.et * ET, pre_row0) && load_b(&tmPre, x.et * ET, pre_row0 + 64);
-        for (int kb = 0; ok && kb < x.nkb; ++kb) {
-          if (kb + 1 < x.nkb) ok = load_k(x.tok0 + (kb + 1) * KB);
-          ok = ok && load_b(&tmV, x.et * ET, x.tok0 + kb * KB) &&
-               load_b(&tmV, x.et * ET, x.tok0 + kb * KB + 64);
-        }
       }
       if (!ok) raise_timeout(bar, p.status);
     }
@@ -317,19 +360,24 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         return true;
       };
       // acc += P * B stage, P: 64 keys = 32 packed columns of TMEM at a_col
-      auto issue_b_tmem = [&](uint32_t a_col) -> bool {
+      auto issue_b_tmem = [&](uint32_t a_col, bool first) -> bool {
         if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
         tc_fence_after();
         const uint64_t db = sw128_desc(sB + br.stage * B_STAGE_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8, desc_advance(db, k * 2048), idesc_v, 1);
+          mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8, desc_advance(db, k * 2048), idesc_v,
+                     !(first && k == 0));
         mma_commit(smem_u32(&bar->b_empty[br.stage]));
         br.next();
         return true;
       };
-      int i = 0;
-      for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
+      for (int i = 0; ok; ++i) {
+        const int u = pop(i);
+        if (u < 0) {
+          ok = u == -1;
+          break;
+        }
         const Unit x = unit_of(p, u);
         const int n0 = n;
         ok = mbar_wait(smem_u32(&bar->q_full), i & 1, abort) && issue_s();
@@ -337,12 +385,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         // this unit's accumulator must have been drained by the epilogue of
         // the unit two before
         acc_col = TM_ACC + (i & 1) * ET;
-        ok = ok && mbar_wait(smem_u32(&bar->acc_empty[i & 1]), ((i >> 1) & 1) ^ 1, abort) &&
-             mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
+        ok = ok && mbar_wait(smem_u32(&bar->acc_empty[i & 1]), ((i >> 1) & 1) ^ 1, abort);
         if (!ok) break;
         tc_fence_after();
-        ok = issue_b_smem(sQL, true) && issue_b_smem(sQL + ATOM_BYTES, false);
-        if (ok) mma_commit(smem_u32(&bar->ql_empty));
+        // local term first, global term (Q_lin Prefix) last
         for (int kb = 0; ok && kb < x.nkb; ++kb) {
           if (kb + 1 < x.nkb) {
             ok = issue_s();
@@ -353,10 +399,16 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           if (!ok) break;
           tc_fence_after();
           const uint32_t pcol = TM_S + sb * KB;
-          ok = issue_b_tmem(pcol) && issue_b_tmem(pcol + 64);
+          ok = issue_b_tmem(pcol, kb == 0) && issue_b_tmem(pcol + 64, false);
           if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
         }
+        ok = ok && mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        ok = issue_b_smem(sQL, false) && issue_b_smem(sQL + ATOM_BYTES, false);
+        if (ok) mma_commit(smem_u32(&bar->ql_empty));
         if (ok) mma_commit(smem_u32(&bar->acc_full[i & 1]));
+        release(i);
       }
       if (!ok) raise_timeout(bar, p.status);
       mma_commit(smem_u32(&bar->drain));
@@ -369,7 +421,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     int n = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x) {
+    for (int q = 0; ok; ++q) {
+      const int u = pop(q);
+      if (u < 0) {
+        ok = u == -1;
+        break;
+      }
       const Unit x = unit_of(p, u);
       for (int kb = 0; kb < x.nkb; ++kb, ++n) {
         const int sb = n & 1;
@@ -383,6 +440,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         tc_fence_before();
         mbar_arrive(smem_u32(&bar->p_full[sb]));
       }
+      __syncwarp();
+      if (lane == 0) release(q);
     }
     if (!ok) raise_timeout(bar, p.status);
   } else {
@@ -390,27 +449,30 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     const int quarter = warp & 3, w = warp - (2 + RELU_WARPS);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t *ebuf = tiles + OFF_E + w * 2 * E_BOX_BYTES;
-    // chunk c of this CTA = 64 value columns of unit (c / 2), part c % 2
-    auto load_u = [&](int c) {
-      const int u = blockIdx.x + (c >> 1) * gridDim.x;
-      if (lane != 0 || u >= p.total) return;
+    // U box of part j (64 value columns) of unit u into buffer b
+    auto load_u = [&](int u, int j, int b) {
+      if (lane != 0 || u < 0) return;
       const Unit x = unit_of(p, u);
-      const int b = c & 1;
       const uint32_t f = smem_u32(&bar->u_full[w][b]);
       mbar_arrive_expect_tx(f, E_BOX_BYTES);
-      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + (c & 1) * 64,
+      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + j * 64,
                   (int)(x.tok0 + x.qt * QT + quarter * 32));
     };
-    load_u(0);
-    load_u(1);
-    int c = 0, i = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.total; u += gridDim.x, ++i) {
-      const Unit x = unit_of(p, u);
-      if (!mbar_wait(smem_u32(&bar->acc_full[i & 1]), (i >> 1) & 1, abort)) {
+    int cur = pop(0);
+    ok = cur != -2;
+    load_u(cur, 0, 0);
+    load_u(cur, 1, 1);
+    int c = 0;
+    for (int i = 0; ok && cur >= 0; ++i) {
+      // the next unit's index, to prefetch its U boxes (released later)
+      const int nxt = pop(i + 1);
+      if (nxt == -2 ||
+          !mbar_wait(smem_u32(&bar->acc_full[i & 1]), (i >> 1) & 1, abort)) {
         ok = false;
         break;
       }
+      const Unit x = unit_of(p, cur);
       tc_fence_after();
       const int grow = (int)(x.tok0 + x.qt * QT + quarter * 32);
       for (int j = 0; j < ET / 64; ++j, ++c) {
@@ -453,8 +515,11 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           tma_store_wait_read<0>();  // the box is refilled next
         }
         __syncwarp();
-        load_u(c + 2);
+        load_u(nxt, j, b);
       }
+      __syncwarp();
+      if (lane == 0) release(i);
+      cur = nxt;
     }
     if (lane == 0) tma_store_wait<0>();
     __syncwarp();
@@ -507,6 +572,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.inv_c = 1.0f / (float)pr.C;
   p.relpos = pr.relpos;
   p.status = pr.status;
+  p.next_unit = pr.status + kNextUnitWord;
   const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;
   return launch_pdl(chunk_attention_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
                     tQq, tKq, tQl, tV, tPre, tU, tG, p);

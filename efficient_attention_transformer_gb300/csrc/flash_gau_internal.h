@@ -33,6 +33,11 @@ struct Problem {
   int num_sms;
 };
 
+// The status word's 256-byte workspace slot also holds, at this int offset,
+// the work counter of the chunk-attention kernel; the chunk-state kernel
+// zeroes it.
+constexpr int kNextUnitWord = 16;
+
 using StageFn = cudaError_t (*)(const Problem &);
 
 // Launches `kernel` on the problem's stream with programmatic stream

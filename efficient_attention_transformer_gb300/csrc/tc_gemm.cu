@@ -42,6 +42,7 @@ struct GemmParams {
   int k_rows_per_batch;  // row offset of a batch along K in the K-indexed maps
   int s;  // rows of one chunk state
   int *status;
+  int *next_unit;  // zeroed here for the chunk-attention kernel
 };
 
 struct Smem {
@@ -152,6 +153,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // setup above overlaps the previous kernel's tail; its outputs are read below
   griddep_wait();
   griddep_launch_dependents();
+  // the chunk-attention kernel's work counter; that kernel starts only once
+  // this one has completed, and the previous forward's is long done
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.next_unit = 0;
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
@@ -306,6 +310,7 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
 GemmParams base_params(const Problem &pr) {
   GemmParams p = {};
   p.status = pr.status;
+  p.next_unit = pr.status + kNextUnitWord;
   p.s = pr.s;
   return p;
 }

@@ -81,7 +81,9 @@ typedef struct flash_gau_weights {
  * io = the io type's size.  The offsets are 256-byte aligned.              */
 typedef struct flash_gau_workspace_layout {
   size_t total_bytes;   /* bytes the workspace must hold                    */
-  size_t status;        /* int32 device status word (FLASH_GAU_ETIMEOUT...) */
+  size_t status;        /* int32 device status word (FLASH_GAU_ETIMEOUT...);
+                           the rest of its 256-byte slot is used by the
+                           kernels for scheduling                            */
   size_t U;             /* [B*T, e] io: swish(X W_u)                        */
   size_t V;             /* [B*T, e] io: swish(X W_v)                        */
   size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
