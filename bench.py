@@ -55,6 +55,9 @@ def stage_work(w):
                        io * (M * d + d * (2 * e + s) + 2 * M * e + 4 * M * s)),
         "chunk_state": (2.0 * M * s * e, io * (M * s + M * e) + 4.0 * B * G * s * e),
         "prefix_scan": (float(B * G * s * e), 4.0 * B * G * s * e + io * pre_rows * s * e),
+        # bf16 schedule: states written and read back in bf16 inside one kernel
+        "chunk_state_scan": (2.0 * M * s * e + B * G * s * e,
+                             io * (M * s + M * e + 2 * B * G * s * e + pre_rows * s * e)),
         "chunk_attention": (2.0 * M * (cbar * s + cbar * e + s * e),
                             io * (2 * M * e + 3 * M * s + pre_rows * s * e + M * e)),
         "output": (2.0 * M * e * d, io * (M * e + e * d + M * d)),

@@ -93,7 +93,7 @@ struct AttnParams {
   float inv_c;
   const float *relpos;
   int *status;
-  int *next_unit;  // work counter, zeroed by the chunk-state kernel
+  int *next_unit;  // work counter, zeroed by the projection kernel
 };
 
 // Agents that consume each queued unit index: the MMA thread, the relu^2
@@ -227,11 +227,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // This kernel runs concurrently with the prefix scan launched before it:
-  // everything except the prefix states (U, V, the heads) was written by
-  // kernels that completed before the scan started, and the producer waits
-  // for the scan itself (griddepcontrol.wait) just before its first prefix
-  // load.  The work counter was zeroed by the chunk-state kernel.
+  // This kernel may start while the chunk-state/scan kernel launched before
+  // it still runs: everything except the prefix states (U, V, the heads, the
+  // zeroed work counter) was written by the projection, which completed
+  // before any CTA of that kernel got past its own griddepcontrol.wait, and
+  // the producer waits for that kernel itself just before its first prefix
+  // load.
   griddep_launch_dependents();
   const uint32_t tmem = bar->tmem_base;
   // unit queue: entry q of this CTA's sequence sits in slot q & 3

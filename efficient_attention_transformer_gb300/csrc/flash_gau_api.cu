@@ -106,8 +106,7 @@ const Stage kStagesF32[] = {
 };
 const Stage kStagesBF16[] = {
     {"projection", tc_projection_bf16},
-    {"chunk_state", tc_chunk_state_bf16},
-    {"prefix_scan", simt_prefix_scan_bf16},
+    {"chunk_state_scan", tc_chunk_state_scan_bf16},
     {"chunk_attention", tc_chunk_attention_bf16},
     {"output", tc_output_bf16},
 };

@@ -33,10 +33,12 @@ struct Problem {
   int num_sms;
 };
 
-// The status word's 256-byte workspace slot also holds, at this int offset,
-// the work counter of the chunk-attention kernel; the chunk-state kernel
-// zeroes it.
+// The status word's 256-byte workspace slot also holds, at these int
+// offsets, the work counter of the chunk-attention kernel and the arrival
+// counter of the chunk-state kernel's grid barrier; the projection kernel
+// zeroes both.
 constexpr int kNextUnitWord = 16;
+constexpr int kGridBarrierWord = 17;
 
 using StageFn = cudaError_t (*)(const Problem &);
 
@@ -72,19 +74,13 @@ cudaError_t simt_prefix_scan_f32(const Problem &p);
 cudaError_t simt_chunk_attention_f32(const Problem &p);
 cudaError_t simt_output_f32(const Problem &p);
 
-// bf16 tensor-core stages (tc_gemm.cu)
+// bf16 tensor-core stages: projection and output (tc_gemm_pair.cu), chunk
+// states followed by their prefix scan (tc_gemm.cu)
 cudaError_t tc_projection_bf16(const Problem &p);
-cudaError_t tc_chunk_state_bf16(const Problem &p);
+cudaError_t tc_chunk_state_scan_bf16(const Problem &p);
 cudaError_t tc_output_bf16(const Problem &p);
 
 // bf16 tensor-core chunk attention (chunk_attention.cu)
 cudaError_t tc_chunk_attention_bf16(const Problem &p);
-
-// bf16 CUDA-core stages
-cudaError_t simt_projection_bf16(const Problem &p);
-cudaError_t simt_chunk_state_bf16(const Problem &p);
-cudaError_t simt_prefix_scan_bf16(const Problem &p);
-cudaError_t simt_chunk_attention_bf16(const Problem &p);
-cudaError_t simt_output_bf16(const Problem &p);
 
 }  // namespace flashgau

@@ -149,52 +149,6 @@ __global__ void simt_prefix_scan(const T *__restrict__ state, T *__restrict__ pr
   }
 }
 
-// bf16 states: one thread per 8 consecutive state elements (16-byte loads
-// and stores), fp32 running sums, chunk states fetched 8 chunks ahead.
-__device__ __forceinline__ void add8(float (&run)[8], const uint4 &v) {
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 f = __bfloat1622float2(h[k]);
-    run[2 * k] += f.x;
-    run[2 * k + 1] += f.y;
-  }
-}
-__device__ __forceinline__ uint4 scaled8(const float (&run)[8], float scale) {
-  uint4 w;
-  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(scale * run[2 * k], scale * run[2 * k + 1]);
-  return w;
-}
-
-__global__ void prefix_scan_bf16x8(const uint4 *__restrict__ state, uint4 *__restrict__ prefix,
-                                   int B, int G, long long se8, int causal, float lin_scale) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (idx >= B * se8) return;
-  const long long b = idx / se8, r = idx % se8;
-  const uint4 *st = state + b * G * se8 + r;
-  uint4 *pre = prefix + (causal ? b * G * se8 : b * se8) + r;
-  float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int g0 = 0; g0 < G; g0 += 8) {
-    const int n = min(8, G - g0);
-    uint4 v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < n) v[k] = __ldg(st + (long long)(g0 + k) * se8);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < n) {
-        if (causal) pre[(long long)(g0 + k) * se8] = scaled8(run, lin_scale);
-        add8(run, v[k]);
-      }
-    }
-  }
-  if (!causal) *pre = scaled8(run, lin_scale);
-}
-
 // ------------------------------------------------------ chunk attention ----
 // Block = (chunk b*G+g, 32 query rows, 64 value columns).  Score rows are
 // built 64 keys at a time in shared memory and consumed immediately; the
@@ -328,12 +282,6 @@ cudaError_t chunk_state(const Problem &p) {
 template <typename T>
 cudaError_t prefix_scan(const Problem &p) {
   long long se = (long long)p.s * p.e;
-  if (sizeof(T) == 2 && se % 8 == 0) {
-    const long long se8 = se / 8;
-    return launch_pdl(prefix_scan_bf16x8, dim3(cdiv(p.B * se8, 256)), dim3(256), 0, p.stream,
-                      (const uint4 *)p.state, (uint4 *)p.prefix, p.B, p.G, se8, p.causal,
-                      p.lin_scale);
-  }
   return launch_pdl(simt_prefix_scan<T>, dim3(cdiv(p.B * se, 256)), dim3(256), 0, p.stream,
                     (const T *)p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
 }
@@ -370,13 +318,5 @@ cudaError_t simt_chunk_state_f32(const Problem &p) { return chunk_state<float>(p
 cudaError_t simt_prefix_scan_f32(const Problem &p) { return prefix_scan<float>(p); }
 cudaError_t simt_chunk_attention_f32(const Problem &p) { return chunk_attention<float>(p); }
 cudaError_t simt_output_f32(const Problem &p) { return output<float>(p); }
-
-cudaError_t simt_projection_bf16(const Problem &p) { return projection<__nv_bfloat16>(p); }
-cudaError_t simt_chunk_state_bf16(const Problem &p) { return chunk_state<__nv_bfloat16>(p); }
-cudaError_t simt_prefix_scan_bf16(const Problem &p) { return prefix_scan<__nv_bfloat16>(p); }
-cudaError_t simt_chunk_attention_bf16(const Problem &p) {
-  return chunk_attention<__nv_bfloat16>(p);
-}
-cudaError_t simt_output_bf16(const Problem &p) { return output<__nv_bfloat16>(p); }
 
 }  // namespace flashgau

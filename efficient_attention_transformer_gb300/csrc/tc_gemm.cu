@@ -1,7 +1,9 @@
-// Chunk states of mixed chunk attention on tcgen05 tensor cores:
-//   State_g = K_lin,g^T V_g   for every chunk g of C tokens
+// Chunk states of mixed chunk attention and their prefix sums, one kernel:
+//   State_g  = K_lin,g^T V_g   for every chunk g of C tokens
+//   Prefix_g = lin_scale * sum_{h<g} State_h   (causal; else the total once)
 // ("Transformer Quality in Linear Time", eq. 7 and eq. 8, the summands of
-// the global term), bf16 operands, fp32 accumulation in TMEM, bf16 result.
+// the global term and their cumulative sum), bf16 operands, fp32
+// accumulation in TMEM, bf16 states; the sums run in fp32.
 //
 // A batched GEMM (one batch per chunk: M = s = 128, N = e, K = C) run by a
 // persistent CTA per SM over 128 x 256 output tiles.  Warp 0 streams
@@ -10,6 +12,12 @@
 // N-major.  One thread of warp 1 issues tcgen05.mma into one of two TMEM
 // accumulators; warps 2-5 drain the other through tcgen05.ld into swizzled
 // staging and TMA stores.
+//
+// Once every CTA's state tiles are in memory (a grid barrier: the grid is at
+// most one CTA per SM and every CTA is resident before the next kernel can
+// start, so all of them arrive; the wait is bounded all the same), the same
+// CTAs scan the states, which are still in L2: one thread per 8 consecutive
+// state elements of a batch row, 16 chunks' loads in flight per thread.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -42,7 +50,14 @@ struct GemmParams {
   int k_rows_per_batch;  // row offset of a batch along K in the K-indexed maps
   int s;  // rows of one chunk state
   int *status;
-  int *next_unit;  // zeroed here for the chunk-attention kernel
+  int *grid_bar;  // arrivals at the grid barrier, zeroed by the projection
+  // prefix scan: states [B, G, s*e] -> prefixes [B, G or 1, s*e], as
+  // 16-byte groups of 8 bf16
+  const uint4 *state8;
+  uint4 *prefix8;
+  int B, G, causal;
+  long long se8;
+  float lin_scale;
 };
 
 struct Smem {
@@ -113,6 +128,55 @@ __device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (
   }
 }
 
+__device__ __forceinline__ void add8(float (&run)[8], const uint4 &v) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    run[2 * k] += f.x;
+    run[2 * k + 1] += f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 scaled8(const float (&run)[8], float scale) {
+  uint4 w;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(scale * run[2 * k], scale * run[2 * k + 1]);
+  return w;
+}
+
+// Running sums over the chunks of each batch row, all CTAs together.  The
+// states were written by other CTAs of this grid, so they are read through
+// L2 (ld.global.cg), not the non-coherent path.
+__device__ void scan_states(const GemmParams &p) {
+  constexpr int DEPTH = 16;  // chunks in flight per thread
+  const long long ncol = (long long)p.B * p.se8;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < ncol;
+       idx += stride) {
+    const long long b = idx / p.se8, r = idx % p.se8;
+    const uint4 *st = p.state8 + b * p.G * p.se8 + r;
+    uint4 *pre = p.prefix8 + (p.causal ? b * p.G * p.se8 : b * p.se8) + r;
+    float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int g0 = 0; g0 < p.G; g0 += DEPTH) {
+      const int n = min(DEPTH, p.G - g0);
+      uint4 v[DEPTH];
+#pragma unroll
+      for (int k = 0; k < DEPTH; ++k)
+        if (k < n) v[k] = __ldcg(st + (long long)(g0 + k) * p.se8);
+#pragma unroll
+      for (int k = 0; k < DEPTH; ++k) {
+        if (k < n) {
+          if (p.causal) pre[(long long)(g0 + k) * p.se8] = scaled8(run, p.lin_scale);
+          add8(run, v[k]);
+        }
+      }
+    }
+    if (!p.causal) *pre = scaled8(run, p.lin_scale);
+  }
+}
+
 // A_MN: A is stored M-contiguous (K_lin^T); otherwise K-contiguous.  tmC
 // is the output map (bf16 [B*G*s, e], 32-row x 64-column boxes).
 template <bool A_MN>
@@ -153,9 +217,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // setup above overlaps the previous kernel's tail; its outputs are read below
   griddep_wait();
   griddep_launch_dependents();
-  // the chunk-attention kernel's work counter; that kernel starts only once
-  // this one has completed, and the previous forward's is long done
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.next_unit = 0;
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
@@ -278,7 +339,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         st.finish(b, &tmC, n0 + c0, batch * p.s + row0);
       }
     }
-    st.drain();
+    st.drain();  // this warp's bulk stores are complete
+    if (lane == 0) {
+      fence_proxy_async_global();
+      __threadfence();
+    }
   }
 
   tc_fence_before();
@@ -287,6 +352,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+
+  // ------------------------------------------------ grid barrier, then scan
+  // Every CTA arrives, also after a timeout, so that the others are not
+  // left waiting; a CTA that gave up skips the scan and reports ETIMEOUT.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    red_release_gpu_add(p.grid_bar, 1);
+    const uint64_t t0 = globaltimer();
+    while (ld_acquire_gpu(p.grid_bar) < (int)gridDim.x) {
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        raise_timeout(sm, p.status);
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
+  if (!sm->abort_flag) scan_states(p);
 }
 
 template <bool A_MN>
@@ -310,14 +393,14 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
 GemmParams base_params(const Problem &pr) {
   GemmParams p = {};
   p.status = pr.status;
-  p.next_unit = pr.status + kNextUnitWord;
+  p.grid_bar = pr.status + kGridBarrierWord;
   p.s = pr.s;
   return p;
 }
 
 }  // namespace
 
-cudaError_t tc_chunk_state_bf16(const Problem &pr) {
+cudaError_t tc_chunk_state_scan_bf16(const Problem &pr) {
   // batch = chunk (b*G + g): State[chunk] = K_lin[chunk rows]^T V[chunk rows]
   const __nv_bfloat16 *Kl = (const __nv_bfloat16 *)pr.heads + 3 * pr.M * pr.s;
   CUtensorMap tmA, tmB, tS;
@@ -334,6 +417,13 @@ cudaError_t tc_chunk_state_bf16(const Problem &pr) {
   p.n_tiles = (pr.e + BN - 1) / BN;
   p.total_tiles = pr.B * pr.G * p.n_tiles;
   p.k_rows_per_batch = pr.C;
+  p.state8 = (const uint4 *)pr.state;
+  p.prefix8 = (uint4 *)pr.prefix;
+  p.B = pr.B;
+  p.G = pr.G;
+  p.causal = pr.causal;
+  p.se8 = (long long)pr.s * pr.e / 8;  // s == 128
+  p.lin_scale = pr.lin_scale;
   return launch<true>(tmA, tmB, tS, p, pr);
 }
 

@@ -56,6 +56,7 @@ struct Params {
   int M_tokens;
   int e, s;
   int *status;
+  int *sched;  // projection: the scheduling words of the workspace, zeroed here
 };
 
 struct Smem {
@@ -168,6 +169,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   // setup above overlaps the previous kernel's tail; its outputs are read below
   griddep_wait();
   griddep_launch_dependents();
+  // The chunk-state kernel's grid barrier and the chunk-attention kernel's
+  // work counter start from zero.  Both kernels touch them only after this
+  // grid has completed (the first after its griddepcontrol.wait, the second
+  // once every CTA of the first has passed that wait), and the previous
+  // forward's kernels had all completed before this one got past its wait.
+  if (EPI == EPI_PROJ && blockIdx.x == 0 && threadIdx.x == 0) {
+    p.sched[kNextUnitWord] = 0;
+    p.sched[kGridBarrierWord] = 0;
+  }
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int first = blockIdx.x / 2, step = gridDim.x / 2;
@@ -398,6 +408,7 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   Params p = base_params(pr, N, pr.d);
   p.gamma = pr.gamma;
   p.beta = pr.beta;
+  p.sched = pr.status;
   return launch<EPI_PROJ>(tmA, tmB, tU, tV, tH, p, pr);
 }
 
