@@ -58,7 +58,8 @@ class Weights(ctypes.Structure):
 
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("total_bytes", "status", "U", "V", "heads", "state", "prefix", "gated")]
+                ("total_bytes", "status", "U", "V", "heads", "state", "prefix", "gated",
+                 "bias")]
 
 
 class FlashGauError(RuntimeError):

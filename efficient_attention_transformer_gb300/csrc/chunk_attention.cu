@@ -25,7 +25,8 @@
 //              with P read from TMEM;
 //   warps 2-9  relu^2, two per TMEM lane quarter, each for 64 of a block's
 //              128 keys: read S with tcgen05.ld, compute relu^2(S/C + b)
-//              with the causal mask in registers, write P as packed bf16
+//              (the bias table carries the causal mask as -inf, written by
+//              the projection kernel), write P as packed bf16
 //              over the start of the same S columns with tcgen05.st (keys
 //              0-63 at packed columns 0-31, keys 64-127 at 64-95); the
 //              C x C scores never leave TMEM and registers;
@@ -91,7 +92,7 @@ struct AttnParams {
   int C, G, causal;
   int n_et, n_qt, total;  // units (chunk, query tile, value tile), value tile fastest
   float inv_c;
-  const float *relpos;
+  const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
 };
@@ -142,15 +143,15 @@ struct Ring {
 
 // Half `half` (64 keys) of one 128-key block of the local term, for this
 // thread's query row r (row i = qt*128 + r of the chunk): reads the 64 S
-// columns (fp32) at sbuf + 64*half, writes P = relu^2(S/C + b), masked, as
-// 32 packed bf16 columns over the start of those same columns.  All 64 S
-// values are in registers before the first store lands.
+// columns (fp32) at sbuf + 64*half, writes P = relu^2(S/C + b) as 32 packed
+// bf16 columns over the start of those same columns.  The bias table holds
+// -inf at the causally masked offsets, so the mask costs nothing here.  All
+// 64 S values are in registers before the first store lands.
 __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, int kb, int qt,
                                            int r, int half) {
   const int i = qt * QT + r;
-  const bool diag = p.causal && kb == qt;
   const int c0 = half * 64;
-  const float *bias_row = p.relpos + (kb * KB + c0 - i + p.C - 1);  // + key index j
+  const float *bias_row = p.bias + (kb * KB + c0 - i + p.C - 1);  // + key index j
   uint32_t va[32], vb[32];
   tmem_ld32(sbuf + c0, va);
   tmem_ld32(sbuf + c0 + 32, vb);
@@ -166,10 +167,6 @@ __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, i
     x1 = fmaxf(x1, 0.f);
     x0 *= x0;
     x1 *= x1;
-    if (diag) {
-      if (c0 + j > r) x0 = 0.f;
-      if (c0 + j + 1 > r) x1 = 0.f;
-    }
     if (j < 32) lo[j / 2] = pack_bf16(x0, x1);
     else hi[(j - 32) / 2] = pack_bf16(x0, x1);
   }
@@ -571,7 +568,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.n_qt = pr.C / QT;
   p.total = pr.B * pr.G * p.n_qt * p.n_et;
   p.inv_c = 1.0f / (float)pr.C;
-  p.relpos = pr.relpos;
+  p.bias = pr.bias;
   p.status = pr.status;
   p.next_unit = pr.status + kNextUnitWord;
   const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;

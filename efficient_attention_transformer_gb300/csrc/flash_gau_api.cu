@@ -92,6 +92,8 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   off = align_up(off + (causal ? (size_t)B * G : (size_t)B) * s * e * io);
   L->gated = off;
   off = align_up(off + M * e * io);
+  L->bias = off;
+  off = align_up(off + (2 * (size_t)C - 1) * sizeof(float));
   L->total_bytes = off;
   return FLASH_GAU_OK;
 }
@@ -209,6 +211,7 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, in
   p.state = ws + L.state;
   p.prefix = ws + L.prefix;
   p.gated = ws + L.gated;
+  p.bias = reinterpret_cast<float *>(ws + L.bias);
   p.stream = (cudaStream_t)stream;
   p.num_sms = num_sms;
 
@@ -264,6 +267,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 100; }
+int flash_gau_version(void) { return 101; }
 
 }  // extern "C"

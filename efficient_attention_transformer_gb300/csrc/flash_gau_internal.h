@@ -29,6 +29,7 @@ struct Problem {
   void *state;  // [B, G, s, e] io type
   void *prefix;
   void *gated;
+  float *bias;  // [2C-1] relpos, causal entries of offset j-i >= 1 set to -inf
   cudaStream_t stream;
   int num_sms;
 };

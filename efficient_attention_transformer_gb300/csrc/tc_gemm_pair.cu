@@ -57,6 +57,10 @@ struct Params {
   int e, s;
   int *status;
   int *sched;  // projection: the scheduling words of the workspace, zeroed here
+  // projection: the attention kernel's bias table, written here
+  const float *relpos;
+  float *bias;
+  int C, causal;
 };
 
 struct Smem {
@@ -174,9 +178,16 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   // grid has completed (the first after its griddepcontrol.wait, the second
   // once every CTA of the first has passed that wait), and the previous
   // forward's kernels had all completed before this one got past its wait.
-  if (EPI == EPI_PROJ && blockIdx.x == 0 && threadIdx.x == 0) {
-    p.sched[kNextUnitWord] = 0;
-    p.sched[kGridBarrierWord] = 0;
+  if (EPI == EPI_PROJ && blockIdx.x == 0) {
+    if (threadIdx.x == 0) {
+      p.sched[kNextUnitWord] = 0;
+      p.sched[kGridBarrierWord] = 0;
+    }
+    // The relative-position bias as the attention kernel reads it.  Causal:
+    // an offset j - i >= 1 (a later key) gets -inf, so that relu^2(S/C + b)
+    // is exactly 0 there and no separate mask is applied.
+    for (int k = threadIdx.x; k < 2 * p.C - 1; k += blockDim.x)
+      p.bias[k] = (p.causal && k >= p.C) ? -INFINITY : p.relpos[k];
   }
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
@@ -409,6 +420,10 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   p.gamma = pr.gamma;
   p.beta = pr.beta;
   p.sched = pr.status;
+  p.relpos = pr.relpos;
+  p.bias = pr.bias;
+  p.C = pr.C;
+  p.causal = pr.causal;
   return launch<EPI_PROJ>(tmA, tmB, tU, tV, tH, p, pr);
 }
 

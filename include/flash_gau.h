@@ -91,6 +91,9 @@ typedef struct flash_gau_workspace_layout {
   size_t prefix;        /* causal [B, G, s, e], non-causal [B, s, e], io:
                            lin_scale * (exclusive / total) chunk-state sum  */
   size_t gated;         /* [B*T, e] io: U * (Vq + Vl)                       */
+  size_t bias;          /* [2C-1] fp32: relpos as the bf16 attention kernel
+                           reads it; causal: the entries of offset j-i >= 1
+                           are -inf, so relu^2 applies the causal mask      */
 } flash_gau_workspace_layout;
 
 /* Supported shapes.  All types: B, T, C, d, e, s > 0 and T % C == 0.
