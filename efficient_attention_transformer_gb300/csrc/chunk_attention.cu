@@ -16,10 +16,9 @@
 // when causal.  Because relu^2 has no row normalisation, the products of
 // successive key blocks simply add into one accumulator.
 //
-// Roles (448 threads):
-//   warp 0     TMA producer: Q_quad, Q_lin, the K_quad ring, and a ring of
-//              64-row x 128-column B operands (prefix state rows, then V
-//              rows);
+// Roles (576 threads):
+//   warp 0     TMA producer: Q_lin, and one ring carrying Q_quad, K_quad,
+//              V and prefix state tiles in the order the MMAs consume them;
 //   warp 1     MMA issuer: S = Q_quad K_quad^T into a 128-column TMEM
 //              buffer (two buffers), acc = Q_lin Prefix (smem A), acc += P V
 //              with P read from TMEM;
@@ -30,13 +29,16 @@
 //              over the start of the same S columns with tcgen05.st (keys
 //              0-63 at packed columns 0-31, keys 64-127 at 64-95); the
 //              C x C scores never leave TMEM and registers;
-//   warps 10-13 epilogue: gated = U * acc, U boxes TMA-loaded into per-warp
-//              double buffers, the product written in place and TMA-stored.
+//   warps 10-17 epilogue: gated = U * acc, two warps per TMEM lane quarter
+//              (one per 64-column half of a value tile); U boxes TMA-loaded
+//              into per-warp double buffers one value tile ahead, the
+//              product written in place and TMA-stored.
 // Two accumulators alternate between units, so while the epilogue warps
 // drain one, the MMAs of the next unit already fill the other.
 //
-// Shared memory (224 KB): Q_quad 32 KB, Q_lin 32 KB, K ring 2 x 32 KB,
-// B ring 4 x 16 KB, epilogue boxes 4 warps x 2 x 4 KB.  TMEM: accumulators
+// Shared memory (224 KB): Q_lin 32 KB, one ring of 8 x 16 KB stages for
+// Q_quad and K_quad atoms and V / prefix half-blocks, epilogue boxes
+// 8 warps x 2 x 4 KB.  TMEM: accumulators
 // at columns 0 and 128, S/P buffers at 256 and 384 (128 columns each).
 #include <cuda_bf16.h>
 
@@ -54,33 +56,33 @@ constexpr int KB = 128;  // keys per block
 constexpr int ET = 128;  // value columns per unit
 constexpr int SD = 128;  // head width s
 constexpr int RELU_WARPS = 8;
-constexpr int NUM_THREADS = 32 * (2 + RELU_WARPS + 4);
+constexpr int EPI_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (2 + RELU_WARPS + EPI_WARPS);
 
-constexpr int ATOM_BYTES = 128 * 64 * 2;        // 128 rows x 64 bf16: 16 KB
-constexpr int Q_BYTES = 2 * ATOM_BYTES;         // 32 KB
-constexpr int K_STAGE_BYTES = 2 * ATOM_BYTES;   // 128 keys x 128: 32 KB
-constexpr int B_BOX_BYTES = 64 * 64 * 2;        // 64 rows x 64 columns: 8 KB
-constexpr int B_STAGES = 4;
-constexpr int B_STAGE_BYTES = 2 * B_BOX_BYTES;  // 64 rows x 128 columns: 16 KB
-constexpr int E_BOX_BYTES = 32 * 128;           // 32 rows x 64 bf16: 4 KB
+constexpr int ATOM_BYTES = 128 * 64 * 2;  // 128 rows x 64 bf16: 16 KB
+constexpr int Q_BYTES = 2 * ATOM_BYTES;   // 32 KB
+constexpr int B_BOX_BYTES = 64 * 64 * 2;  // 64 rows x 64 columns: 8 KB
+// One ring of 16 KB stages carries every streamed operand in the MMA
+// issuer's order: a Q_quad or K_quad atom (128 rows x 64 columns) or half
+// of a V / prefix block (64 rows x 128 columns, two 64 x 64 boxes).
+constexpr int STAGE_BYTES = 16 * 1024;
+constexpr int RING = 8;
+constexpr int E_BOX_BYTES = 32 * 128;     // 32 rows x 64 bf16: 4 KB
 
-constexpr int OFF_QQ = 0;
-constexpr int OFF_QL = OFF_QQ + Q_BYTES;
-constexpr int OFF_K = OFF_QL + Q_BYTES;
-constexpr int OFF_B = OFF_K + 2 * K_STAGE_BYTES;
-constexpr int OFF_E = OFF_B + B_STAGES * B_STAGE_BYTES;
-constexpr int TILE_BYTES = OFF_E + 4 * 2 * E_BOX_BYTES;  // 224 KB
+constexpr int OFF_QL = 0;
+constexpr int OFF_RING = OFF_QL + Q_BYTES;
+constexpr int OFF_E = OFF_RING + RING * STAGE_BYTES;
+constexpr int TILE_BYTES = OFF_E + EPI_WARPS * 2 * E_BOX_BYTES;  // 224 KB
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 512;
 
 constexpr uint32_t TM_ACC = 0, TM_S = 256;
 
 struct Bars {
-  uint64_t q_full, q_empty, ql_full, ql_empty;
-  uint64_t k_full[2], k_empty[2];
-  uint64_t b_full[B_STAGES], b_empty[B_STAGES];
+  uint64_t ql_full, ql_empty;
+  uint64_t full[RING], empty[RING];
   uint64_t s_full[2], p_full[2], sb_free[2];
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t u_full[4][2];
+  uint64_t u_full[EPI_WARPS][2];
   uint64_t uq_full[4], uq_empty[4];  // unit-index queue
   volatile int unit_q[4];
   uint64_t drain;
@@ -90,7 +92,9 @@ struct Bars {
 
 struct AttnParams {
   int C, G, causal;
-  int n_et, n_qt, total;  // units (chunk, query tile, value tile), value tile fastest
+  int n_et, n_qt;  // value tiles (128 columns of e), query tiles per chunk
+  int ng, n_vg;    // value tiles per unit, value-tile groups
+  int total;       // units (chunk, query tile, value-tile group), group fastest
   float inv_c;
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
@@ -99,21 +103,27 @@ struct AttnParams {
 
 // Agents that consume each queued unit index: the MMA thread, the relu^2
 // warps and the epilogue warps (one arrival per warp).
-constexpr int QUEUE_AGENTS = 1 + 8 + 4;
+constexpr int QUEUE_AGENTS = 1 + RELU_WARPS + EPI_WARPS;
 
 struct Unit {
-  int chunk, b, qt, et, nkb;
-  long long tok0;  // first token of the chunk
+  int chunk, b, qt, et0, nkb;  // et0: first value tile of the group
+  long long tok0;              // first token of the chunk
+  // Q_quad comes through the ring once per unit and stays until its last S
+  // when the unit's last K block (ring position 4 (nkb - 1) + 1, counting
+  // from Q) lands before the ring wraps onto Q; longer units load Q_quad
+  // with every K block instead.
+  bool q_per_block;
 };
 
 __device__ __forceinline__ Unit unit_of(const AttnParams &p, int u) {
   Unit x;
-  x.et = u % p.n_et;
-  x.qt = p.n_qt - 1 - (u / p.n_et) % p.n_qt;  // more key blocks first
-  x.chunk = u / (p.n_et * p.n_qt);
+  x.et0 = (u % p.n_vg) * p.ng;
+  x.qt = p.n_qt - 1 - (u / p.n_vg) % p.n_qt;  // more key blocks first
+  x.chunk = u / (p.n_vg * p.n_qt);
   x.b = x.chunk / p.G;
   x.tok0 = (long long)x.chunk * p.C;
   x.nkb = p.causal ? x.qt + 1 : p.C / KB;
+  x.q_per_block = 4 * (x.nkb - 1) + 1 >= RING;
   return x;
 }
 
@@ -190,23 +200,19 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   const volatile int *abort = &bar->abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar->q_full), 1);
-    mbar_init(smem_u32(&bar->q_empty), 1);
     mbar_init(smem_u32(&bar->ql_full), 1);
     mbar_init(smem_u32(&bar->ql_empty), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar->k_full[i]), 1);
-      mbar_init(smem_u32(&bar->k_empty[i]), 1);
       mbar_init(smem_u32(&bar->acc_full[i]), 1);
-      mbar_init(smem_u32(&bar->acc_empty[i]), 128);
+      mbar_init(smem_u32(&bar->acc_empty[i]), 32 * EPI_WARPS);
       mbar_init(smem_u32(&bar->s_full[i]), 1);
       mbar_init(smem_u32(&bar->p_full[i]), 32 * RELU_WARPS);
       mbar_init(smem_u32(&bar->sb_free[i]), 1);
-      for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&bar->u_full[w][i]), 1);
+      for (int w = 0; w < EPI_WARPS; ++w) mbar_init(smem_u32(&bar->u_full[w][i]), 1);
     }
-    for (int i = 0; i < B_STAGES; ++i) {
-      mbar_init(smem_u32(&bar->b_full[i]), 1);
-      mbar_init(smem_u32(&bar->b_empty[i]), 1);
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(smem_u32(&bar->full[i]), 1);
+      mbar_init(smem_u32(&bar->empty[i]), 1);
     }
     for (int q = 0; q < 4; ++q) {
       mbar_init(smem_u32(&bar->uq_full[q]), 1);
@@ -241,29 +247,29 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
+    // Stages in the MMA issuer's order: per unit, Q_quad (two atoms) and
+    // K block 0 (two atoms); then per value tile of the group, per key
+    // block, the next K block (first value tile only, one block ahead of
+    // its S; preceded by Q_quad again for units that stream it per block)
+    // and the block's V rows (two halves), then the value tile's prefix
+    // state rows (two halves).  Q_lin, read by every value tile of the
+    // unit, has a buffer of its own.
     if (elect_one()) {
-      Ring kr(2), br(B_STAGES);
+      Ring rr(RING);
       bool ok = true;
-      auto load_k = [&](long long krow) -> bool {
-        if (!mbar_wait(smem_u32(&bar->k_empty[kr.stage]), kr.phase ^ 1, abort)) return false;
-        const uint32_t f = smem_u32(&bar->k_full[kr.stage]);
-        uint8_t *dst = tiles + OFF_K + kr.stage * K_STAGE_BYTES;
-        mbar_arrive_expect_tx(f, K_STAGE_BYTES);
-        tma_load_2d(smem_u32(dst), &tmKq, f, 0, (int)krow);
-        tma_load_2d(smem_u32(dst + ATOM_BYTES), &tmKq, f, 64, (int)krow);
-        kr.next();
+      // one stage: nbox boxes of map tm at columns x0, x0 + 64, .., row
+      auto load = [&](const CUtensorMap *tm, int nbox, int x0, long long row) -> bool {
+        if (!mbar_wait(smem_u32(&bar->empty[rr.stage]), rr.phase ^ 1, abort)) return false;
+        const uint32_t f = smem_u32(&bar->full[rr.stage]);
+        uint8_t *dst = tiles + OFF_RING + rr.stage * STAGE_BYTES;
+        mbar_arrive_expect_tx(f, STAGE_BYTES);
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(smem_u32(dst + j * (STAGE_BYTES / nbox)), tm, f, x0 + j * 64, (int)row);
+        rr.next();
         return true;
       };
-      auto load_b = [&](const CUtensorMap *tm, int col0, long long row) -> bool {
-        if (!mbar_wait(smem_u32(&bar->b_empty[br.stage]), br.phase ^ 1, abort)) return false;
-        const uint32_t f = smem_u32(&bar->b_full[br.stage]);
-        uint8_t *dst = tiles + OFF_B + br.stage * B_STAGE_BYTES;
-        mbar_arrive_expect_tx(f, B_STAGE_BYTES);
-#pragma unroll
-        for (int j = 0; j < ET / 64; ++j)
-          tma_load_2d(smem_u32(dst + j * B_BOX_BYTES), tm, f, col0 + j * 64, (int)row);
-        br.next();
-        return true;
+      auto load_atoms = [&](const CUtensorMap *tm, long long row) -> bool {
+        return load(tm, 1, 0, row) && load(tm, 1, 64, row);
       };
       // next unit: from the global counter, announced through the queue
       auto push = [&](int q, int u) -> bool {
@@ -273,8 +279,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         return true;
       };
       bool prefix_ready = false;
-      int i = 0;
-      for (;; ++i) {
+      for (int i = 0;; ++i) {
         int u = atomicAdd(p.next_unit, 1);
         if (u >= p.total) u = -1;
         ok = push(i, u);
@@ -282,31 +287,33 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const Unit x = unit_of(p, u);
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
-        ok = mbar_wait(smem_u32(&bar->q_empty), (i & 1) ^ 1, abort);
-        if (!ok) break;
-        uint32_t f = smem_u32(&bar->q_full);
-        mbar_arrive_expect_tx(f, Q_BYTES);
-        tma_load_2d(smem_u32(tiles + OFF_QQ), &tmQq, f, 0, (int)qrow);
-        tma_load_2d(smem_u32(tiles + OFF_QQ + ATOM_BYTES), &tmQq, f, 64, (int)qrow);
-        ok = load_k(x.tok0);
-        for (int kb = 0; ok && kb < x.nkb; ++kb) {
-          if (kb + 1 < x.nkb) ok = load_k(x.tok0 + (kb + 1) * KB);
-          ok = ok && load_b(&tmV, x.et * ET, x.tok0 + kb * KB) &&
-               load_b(&tmV, x.et * ET, x.tok0 + kb * KB + 64);
+        ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
+        for (int t = 0; ok && t < p.ng; ++t) {
+          const int col = (x.et0 + t) * ET;
+          for (int kb = 0; ok && kb < x.nkb; ++kb) {
+            if (t == 0 && kb + 1 < x.nkb)
+              ok = (!x.q_per_block || load_atoms(&tmQq, qrow)) &&
+                   load_atoms(&tmKq, x.tok0 + (kb + 1) * KB);
+            ok = ok && load(&tmV, 2, col, x.tok0 + kb * KB) &&
+                 load(&tmV, 2, col, x.tok0 + kb * KB + 64);
+          }
+          if (ok && t == 0) {
+            // the global term last: the prefix states come from the kernel
+            // launched just before this one, which may still be running
+            if (!prefix_ready) {
+              griddep_wait();
+              prefix_ready = true;
+            }
+            ok = mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
+            if (!ok) break;
+            const uint32_t f = smem_u32(&bar->ql_full);
+            mbar_arrive_expect_tx(f, Q_BYTES);
+            tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
+            tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
+          }
+          ok = ok && load(&tmPre, 2, col, pre_row0) && load(&tmPre, 2, col, pre_row0 + 64);
         }
-        // the global term last: the prefix states come from the kernel
-        // launched just before this one, which may still be running
-        if (ok && !prefix_ready) {
-          griddep_wait();
-          prefix_ready = true;
-        }
-        ok = ok && mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
         if (!ok) break;
-        f = smem_u32(&bar->ql_full);
-        mbar_arrive_expect_tx(f, Q_BYTES);
-        tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
-        tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
-        ok = load_b(&tmPre, x.et * ET, pre_row0) && load_b(&tmPre, x.et * ET, pre_row0 + 64);
       }
       if (!ok) raise_timeout(bar, p.status);
     }
@@ -315,59 +322,75 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     if (elect_one()) {
       const uint32_t idesc_s = idesc_bf16_f32(128, KB, 0, 0);
       const uint32_t idesc_v = idesc_bf16_f32(128, ET, 0, 1);
-      const uint64_t dq = sw128_desc(smem_u32(tiles + OFF_QQ), 16, 1024);
       const uint32_t sQL = smem_u32(tiles + OFF_QL);
-      const uint32_t sK = smem_u32(tiles + OFF_K);
-      const uint32_t sB = smem_u32(tiles + OFF_B);
-      Ring kr(2), br(B_STAGES);
+      const uint32_t sRing = smem_u32(tiles + OFF_RING);
+      Ring rr(RING);
       int n = 0;  // S blocks issued so far (all units): buffer n & 1
-      uint32_t acc_col = TM_ACC;  // accumulator of the current unit
+      int v = 0;  // value tiles issued so far (all units): accumulator v & 1
+      uint32_t acc_col = TM_ACC;  // accumulator of the current value tile
+      int q_stage[2] = {0, 0};    // ring stages of the unit's Q_quad atoms
       bool ok = true;
-      // S[n] = Q_quad K_quad^T into TMEM buffer n & 1
-      auto issue_s = [&]() -> bool {
+      // the next ring stage, once full: its index
+      auto next_stage = [&](int &st) -> bool {
+        if (!mbar_wait(smem_u32(&bar->full[rr.stage]), rr.phase, abort)) return false;
+        st = rr.stage;
+        rr.next();
+        return true;
+      };
+      auto stage_addr = [&](int st) -> uint32_t { return sRing + st * STAGE_BYTES; };
+      // S[n] = Q_quad K_quad^T into TMEM buffer n & 1.  Q_quad's atoms come
+      // from the ring with the unit's first S and stay until its last, or
+      // come with every S (q_per_block).
+      auto issue_s = [&](bool q_new, bool q_done) -> bool {
         const int sb = n & 1;
         if (n >= 2 && !mbar_wait(smem_u32(&bar->sb_free[sb]), ((n >> 1) - 1) & 1, abort))
           return false;
-        if (!mbar_wait(smem_u32(&bar->k_full[kr.stage]), kr.phase, abort)) return false;
+        if (q_new && !(next_stage(q_stage[0]) && next_stage(q_stage[1]))) return false;
+        int k_stage[2];
+        if (!(next_stage(k_stage[0]) && next_stage(k_stage[1]))) return false;
         tc_fence_after();
-        const uint64_t dk = sw128_desc(sK + kr.stage * K_STAGE_BYTES, 16, 1024);
 #pragma unroll
         for (int k = 0; k < SD / 16; ++k) {
-          const uint32_t off = (k >> 2) * ATOM_BYTES + (k & 3) * 32;
-          mma_f16_ss(tmem + TM_S + sb * KB, desc_advance(dq, off), desc_advance(dk, off), idesc_s,
-                     k != 0);
+          const uint64_t dq = sw128_desc(stage_addr(q_stage[k >> 2]), 16, 1024);
+          const uint64_t dk = sw128_desc(stage_addr(k_stage[k >> 2]), 16, 1024);
+          mma_f16_ss(tmem + TM_S + sb * KB, desc_advance(dq, (k & 3) * 32),
+                     desc_advance(dk, (k & 3) * 32), idesc_s, k != 0);
         }
-        mma_commit(smem_u32(&bar->k_empty[kr.stage]));
+        mma_commit(smem_u32(&bar->empty[k_stage[0]]));
+        mma_commit(smem_u32(&bar->empty[k_stage[1]]));
         mma_commit(smem_u32(&bar->s_full[sb]));
-        kr.next();
+        if (q_done) {
+          mma_commit(smem_u32(&bar->empty[q_stage[0]]));
+          mma_commit(smem_u32(&bar->empty[q_stage[1]]));
+        }
         ++n;
         return true;
       };
       // acc (+)= A * B stage, A a 64-wide K-major atom in shared memory
       auto issue_b_smem = [&](uint32_t a_atom, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
+        int st;
+        if (!next_stage(st)) return false;
         tc_fence_after();
         const uint64_t da = sw128_desc(a_atom, 16, 1024);
-        const uint64_t db = sw128_desc(sB + br.stage * B_STAGE_BYTES, B_BOX_BYTES, 1024);
+        const uint64_t db = sw128_desc(stage_addr(st), B_BOX_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_f16_ss(tmem + acc_col, desc_advance(da, k * 32), desc_advance(db, k * 2048), idesc_v,
                      !(first && k == 0));
-        mma_commit(smem_u32(&bar->b_empty[br.stage]));
-        br.next();
+        mma_commit(smem_u32(&bar->empty[st]));
         return true;
       };
       // acc += P * B stage, P: 64 keys = 32 packed columns of TMEM at a_col
       auto issue_b_tmem = [&](uint32_t a_col, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&bar->b_full[br.stage]), br.phase, abort)) return false;
+        int st;
+        if (!next_stage(st)) return false;
         tc_fence_after();
-        const uint64_t db = sw128_desc(sB + br.stage * B_STAGE_BYTES, B_BOX_BYTES, 1024);
+        const uint64_t db = sw128_desc(stage_addr(st), B_BOX_BYTES, 1024);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_f16_ts(tmem + acc_col, tmem + a_col + k * 8, desc_advance(db, k * 2048), idesc_v,
                      !(first && k == 0));
-        mma_commit(smem_u32(&bar->b_empty[br.stage]));
-        br.next();
+        mma_commit(smem_u32(&bar->empty[st]));
         return true;
       };
       for (int i = 0; ok; ++i) {
@@ -378,34 +401,40 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         }
         const Unit x = unit_of(p, u);
         const int n0 = n;
-        ok = mbar_wait(smem_u32(&bar->q_full), i & 1, abort) && issue_s();
-        if (ok && x.nkb == 1) mma_commit(smem_u32(&bar->q_empty));
-        // this unit's accumulator must have been drained by the epilogue of
-        // the unit two before
-        acc_col = TM_ACC + (i & 1) * ET;
-        ok = ok && mbar_wait(smem_u32(&bar->acc_empty[i & 1]), ((i >> 1) & 1) ^ 1, abort);
-        if (!ok) break;
-        tc_fence_after();
-        // local term first, global term (Q_lin Prefix) last
-        for (int kb = 0; ok && kb < x.nkb; ++kb) {
-          if (kb + 1 < x.nkb) {
-            ok = issue_s();
-            if (ok && kb + 2 == x.nkb) mma_commit(smem_u32(&bar->q_empty));
-          }
-          const int si = n0 + kb, sb = si & 1;
-          ok = ok && mbar_wait(smem_u32(&bar->p_full[sb]), (si >> 1) & 1, abort);
+        ok = issue_s(true, x.q_per_block || x.nkb == 1);
+        // P of the unit's key blocks stays in TMEM for all its value tiles
+        for (int t = 0; ok && t < p.ng; ++t, ++v) {
+          const bool last_t = t + 1 == p.ng;
+          // this value tile's accumulator must have been drained by the
+          // epilogue of the value tile two before
+          acc_col = TM_ACC + (v & 1) * ET;
+          ok = mbar_wait(smem_u32(&bar->acc_empty[v & 1]), ((v >> 1) & 1) ^ 1, abort);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pcol = TM_S + sb * KB;
-          ok = issue_b_tmem(pcol, kb == 0) && issue_b_tmem(pcol + 64, false);
-          if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
+          // local term first, global term (Q_lin Prefix) last
+          for (int kb = 0; ok && kb < x.nkb; ++kb) {
+            const int si = n0 + kb, sb = si & 1;
+            if (t == 0) {
+              if (kb + 1 < x.nkb)
+                ok = issue_s(x.q_per_block, x.q_per_block || kb + 2 == x.nkb);
+              ok = ok && mbar_wait(smem_u32(&bar->p_full[sb]), (si >> 1) & 1, abort);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const uint32_t pcol = TM_S + sb * KB;
+            ok = issue_b_tmem(pcol, kb == 0) && issue_b_tmem(pcol + 64, false);
+            if (ok && last_t) mma_commit(smem_u32(&bar->sb_free[sb]));
+          }
+          if (ok && t == 0) {
+            ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
+            if (ok) tc_fence_after();
+          }
+          ok = ok && issue_b_smem(sQL, false) && issue_b_smem(sQL + ATOM_BYTES, false);
+          if (!ok) break;
+          if (last_t) mma_commit(smem_u32(&bar->ql_empty));
+          mma_commit(smem_u32(&bar->acc_full[v & 1]));
         }
-        ok = ok && mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
         if (!ok) break;
-        tc_fence_after();
-        ok = issue_b_smem(sQL, false) && issue_b_smem(sQL + ATOM_BYTES, false);
-        if (ok) mma_commit(smem_u32(&bar->ql_empty));
-        if (ok) mma_commit(smem_u32(&bar->acc_full[i & 1]));
         release(i);
       }
       if (!ok) raise_timeout(bar, p.status);
@@ -444,50 +473,63 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     if (!ok) raise_timeout(bar, p.status);
   } else {
     // ------------------------------------------------------- epilogue
-    const int quarter = warp & 3, w = warp - (2 + RELU_WARPS);
+    // Two warps per TMEM lane quarter, one per 64-column half of every
+    // value tile.  A warp's two boxes alternate between value tiles: the U
+    // box of the next value tile is requested when the current one starts,
+    // the gated product is written over the current box and TMA-stored.
+    const int w = warp - (2 + RELU_WARPS);
+    const int quarter = warp & 3, half = w >> 2;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint8_t *ebuf = tiles + OFF_E + w * 2 * E_BOX_BYTES;
-    // U box of part j (64 value columns) of unit u into buffer b
-    auto load_u = [&](int u, int j, int b) {
+    // this warp's U box of value tile t of unit u into buffer b
+    auto load_u = [&](int u, int t, int b) {
       if (lane != 0 || u < 0) return;
       const Unit x = unit_of(p, u);
       const uint32_t f = smem_u32(&bar->u_full[w][b]);
       mbar_arrive_expect_tx(f, E_BOX_BYTES);
-      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, x.et * ET + j * 64,
+      tma_load_2d(smem_u32(ebuf + b * E_BOX_BYTES), &tmU, f, (x.et0 + t) * ET + half * 64,
                   (int)(x.tok0 + x.qt * QT + quarter * 32));
     };
     bool ok = true;
     int cur = pop(0);
     ok = cur != -2;
     load_u(cur, 0, 0);
-    load_u(cur, 1, 1);
-    int c = 0;
+    int v = 0;
     for (int i = 0; ok && cur >= 0; ++i) {
-      // the next unit's index, to prefetch its U boxes (released later)
-      const int nxt = pop(i + 1);
-      if (nxt == -2 ||
-          !mbar_wait(smem_u32(&bar->acc_full[i & 1]), (i >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
       const Unit x = unit_of(p, cur);
-      tc_fence_after();
       const int grow = (int)(x.tok0 + x.qt * QT + quarter * 32);
-      for (int j = 0; j < ET / 64; ++j, ++c) {
-        const int b = c & 1;
-        if (!mbar_wait(smem_u32(&bar->u_full[w][b]), (c >> 1) & 1, abort)) {
+      int nxt = -1;
+      for (int t = 0; ok && t < p.ng; ++t, ++v) {
+        const int b = v & 1;
+        // At the unit's last value tile, the next unit's index (released
+        // later).  Not earlier: the producer announces it only after all of
+        // this unit's loads, which need the earlier value tiles drained.
+        if (t + 1 == p.ng) {
+          nxt = pop(i + 1);
+          if (nxt == -2) {
+            ok = false;
+            break;
+          }
+        }
+        // the other box: its store (of the previous value tile) has read
+        // it, refill it with the next value tile's U
+        if (lane == 0) tma_store_wait_read<0>();
+        __syncwarp();
+        if (t + 1 < p.ng) load_u(cur, t + 1, b ^ 1);
+        else load_u(nxt, 0, b ^ 1);
+        if (!mbar_wait(smem_u32(&bar->acc_full[v & 1]), (v >> 1) & 1, abort) ||
+            !mbar_wait(smem_u32(&bar->u_full[w][b]), (v >> 1) & 1, abort)) {
           ok = false;
           break;
         }
+        tc_fence_after();
         uint32_t va[32], vb[32];
-        const uint32_t acc = tmem + lane_off + TM_ACC + (i & 1) * ET + j * 64;
+        const uint32_t acc = tmem + lane_off + TM_ACC + (v & 1) * ET + half * 64;
         tmem_ld32(acc, va);
         tmem_ld32(acc + 32, vb);
         tmem_ld_wait();
-        if (j == ET / 64 - 1) {
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bar->acc_empty[i & 1]));
-        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar->acc_empty[v & 1]));
         uint8_t *box = ebuf + b * E_BOX_BYTES;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -508,12 +550,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmG, smem_u32(box), x.et * ET + j * 64, grow);
+          tma_store_2d(&tmG, smem_u32(box), (x.et0 + t) * ET + half * 64, grow);
           tma_store_commit();
-          tma_store_wait_read<0>();  // the box is refilled next
         }
         __syncwarp();
-        load_u(nxt, j, b);
       }
       __syncwarp();
       if (lane == 0) release(i);
@@ -566,7 +606,19 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.causal = pr.causal;
   p.n_et = pr.e / ET;
   p.n_qt = pr.C / QT;
-  p.total = pr.B * pr.G * p.n_qt * p.n_et;
+  // Value tiles per unit: the unit's P is computed once and stays in TMEM
+  // for each of them, which takes a unit's key blocks fitting the two S/P
+  // buffers (C <= 256); else one.  As many as divide the value tiles while
+  // leaving about three units per SM for the dynamic scheduler to balance.
+  const long long tiles = (long long)pr.B * pr.G * p.n_qt * p.n_et;
+  p.ng = 1;
+  for (int ng : {4, 3, 2})
+    if (pr.C <= 2 * KB && p.n_et % ng == 0 && tiles / ng >= 3LL * pr.num_sms) {
+      p.ng = ng;
+      break;
+    }
+  p.n_vg = p.n_et / p.ng;
+  p.total = (int)(tiles / p.ng);
   p.inv_c = 1.0f / (float)pr.C;
   p.bias = pr.bias;
   p.status = pr.status;
