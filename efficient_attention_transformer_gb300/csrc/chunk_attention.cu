@@ -92,9 +92,15 @@ struct Bars {
 
 struct AttnParams {
   int C, G, causal;
-  int n_et, n_qt;  // value tiles (128 columns of e), query tiles per chunk
-  int ng, n_vg;    // value tiles per unit, value-tile groups
-  int total;       // units (chunk, query tile, value-tile group), group fastest
+  int n_et, n_qt;   // value tiles (128 columns of e), query tiles per chunk
+  int ng, n_vg;     // value tiles per grouped unit, groups per query tile
+  int n_grouped;    // units (chunk, query tile, group of ng value tiles) of
+                    // the first chunks, group fastest; after them, one
+                    // unit per value tile (chunk, query tile, value tile)
+                    // for the remaining chunks, so the schedule ends on
+                    // small pieces of work
+  int g_split;      // first chunk of the single-tile units
+  int total;
   float inv_c;
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
@@ -106,8 +112,8 @@ struct AttnParams {
 constexpr int QUEUE_AGENTS = 1 + RELU_WARPS + EPI_WARPS;
 
 struct Unit {
-  int chunk, b, qt, et0, nkb;  // et0: first value tile of the group
-  long long tok0;              // first token of the chunk
+  int chunk, b, qt, et0, ng, nkb;  // value tiles et0 .. et0 + ng - 1
+  long long tok0;                  // first token of the chunk
   // Q_quad comes through the ring once per unit and stays until its last S
   // when the unit's last K block (ring position 4 (nkb - 1) + 1, counting
   // from Q) lands before the ring wraps onto Q; longer units load Q_quad
@@ -117,9 +123,19 @@ struct Unit {
 
 __device__ __forceinline__ Unit unit_of(const AttnParams &p, int u) {
   Unit x;
-  x.et0 = (u % p.n_vg) * p.ng;
-  x.qt = p.n_qt - 1 - (u / p.n_vg) % p.n_qt;  // more key blocks first
-  x.chunk = u / (p.n_vg * p.n_qt);
+  int per_qt, chunk0 = 0;  // units per (chunk, query tile), first chunk
+  if (u < p.n_grouped) {
+    x.ng = p.ng;
+    per_qt = p.n_vg;
+  } else {
+    u -= p.n_grouped;
+    x.ng = 1;
+    per_qt = p.n_et;
+    chunk0 = p.g_split;
+  }
+  x.et0 = (u % per_qt) * x.ng;
+  x.qt = p.n_qt - 1 - (u / per_qt) % p.n_qt;  // more key blocks first
+  x.chunk = chunk0 + u / (per_qt * p.n_qt);
   x.b = x.chunk / p.G;
   x.tok0 = (long long)x.chunk * p.C;
   x.nkb = p.causal ? x.qt + 1 : p.C / KB;
@@ -288,7 +304,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
         ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
-        for (int t = 0; ok && t < p.ng; ++t) {
+        for (int t = 0; ok && t < x.ng; ++t) {
           const int col = (x.et0 + t) * ET;
           for (int kb = 0; ok && kb < x.nkb; ++kb) {
             if (t == 0 && kb + 1 < x.nkb)
@@ -403,8 +419,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const int n0 = n;
         ok = issue_s(true, x.q_per_block || x.nkb == 1);
         // P of the unit's key blocks stays in TMEM for all its value tiles
-        for (int t = 0; ok && t < p.ng; ++t, ++v) {
-          const bool last_t = t + 1 == p.ng;
+        for (int t = 0; ok && t < x.ng; ++t, ++v) {
+          const bool last_t = t + 1 == x.ng;
           // this value tile's accumulator must have been drained by the
           // epilogue of the value tile two before
           acc_col = TM_ACC + (v & 1) * ET;
@@ -499,12 +515,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       const Unit x = unit_of(p, cur);
       const int grow = (int)(x.tok0 + x.qt * QT + quarter * 32);
       int nxt = -1;
-      for (int t = 0; ok && t < p.ng; ++t, ++v) {
+      for (int t = 0; ok && t < x.ng; ++t, ++v) {
         const int b = v & 1;
         // At the unit's last value tile, the next unit's index (released
         // later).  Not earlier: the producer announces it only after all of
         // this unit's loads, which need the earlier value tiles drained.
-        if (t + 1 == p.ng) {
+        if (t + 1 == x.ng) {
           nxt = pop(i + 1);
           if (nxt == -2) {
             ok = false;
@@ -515,7 +531,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         // it, refill it with the next value tile's U
         if (lane == 0) tma_store_wait_read<0>();
         __syncwarp();
-        if (t + 1 < p.ng) load_u(cur, t + 1, b ^ 1);
+        if (t + 1 < x.ng) load_u(cur, t + 1, b ^ 1);
         else load_u(nxt, 0, b ^ 1);
         if (!mbar_wait(smem_u32(&bar->acc_full[v & 1]), (v >> 1) & 1, abort) ||
             !mbar_wait(smem_u32(&bar->u_full[w][b]), (v >> 1) & 1, abort)) {
@@ -609,16 +625,22 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   // Value tiles per unit: the unit's P is computed once and stays in TMEM
   // for each of them, which takes a unit's key blocks fitting the two S/P
   // buffers (C <= 256); else one.  As many as divide the value tiles while
-  // leaving about three units per SM for the dynamic scheduler to balance.
+  // leaving about two units per SM for the dynamic scheduler to balance.
   const long long tiles = (long long)pr.B * pr.G * p.n_qt * p.n_et;
   p.ng = 1;
   for (int ng : {4, 3, 2})
-    if (pr.C <= 2 * KB && p.n_et % ng == 0 && tiles / ng >= 3LL * pr.num_sms) {
+    if (pr.C <= 2 * KB && p.n_et % ng == 0 && tiles / ng >= 2LL * pr.num_sms) {
       p.ng = ng;
       break;
     }
   p.n_vg = p.n_et / p.ng;
-  p.total = (int)(tiles / p.ng);
+  // the last chunks as single-tile units: about one per SM
+  const int BG = pr.B * pr.G, per_chunk = p.n_qt * p.n_et;
+  int singles = p.ng > 1 ? (pr.num_sms + per_chunk - 1) / per_chunk : BG;
+  if (singles > BG) singles = BG;
+  p.g_split = BG - singles;
+  p.n_grouped = p.g_split * p.n_qt * p.n_vg;
+  p.total = p.n_grouped + singles * per_chunk;
   p.inv_c = 1.0f / (float)pr.C;
   p.bias = pr.bias;
   p.status = pr.status;
