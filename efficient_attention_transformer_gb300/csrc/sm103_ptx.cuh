@@ -120,6 +120,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
 
 // 2-D tiled load of one box into shared memory, completing on `bar`.
 // x is the innermost (contiguous) coordinate in elements, y the row.
+// Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing on
+// mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y) {
   asm volatile(

@@ -16,8 +16,10 @@
 // Once every CTA's state tiles are in memory (a grid barrier: the grid is at
 // most one CTA per SM and every CTA is resident before the next kernel can
 // start, so all of them arrive; the wait is bounded all the same), the same
-// CTAs scan the states, which are still in L2: one thread per 8 consecutive
-// state elements of a batch row, 16 chunks' loads in flight per thread.
+// CTAs scan the states, which are still in L2.  A work item is a range of
+// columns of one batch row for all G chunks: one bulk copy per chunk brings
+// it into the (now idle) tile buffers, then each thread runs the sums for 8
+// consecutive columns and writes the prefix states.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -66,6 +68,7 @@ struct Smem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
+  uint64_t scan_full;  // the scan phase's bulk copies of one work item
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -146,35 +149,48 @@ __device__ __forceinline__ uint4 scaled8(const float (&run)[8], float scale) {
   return w;
 }
 
-// Running sums over the chunks of each batch row, all CTAs together.  The
-// states were written by other CTAs of this grid, so they are read through
-// L2 (ld.global.cg), not the non-coherent path.
-__device__ void scan_states(const GemmParams &p) {
-  constexpr int DEPTH = 16;  // chunks in flight per thread
-  const long long ncol = (long long)p.B * p.se8;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < ncol;
-       idx += stride) {
-    const long long b = idx / p.se8, r = idx % p.se8;
-    const uint4 *st = p.state8 + b * p.G * p.se8 + r;
-    uint4 *pre = p.prefix8 + (p.causal ? b * p.G * p.se8 : b * p.se8) + r;
-    float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int g0 = 0; g0 < p.G; g0 += DEPTH) {
-      const int n = min(DEPTH, p.G - g0);
-      uint4 v[DEPTH];
-#pragma unroll
-      for (int k = 0; k < DEPTH; ++k)
-        if (k < n) v[k] = __ldcg(st + (long long)(g0 + k) * p.se8);
-#pragma unroll
-      for (int k = 0; k < DEPTH; ++k) {
-        if (k < n) {
-          if (p.causal) pre[(long long)(g0 + k) * p.se8] = scaled8(run, p.lin_scale);
-          add8(run, v[k]);
-        }
-      }
+// Running sums over the chunks of each batch row, all CTAs together.  Work
+// item = (batch row b, columns [r0, r0 + w) in 16-byte groups): thread 0
+// copies state[b][g][r0 .. r0 + w) for every chunk g into `buf` (G bulk
+// copies on one barrier), then the threads scan it column by column.  The
+// states were written by other CTAs of this grid (async-proxy stores,
+// ordered before the grid barrier); the caller fenced the async proxy after
+// the barrier.  Returns false (status ETIMEOUT) on a timed-out wait.
+__device__ bool scan_states(const GemmParams &p, uint8_t *buf, int buf_bytes, Smem *sm) {
+  // columns per item: the chunks' slices fit `buf`, and about one item per CTA
+  long long w = buf_bytes / (16LL * p.G);
+  const long long even = ((long long)p.B * p.se8 + gridDim.x - 1) / gridDim.x;
+  if (even < w) w = even;
+  if (w < 1) w = 1;
+  const long long per_b = (p.se8 + w - 1) / w, items = p.B * per_b;
+  const uint32_t bar = smem_u32(&sm->scan_full);
+  const uint4 *sbuf = reinterpret_cast<const uint4 *>(buf);
+  uint32_t phase = 0;
+  for (long long it = blockIdx.x; it < items; it += gridDim.x, phase ^= 1) {
+    const long long b = it / per_b, r0 = (it % per_b) * w;
+    const int wc = (int)min(w, p.se8 - r0);  // columns of this item
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)(p.G * wc * 16));
+      for (int g = 0; g < p.G; ++g)
+        bulk_load(smem_u32(buf + (size_t)g * wc * 16), p.state8 + (b * p.G + g) * p.se8 + r0,
+                  (uint32_t)(wc * 16), bar);
     }
-    if (!p.causal) *pre = scaled8(run, p.lin_scale);
+    // one thread waits; every thread sees its verdict after the barrier
+    if (threadIdx.x == 0 && !mbar_wait(bar, phase, &sm->abort_flag)) raise_timeout(sm, p.status);
+    __syncthreads();
+    if (sm->abort_flag) return false;
+    uint4 *pre = p.prefix8 + (p.causal ? b * p.G * p.se8 : b * p.se8) + r0;
+    for (int c = threadIdx.x; c < wc; c += blockDim.x) {
+      float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int g = 0; g < p.G; ++g) {
+        if (p.causal) pre[(long long)g * p.se8 + c] = scaled8(run, p.lin_scale);
+        add8(run, sbuf[g * wc + c]);
+      }
+      if (!p.causal) pre[c] = scaled8(run, p.lin_scale);
+    }
+    __syncthreads();  // the buffer is refilled by the next item
   }
+  return true;
 }
 
 // A_MN: A is stored M-contiguous (K_lin^T); otherwise K-contiguous.  tmC
@@ -199,6 +215,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(smem_u32(&sm->acc_empty[i]), 128);
     }
     mbar_init(smem_u32(&sm->drain), 1);
+    mbar_init(smem_u32(&sm->scan_full), 1);
     sm->abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -369,7 +386,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
   __syncthreads();
-  if (!sm->abort_flag) scan_states(p);
+  // the bulk copies below (async proxy) read what the barrier made visible
+  fence_proxy_async_global();
+  if (!sm->abort_flag) scan_states(p, tiles, TILE_BYTES, sm);
 }
 
 template <bool A_MN>
