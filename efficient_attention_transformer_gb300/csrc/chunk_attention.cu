@@ -303,6 +303,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const Unit x = unit_of(p, u);
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
+        const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
         ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
         for (int t = 0; ok && t < x.ng; ++t) {
           const int col = (x.et0 + t) * ET;
@@ -310,8 +311,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             if (t == 0 && kb + 1 < x.nkb)
               ok = (!x.q_per_block || load_atoms(&tmQq, qrow)) &&
                    load_atoms(&tmKq, x.tok0 + (kb + 1) * KB);
-            ok = ok && load(&tmV, 2, col, x.tok0 + kb * KB) &&
-                 load(&tmV, 2, col, x.tok0 + kb * KB + 64);
+            ok = ok && load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB, col, ncb)) &&
+                 load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB + 64, col, ncb));
           }
           if (ok && t == 0) {
             // the global term last: the prefix states come from the kernel
@@ -327,7 +328,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
             tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
           }
-          ok = ok && load(&tmPre, 2, col, pre_row0) && load(&tmPre, 2, col, pre_row0 + 64);
+          ok = ok && load(&tmPre, 1, 0, rb64_row(pre_row0, col, ncb)) &&
+               load(&tmPre, 1, 0, rb64_row(pre_row0 + 64, col, ncb));
         }
         if (!ok) break;
       }
@@ -600,11 +602,15 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
     return err;
   if ((err = make_tmap_bf16_2d(&tQl, heads + 2 * Ms, pr.M, pr.s, pr.s, QT, 64)) != cudaSuccess)
     return err;
-  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 64, 64)) != cudaSuccess) return err;
+  // V and the prefix states in 64 x 64 blocks (flat 128-byte rows): 64 rows
+  // of a value tile are one contiguous 128-row box
+  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M * pr.e / 64, 64, 64, 128, 64)) != cudaSuccess)
+    return err;
   if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tG, pr.gated, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   const long long pre_rows = (long long)(pr.causal ? pr.B * pr.G : pr.B) * pr.s;
-  if ((err = make_tmap_bf16_2d(&tPre, pr.prefix, pre_rows, pr.e, pr.e, 64, 64)) != cudaSuccess)
+  if ((err = make_tmap_bf16_2d(&tPre, pr.prefix, pre_rows * pr.e / 64, 64, 64, 128, 64)) !=
+      cudaSuccess)
     return err;
 
   static unsigned long long configured = 0;

@@ -267,6 +267,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 101; }
+int flash_gau_version(void) { return 102; }
 
 }  // extern "C"

@@ -39,6 +39,16 @@ struct Problem {
 // counter of the chunk-state kernel's grid barrier; the projection kernel
 // zeroes both.
 constexpr int kNextUnitWord = 16;
+
+// The bf16 path keeps V, the chunk states and the prefix states in 64 x 64
+// blocks, row-block-major: block (i, j) of a [rows, cols] matrix is 8 KB of
+// row-major data at block index i * (cols / 64) + j.  Seen as a flat matrix
+// of 128-byte rows ([rows * cols / 64, 64]), element (r, c) sits in flat row
+// rb64_row(r, c, cols / 64), column c % 64; 64 rows of 64 k adjacent column
+// blocks are 64 k consecutive flat rows, one contiguous TMA box.
+__host__ __device__ inline long long rb64_row(long long r, long long c, long long ncb) {
+  return ((r >> 6) * ncb + (c >> 6)) * 64 + (r & 63);
+}
 constexpr int kGridBarrierWord = 17;
 
 using StageFn = cudaError_t (*)(const Problem &);

@@ -264,9 +264,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           } else {
             tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, mt * BM);
           }
-          for (int j = 0; j < nboxes; ++j)
-            tma_load_2d(smem_u32(sB + j * B_BOX_BYTES), &tmB, full, n0 + j * 64,
-                        krow0 + kb * BK);
+          // V rows of this k-block, 64-blocked: the tile's column blocks
+          // are consecutive, one box of 64 * nboxes flat rows
+          tma_load_2d(smem_u32(sB), &tmB, full, 0,
+                      (int)rb64_row(krow0 + kb * BK, n0, p.N / 64));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -353,7 +354,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         pack64(ra, rb, [](float x, int) { return x; }, w);
         uint8_t *b = st.begin();
         st.put(b, w);
-        st.finish(b, &tmC, n0 + c0, batch * p.s + row0);
+        st.finish(b, &tmC, 0, (int)rb64_row(batch * p.s + row0, n0 + c0, p.N / 64));
       }
     }
     st.drain();  // this warp's bulk stores are complete
@@ -425,9 +426,13 @@ cudaError_t tc_chunk_state_scan_bf16(const Problem &pr) {
   CUtensorMap tmA, tmB, tS;
   cudaError_t err;
   if ((err = make_tmap_bf16_2d(&tmA, Kl, pr.M, pr.s, pr.s, BK, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tmB, pr.V, pr.M, pr.e, pr.e, BK, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tS, pr.state, (long long)pr.B * pr.G * pr.s, pr.e, pr.e, 32, 64)) !=
-      cudaSuccess)
+  // V and the states in 64 x 64 blocks (flat 128-byte rows): a k-block of V
+  // for a 256-column tile is one 256-row box, a state store one 32-row box
+  if (pr.e % BN != 0) return cudaErrorInvalidValue;
+  if ((err = make_tmap_bf16_2d(&tmB, pr.V, pr.M * pr.e / 64, 64, 64, BN, 64)) != cudaSuccess)
+    return err;
+  if ((err = make_tmap_bf16_2d(&tS, pr.state, (long long)pr.B * pr.G * pr.s * pr.e / 64, 64, 64,
+                               32, 64)) != cudaSuccess)
     return err;
   GemmParams p = base_params(pr);
   p.N = pr.e;

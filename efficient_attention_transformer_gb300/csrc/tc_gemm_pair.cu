@@ -317,7 +317,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint8_t *b = st.begin();
             st.put(b, w);
             if (n < p.e) st.finish(b, &tmC0, n, row0);
-            else st.finish(b, &tmC1, n - p.e, row0);
+            else st.finish(b, &tmC1, 0, (int)rb64_row(row0, n - p.e, p.e / 64));
           } else {
             const int c = n - 2 * p.e;  // column inside Z
 #pragma unroll
@@ -413,7 +413,9 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
-  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
+  // V in 64 x 64 blocks (flat 128-byte rows), 32-row store boxes
+  if ((err = make_tmap_bf16_2d(&tV, pr.V, pr.M * pr.e / 64, 64, 64, 32, 64)) != cudaSuccess)
+    return err;
   if ((err = make_tmap_bf16_2d(&tH, pr.heads, 4 * pr.M, pr.s, pr.s, 32, 64)) != cudaSuccess)
     return err;
   Params p = base_params(pr, N, pr.d);

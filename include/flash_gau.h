@@ -85,16 +85,23 @@ typedef struct flash_gau_workspace_layout {
                            the rest of its 256-byte slot is used by the
                            kernels for scheduling                            */
   size_t U;             /* [B*T, e] io: swish(X W_u)                        */
-  size_t V;             /* [B*T, e] io: swish(X W_v)                        */
+  size_t V;             /* [B*T, e] io: swish(X W_v)                 (*)    */
   size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
-  size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk          */
+  size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk   (*)    */
   size_t prefix;        /* causal [B, G, s, e], non-causal [B, s, e], io:
-                           lin_scale * (exclusive / total) chunk-state sum  */
+                           lin_scale * (exclusive / total) chunk-state sum
+                                                                      (*)   */
   size_t gated;         /* [B*T, e] io: U * (Vq + Vl)                       */
   size_t bias;          /* [2C-1] fp32: relpos as the bf16 attention kernel
                            reads it; causal: the entries of offset j-i >= 1
                            are -inf, so relu^2 applies the causal mask      */
 } flash_gau_workspace_layout;
+/* Intermediates are row-major, except those marked (*) for FLASH_GAU_BF16:
+ * these, seen as [rows, e] matrices (rows = B*T, B*G*s or B*s), are stored
+ * in 64 x 64 blocks, row-block-major: block (i, j) holds rows 64i..64i+63
+ * and columns 64j..64j+63 as 8 KB of row-major data, at block index
+ * i * (e / 64) + j.  Element (r, c) is at offset
+ * ((r / 64) * (e / 64) + c / 64) * 4096 + (r % 64) * 64 + c % 64.          */
 
 /* Supported shapes.  All types: B, T, C, d, e, s > 0 and T % C == 0.
  *   FP32: any such shape with s <= 128 and C <= 4096.

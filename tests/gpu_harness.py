@@ -55,7 +55,8 @@ class Case:
                          i["beta"], i["relpos"], self.C, self.causal, self.lin_scale)
 
     def intermediate(self, name):
-        """An intermediate read back from the workspace, as float64."""
+        """An intermediate read back from the workspace, as float64, in its
+        logical (row-major) shape."""
         tdt = torch_dtype(self.dtype)
         B, T, e, s, M = self.B, self.T, self.e, self.s, self.B * self.T
         G = T // self.C
@@ -64,11 +65,27 @@ class Case:
         shape = shapes[name]
         n = int(np.prod(shape))
         raw = self.workspace[self.layout[name]:]
-        t = raw[: n * (2 if tdt == torch.bfloat16 else 4)].view(tdt).view(shape)
-        return t.double().cpu().numpy()
+        t = raw[: n * (2 if tdt == torch.bfloat16 else 4)].view(tdt)
+        a = t.double().cpu().numpy()
+        if tdt == torch.bfloat16 and name in BLOCKED64:
+            rows = n // e
+            return unblock64(a, rows, e).reshape(shape)
+        return a.reshape(shape)
 
     def status(self):
         return bd.workspace_status(self.workspace)
+
+
+# bf16 intermediates kept in 64 x 64 blocks, row-block-major (see the
+# workspace layout in include/flash_gau.h)
+BLOCKED64 = ("V", "state", "prefix")
+
+
+def unblock64(flat, rows, cols):
+    """[rows, cols] from its 64 x 64-blocked storage: block (i, j) is the
+    row-major 64 x 64 tile at block index i * (cols / 64) + j."""
+    return (flat.reshape(rows // 64, cols // 64, 64, 64).transpose(0, 2, 1, 3)
+            .reshape(rows, cols))
 
 
 def rel_err(got, ref):
