@@ -132,26 +132,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-// 4-D tiled load (the 64 x 64-blocked maps): coordinates {x, y, z, w}.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                            int y, int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-
-// 4-D tiled store from shared memory (bulk group completion).
-__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int x, int y, int z,
-                                             int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y) {
   asm volatile(

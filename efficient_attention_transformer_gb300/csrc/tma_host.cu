@@ -48,25 +48,6 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t rows,
                    box_cols);
 }
 
-cudaError_t make_tmap_bf16_blocked(CUtensorMap *map, const void *base, uint64_t rows,
-                                   uint64_t cols, uint32_t box_rows, uint32_t box_cblocks) {
-  std::call_once(g_once, load_entry_point);
-  if (!g_encode) return cudaErrorNotSupported;
-  if (rows % 64 || cols % 64 || !(box_rows == 32 || box_rows % 64 == 0) || box_cblocks < 1 ||
-      (box_cblocks > 1 && box_rows != 64))
-    return cudaErrorInvalidValue;
-  cuuint64_t dims[4] = {64, 64, cols / 64, rows / 64};
-  cuuint64_t strides[3] = {64 * 2, 64 * 64 * 2, cols / 64 * 64 * 64 * 2};
-  cuuint32_t box[4] = {64, box_rows < 64 ? box_rows : 64, box_cblocks,
-                       box_rows < 64 ? 1 : box_rows / 64};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 cudaError_t make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                              uint64_t ld, uint32_t box_rows, uint32_t box_cols) {
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, cols, ld, box_rows,
