@@ -237,6 +237,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  // Batches (chunks) are visited last first: the projection wrote the last
+  // rows most recently, so their V and K_lin are still in L2; the attention
+  // kernel, which walks the chunks forward, then finds in L2 the V of the
+  // first chunks, read here last.
+  const int n_batches = p.total_tiles / tiles_per_batch;
+  auto batch_of = [&](int t) { return n_batches - 1 - t / tiles_per_batch; };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -244,7 +250,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x) {
-        const int batch = t / tiles_per_batch, rem = t % tiles_per_batch;
+        const int batch = batch_of(t), rem = t % tiles_per_batch;
         const int mt = rem / p.n_tiles, nt = rem % p.n_tiles;
         const int n0 = nt * BN, nboxes = min(BN, p.N - n0) / 64;
         const int krow0 = batch * p.k_rows_per_batch;
@@ -330,7 +336,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     Stager st{tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES, lane};
     int local = 0;
     for (int t = blockIdx.x; t < p.total_tiles && !sm->abort_flag; t += gridDim.x, ++local) {
-      const int batch = t / tiles_per_batch, rem = t % tiles_per_batch;
+      const int batch = batch_of(t), rem = t % tiles_per_batch;
       const int mt = rem / p.n_tiles, nt = rem % p.n_tiles;
       const int n0 = nt * BN, nsz = min(BN, p.N - n0);
       const int acc = local & 1;
