@@ -192,6 +192,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int first = blockIdx.x / 2, step = gridDim.x / 2;
+  // Pair tile t covers row pair row_pair(t), n-tile t % n_tiles.  The output
+  // projection walks the rows last first: the attention kernel wrote the
+  // last rows of the gated product most recently, so they are still in L2.
+  auto row_pair = [&](int t) {
+    const int rp = t / p.n_tiles;
+    return EPI == EPI_STORE ? (p.m_tiles + 1) / 2 - 1 - rp : rp;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both)
@@ -199,7 +206,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       for (int t = first; t < p.total && !sm->abort_flag; t += step) {
-        const int mt = (t / p.n_tiles) * 2 + rank, nt = t % p.n_tiles;
+        const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
         // an overhanging CTA of the last pair re-reads the last valid rows
         // (its results are discarded) so every box is in bounds
         const int arow = min(mt, p.m_tiles - 1) * BM;
@@ -279,7 +286,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     Stager st{tiles + STG_OFF + (warp - 2) * STG_BYTES, lane};
     int local = 0;
     for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
-      const int mt = (t / p.n_tiles) * 2 + rank, nt = t % p.n_tiles;
+      const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
       const bool valid = mt < p.m_tiles;
       const int n0 = nt * BN, nsz = min(BN, p.N - n0);
       const int acc = local & 1;
