@@ -10,6 +10,10 @@ from .flash_gau import (  # noqa: F401
     scale_offset,
     relpos_bias,
     chunk_scores,
+    layer_norm,
+    scale_norm,
+    rope,
     flash_gau,
+    flash_block,
     algorithmic_flops_per_token,
 )

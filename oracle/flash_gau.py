@@ -28,7 +28,16 @@ Readings taken where the pages disagree or are silent:
     builds from 2C-1 weights, used for every C;
   * the causal mask keeps the diagonal (j <= i) and is applied after relu^2;
   * the causal global term of the first chunk is the empty sum, i.e. zero;
-  * no bias terms, norm, RoPE or residual (the layer as eq. 3-8 write it).
+  * no bias terms, norm, RoPE or residual in ``flash_gau`` (the layer as
+    eq. 3-8 write it); ``flash_block`` adds the pre-norm, RoPE on the four
+    heads over global token positions and the residual of the pages'
+    flash_block, with these readings of what the pages leave unprinted:
+    the norm is LayerNorm (mean / biased variance, eps inside the square
+    root, learned scale and shift) or ScaleNorm (g * x / ||x||), the two the
+    pages name; RoPE rotates consecutive pairs (h_2i, h_2i+1) of each head by
+    the angle p * base^(-2i/s), p the token's position in its sequence (plus
+    an optional offset), base 10000 by default (the rotary embedding as its
+    author defines it; the pages print no rope function).
 
 Parity: every function here is pinned by tests/test_oracle.py against
 independent formulations (a scalar token loop, the full-length linear
@@ -44,7 +53,11 @@ __all__ = [
     "scale_offset",
     "relpos_bias",
     "chunk_scores",
+    "layer_norm",
+    "scale_norm",
+    "rope",
     "flash_gau",
+    "flash_block",
     "algorithmic_flops_per_token",
 ]
 
@@ -111,8 +124,51 @@ def chunk_scores(q, k, bias, C, causal):
     return a
 
 
+def layer_norm(x, g, b, eps=1e-5):
+    """LayerNorm over the last axis: (x - mean) / sqrt(var + eps) * g + b,
+    var the biased (1/d) variance.  One of the two pre-norms the pages name
+    ([TQLT] gau_block / flash_block pseudocode "norm(x)"; [TQLT-zh]
+    appendix B.2 and D, Code 5, whose body the page does not print)."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * np.asarray(g, dtype=np.float64) + \
+        np.asarray(b, dtype=np.float64)
+
+
+def scale_norm(x, g, eps=1e-5):
+    """ScaleNorm over the last axis: g * x / max(||x||_2, eps), with a single
+    learned scalar g ([TQLT-zh] appendix B.2: ScaleNorm in some masked-LM
+    models, as a faster stand-in for LayerNorm)."""
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    return float(g) * x / np.maximum(n, eps)
+
+
+def rope(h, positions, base=10000.0):
+    """Rotary position embedding of the last axis (s even): the pair
+    (h[2i], h[2i+1]) of the vector at position p is rotated by the angle
+    p * base^(-2i/s).  [TQLT] flash_block pseudocode: RoPE on the four heads,
+    "over the whole sequence, not restarted per chunk"; [FLASH-blog]: the
+    models use RoPE.
+
+    h: [..., T, s]; positions: [T] (one position per row of h)."""
+    h = np.asarray(h, dtype=np.float64)
+    s = h.shape[-1]
+    if s % 2:
+        raise ValueError("RoPE needs an even head width")
+    inv_freq = float(base) ** (-2.0 * np.arange(s // 2) / s)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]
+    cos, sin = np.cos(ang), np.sin(ang)
+    even, odd = h[..., 0::2], h[..., 1::2]
+    out = np.empty_like(h)
+    out[..., 0::2] = even * cos - odd * sin
+    out[..., 1::2] = even * sin + odd * cos
+    return out
+
+
 def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
-              lin_scale=1.0):
+              lin_scale=1.0, positions=None, rope_base=10000.0):
     """FLASH GAU layer forward with mixed chunk attention, in float64.
 
     Steps ([TQLT] Method and flash_block; [FLASH-blog] "Mixed Chunking"):
@@ -128,7 +184,9 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
 
     X: [B, T, d]; W_u, W_v: [d, e]; W_z: [d, s]; W_o: [e, d];
     gamma, beta: [4, s]; relpos: [2C-1]; T must be a multiple of C
-    ([FLASH-blog] "Mixed Chunking" assumes divisibility).
+    ([FLASH-blog] "Mixed Chunking" assumes divisibility).  With
+    ``positions`` ([T]) the four heads are rotated by ``rope`` after step 2
+    (the flash_block reading); the default keeps eq. 3-8 as written.
 
     Returns (O, inter) with O: [B, T, d] float64 and ``inter`` a dict of the
     intermediates U, V, Z, heads [4, B, T, s], state [B, G, s, e],
@@ -146,6 +204,8 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
     V = swish(X @ np.asarray(W_v, dtype=np.float64))
     Z = swish(X @ np.asarray(W_z, dtype=np.float64))
     Qq, Kq, Ql, Kl = scale_offset(Z, gamma, beta)
+    if positions is not None:
+        Qq, Kq, Ql, Kl = (rope(h, positions, rope_base) for h in (Qq, Kq, Ql, Kl))
     bias = relpos_bias(relpos, C)
 
     Vq = np.zeros((B, T, e))
@@ -178,6 +238,34 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
     inter = dict(U=U, V=V, Z=Z, heads=np.stack([Qq, Kq, Ql, Kl]),
                  state=state, prefix=prefix, Vq=Vq, Vl=Vl, gated=gated)
     return O, inter
+
+
+def flash_block(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
+                lin_scale=1.0, norm="layer", norm_g=None, norm_b=None, norm_eps=1e-5,
+                rope_on=True, rope_base=10000.0, pos_offset=0):
+    """The pages' FLASH block around the layer ([TQLT] flash_block
+    pseudocode): shortcut = x; x = norm(x); the GAU of ``flash_gau`` with
+    RoPE on its four heads at the tokens' global positions (t + pos_offset
+    for token t of a sequence); return out + shortcut.
+
+    norm: "layer" (``layer_norm`` with norm_g, norm_b [d]), "scale"
+    (``scale_norm`` with the scalar norm_g) or None.  Returns (Y, inter)
+    with inter from ``flash_gau`` plus Xn, the normalised input."""
+    X = np.asarray(X, dtype=np.float64)
+    if norm == "layer":
+        Xn = layer_norm(X, norm_g, norm_b, norm_eps)
+    elif norm == "scale":
+        Xn = scale_norm(X, norm_g, norm_eps)
+    elif norm is None:
+        Xn = X
+    else:
+        raise ValueError("norm must be 'layer', 'scale' or None")
+    T = X.shape[1]
+    positions = np.arange(T) + pos_offset if rope_on else None
+    O, inter = flash_gau(Xn, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
+                         lin_scale, positions=positions, rope_base=rope_base)
+    inter["Xn"] = Xn
+    return O + X, inter
 
 
 def algorithmic_flops_per_token(d, e, s, C, causal, quad_only=False):

@@ -275,3 +275,160 @@ def test_bf16_rounding_is_nearest_even():
     x = np.random.default_rng(0).standard_normal(10000) * 100
     ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(round_bf16(x), ref)
+
+
+# ------------------------------------------------- flash_block: norm, RoPE --
+
+from oracle import flash_block, layer_norm, rope, scale_norm  # noqa: E402
+
+
+def test_rope_golden_worked_example():
+    """Hand-worked rotation of one 4-wide vector (tests/golden)."""
+    want = None
+    with open(os.path.join(GOLDEN, "rope_s4_base10000.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                want = np.array([float(t) for t in line.split()])
+    got = rope(np.array([[1.0, 2.0, 3.0, 4.0]]), np.array([100.0]), 10000.0)[0]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+
+
+def test_rope_equals_complex_rotation_and_keeps_norms():
+    """Pairs as complex numbers h2i + i h2i+1 multiplied by e^(i p theta_i),
+    theta_i = base^(-2i/s): an independent formulation.  Rotations keep each
+    pair's length, and position 0 is the identity."""
+    rng = np.random.default_rng(3)
+    T, s, base = 9, 8, 500.0
+    h = rng.normal(size=(2, T, s))
+    pos = rng.uniform(0, 50, size=T)
+    z = h[..., 0::2] + 1j * h[..., 1::2]
+    theta = base ** (-2.0 * np.arange(s // 2) / s)
+    zr = z * np.exp(1j * pos[:, None] * theta[None, :])
+    ref = np.empty_like(h)
+    ref[..., 0::2], ref[..., 1::2] = zr.real, zr.imag
+    got = rope(h, pos, base)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(np.abs(got[..., 0::2] + 1j * got[..., 1::2]), np.abs(z),
+                               rtol=1e-12)
+    np.testing.assert_allclose(rope(h, np.zeros(T), base), h, rtol=0, atol=0)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<rope(q, m), rope(k, n)> = <rope(q, m + d), rope(k, n + d)>."""
+    rng = np.random.default_rng(4)
+    q, k = rng.normal(size=(1, 6)), rng.normal(size=(1, 6))
+    for m, n, dlt in [(3, 7, 11), (0, 5, 100), (40, 2, -30)]:
+        a = rope(q, np.array([m]))[0] @ rope(k, np.array([n]))[0]
+        b = rope(q, np.array([m + dlt]))[0] @ rope(k, np.array([n + dlt]))[0]
+        assert abs(a - b) < 1e-12
+
+
+def test_layer_norm_matches_torch_and_scale_norm_sets_the_length():
+    import torch
+    rng = np.random.default_rng(5)
+    x = rng.normal(1.5, 3.0, size=(4, 7, 24))
+    g, b = rng.normal(1, 0.1, 24), rng.normal(0, 0.1, 24)
+    ref = torch.nn.functional.layer_norm(torch.tensor(x), (24,), torch.tensor(g),
+                                         torch.tensor(b), eps=1e-5).numpy()
+    np.testing.assert_allclose(layer_norm(x, g, b, 1e-5), ref, rtol=1e-12, atol=1e-12)
+    y = scale_norm(x, 2.5)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 2.5, rtol=1e-12)
+
+
+def _brute_force_block(inp, C, causal, lin_scale, pos_offset, base):
+    """Scalar restatement of the block with RoPE and no norm: the heads of
+    each token are rotated as complex numbers at the token's global position,
+    the global term is token-level linear attention (never chunk states), and
+    the residual is added per element."""
+    X = inp["X"]
+    B, T, d = X.shape
+    e, s = inp["W_u"].shape[1], inp["W_z"].shape[1]
+    Xl, Wu, Wv, Wz, Wo = (inp[k].tolist() for k in ("X", "W_u", "W_v", "W_z", "W_o"))
+    ga, be, rp = inp["gamma"].tolist(), inp["beta"].tolist(), inp["relpos"].tolist()
+
+    def sw(a):
+        return a / (1.0 + math.exp(-a))
+
+    def proj(x, W, n):
+        return [sw(sum(x[k] * W[k][j] for k in range(d))) for j in range(n)]
+
+    def rot(vec, p):
+        out = []
+        for i in range(s // 2):
+            z = complex(vec[2 * i], vec[2 * i + 1]) * complex(
+                math.cos(p * base ** (-2.0 * i / s)), math.sin(p * base ** (-2.0 * i / s)))
+            out += [z.real, z.imag]
+        return out
+
+    Y = np.zeros((B, T, d))
+    for b in range(B):
+        u = [proj(Xl[b][t], Wu, e) for t in range(T)]
+        v = [proj(Xl[b][t], Wv, e) for t in range(T)]
+        z = [proj(Xl[b][t], Wz, s) for t in range(T)]
+        head = [[rot([z[t][k] * ga[h][k] + be[h][k] for k in range(s)], t + pos_offset)
+                 for t in range(T)] for h in range(4)]
+        qq, kq, ql, kl = head
+        for t in range(T):
+            g, i = divmod(t, C)
+            mix = [0.0] * e
+            for j in range(C):
+                if causal and j > i:
+                    continue
+                tj = g * C + j
+                sc = sum(qq[t][k] * kq[tj][k] for k in range(s)) / C + rp[j - i + C - 1]
+                a = max(sc, 0.0) ** 2
+                for c in range(e):
+                    mix[c] += a * v[tj][c]
+            for tp in range(T):
+                if causal and tp // C >= g:
+                    continue
+                w = lin_scale * sum(ql[t][k] * kl[tp][k] for k in range(s))
+                for c in range(e):
+                    mix[c] += w * v[tp][c]
+            for o in range(d):
+                Y[b, t, o] = Xl[b][t][o] + sum(u[t][c] * mix[c] * Wo[c][o] for c in range(e))
+    return Y
+
+
+def _block(inp, C, causal, **kw):
+    return flash_block(inp["X"], inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"],
+                       inp["gamma"], inp["beta"], inp["relpos"], C, causal, **kw)[0]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_block_matches_scalar_loop_with_global_rope_positions(causal):
+    """RoPE at global positions (not restarted per chunk) reaches the global
+    term through Q_lin K_lin^T across chunks; the token loop pins that."""
+    inp = make_inputs(B=1, T=8, d=3, e=4, s=4, C=4, dtype="fp32", seed=8)
+    inp["gamma"] = inp["gamma"] * 3.0
+    Y = _block(inp, 4, causal, lin_scale=0.5, norm=None, rope_base=7.0, pos_offset=3)
+    ref = _brute_force_block(inp, 4, causal, 0.5, 3, 7.0)
+    np.testing.assert_allclose(Y, ref, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_block_invariant_to_global_position_shift(causal):
+    """Positions enter only through rotations of both sides of every score, so
+    shifting all of them changes nothing."""
+    inp = make_inputs(B=2, T=16, d=8, e=12, s=8, C=4, dtype="fp32", seed=9)
+    g, b = np.ones(8), np.zeros(8)
+    a = _block(inp, 4, causal, norm="layer", norm_g=g, norm_b=b, pos_offset=0)
+    c = _block(inp, 4, causal, norm="layer", norm_g=g, norm_b=b, pos_offset=1234)
+    np.testing.assert_allclose(a, c, rtol=1e-10, atol=1e-10)
+
+
+def test_block_is_residual_around_the_layer_of_the_normalised_input():
+    """Without RoPE: Y - X = flash_gau(LayerNorm(X)), LayerNorm taken from
+    torch; with RoPE off and no norm it is X + flash_gau(X)."""
+    import torch
+    inp = make_inputs(B=2, T=8, d=6, e=8, s=4, C=4, dtype="fp32", seed=10)
+    rng = np.random.default_rng(11)
+    g, b = rng.normal(1, 0.1, 6), rng.normal(0, 0.1, 6)
+    Xn = torch.nn.functional.layer_norm(torch.tensor(inp["X"], dtype=torch.float64), (6,),
+                                        torch.tensor(g), torch.tensor(b), eps=1e-5).numpy()
+    Y = _block(inp, 4, True, norm="layer", norm_g=g, norm_b=b, rope_on=False)
+    ref, _ = flash_gau(Xn, inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"], inp["gamma"],
+                       inp["beta"], inp["relpos"], 4, True)
+    np.testing.assert_allclose(Y - inp["X"], ref, rtol=1e-10, atol=1e-12)
+    Y0 = _block(inp, 4, True, norm=None, rope_on=False)
+    np.testing.assert_allclose(Y0 - inp["X"], _run(inp, 4, True)[0], rtol=1e-12, atol=1e-12)
