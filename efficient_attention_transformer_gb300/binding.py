@@ -24,6 +24,10 @@ ECUDA = -4
 EDEVICE = -5
 ETIMEOUT = -6
 
+NORM_NONE = 0
+NORM_LAYER = 1
+NORM_SCALE = 2
+
 # Every function the header declares; the library must export all of them.
 EXPORTED = (
     "flash_gau_workspace_layout_query",
@@ -36,6 +40,7 @@ EXPORTED = (
     "flash_gau_strerror",
     "flash_gau_version",
     "flash_gau_forward_noalloc",
+    "flash_gau_block_forward",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -59,7 +64,21 @@ class Weights(ctypes.Structure):
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("total_bytes", "status", "U", "V", "heads", "state", "prefix", "gated",
-                 "bias")]
+                 "bias", "xn")]
+
+
+class Block(ctypes.Structure):
+    """flash_gau_block: the flash_block options (norm, RoPE, residual)."""
+    _fields_ = [
+        ("norm", ctypes.c_int),
+        ("norm_g", ctypes.c_void_p),
+        ("norm_b", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
+        ("rope", ctypes.c_int),
+        ("rope_base", ctypes.c_float),
+        ("pos_offset", ctypes.c_int),
+        ("residual", ctypes.c_int),
+    ]
 
 
 class FlashGauError(RuntimeError):
@@ -103,6 +122,9 @@ def lib():
         L.flash_gau_version.restype = i
         L.flash_gau_forward_noalloc.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p]
         L.flash_gau_forward_noalloc.restype = i
+        L.flash_gau_block_forward.argtypes = [p, ctypes.POINTER(Weights), ctypes.POINTER(Block),
+                                              i, i, i, i, i, p, p, sz, p]
+        L.flash_gau_block_forward.restype = i
         _lib = L
     return _lib
 
@@ -233,6 +255,37 @@ def forward_noalloc(X, weights, C, causal, out=None, stream=None):
     _check(lib().flash_gau_forward_noalloc(
         _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), B, T, C, int(bool(causal)),
         weights.dtype, _dev_ptr(out, "out", X.dtype), stream.cuda_stream))
+    return out
+
+
+def block_forward(X, weights, C, causal, norm=NORM_LAYER, norm_g=None, norm_b=None,
+                  norm_eps=1e-5, rope=True, rope_base=10000.0, pos_offset=0, residual=True,
+                  out=None, workspace=None, stream=None):
+    """Y = X + layer(norm(X)) with RoPE on the heads, through
+    flash_gau_block_forward.  norm_g / norm_b: fp32 CUDA tensors ([d] for
+    LayerNorm, [1] for ScaleNorm's g; norm_b may be None)."""
+    if X.dim() != 3:
+        raise ValueError("X must be [B, T, d]")
+    B, T, d = X.shape
+    if d != weights.d or X.dtype != weights.W_uvz.dtype:
+        raise ValueError("X does not match the weights")
+    f32 = torch.float32
+    blk = Block(int(norm),
+                _dev_ptr(norm_g, "norm_g", f32) if norm_g is not None else None,
+                _dev_ptr(norm_b, "norm_b", f32) if norm_b is not None else None,
+                float(norm_eps), int(bool(rope)), float(rope_base), int(pos_offset),
+                int(bool(residual)))
+    if out is None:
+        out = torch.empty_like(X)
+    if workspace is None:
+        workspace = weights.new_workspace(B, T, C, causal, X.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(X.device)
+    _check(lib().flash_gau_block_forward(
+        _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), ctypes.byref(blk), B, T, C,
+        int(bool(causal)), weights.dtype, _dev_ptr(out, "out", X.dtype),
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        stream.cuda_stream))
     return out
 
 

@@ -94,6 +94,8 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   off = align_up(off + M * e * io);
   L->bias = off;
   off = align_up(off + (2 * (size_t)C - 1) * sizeof(float));
+  L->xn = off;
+  off = align_up(off + M * d * io);
   L->total_bytes = off;
   return FLASH_GAU_OK;
 }
@@ -131,41 +133,21 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
-}  // namespace
-
-extern "C" {
-
-int flash_gau_workspace_layout_query(int B, int T, int C, int d, int e, int s, int causal,
-                                     int dtype, flash_gau_workspace_layout *out) {
-  if (!out) return FLASH_GAU_EINVAL;
-  return layout(B, T, C, d, e, s, causal, dtype, out);
+int check_block(const flash_gau_block *blk, int s) {
+  if (!blk) return FLASH_GAU_OK;
+  if (blk->norm < FLASH_GAU_NORM_NONE || blk->norm > FLASH_GAU_NORM_SCALE) return FLASH_GAU_EINVAL;
+  if (blk->norm != FLASH_GAU_NORM_NONE && (!blk->norm_g || !(blk->norm_eps > 0.f)))
+    return FLASH_GAU_EINVAL;
+  if (blk->rope && (s % 2 != 0 || !(blk->rope_base > 1.f))) return FLASH_GAU_EINVAL;
+  if (blk->pos_offset < 0) return FLASH_GAU_EINVAL;
+  return FLASH_GAU_OK;
 }
 
-size_t flash_gau_workspace_bytes(int B, int T, int C, const flash_gau_weights *w, int causal,
-                                 int dtype) {
-  if (!w) return 0;
-  flash_gau_workspace_layout L;
-  if (layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L) != FLASH_GAU_OK) return 0;
-  return L.total_bytes;
-}
-
-int flash_gau_num_stages(int dtype, int causal) {
-  int n = 0;
-  stages(dtype, causal, &n);
-  return n;
-}
-
-const char *flash_gau_stage_name(int dtype, int causal, int k) {
-  int n = 0;
-  const Stage *st = stages(dtype, causal, &n);
-  if (!st || k < 0 || k >= n) return nullptr;
-  return st[k].name;
-}
-
-int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, int T, int C,
-                            int causal, int dtype, void *out, void *workspace,
-                            size_t workspace_bytes, void *stream, void *const *stage_events,
-                            int n_events) {
+// One forward: the layer alone (blk == null) or the flash_block wrapper.
+int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block *blk, int B,
+                int T, int C, int causal, int dtype, void *out, void *workspace,
+                size_t workspace_bytes, void *stream, void *const *stage_events,
+                int n_events) {
   if (!X || !w || !out || !workspace || !w->W_uvz || !w->W_o || !w->gamma || !w->beta ||
       !w->relpos)
     return FLASH_GAU_EINVAL;
@@ -174,6 +156,7 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, in
   flash_gau_workspace_layout L;
   int st = layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
   if (st != FLASH_GAU_OK) return st;
+  if ((st = check_block(blk, w->s)) != FLASH_GAU_OK) return st;
   if (workspace_bytes < L.total_bytes || ((uintptr_t)workspace % kAlign) != 0)
     return FLASH_GAU_EWORKSPACE;
   const size_t io = dtype == FLASH_GAU_BF16 ? 2 : 4;
@@ -212,22 +195,87 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, in
   p.prefix = ws + L.prefix;
   p.gated = ws + L.gated;
   p.bias = reinterpret_cast<float *>(ws + L.bias);
+  p.xn = ws + L.xn;
   p.stream = (cudaStream_t)stream;
   p.num_sms = num_sms;
+  p.norm = blk ? blk->norm : FLASH_GAU_NORM_NONE;
+  p.norm_g = blk ? blk->norm_g : nullptr;
+  p.norm_b = blk ? blk->norm_b : nullptr;
+  p.norm_eps = blk ? blk->norm_eps : 0.f;
+  p.rope = blk ? (blk->rope ? 1 : 0) : 0;
+  p.rope_base = blk ? blk->rope_base : 0.f;
+  p.pos_offset = blk ? blk->pos_offset : 0;
+  p.residual = (blk && blk->residual) ? X : nullptr;
+  p.A_in = p.norm != FLASH_GAU_NORM_NONE ? p.xn : X;
 
   int n = 0;
   const Stage *sched = stages(dtype, causal, &n);
+  Stage full[8];
+  int nf = 0;
+  if (p.norm != FLASH_GAU_NORM_NONE) full[nf++] = {"norm", block_norm};
+  for (int k = 0; k < n; ++k) {
+    full[nf++] = sched[k];
+    if (p.rope && dtype == FLASH_GAU_FP32 && strcmp(sched[k].name, "projection") == 0)
+      full[nf++] = {"rope", simt_rope_heads_f32};
+  }
   cudaError_t err;
   if (n_events > 0 &&
       (err = cudaEventRecord((cudaEvent_t)stage_events[0], p.stream)) != cudaSuccess)
     return record_cuda(err);
-  for (int k = 0; k < n; ++k) {
-    if ((err = sched[k].fn(p)) != cudaSuccess) return record_cuda(err);
+  for (int k = 0; k < nf; ++k) {
+    if ((err = full[k].fn(p)) != cudaSuccess) return record_cuda(err);
     if (k + 1 < n_events &&
         (err = cudaEventRecord((cudaEvent_t)stage_events[k + 1], p.stream)) != cudaSuccess)
       return record_cuda(err);
   }
   return FLASH_GAU_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int flash_gau_workspace_layout_query(int B, int T, int C, int d, int e, int s, int causal,
+                                     int dtype, flash_gau_workspace_layout *out) {
+  if (!out) return FLASH_GAU_EINVAL;
+  return layout(B, T, C, d, e, s, causal, dtype, out);
+}
+
+size_t flash_gau_workspace_bytes(int B, int T, int C, const flash_gau_weights *w, int causal,
+                                 int dtype) {
+  if (!w) return 0;
+  flash_gau_workspace_layout L;
+  if (layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L) != FLASH_GAU_OK) return 0;
+  return L.total_bytes;
+}
+
+int flash_gau_num_stages(int dtype, int causal) {
+  int n = 0;
+  stages(dtype, causal, &n);
+  return n;
+}
+
+const char *flash_gau_stage_name(int dtype, int causal, int k) {
+  int n = 0;
+  const Stage *st = stages(dtype, causal, &n);
+  if (!st || k < 0 || k >= n) return nullptr;
+  return st[k].name;
+}
+
+int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, int T, int C,
+                            int causal, int dtype, void *out, void *workspace,
+                            size_t workspace_bytes, void *stream, void *const *stage_events,
+                            int n_events) {
+  return run_forward(X, w, nullptr, B, T, C, causal, dtype, out, workspace, workspace_bytes,
+                     stream, stage_events, n_events);
+}
+
+int flash_gau_block_forward(const void *X, const flash_gau_weights *w, const flash_gau_block *blk,
+                            int B, int T, int C, int causal, int dtype, void *out,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  if (!blk) return FLASH_GAU_EINVAL;
+  return run_forward(X, w, blk, B, T, C, causal, dtype, out, workspace, workspace_bytes, stream,
+                     nullptr, 0);
 }
 
 int flash_gau_forward(const void *X, const flash_gau_weights *w, int B, int T, int C, int causal,
@@ -267,6 +315,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 102; }
+int flash_gau_version(void) { return 103; }
 
 }  // extern "C"

@@ -30,6 +30,17 @@ struct Problem {
   void *prefix;
   void *gated;
   float *bias;  // [2C-1] relpos, causal entries of offset j-i >= 1 set to -inf
+  // flash_block options: the projection reads A_in (X, or the normalised
+  // input xn); rope rotates the heads; residual (X or null) is added to O
+  const void *A_in;
+  void *xn;
+  int norm;
+  const float *norm_g, *norm_b;
+  float norm_eps;
+  int rope;
+  float rope_base;
+  int pos_offset;
+  const void *residual;
   cudaStream_t stream;
   int num_sms;
 };
@@ -50,6 +61,17 @@ __host__ __device__ inline long long rb64_row(long long r, long long c, long lon
   return ((r >> 6) * ncb + (c >> 6)) * 64 + (r & 63);
 }
 constexpr int kGridBarrierWord = 17;
+
+// RoPE angle of pair i (of s / 2) at position pos: pos * base^(-2i/s),
+// formed and reduced modulo 2 pi in fp64 (positions reach the thousands, so
+// an fp32 product would lose the angle's low bits), then sin and cos in fp32.
+__device__ __forceinline__ void rope_sincos(double pos, int i, int s, double log2_base,
+                                            float *sn, float *cs) {
+  const double two_pi = 6.283185307179586476925287;
+  double a = pos * exp2(-2.0 * i / s * log2_base);
+  a -= two_pi * floor(a / two_pi);
+  sincosf((float)a, sn, cs);
+}
 
 using StageFn = cudaError_t (*)(const Problem &);
 
@@ -77,6 +99,11 @@ struct Stage {
   const char *name;
   StageFn fn;
 };
+
+// flash_block stages (block_kernels.cu): the pre-norm into xn, and for fp32
+// the RoPE rotation of the heads in place
+cudaError_t block_norm(const Problem &p);
+cudaError_t simt_rope_heads_f32(const Problem &p);
 
 // fp32 SIMT stages (simt_kernels.cu)
 cudaError_t simt_projection_f32(const Problem &p);

@@ -120,8 +120,10 @@ template <typename T>
 struct StoreEpi {
   T *out;
   int ld;
+  const T *residual;  // added when not null (the block's shortcut)
   __device__ void operator()(int, int m, int n, float acc) const {
-    out[(long long)m * ld + n] = from_f<T>(acc);
+    const long long i = (long long)m * ld + n;
+    out[i] = from_f<T>(residual ? acc + to_f(residual[i]) : acc);
   }
 };
 
@@ -263,7 +265,7 @@ cudaError_t projection(const Problem &p) {
   const int N = 2 * p.e + p.s;
   dim3 grid(cdiv(N, kTile), cdiv(p.M, kTile), 1);
   ProjEpi<T> epi{(T *)p.U, (T *)p.V, (T *)p.heads, p.gamma, p.beta, p.M, p.e, p.s};
-  simt_gemm<T><<<grid, 256, 0, p.stream>>>((int)p.M, N, p.d, (const T *)p.X, p.d, 1, 0,
+  simt_gemm<T><<<grid, 256, 0, p.stream>>>((int)p.M, N, p.d, (const T *)p.A_in, p.d, 1, 0,
                                            (const T *)p.W_uvz, N, 1, 0, epi);
   return cudaGetLastError();
 }
@@ -305,7 +307,7 @@ cudaError_t chunk_attention(const Problem &p) {
 template <typename T>
 cudaError_t output(const Problem &p) {
   dim3 grid(cdiv(p.d, kTile), cdiv(p.M, kTile), 1);
-  StoreEpi<T> epi{(T *)p.out, p.d};
+  StoreEpi<T> epi{(T *)p.out, p.d, (const T *)p.residual};
   simt_gemm<T><<<grid, 256, 0, p.stream>>>((int)p.M, p.d, p.e, (const T *)p.gated, p.e, 1, 0,
                                            (const T *)p.W_o, p.d, 1, 0, epi);
   return cudaGetLastError();

@@ -45,7 +45,9 @@ constexpr int TILE_BYTES = STG_OFF + EPI_WARPS * STG_BYTES;
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint16_t kPair = 0x3, kLeader = 0x1;
 
-enum Epi { EPI_PROJ = 0, EPI_STORE = 1 };
+// EPI_PROJ_ROPE: the projection with the flash_block RoPE of the heads, a
+// separate instance so that its register needs stay out of the plain one.
+enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2 };
 
 struct Params {
   int N, K;        // output columns, contraction depth
@@ -61,6 +63,12 @@ struct Params {
   const float *relpos;
   float *bias;
   int C, causal;
+  // projection with RoPE (flash_block): heads rotated at positions
+  // t + pos_offset
+  int T_seq, pos_offset;
+  double log2_base;
+  // output (flash_block): the shortcut added to O, or null
+  const __nv_bfloat16 *residual;
 };
 
 struct Smem {
@@ -178,7 +186,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   // grid has completed (the first after its griddepcontrol.wait, the second
   // once every CTA of the first has passed that wait), and the previous
   // forward's kernels had all completed before this one got past its wait.
-  if (EPI == EPI_PROJ && blockIdx.x == 0) {
+  if (EPI != EPI_STORE && blockIdx.x == 0) {
     if (threadIdx.x == 0) {
       p.sched[kNextUnitWord] = 0;
       p.sched[kGridBarrierWord] = 0;
@@ -312,7 +320,18 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!valid) continue;
         if constexpr (EPI == EPI_STORE) {
           uint4 w[8];
-          pack64(ra, rb, [](float x, int) { return x; }, w);
+          if (p.residual) {
+            // the block's shortcut: this thread's row, 64 columns of X
+            const uint4 *xr = reinterpret_cast<const uint4 *>(
+                p.residual + (size_t)(row0 + lane) * p.N + n0 + c0);
+            uint4 xv[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xv[q] = __ldg(xr + q);
+            const __nv_bfloat16 *xh = reinterpret_cast<const __nv_bfloat16 *>(xv);
+            pack64(ra, rb, [&](float x, int col) { return x + __bfloat162float(xh[col]); }, w);
+          } else {
+            pack64(ra, rb, [](float x, int) { return x; }, w);
+          }
           uint8_t *b = st.begin();
           st.put(b, w);
           st.finish(b, &tmC0, n0 + c0, row0);
@@ -332,13 +351,33 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               ra[j] = __float_as_uint(swish_tanh(__uint_as_float(ra[j])));
               rb[j] = __float_as_uint(swish_tanh(__uint_as_float(rb[j])));
             }
+            // flash_block RoPE: the angle of each (even, odd) column pair of
+            // this row, shared by the four heads
+            float cs[32], sn[32];
+            if constexpr (EPI == EPI_PROJ_ROPE) {
+              const double pos = (double)((row0 + lane) % p.T_seq + p.pos_offset);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) rope_sincos(pos, c / 2 + k, p.s, p.log2_base, &sn[k], &cs[k]);
+            }
 #pragma unroll 1
             for (int h = 0; h < 4; ++h) {
               const float *g = p.gamma + h * p.s + c;
               const float *be = p.beta + h * p.s + c;
               uint4 w[8];
-              pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); },
-                     w);
+              if constexpr (EPI == EPI_PROJ_ROPE) {
+                uint32_t *wp = reinterpret_cast<uint32_t *>(w);  // word k: columns 2k, 2k+1
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                  const uint32_t *src = k < 16 ? &ra[2 * k] : &rb[2 * k - 32];
+                  const float y0 = fmaf(__uint_as_float(src[0]), __ldg(g + 2 * k), __ldg(be + 2 * k));
+                  const float y1 =
+                      fmaf(__uint_as_float(src[1]), __ldg(g + 2 * k + 1), __ldg(be + 2 * k + 1));
+                  wp[k] = pack_bf16(y0 * cs[k] - y1 * sn[k], y0 * sn[k] + y1 * cs[k]);
+                }
+              } else {
+                pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); },
+                       w);
+              }
               uint8_t *b = st.begin();
               st.put(b, w);
               st.finish(b, &tmC2, c, h * p.M_tokens + row0);
@@ -417,7 +456,9 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   const int N = 2 * pr.e + pr.s;
   CUtensorMap tmA, tmB, tU, tV, tH;
   cudaError_t err;
-  if ((err = make_tmap_bf16_2d(&tmA, pr.X, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess) return err;
+  // A: the input, or its normalised copy (flash_block pre-norm)
+  if ((err = make_tmap_bf16_2d(&tmA, pr.A_in, pr.M, pr.d, pr.d, BM, 64)) != cudaSuccess)
+    return err;
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_uvz, pr.d, N, N, BK, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   // V in 64 x 64 blocks (flat 128-byte rows), 32-row store boxes
@@ -429,10 +470,14 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   p.gamma = pr.gamma;
   p.beta = pr.beta;
   p.sched = pr.status;
+  p.T_seq = pr.T;
+  p.pos_offset = pr.pos_offset;
+  p.log2_base = pr.rope ? log2((double)pr.rope_base) : 0.0;
   p.relpos = pr.relpos;
   p.bias = pr.bias;
   p.C = pr.C;
   p.causal = pr.causal;
+  if (pr.rope) return launch<EPI_PROJ_ROPE>(tmA, tmB, tU, tV, tH, p, pr);
   return launch<EPI_PROJ>(tmA, tmB, tU, tV, tH, p, pr);
 }
 
@@ -445,6 +490,7 @@ cudaError_t tc_output_bf16(const Problem &pr) {
     return err;
   if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
   Params p = base_params(pr, pr.d, pr.e);
+  p.residual = (const __nv_bfloat16 *)pr.residual;
   return launch<EPI_STORE>(tmA, tmB, tO, tO, tO, p, pr);
 }
 

@@ -95,6 +95,8 @@ typedef struct flash_gau_workspace_layout {
   size_t bias;          /* [2C-1] fp32: relpos as the bf16 attention kernel
                            reads it; causal: the entries of offset j-i >= 1
                            are -inf, so relu^2 applies the causal mask      */
+  size_t xn;            /* [B*T, d] io: the normalised input of
+                           flash_gau_block_forward (unused otherwise)       */
 } flash_gau_workspace_layout;
 /* Intermediates are row-major, except those marked (*) for FLASH_GAU_BF16:
  * these, seen as [rows, e] matrices (rows = B*T, B*G*s or B*s), are stored
@@ -166,6 +168,44 @@ const char *flash_gau_strerror(int status);
 
 /* Library version as major*10000 + minor*100 + patch.                      */
 int flash_gau_version(void);
+
+/* ---- the flash_block wrapper -------------------------------------------- */
+/* The block around the layer in the pages' flash_block pseudocode
+ * ("Transformer Quality in Linear Time", flash_block; gau_block has the same
+ * frame):  Y = X + layer(norm(X)),  where the layer's four heads are rotated
+ * by RoPE at the tokens' global positions before use.  The pages print
+ * neither the norm nor the rope function; this library's readings:
+ *   LayerNorm  (x - mean) / sqrt(var + eps) * g + b   (biased variance)
+ *   ScaleNorm  g * x / max(||x||_2, eps)              (g a single scalar)
+ *   RoPE       the pair (h[2i], h[2i+1]) of a head of the token at position
+ *              p = t + pos_offset (t its index in its sequence) is rotated
+ *              by the angle p * rope_base^(-2i/s).                          */
+#define FLASH_GAU_NORM_NONE 0
+#define FLASH_GAU_NORM_LAYER 1
+#define FLASH_GAU_NORM_SCALE 2
+
+typedef struct flash_gau_block {
+  int norm;             /* FLASH_GAU_NORM_NONE / _LAYER / _SCALE             */
+  const float *norm_g;  /* device fp32: LayerNorm scale [d], ScaleNorm g [1] */
+  const float *norm_b;  /* device fp32: LayerNorm shift [d], or NULL (zero)  */
+  float norm_eps;       /* > 0                                               */
+  int rope;             /* nonzero: rotate the four heads (s must be even)   */
+  float rope_base;      /* > 1 (10000 in the rotary embedding's definition)  */
+  int pos_offset;       /* >= 0: position of each sequence's first token     */
+  int residual;         /* nonzero: add X (the shortcut) to the output       */
+} flash_gau_block;
+
+/* Y = [X +] layer(norm(X)) with RoPE on the heads, per the options in *blk
+ * (host pointer, read during the call).  The other arguments, the
+ * workspace and the status word are as for flash_gau_forward; the workspace
+ * region xn holds the normalised input.  blk->norm == NONE, rope == 0 and
+ * residual == 0 compute exactly flash_gau_forward.  Returns FLASH_GAU_EINVAL
+ * for bad options (unknown norm, missing norm_g, eps <= 0, rope with an odd
+ * s or base <= 1, negative pos_offset).                                      */
+int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
+                            const flash_gau_block *blk, int B, int T, int C,
+                            int causal, int dtype, void *out, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /* ---- allocation-free variant ------------------------------------------- */
 /* No counterpart on the pages: this entry point exists for deployment, not

@@ -44,7 +44,7 @@ def test_version_and_strerror(L):
 def test_layout_offsets_aligned_and_sized(L):
     B, T, C, d, e, s = 2, 8192, 256, 768, 1536, 128
     lay = bd.workspace_layout(B, T, C, d, e, s, True, bd.BF16)
-    order = ["status", "U", "V", "heads", "state", "prefix", "gated", "bias"]
+    order = ["status", "U", "V", "heads", "state", "prefix", "gated", "bias", "xn"]
     offs = [lay[k] for k in order]
     assert offs == sorted(offs)
     assert all(o % 256 == 0 for o in offs)
@@ -55,7 +55,8 @@ def test_layout_offsets_aligned_and_sized(L):
     assert lay["prefix"] - lay["state"] >= B * G * s * e * 2
     assert lay["gated"] - lay["prefix"] >= B * G * s * e * 2
     assert lay["bias"] - lay["gated"] >= M * e * 2
-    assert lay["total_bytes"] - lay["bias"] >= (2 * C - 1) * 4
+    assert lay["xn"] - lay["bias"] >= (2 * C - 1) * 4
+    assert lay["total_bytes"] - lay["xn"] >= M * d * 2
     nc = bd.workspace_layout(B, T, C, d, e, s, False, bd.BF16)
     assert nc["gated"] - nc["prefix"] < lay["gated"] - lay["prefix"]  # [B,s,e] only
 
@@ -112,3 +113,32 @@ def test_stage_names(L):
         names = bd.stage_names(dt, True)
         assert len(names) == bd.num_stages(dt, True) >= 1
         assert L.flash_gau_stage_name(dt, 1, len(names)) is None
+
+
+@pytest.mark.parametrize("opts", [
+    dict(norm=7),                                   # unknown norm
+    dict(norm=bd.NORM_LAYER, norm_g=None),          # missing scale
+    dict(norm=bd.NORM_LAYER, norm_eps=0.0),         # eps <= 0
+    dict(rope=1, rope_base=1.0),                    # base <= 1
+    dict(pos_offset=-1),                            # negative position
+])
+def test_block_forward_rejects_bad_options_before_any_launch(L, opts):
+    w = bd.Weights(1, 2, 3, 4, 5, 128, 256, 128, 1.0)
+    base = dict(norm=bd.NORM_LAYER, norm_g=6, norm_b=None, norm_eps=1e-5, rope=1,
+                rope_base=10000.0, pos_offset=0, residual=1)
+    base.update(opts)
+    blk = bd.Block(base["norm"], base["norm_g"], base["norm_b"], base["norm_eps"], base["rope"],
+                   base["rope_base"], base["pos_offset"], base["residual"])
+    n = bd.workspace_layout(1, 256, 128, 128, 256, 128, True, bd.BF16)["total_bytes"]
+    assert L.flash_gau_block_forward(16, ctypes.byref(w), ctypes.byref(blk), 1, 256, 128, 1,
+                                     bd.BF16, 1 << 40, 256, n, None) == bd.EINVAL
+    assert L.flash_gau_block_forward(16, ctypes.byref(w), None, 1, 256, 128, 1, bd.BF16,
+                                     1 << 40, 256, n, None) == bd.EINVAL
+
+
+def test_block_forward_rejects_rope_with_odd_head_width(L):
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 33, 1.0)
+    blk = bd.Block(bd.NORM_NONE, None, None, 1e-5, 1, 10000.0, 0, 1)
+    n = bd.workspace_layout(1, 256, 64, 64, 128, 33, True, bd.FP32)["total_bytes"]
+    assert L.flash_gau_block_forward(16, ctypes.byref(w), ctypes.byref(blk), 1, 256, 64, 1,
+                                     bd.FP32, 1 << 40, 256, n, None) == bd.EINVAL
