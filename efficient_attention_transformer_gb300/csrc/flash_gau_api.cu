@@ -96,6 +96,8 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   off = align_up(off + (2 * (size_t)C - 1) * sizeof(float));
   L->xn = off;
   off = align_up(off + M * d * io);
+  L->rope = off;
+  off = align_up(off + (size_t)T * (s / 2) * 4);
   L->total_bytes = off;
   return FLASH_GAU_OK;
 }
@@ -127,6 +129,19 @@ const Stage *stages(int dtype, int /*causal*/, int *n) {
   *n = 0;
   return nullptr;
 }
+
+}  // namespace
+
+void flashgau::rope_table(RopeTable *tab, int s, float base) {
+  const double two_pi = 6.283185307179586476925287;
+  for (int i = 0; i < kMaxRopePairs; ++i) {
+    const double phi = i < s / 2 ? pow((double)base, -2.0 * i / s) / two_pi : 0.0;
+    const float hi = (float)phi;
+    tab->phi[i] = make_float2(hi, (float)(phi - (double)hi));
+  }
+}
+
+namespace {
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   const char *pa = (const char *)a, *pb = (const char *)b;
@@ -196,6 +211,7 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.gated = ws + L.gated;
   p.bias = reinterpret_cast<float *>(ws + L.bias);
   p.xn = ws + L.xn;
+  p.rope_cs = ws + L.rope;
   p.stream = (cudaStream_t)stream;
   p.num_sms = num_sms;
   p.norm = blk ? blk->norm : FLASH_GAU_NORM_NONE;
@@ -207,12 +223,14 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.pos_offset = blk ? blk->pos_offset : 0;
   p.residual = (blk && blk->residual) ? X : nullptr;
   p.A_in = p.norm != FLASH_GAU_NORM_NONE ? p.xn : X;
+  if (p.rope) rope_table(&p.rope_tab, p.s, p.rope_base);
 
   int n = 0;
   const Stage *sched = stages(dtype, causal, &n);
   Stage full[8];
   int nf = 0;
   if (p.norm != FLASH_GAU_NORM_NONE) full[nf++] = {"norm", block_norm};
+  if (p.rope && dtype == FLASH_GAU_BF16) full[nf++] = {"rope_table", rope_table_stage};
   for (int k = 0; k < n; ++k) {
     full[nf++] = sched[k];
     if (p.rope && dtype == FLASH_GAU_FP32 && strcmp(sched[k].name, "projection") == 0)
@@ -315,6 +333,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 103; }
+int flash_gau_version(void) { return 104; }
 
 }  // extern "C"

@@ -9,6 +9,26 @@
 
 namespace flashgau {
 
+// RoPE of pair i at position pos: the angle pos * base^(-2i/s).  Positions
+// reach the thousands, so a plain fp32 product would lose the angle's low
+// bits, and fp64 arithmetic is slow on this GPU.  The host gives each
+// pair's frequency in turns, phi_i = base^(-2i/s) / (2 pi), as an fp32
+// hi + lo pair (computed in double); pos * phi is formed exactly enough
+// with an fma-based product, its integer turns dropped, and the fraction
+// goes to sincospif.
+constexpr int kMaxRopePairs = 64;
+struct RopeTable {
+  float2 phi[kMaxRopePairs];  // (hi, lo) of base^(-2i/s) / (2 pi)
+};
+__device__ __forceinline__ void rope_sincos(float pos, float2 phi, float *sn, float *cs) {
+  const float t_hi = pos * phi.x;
+  const float t_lo = fmaf(pos, phi.y, fmaf(pos, phi.x, -t_hi));  // exact product error
+  const float f = (t_hi - rintf(t_hi)) + t_lo;                   // turns, |f| <~ 0.5
+  sincospif(2.0f * f, sn, cs);
+}
+// Fills the table for head width s and the given base (host side).
+void rope_table(RopeTable *tab, int s, float base);
+
 // One forward call, with every device pointer resolved.
 struct Problem {
   int B, T, C, G, d, e, s, causal, dtype;
@@ -40,6 +60,8 @@ struct Problem {
   int rope;
   float rope_base;
   int pos_offset;
+  RopeTable rope_tab;  // filled when rope is set
+  void *rope_cs;       // [s / 2][T] half2 (cos, sin), bf16 path
   const void *residual;
   cudaStream_t stream;
   int num_sms;
@@ -62,16 +84,6 @@ __host__ __device__ inline long long rb64_row(long long r, long long c, long lon
 }
 constexpr int kGridBarrierWord = 17;
 
-// RoPE angle of pair i (of s / 2) at position pos: pos * base^(-2i/s),
-// formed and reduced modulo 2 pi in fp64 (positions reach the thousands, so
-// an fp32 product would lose the angle's low bits), then sin and cos in fp32.
-__device__ __forceinline__ void rope_sincos(double pos, int i, int s, double log2_base,
-                                            float *sn, float *cs) {
-  const double two_pi = 6.283185307179586476925287;
-  double a = pos * exp2(-2.0 * i / s * log2_base);
-  a -= two_pi * floor(a / two_pi);
-  sincosf((float)a, sn, cs);
-}
 
 using StageFn = cudaError_t (*)(const Problem &);
 
@@ -103,6 +115,7 @@ struct Stage {
 // flash_block stages (block_kernels.cu): the pre-norm into xn, and for fp32
 // the RoPE rotation of the heads in place
 cudaError_t block_norm(const Problem &p);
+cudaError_t rope_table_stage(const Problem &p);
 cudaError_t simt_rope_heads_f32(const Problem &p);
 
 // fp32 SIMT stages (simt_kernels.cu)

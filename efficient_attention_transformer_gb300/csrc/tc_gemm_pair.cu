@@ -18,6 +18,7 @@
 // columns) drain them through tcgen05.ld into swizzled staging and TMA
 // stores, and report the accumulator free to the leader.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "flash_gau_internal.h"
 #include "sm103_ptx.cuh"
@@ -65,8 +66,8 @@ struct Params {
   int C, causal;
   // projection with RoPE (flash_block): heads rotated at positions
   // t + pos_offset
-  int T_seq, pos_offset;
-  double log2_base;
+  int T_seq;
+  const uint32_t *rope_cs;  // [s / 2][T] half2 (cos, sin)
   // output (flash_block): the shortcut added to O, or null
   const __nv_bfloat16 *residual;
 };
@@ -351,36 +352,59 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               ra[j] = __float_as_uint(swish_tanh(__uint_as_float(ra[j])));
               rb[j] = __float_as_uint(swish_tanh(__uint_as_float(rb[j])));
             }
-            // flash_block RoPE: the angle of each (even, odd) column pair of
-            // this row, shared by the four heads
-            float cs[32], sn[32];
             if constexpr (EPI == EPI_PROJ_ROPE) {
-              const double pos = (double)((row0 + lane) % p.T_seq + p.pos_offset);
+              // flash_block RoPE: the (even, odd) column pairs of this row
+              // rotated by the table's (cos, sin) at its position; the 32
+              // pairs' entries, one coalesced load each, stay packed
+              uint32_t csn[32];
+              {
+                const uint32_t *tab =
+                    p.rope_cs + (size_t)(c / 2) * p.T_seq + (row0 + lane) % p.T_seq;
 #pragma unroll
-              for (int k = 0; k < 32; ++k) rope_sincos(pos, c / 2 + k, p.s, p.log2_base, &sn[k], &cs[k]);
-            }
+                for (int k = 0; k < 32; ++k) csn[k] = __ldg(tab + (size_t)k * p.T_seq);
+              }
 #pragma unroll 1
-            for (int h = 0; h < 4; ++h) {
-              const float *g = p.gamma + h * p.s + c;
-              const float *be = p.beta + h * p.s + c;
-              uint4 w[8];
-              if constexpr (EPI == EPI_PROJ_ROPE) {
-                uint32_t *wp = reinterpret_cast<uint32_t *>(w);  // word k: columns 2k, 2k+1
+              for (int h = 0; h < 4; ++h) {
+                const float *g = p.gamma + h * p.s + c;
+                const float *be = p.beta + h * p.s + c;
+                uint8_t *b = st.begin();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                  const uint32_t *src = k < 16 ? &ra[2 * k] : &rb[2 * k - 32];
-                  const float y0 = fmaf(__uint_as_float(src[0]), __ldg(g + 2 * k), __ldg(be + 2 * k));
-                  const float y1 =
-                      fmaf(__uint_as_float(src[1]), __ldg(g + 2 * k + 1), __ldg(be + 2 * k + 1));
-                  wp[k] = pack_bf16(y0 * cs[k] - y1 * sn[k], y0 * sn[k] + y1 * cs[k]);
+                for (int hf = 0; hf < 2; ++hf) {
+                  const uint32_t *src = hf == 0 ? ra : rb;  // columns 32 hf .. 32 hf + 31
+                  uint4 w4[4];
+                  uint32_t *wp = reinterpret_cast<uint32_t *>(w4);  // word k: pair 16 hf + k
+#pragma unroll
+                  for (int k2 = 0; k2 < 8; ++k2) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                      const int k = 2 * k2 + j, col = 32 * hf + 2 * k;
+                      const float2 q = __half22float2(
+                          *reinterpret_cast<const __half2 *>(&csn[16 * hf + k]));
+                      const float cs = q.x, sn = q.y;
+                      const float y0 = fmaf(__uint_as_float(src[2 * k]), __ldg(g + col), __ldg(be + col));
+                      const float y1 = fmaf(__uint_as_float(src[2 * k + 1]), __ldg(g + col + 1),
+                                            __ldg(be + col + 1));
+                      wp[k] = pack_bf16(y0 * cs - y1 * sn, y0 * sn + y1 * cs);
+                    }
+                  }
+#pragma unroll
+                  for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(b + sw128_offset(lane, 4 * hf + cc)) = w4[cc];
                 }
-              } else {
+                st.finish(b, &tmC2, c, h * p.M_tokens + row0);
+              }
+            } else {
+#pragma unroll 1
+              for (int h = 0; h < 4; ++h) {
+                const float *g = p.gamma + h * p.s + c;
+                const float *be = p.beta + h * p.s + c;
+                uint4 w[8];
                 pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); },
                        w);
+                uint8_t *b = st.begin();
+                st.put(b, w);
+                st.finish(b, &tmC2, c, h * p.M_tokens + row0);
               }
-              uint8_t *b = st.begin();
-              st.put(b, w);
-              st.finish(b, &tmC2, c, h * p.M_tokens + row0);
             }
           }
         }
@@ -471,8 +495,7 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   p.beta = pr.beta;
   p.sched = pr.status;
   p.T_seq = pr.T;
-  p.pos_offset = pr.pos_offset;
-  p.log2_base = pr.rope ? log2((double)pr.rope_base) : 0.0;
+  p.rope_cs = (const uint32_t *)pr.rope_cs;
   p.relpos = pr.relpos;
   p.bias = pr.bias;
   p.C = pr.C;

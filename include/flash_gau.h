@@ -97,6 +97,8 @@ typedef struct flash_gau_workspace_layout {
                            are -inf, so relu^2 applies the causal mask      */
   size_t xn;            /* [B*T, d] io: the normalised input of
                            flash_gau_block_forward (unused otherwise)       */
+  size_t rope;          /* [s/2, T] fp16 (cos, sin) pairs: the RoPE table of
+                           flash_gau_block_forward, bf16 (unused otherwise) */
 } flash_gau_workspace_layout;
 /* Intermediates are row-major, except those marked (*) for FLASH_GAU_BF16:
  * these, seen as [rows, e] matrices (rows = B*T, B*G*s or B*s), are stored

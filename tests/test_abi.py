@@ -44,7 +44,7 @@ def test_version_and_strerror(L):
 def test_layout_offsets_aligned_and_sized(L):
     B, T, C, d, e, s = 2, 8192, 256, 768, 1536, 128
     lay = bd.workspace_layout(B, T, C, d, e, s, True, bd.BF16)
-    order = ["status", "U", "V", "heads", "state", "prefix", "gated", "bias", "xn"]
+    order = ["status", "U", "V", "heads", "state", "prefix", "gated", "bias", "xn", "rope"]
     offs = [lay[k] for k in order]
     assert offs == sorted(offs)
     assert all(o % 256 == 0 for o in offs)
@@ -56,7 +56,8 @@ def test_layout_offsets_aligned_and_sized(L):
     assert lay["gated"] - lay["prefix"] >= B * G * s * e * 2
     assert lay["bias"] - lay["gated"] >= M * e * 2
     assert lay["xn"] - lay["bias"] >= (2 * C - 1) * 4
-    assert lay["total_bytes"] - lay["xn"] >= M * d * 2
+    assert lay["rope"] - lay["xn"] >= M * d * 2
+    assert lay["total_bytes"] - lay["rope"] >= T * (s // 2) * 4
     nc = bd.workspace_layout(B, T, C, d, e, s, False, bd.BF16)
     assert nc["gated"] - nc["prefix"] < lay["gated"] - lay["prefix"]  # [B,s,e] only
 
