@@ -253,6 +253,38 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t[0])
 
+    # ---- next row: the flash_block wrapper (LayerNorm, RoPE on the four heads,
+    # residual) around the same layer on the same workload, timed the same way
+    nrng = np.random.default_rng(1000 + w["seed"])
+    norm_g = torch.tensor(nrng.normal(1.0, 0.1, d), dtype=torch.float32, device=dev)
+    norm_b = torch.tensor(nrng.normal(0.0, 0.1, d), dtype=torch.float32, device=dev)
+
+    def block_step():
+        bd.block_forward(X, weights, C, causal, norm=bd.NORM_LAYER, norm_g=norm_g,
+                         norm_b=norm_b, rope=True, residual=True, out=out, workspace=ws,
+                         stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        block_step()
+    blk_steps = max(1, min(args.steps, 200))
+    b0 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+    b1 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+    torch.cuda.synchronize()
+    for k in range(blk_steps):
+        flush.fill_(1.0)
+        b0[k].record(stream)
+        block_step()
+        b1[k].record(stream)
+    torch.cuda.synchronize()
+    block_ms = sum(a.elapsed_time(b) for a, b in zip(b0, b1)) / blk_steps
+    if bd.workspace_status(ws) != 0:
+        raise RuntimeError("kernel status after the flash_block runs")
+    if world > 1:
+        t = torch.tensor([block_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        block_ms = float(t[0])
+
     if rank != 0:
         return None
     peaks = _peaks()
@@ -318,6 +350,12 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
                 "ms_per_step": round(e2e_ms, 5)},
         "clocks": clocks,
+        "next_rows": {"flash_block": {
+            "what": "LayerNorm + RoPE on the four heads (global positions) + residual "
+                    "around the same layer, same workload",
+            "value": round(tokens / (block_ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(block_ms, 5),
+            "extra_ms_over_layer": round(block_ms - step_ms, 5)}},
     }
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
