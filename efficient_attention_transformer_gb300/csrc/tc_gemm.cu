@@ -38,7 +38,8 @@ constexpr int B_BYTES = BN * BK * 2;      // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
-constexpr int NUM_THREADS = 192;  // producer warp, MMA warp, 4 epilogue warps
+// producer warp, MMA warp, 4 epilogue warps; 6 more warps join the scan
+constexpr int NUM_THREADS = 384;
 constexpr int STG_BYTES = 32 * 128;                  // one 32-row x 128-byte store box
 constexpr int STG_OFF = STAGES * STAGE_BYTES;        // 2 staging boxes per epilogue warp
 constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
@@ -330,7 +331,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mma_commit(smem_u32(&sm->drain));
       if (!mbar_wait(smem_u32(&sm->drain), 0)) raise_timeout(sm, p.status);
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     Stager st{tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES, lane};
