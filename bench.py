@@ -290,7 +290,8 @@ def run_ours(args, rank, world, local_rank):
     peaks = _peaks()
     work = stage_work(w)
     tokens = B * T * world
-    total_flops = sum(f for f, _ in work.values())
+    # the stages this schedule runs (the table also lists the other dtype's)
+    total_flops = sum(work[n][0] for n in names)
     stages = {}
     for j, n in enumerate(names):
         f, b = work[n]

@@ -141,6 +141,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
+// L2 eviction priority policies for bulk tensor copies: evict_last keeps the
+// lines a later kernel reads again ahead of other data; evict_first lets a
+// last read leave first.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_load_2d with an L2 policy
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, uint32_t bar,
+                                                 int x, int y, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(pol)
+      : "memory");
+}
+
 // Same load, written to the same shared-memory offset of every CTA of the
 // cluster in `mask` and signalling the mbarrier at the same offset in each.
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int x,
@@ -171,6 +194,15 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(tmap)),
       "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+// tma_store_2d with an L2 policy
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src, int x, int y,
+                                                  uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tma_store_commit() {

@@ -110,11 +110,14 @@ struct Stager {
 #pragma unroll
     for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(b + sw128_offset(lane, c)) = w[c];
   }
-  __device__ void finish(uint8_t *b, const CUtensorMap *tm, int x, int y) {
+  // keep: store with the L2 evict_last policy, for data the next kernels
+  // read again
+  __device__ void finish(uint8_t *b, const CUtensorMap *tm, int x, int y, bool keep = false) {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tm, smem_u32(b), x, y);
+      if (keep) tma_store_2d_hint(tm, smem_u32(b), x, y, l2_evict_last());
+      else tma_store_2d(tm, smem_u32(b), x, y);
       tma_store_commit();
     }
     ++count;
@@ -343,8 +346,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             pack64(ra, rb, [](float x, int) { return swish_tanh(x); }, w);
             uint8_t *b = st.begin();
             st.put(b, w);
+            // V is read by the chunk-state and the attention kernels: kept in
+            // L2 ahead of U, which only the attention reads
             if (n < p.e) st.finish(b, &tmC0, n, row0);
-            else st.finish(b, &tmC1, 0, (int)rb64_row(row0, n - p.e, p.e / 64));
+            else st.finish(b, &tmC1, 0, (int)rb64_row(row0, n - p.e, p.e / 64), true);
           } else {
             const int c = n - 2 * p.e;  // column inside Z
 #pragma unroll
