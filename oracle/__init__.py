@@ -13,6 +13,8 @@ from .flash_gau import (  # noqa: F401
     layer_norm,
     scale_norm,
     rope,
+    rope_toeplitz_bias,
+    toeplitz_relpos,
     flash_gau,
     flash_block,
     algorithmic_flops_per_token,

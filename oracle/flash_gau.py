@@ -56,6 +56,8 @@ __all__ = [
     "layer_norm",
     "scale_norm",
     "rope",
+    "rope_toeplitz_bias",
+    "toeplitz_relpos",
     "flash_gau",
     "flash_block",
     "algorithmic_flops_per_token",
@@ -164,6 +166,39 @@ def rope(h, positions, base=10000.0):
     out = np.empty_like(h)
     out[..., 0::2] = even * cos - odd * sin
     out[..., 1::2] = even * sin + odd * cos
+    return out
+
+
+def rope_toeplitz_bias(a, b, n, base=10000.0):
+    """Relative position bias of a length-n window built from two learned
+    vectors with RoPE: [TQLT-zh] appendix D, Code 4, the branch for windows
+    of 512 positions and more.  Both vectors are tiled over the n positions,
+    each copy rotated by RoPE at its row's position, and the bias is the
+    n x n matrix of their dot products: bias[i, j] = rope(a)_i . rope(b)_j.
+
+    a, b: [m], m even (the listing uses m = 128).  Same rotary convention as
+    ``rope`` (consecutive pairs, angle p * base^(-2i/m))."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape or a.ndim != 1:
+        raise ValueError("a and b must be vectors of the same length")
+    pos = np.arange(n)
+    A = rope(np.tile(a[None, :], (n, 1)), pos, base)
+    Bm = rope(np.tile(b[None, :], (n, 1)), pos, base)
+    return A @ Bm.T
+
+
+def toeplitz_relpos(T):
+    """The 2n-1 weights of an n x n Toeplitz matrix in the layer's table
+    form, relpos[j - i + n - 1] = T[i, j]: offsets j - i < 0 read down the
+    first column, offsets >= 0 along the first row.  The inverse of
+    ``relpos_bias``."""
+    T = np.asarray(T, dtype=np.float64)
+    n = T.shape[0]
+    out = np.empty(2 * n - 1)
+    for k in range(2 * n - 1):
+        d = k - (n - 1)
+        out[k] = T[0, d] if d >= 0 else T[-d, 0]
     return out
 
 

@@ -432,3 +432,44 @@ def test_block_is_residual_around_the_layer_of_the_normalised_input():
     np.testing.assert_allclose(Y - inp["X"], ref, rtol=1e-10, atol=1e-12)
     Y0 = _block(inp, 4, True, norm=None, rope_on=False)
     np.testing.assert_allclose(Y0 - inp["X"], _run(inp, 4, True)[0], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- RoPE-Toeplitz bias
+import oracle as O  # noqa: E402
+def test_rope_toeplitz_golden_worked_example():
+    """Hand-worked 3 x 3 bias from a = (1, 0), b = (0, 1) (tests/golden)."""
+    with open(os.path.join(GOLDEN, "rope_toeplitz_m2_n3.txt")) as f:
+        want = np.array([[float(x) for x in ln.split()] for ln in f
+                         if ln.strip() and not ln.startswith("#")])
+    got = O.rope_toeplitz_bias(np.array([1.0, 0.0]), np.array([0.0, 1.0]), 3)
+    assert np.allclose(got, want, rtol=0, atol=1e-15)
+
+
+def test_rope_toeplitz_depends_on_offset_only():
+    """Rotations compose (R(i)^T R(j) = R(j - i)), so the bias is Toeplitz:
+    every diagonal is constant, for any vectors and base."""
+    rng = np.random.default_rng(21)
+    for m, n, base in [(8, 9, 10000.0), (128, 40, 10000.0), (6, 17, 37.0)]:
+        T = O.rope_toeplitz_bias(rng.normal(size=m), rng.normal(size=m), n, base)
+        assert np.allclose(T[1:, 1:], T[:-1, :-1], rtol=0, atol=1e-12)
+        # and it is not symmetric in general (a and b play different roles)
+        assert not np.allclose(T, T.T)
+
+
+def test_rope_toeplitz_diagonal_is_inner_product():
+    """On the diagonal both copies turn by the same angle: bias[i, i] = a . b."""
+    rng = np.random.default_rng(22)
+    a, b = rng.normal(size=128), rng.normal(size=128)
+    T = O.rope_toeplitz_bias(a, b, 33)
+    assert np.allclose(np.diag(T), a @ b, rtol=1e-12, atol=1e-12)
+
+
+def test_toeplitz_relpos_round_trip():
+    """Reading the table back and rebuilding the matrix with relpos_bias
+    gives the same matrix (the layer's bias index rule, pinned by the Code 4
+    fixtures, is the inverse)."""
+    rng = np.random.default_rng(23)
+    T = O.rope_toeplitz_bias(rng.normal(size=16), rng.normal(size=16), 12)
+    rp = O.toeplitz_relpos(T)
+    assert rp.shape == (23,)
+    assert np.allclose(O.relpos_bias(rp, 12), T, rtol=0, atol=1e-12)
