@@ -285,6 +285,23 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         block_ms = float(t[0])
 
+    # ---- next row: the RoPE construction of the relative-position table
+    # (windows of 512 and more), 128-wide learned vectors, C = 512
+    trng = np.random.default_rng(2000 + w["seed"])
+    ta = torch.tensor(trng.normal(0, 0.1, 128), dtype=torch.float32, device=dev)
+    tb = torch.tensor(trng.normal(0, 0.1, 128), dtype=torch.float32, device=dev)
+    tout = torch.empty(2 * 512 - 1, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        bd.rope_toeplitz_bias(ta, tb, 512, out=tout, stream=stream)
+    tn = 100
+    te0, te1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    te0.record(stream)
+    for _ in range(tn):
+        bd.rope_toeplitz_bias(ta, tb, 512, out=tout, stream=stream)
+    te1.record(stream)
+    torch.cuda.synchronize()
+    toeplitz_us = te0.elapsed_time(te1) * 1e3 / tn
+
     if rank != 0:
         return None
     peaks = _peaks()
@@ -356,7 +373,11 @@ def run_ours(args, rank, world, local_rank):
                     "around the same layer, same workload",
             "value": round(tokens / (block_ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(block_ms, 5),
-            "extra_ms_over_layer": round(block_ms - step_ms, 5)}},
+            "extra_ms_over_layer": round(block_ms - step_ms, 5)},
+            "rope_toeplitz_bias": {
+                "what": "relative-position table of the RoPE bias construction, C = 512, "
+                        "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",
+                "us_per_call": round(toeplitz_us, 2)}},
     }
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)

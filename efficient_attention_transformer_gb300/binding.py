@@ -41,6 +41,7 @@ EXPORTED = (
     "flash_gau_version",
     "flash_gau_forward_noalloc",
     "flash_gau_block_forward",
+    "flash_gau_rope_toeplitz_bias",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -125,6 +126,8 @@ def lib():
         L.flash_gau_block_forward.argtypes = [p, ctypes.POINTER(Weights), ctypes.POINTER(Block),
                                               i, i, i, i, i, p, p, sz, p]
         L.flash_gau_block_forward.restype = i
+        L.flash_gau_rope_toeplitz_bias.argtypes = [p, p, i, i, ctypes.c_float, p, p]
+        L.flash_gau_rope_toeplitz_bias.restype = i
         _lib = L
     return _lib
 
@@ -294,3 +297,20 @@ def workspace_status(workspace, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(workspace.device)
     return lib().flash_gau_workspace_status(_dev_ptr(workspace, "workspace"), stream.cuda_stream)
+
+
+def rope_toeplitz_bias(a, b, C, rope_base=10000.0, out=None, stream=None):
+    """The layer's relative-position table [2C-1] (fp32, device) of the RoPE
+    bias construction from the learned vectors a, b ([m] fp32 CUDA tensors),
+    through flash_gau_rope_toeplitz_bias."""
+    f32 = torch.float32
+    if a.shape != b.shape or a.dim() != 1:
+        raise ValueError("a and b must be vectors of the same length")
+    if out is None:
+        out = torch.empty(2 * C - 1, dtype=f32, device=a.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    _check(lib().flash_gau_rope_toeplitz_bias(
+        _dev_ptr(a, "a", f32), _dev_ptr(b, "b", f32), a.numel(), C, float(rope_base),
+        _dev_ptr(out, "out", f32), stream.cuda_stream))
+    return out

@@ -3,7 +3,9 @@
 // residual): the pre-norm of X into the workspace region xn, for both io
 // types, and for fp32 the RoPE rotation of the heads in place (the bf16
 // projection rotates them in its epilogue, the output epilogues add the
-// residual).
+// residual).  Also the RoPE construction of the relative position bias for
+// long windows (appendix D, Code 4): the table of the layer's bias from two
+// learned vectors.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -235,6 +237,28 @@ bool norm_fills_rope_table(const Problem &p) {
          (p.norm != FLASH_GAU_NORM_LAYER || (al16(p.norm_g) && al16(p.norm_b)));
 }
 
+// relpos[k] = rope(a)_i . rope(b)_j for any i, j with j - i = k - (C - 1):
+// rotating a by i and b by j leaves a . R(j - i) b, per pair
+// (a0 b0 + a1 b1) cos(delta) + (a1 b0 - a0 b1) sin(delta), delta = (j - i)
+// times the pair's frequency.  One thread per entry, fp32 sums over the
+// pairs, the angles from the same exact-turns method as the heads' RoPE.
+__global__ void __launch_bounds__(256)
+rope_toeplitz_kernel(const float *__restrict__ a, const float *__restrict__ b, int pairs, int C,
+                     const RopeTable phi, float *__restrict__ relpos) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= 2 * C - 1) return;
+  const float off = (float)(k - (C - 1));  // exact: |off| < 2^24
+  float acc = 0.f;
+  for (int q = 0; q < pairs; ++q) {
+    float sn, cs;
+    rope_sincos(off, phi.phi[q], &sn, &cs);
+    const float a0 = a[2 * q], a1 = a[2 * q + 1], b0 = b[2 * q], b1 = b[2 * q + 1];
+    acc = fmaf(fmaf(a0, b0, a1 * b1), cs, acc);
+    acc = fmaf(fmaf(a1, b0, -a0 * b1), sn, acc);
+  }
+  relpos[k] = acc;
+}
+
 }  // namespace
 
 cudaError_t block_norm(const Problem &p) {
@@ -256,6 +280,15 @@ cudaError_t rope_table_stage(const Problem &p) {
   if (p.norm != FLASH_GAU_NORM_NONE && norm_fills_rope_table(p)) return cudaSuccess;
   const RopeJob r = rope_job(p);
   return launch_pdl(rope_table_kernel, dim3(rope_blocks(r)), dim3(256), 0, p.stream, r);
+}
+
+cudaError_t rope_toeplitz_bias(const float *a, const float *b, int m, int C, float base,
+                               float *relpos, cudaStream_t stream) {
+  RopeTable phi;
+  rope_table(&phi, m, base);
+  const unsigned n = (unsigned)(2 * C - 1);
+  rope_toeplitz_kernel<<<(n + 255) / 256, 256, 0, stream>>>(a, b, m / 2, C, phi, relpos);
+  return cudaGetLastError();
 }
 
 cudaError_t simt_rope_heads_f32(const Problem &p) {

@@ -288,6 +288,16 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B, in
                      stream, stage_events, n_events);
 }
 
+int flash_gau_rope_toeplitz_bias(const float *a, const float *b, int m, int C, float rope_base,
+                                 float *relpos, void *stream) {
+  if (!a || !b || !relpos) return FLASH_GAU_EINVAL;
+  if (m < 2 || m % 2 != 0 || m > 128 || C < 1 || C > 4096 || !(rope_base > 1.f))
+    return FLASH_GAU_EINVAL;
+  const cudaError_t err =
+      rope_toeplitz_bias(a, b, m, C, rope_base, relpos, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? FLASH_GAU_OK : record_cuda(err);
+}
+
 int flash_gau_block_forward(const void *X, const flash_gau_weights *w, const flash_gau_block *blk,
                             int B, int T, int C, int causal, int dtype, void *out,
                             void *workspace, size_t workspace_bytes, void *stream) {

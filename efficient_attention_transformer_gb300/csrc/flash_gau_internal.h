@@ -117,6 +117,9 @@ struct Stage {
 cudaError_t block_norm(const Problem &p);
 cudaError_t rope_table_stage(const Problem &p);
 cudaError_t simt_rope_heads_f32(const Problem &p);
+// the relative-position table of the RoPE bias construction (block_kernels.cu)
+cudaError_t rope_toeplitz_bias(const float *a, const float *b, int m, int C, float base,
+                               float *relpos, cudaStream_t stream);
 
 // fp32 SIMT stages (simt_kernels.cu)
 cudaError_t simt_projection_f32(const Problem &p);

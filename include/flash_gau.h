@@ -209,6 +209,23 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
                             int causal, int dtype, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* ---- RoPE construction of the relative position bias ------------------- */
+/* Appendix D, Code 4 of "Transformer Quality in Linear Time" builds the bias
+ * of windows of 512 positions and more from two learned vectors a, b of
+ * width m (128 there): both are tiled over the window, each row rotated by
+ * RoPE at its position, and bias[i][j] = rope(a)_i . rope(b)_j.  Rotations
+ * compose, so the matrix depends on j - i only; this call writes it in the
+ * layer's table form, relpos[j - i + C - 1] (2C - 1 fp32 values), ready to
+ * pass as flash_gau_weights.relpos.
+ *   a, b       device fp32 [m], m even, 2 <= m <= 128
+ *   C          window (chunk) length, 1 <= C <= 4096
+ *   rope_base  > 1; the pair (2k, 2k+1) turns by p * rope_base^(-2k/m)
+ *   relpos     device fp32 [2C - 1], written
+ * Enqueued on `stream`, no synchronisation.  Returns FLASH_GAU_OK,
+ * FLASH_GAU_EINVAL (null pointer or sizes out of range) or FLASH_GAU_ECUDA. */
+int flash_gau_rope_toeplitz_bias(const float *a, const float *b, int m, int C,
+                                 float rope_base, float *relpos, void *stream);
+
 /* ---- allocation-free variant ------------------------------------------- */
 /* No counterpart on the pages: this entry point exists for deployment, not
  * for the method.
