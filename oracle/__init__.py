@@ -19,3 +19,4 @@ from .flash_gau import (  # noqa: F401
     flash_block,
     algorithmic_flops_per_token,
 )
+from .backward import swish_grad, flash_gau_backward  # noqa: F401,E402

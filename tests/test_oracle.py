@@ -473,3 +473,51 @@ def test_toeplitz_relpos_round_trip():
     rp = O.toeplitz_relpos(T)
     assert rp.shape == (23,)
     assert np.allclose(O.relpos_bias(rp, 12), T, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+@pytest.mark.parametrize("causal,lin_scale,C", [(True, 1.0, 4), (False, 1.0, 4),
+                                                (True, 0.25, 2), (False, 0.0, 8)])
+def test_backward_matches_finite_differences(causal, lin_scale, C):
+    """Every gradient entry of L = sum(dO * O) against central differences of
+    the forward oracle (step 1e-6, float64), on a problem small enough to
+    perturb each input and parameter once."""
+    rng = np.random.default_rng(51 + C)
+    B, T, d, e, s = 2, 8, 4, 6, 4
+    args = dict(
+        X=rng.normal(size=(B, T, d)), W_u=rng.normal(size=(d, e)) / 2,
+        W_v=rng.normal(size=(d, e)) / 2, W_z=rng.normal(size=(d, s)) / 2,
+        W_o=rng.normal(size=(e, d)) / 2, gamma=rng.normal(1.0, 0.3, (4, s)),
+        beta=rng.normal(0.0, 0.3, (4, s)), relpos=rng.normal(0.0, 0.5, 2 * C - 1))
+    dO = rng.normal(size=(B, T, d))
+
+    def loss(a):
+        O, _ = flash_gau(a["X"], a["W_u"], a["W_v"], a["W_z"], a["W_o"], a["gamma"],
+                         a["beta"], a["relpos"], C, causal, lin_scale)
+        return float(np.sum(dO * O))
+
+    grads = O.flash_gau_backward(args["X"], args["W_u"], args["W_v"], args["W_z"], args["W_o"],
+                                 args["gamma"], args["beta"], args["relpos"], C, causal, dO,
+                                 lin_scale)
+    h = 1e-6
+    for name in args:
+        g = grads["d" + name]
+        assert g.shape == args[name].shape
+        num = np.zeros_like(g)
+        for idx in np.ndindex(*g.shape):
+            plus = {k: v.copy() for k, v in args.items()}
+            minus = {k: v.copy() for k, v in args.items()}
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            num[idx] = (loss(plus) - loss(minus)) / (2 * h)
+        scale = max(1.0, float(np.max(np.abs(num))))
+        assert np.max(np.abs(num - g)) <= 1e-6 * scale, (name, np.max(np.abs(num - g)))
+
+
+def test_swish_grad_against_library_derivative():
+    """swish'(x) = d/dx [x * expit(x)] computed with scipy's expit and the
+    product rule on a grid, including large |x|."""
+    x = np.linspace(-30, 30, 1201)
+    sg = scipy.special.expit(x)
+    want = sg + x * sg * (1 - sg)
+    assert np.allclose(O.swish_grad(x), want, rtol=1e-12, atol=1e-15)
