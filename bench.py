@@ -27,6 +27,18 @@ sys.path.insert(0, ROOT)
 METRIC = "FLASH GAU layer forward tokens/sec at T=8192 causal; % of bf16 TC roofline"
 DEFAULT_WORKLOAD = "long_causal_B2_T8192"
 L2_FLUSH_BYTES = 512 << 20
+# CUDA-core fp32 peak of a GB300, from unit counts and the clock: 152 SMs x
+# 128 fp32 lanes x 2 flops per FMA x 2.07 GHz (maximum SM clock)
+FP32_CORE_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def lib_backward_bytes(bd, weights, B, T, C, causal):
+    import ctypes
+    n = bd.lib().flash_gau_backward_workspace_bytes(B, T, C, ctypes.byref(weights.c),
+                                                    int(bool(causal)), weights.dtype)
+    if n == 0:
+        raise RuntimeError("backward workspace size")
+    return n
 
 
 def _peaks():
@@ -302,6 +314,24 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     toeplitz_us = te0.elapsed_time(te1) * 1e3 / tn
 
+    # ---- next row: the backward pass on the same workload (gradients of
+    # sum(dO * O) for X and every parameter), dO seeded like X
+    dO = torch.tensor(np.random.default_rng(3000 + w["seed"]).normal(size=(B, T, d)), dtype=tdt,
+                      device=dev)
+    bws = torch.empty(lib_backward_bytes(bd, weights, B, T, C, causal), dtype=torch.uint8,
+                      device=dev)
+    bd.backward(X, dO, weights, C, causal, workspace=bws, stream=stream)  # warm-up
+    bn = 3
+    be0, be1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    be0.record(stream)
+    for _ in range(bn):
+        bd.backward(X, dO, weights, C, causal, workspace=bws, stream=stream)
+    be1.record(stream)
+    torch.cuda.synchronize()
+    backward_ms = be0.elapsed_time(be1) / bn
+    del bws
+
     if rank != 0:
         return None
     peaks = _peaks()
@@ -374,6 +404,15 @@ def run_ours(args, rank, world, local_rank):
             "value": round(tokens / (block_ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(block_ms, 5),
             "extra_ms_over_layer": round(block_ms - step_ms, 5)},
+            "backward": {
+                "what": "gradients of sum(dO * O) for X, W_uvz, W_o, gamma, beta, relpos "
+                        "(recomputes the forward's intermediates), fp32 CUDA-core GEMMs",
+                "ms_per_call": round(backward_ms, 3),
+                "value": round(tokens / (backward_ms * 1e-3), 1), "unit": "tokens/s",
+                # two contractions per forward contraction, plus the recompute
+                "algorithmic_tflops": round(2 * total_flops / (backward_ms * 1e-3) / 1e12, 2),
+                "executed_tflops": round(3 * total_flops / (backward_ms * 1e-3) / 1e12, 2),
+                "fp32_core_peak_tflops": round(FP32_CORE_PEAK_TFLOPS, 1)},
             "rope_toeplitz_bias": {
                 "what": "relative-position table of the RoPE bias construction, C = 512, "
                         "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",

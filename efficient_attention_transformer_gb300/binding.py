@@ -42,6 +42,8 @@ EXPORTED = (
     "flash_gau_forward_noalloc",
     "flash_gau_block_forward",
     "flash_gau_rope_toeplitz_bias",
+    "flash_gau_backward_workspace_bytes",
+    "flash_gau_backward",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -128,6 +130,11 @@ def lib():
         L.flash_gau_block_forward.restype = i
         L.flash_gau_rope_toeplitz_bias.argtypes = [p, p, i, i, ctypes.c_float, p, p]
         L.flash_gau_rope_toeplitz_bias.restype = i
+        L.flash_gau_backward_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights), i, i]
+        L.flash_gau_backward_workspace_bytes.restype = sz
+        L.flash_gau_backward.argtypes = [p, p, ctypes.POINTER(Weights), i, i, i, i, i,
+                                         ctypes.POINTER(Grads), p, sz, p]
+        L.flash_gau_backward.restype = i
         _lib = L
     return _lib
 
@@ -174,6 +181,12 @@ def _dev_ptr(t, name, dtype=None):
     if dtype is not None and t.dtype != dtype:
         raise ValueError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
     return t.data_ptr()
+
+
+class Grads(ctypes.Structure):
+    _fields_ = [("dX", ctypes.c_void_p), ("dW_uvz", ctypes.c_void_p), ("dW_o", ctypes.c_void_p),
+                ("dgamma", ctypes.c_void_p), ("dbeta", ctypes.c_void_p),
+                ("drelpos", ctypes.c_void_p)]
 
 
 class GauWeights:
@@ -313,4 +326,38 @@ def rope_toeplitz_bias(a, b, C, rope_base=10000.0, out=None, stream=None):
     _check(lib().flash_gau_rope_toeplitz_bias(
         _dev_ptr(a, "a", f32), _dev_ptr(b, "b", f32), a.numel(), C, float(rope_base),
         _dev_ptr(out, "out", f32), stream.cuda_stream))
+    return out
+
+
+def backward(X, dO, weights, C, causal, workspace=None, stream=None):
+    """Gradients of sum(dO * O) through flash_gau_backward: a dict with dX
+    (io type) and dW_uvz, dW_o, dgamma, dbeta, drelpos (fp32), on X's
+    device."""
+    if X.dim() != 3 or dO.shape != X.shape:
+        raise ValueError("X and dO must be [B, T, d]")
+    B, T, d = X.shape
+    if d != weights.d or X.dtype != weights.W_uvz.dtype or dO.dtype != X.dtype:
+        raise ValueError("X, dO and the weights must agree")
+    f32, dev = torch.float32, X.device
+    e, s = weights.e, weights.s
+    out = dict(dX=torch.empty_like(X),
+               dW_uvz=torch.empty(d, 2 * e + s, dtype=f32, device=dev),
+               dW_o=torch.empty(e, d, dtype=f32, device=dev),
+               dgamma=torch.empty(4, s, dtype=f32, device=dev),
+               dbeta=torch.empty(4, s, dtype=f32, device=dev),
+               drelpos=torch.empty(2 * C - 1, dtype=f32, device=dev))
+    g = Grads(*(_dev_ptr(out[k], k) for k in ("dX", "dW_uvz", "dW_o", "dgamma", "dbeta",
+                                             "drelpos")))
+    n = lib().flash_gau_backward_workspace_bytes(B, T, C, ctypes.byref(weights.c),
+                                                 int(bool(causal)), weights.dtype)
+    if n == 0:
+        raise FlashGauError(EINVAL, "invalid or unsupported problem")
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    _check(lib().flash_gau_backward(
+        _dev_ptr(X, "X", X.dtype), _dev_ptr(dO, "dO", X.dtype), ctypes.byref(weights.c), B, T, C,
+        int(bool(causal)), weights.dtype, ctypes.byref(g), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), stream.cuda_stream))
     return out

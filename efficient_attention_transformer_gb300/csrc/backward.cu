@@ -1,0 +1,402 @@
+// Backward pass of the FLASH GAU layer: the gradients of sum(dO * O) with
+// respect to X and every parameter ("Transformer Quality in Linear Time",
+// Method, eq. 5, eq. 7, eq. 8 and the display after it, differentiated by
+// the chain rule).  CUDA-core fp32 throughout, for both io types (bf16
+// operands are widened as they are loaded):
+//
+//   recompute  Pre = X W_uvz;  U, V, Z = swish(Pre);  heads = Z gamma + beta
+//              S = Qq Kq^T / C + b,  P = relu(S)^2 (masked)      per chunk
+//              Vh = P V + lin_scale Q_lin Prefix_g,  A = U * Vh
+//   output     dW_o = A^T dO,  dA = dO W_o^T,  dU = dA * Vh,  dVh = dA * U
+//   local      dP = dVh V^T,  dV = P^T dVh,  dS = 2 relu(S) dP (masked),
+//              dQq = dS Kq / C,  dKq = dS^T Qq / C,  db[j-i] += dS[i, j]
+//   global     dQl = lin_scale dVh Prefix^T,  dPrefix = lin_scale Ql^T dVh,
+//              dState_h = sum_{g>h} dPrefix_g (or the total),
+//              dKl = V dState^T,  dV += Kl dState
+//   heads      dZ = sum_k dhead_k gamma_k,  dgamma, dbeta = column sums
+//   input      dPre = d(U|V|Z) * swish'(Pre),  dX = dPre W_uvz^T,
+//              dW_uvz = X^T dPre
+//
+// The contractions run on one batched, strided GEMM kernel (64 x 64 tiles,
+// 4 x 4 per thread), so transposed views cost no copies; the rest are
+// elementwise or column-reduction kernels.
+#include <cuda_bf16.h>
+
+#include "flash_gau_internal.h"
+
+namespace flashgau {
+namespace {
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float sigmoid(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float swish(float x) { return x * sigmoid(x); }
+__device__ __forceinline__ float swish_grad(float x) {
+  const float sg = sigmoid(x);
+  return sg * (1.0f + x * (1.0f - sg));
+}
+
+// ------------------------------------------------------------------ GEMM --
+// C[z](m, n) = sum_k A[z / adiv](m, k) B[z / bdiv](k, n), handed to the
+// epilogue per element.  Element strides: A(m, k) at m * sam + k * sak, B(k,
+// n) at k * sbk + n * sbn; batches z = blockIdx.z.
+constexpr int kTile = 64;
+constexpr int kTileK = 16;
+
+struct Operand {
+  long long sm, sk, sb;  // for B: sm is the k stride and sk the n stride
+  int div;
+};
+
+template <typename TA, typename TB, typename Epi>
+__global__ void __launch_bounds__(256)
+bw_gemm(int M, int N, int K, const TA *__restrict__ A, Operand oa, const TB *__restrict__ Bm,
+        Operand ob, Epi epi) {
+  __shared__ float As[kTileK][kTile + 1];
+  __shared__ float Bs[kTileK][kTile + 1];
+  const int z = blockIdx.z;
+  const int m0 = blockIdx.y * kTile, n0 = blockIdx.x * kTile;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  A += (long long)(z / oa.div) * oa.sb;
+  Bm += (long long)(z / ob.div) * ob.sb;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += kTileK) {
+    for (int idx = threadIdx.x; idx < kTile * kTileK; idx += 256) {
+      const int kk = idx % kTileK, mm = idx / kTileK;
+      const int gm = m0 + mm, gk = k0 + kk;
+      As[kk][mm] = (gm < M && gk < K) ? to_f(A[gm * oa.sm + gk * oa.sk]) : 0.f;
+      const int nn = idx % kTile, kb = idx / kTile;
+      const int gn = n0 + nn, gk2 = k0 + kb;
+      Bs[kb][nn] = (gn < N && gk2 < K) ? to_f(Bm[gk2 * ob.sm + gn * ob.sk]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kTileK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+      if (m < M && n < N) epi(z, m, n, acc[i][j]);
+    }
+}
+
+// C[z](m, n) = alpha * acc (+ C when accumulating), fp32
+struct StoreF32 {
+  float *C;
+  long long scm, scn, scb;
+  float alpha;
+  int accumulate;
+  __device__ void operator()(int z, int m, int n, float v) const {
+    float *p = C + z * scb + m * scm + n * scn;
+    *p = accumulate ? *p + alpha * v : alpha * v;
+  }
+};
+
+// dX in the io type
+template <typename T>
+struct StoreIo;
+template <>
+struct StoreIo<float> {
+  float *C;
+  long long ld;
+  __device__ void operator()(int, int m, int n, float v) const { C[m * ld + n] = v; }
+};
+template <>
+struct StoreIo<__nv_bfloat16> {
+  __nv_bfloat16 *C;
+  long long ld;
+  __device__ void operator()(int, int m, int n, float v) const {
+    C[m * ld + n] = __float2bfloat16_rn(v);
+  }
+};
+
+// scores of chunk z: S = acc / C + relpos[j - i + C - 1], P = relu(S)^2,
+// zero above the diagonal when causal
+struct ScoreEpi {
+  float *S, *P;
+  const float *relpos;
+  int C, causal;
+  float inv_c;
+  __device__ void operator()(int z, int i, int j, float v) const {
+    const float s = fmaf(v, inv_c, relpos[j - i + C - 1]);
+    const long long o = ((long long)z * C + i) * C + j;
+    S[o] = s;
+    const float r = fmaxf(s, 0.f);
+    P[o] = (causal && j > i) ? 0.f : r * r;
+  }
+};
+
+template <typename TA, typename TB, typename Epi>
+cudaError_t gemm(cudaStream_t st, int M, int N, int K, int batches, const TA *A, Operand oa,
+                 const TB *Bm, Operand ob, Epi epi) {
+  if (M <= 0 || N <= 0 || batches <= 0) return cudaSuccess;
+  dim3 grid((N + kTile - 1) / kTile, (M + kTile - 1) / kTile, batches);
+  bw_gemm<TA, TB, Epi><<<grid, 256, 0, st>>>(M, N, K, A, oa, Bm, ob, epi);
+  return cudaGetLastError();
+}
+
+Operand op(long long sm, long long sk, long long sb = 0, int div = 1) { return {sm, sk, sb, div}; }
+
+// ------------------------------------------------------------ elementwise --
+// U, V, Z = swish(Pre) and the four heads Z gamma_k + beta_k
+__global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
+                          float *__restrict__ V, float *__restrict__ Z, float *__restrict__ H,
+                          const float *__restrict__ gamma, const float *__restrict__ beta,
+                          long long M, int e, int s) {
+  const int N = 2 * e + s;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / N;
+    const int c = (int)(i - m * N);
+    const float y = swish(pre[i]);
+    if (c < e) {
+      U[m * e + c] = y;
+    } else if (c < 2 * e) {
+      V[m * e + c - e] = y;
+    } else {
+      const int k = c - 2 * e;
+      Z[m * s + k] = y;
+      for (int h = 0; h < 4; ++h) H[(h * M + m) * s + k] = fmaf(y, gamma[h * s + k], beta[h * s + k]);
+    }
+  }
+}
+
+// A = U * Vh
+__global__ void gate(const float *__restrict__ U, const float *__restrict__ Vh,
+                     float *__restrict__ A, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    A[i] = U[i] * Vh[i];
+}
+
+// dU = dA * Vh, dVh = dA * U
+__global__ void gate_grad(const float *__restrict__ dA, const float *__restrict__ U,
+                          const float *__restrict__ Vh, float *__restrict__ dU,
+                          float *__restrict__ dVh, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    dU[i] = dA[i] * Vh[i];
+    dVh[i] = dA[i] * U[i];
+  }
+}
+
+// dS = 2 relu(S) dP, zero above the diagonal when causal (in place over dP)
+__global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, long long chunks,
+                           int C, int causal) {
+  const long long n = chunks * C * C;
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n;
+       o += (long long)gridDim.x * blockDim.x) {
+    const int j = (int)(o % C), i = (int)((o / C) % C);
+    dP[o] = (causal && j > i) ? 0.f : 2.f * fmaxf(S[o], 0.f) * dP[o];
+  }
+}
+
+// drelpos[k] = sum over chunks and over (i, j) with j - i = k - (C - 1)
+__global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ drelpos,
+                            long long chunks, int C) {
+  const int k = blockIdx.x;  // 0 .. 2C - 2
+  const int off = k - (C - 1);
+  const int i0 = off < 0 ? -off : 0, n = C - (off < 0 ? -off : off);
+  float acc = 0.f;
+  for (long long t = threadIdx.x; t < chunks * n; t += blockDim.x) {
+    const long long z = t / n;
+    const int i = i0 + (int)(t - z * n);
+    acc += dS[(z * C + i) * C + i + off];
+  }
+  __shared__ float red[256];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w /= 2) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) drelpos[k] = red[0];
+}
+
+// prefix[b][g] = lin_scale * (exclusive sum over chunks, or the total)
+__global__ void scan_forward(const float *__restrict__ state, float *__restrict__ prefix, int B,
+                             int G, long long se, int causal, float lin_scale) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long b = i / se, r = i - b * se;
+    float run = 0.f;
+    for (int g = 0; g < G; ++g) {
+      if (causal) prefix[(b * G + g) * se + r] = lin_scale * run;
+      run += state[(b * G + g) * se + r];
+    }
+    if (!causal) prefix[b * se + r] = lin_scale * run;
+  }
+}
+
+// dState_h = sum_{g>h} dPrefix_g (causal) or the total (in place), with the
+// lin_scale factor already inside dPrefix
+__global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long se, int causal) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long b = i / se, r = i - b * se;
+    if (causal) {
+      float run = 0.f;
+      for (int g = G - 1; g >= 0; --g) {
+        float *p = dpre + (b * G + g) * se + r;
+        const float v = *p;
+        *p = run;
+        run += v;
+      }
+    } else {
+      float tot = 0.f;
+      for (int g = 0; g < G; ++g) tot += dpre[(b * G + g) * se + r];
+      for (int g = 0; g < G; ++g) dpre[(b * G + g) * se + r] = tot;
+    }
+  }
+}
+
+// dZ = sum_k dH_k * gamma_k; dgamma, dbeta as column sums of dH_k * Z, dH_k
+// (per block partial sums over its rows, added atomically)
+__global__ void heads_grad(const float *__restrict__ dH, const float *__restrict__ Z,
+                           const float *__restrict__ gamma, float *__restrict__ dZ,
+                           float *__restrict__ dgamma, float *__restrict__ dbeta, long long M,
+                           int s, int rows_per_block) {
+  const long long r0 = (long long)blockIdx.x * rows_per_block;
+  const long long r1 = r0 + rows_per_block < M ? r0 + rows_per_block : M;
+  for (int c = threadIdx.x; c < s; c += blockDim.x) {
+    float g[4], bsum[4] = {0.f, 0.f, 0.f, 0.f}, gsum[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < 4; ++k) g[k] = gamma[k * s + c];
+    for (long long m = r0; m < r1; ++m) {
+      const float z = Z[m * s + c];
+      float dz = 0.f;
+      for (int k = 0; k < 4; ++k) {
+        const float dh = dH[((long long)k * M + m) * s + c];
+        dz = fmaf(dh, g[k], dz);
+        gsum[k] = fmaf(dh, z, gsum[k]);
+        bsum[k] += dh;
+      }
+      dZ[m * s + c] = dz;
+    }
+    for (int k = 0; k < 4; ++k) {
+      atomicAdd(dgamma + k * s + c, gsum[k]);
+      atomicAdd(dbeta + k * s + c, bsum[k]);
+    }
+  }
+}
+
+// dPre = d(U | V | Z) * swish'(Pre), in place over Pre
+__global__ void pre_grad(float *__restrict__ pre, const float *__restrict__ dU,
+                         const float *__restrict__ dV, const float *__restrict__ dZ, long long M,
+                         int e, int s) {
+  const int N = 2 * e + s;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / N;
+    const int c = (int)(i - m * N);
+    const float g = c < e ? dU[m * e + c] : c < 2 * e ? dV[m * e + c - e] : dZ[m * s + c - 2 * e];
+    pre[i] = g * swish_grad(pre[i]);
+  }
+}
+
+__global__ void zero_f32(float *p, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0.f;
+}
+
+unsigned blocks_for(long long n) {
+  const long long b = (n + 255) / 256;
+  return (unsigned)(b < 16384 ? b : 16384);
+}
+
+template <typename T>
+cudaError_t run(const BackwardProblem &q) {
+  cudaStream_t st = q.stream;
+  const long long M = q.M;
+  const int d = q.d, e = q.e, s = q.s, C = q.C, G = q.G, N = 2 * e + s;
+  const long long BG = (long long)q.B * G, se = (long long)s * e;
+  const T *X = (const T *)q.X, *Wuvz = (const T *)q.W_uvz, *Wo = (const T *)q.W_o;
+  const T *dO = (const T *)q.dO;
+  const BackwardLayout &L = q.L;
+  float *pre = L.pre, *U = L.U, *V = L.V, *Z = L.Z, *H = L.H, *S = L.S, *P = L.P;
+  float *Vh = L.Vh, *Ag = L.A, *state = L.state, *prefix = L.prefix, *dA = L.dA, *dU = L.dU;
+  float *dVh = L.dVh, *dV = L.dV, *dP = L.dP, *dH = L.dH, *dpre = L.dprefix, *dZ = L.dZ;
+  const long long Ms = M * s;
+  cudaError_t err;
+#define BW_TRY(x)                         \
+  if ((err = (x)) != cudaSuccess) return err
+  // ---- recompute the forward
+  BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
+  act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s);
+  const float *Qq = H, *Kq = H + Ms, *Ql = H + 2 * Ms, *Kl = H + 3 * Ms;
+  // per chunk z: rows z*C .. of the [M, *] matrices
+  BW_TRY(gemm(st, C, C, s, (int)BG, Qq, op(s, 1, (long long)C * s), Kq,
+              op(1, s, (long long)C * s), ScoreEpi{S, P, q.relpos, C, q.causal, 1.f / C}));
+  BW_TRY(gemm(st, C, e, C, (int)BG, P, op(C, 1, (long long)C * C), V, op(e, 1, (long long)C * e),
+              StoreF32{Vh, e, 1, (long long)C * e, 1.f, 0}));
+  BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
+              op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
+  scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, prefix, q.B, G, se, q.causal,
+                                                      q.lin_scale);
+  // Vh += Q_lin Prefix (a chunk's prefix, or its batch row's total)
+  const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
+  BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
+              StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
+  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, M * e);
+  // ---- output projection and gate
+  BW_TRY(gemm(st, e, d, (int)M, 1, Ag, op(1, e), dO, op(d, 1), StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
+  BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
+  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e);
+  // ---- local part
+  BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
+              op(1, e, (long long)C * e), StoreF32{dP, C, 1, (long long)C * C, 1.f, 0}));
+  BW_TRY(gemm(st, C, e, C, (int)BG, P, op(1, C, (long long)C * C), dVh,
+              op(e, 1, (long long)C * e), StoreF32{dV, e, 1, (long long)C * e, 1.f, 0}));
+  score_grad<<<blocks_for(BG * C * C), 256, 0, st>>>(S, dP, BG, C, q.causal);
+  relpos_grad<<<2 * C - 1, 256, 0, st>>>(dP, q.drelpos, BG, C);
+  float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;
+  BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(C, 1, (long long)C * C), Kq,
+              op(s, 1, (long long)C * s), StoreF32{dQq, s, 1, (long long)C * s, 1.f / C, 0}));
+  BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(1, C, (long long)C * C), Qq,
+              op(s, 1, (long long)C * s), StoreF32{dKq, s, 1, (long long)C * s, 1.f / C, 0}));
+  // ---- global part
+  const Operand opreT = q.causal ? op(1, e, se) : op(1, e, se, G);
+  BW_TRY(gemm(st, C, s, e, (int)BG, dVh, op(e, 1, (long long)C * e), prefix, opreT,
+              StoreF32{dQl, s, 1, (long long)C * s, 1.f, 0}));
+  BW_TRY(gemm(st, s, e, C, (int)BG, Ql, op(1, s, (long long)C * s), dVh,
+              op(e, 1, (long long)C * e), StoreF32{dpre, e, 1, se, q.lin_scale, 0}));
+  scan_backward<<<blocks_for(q.B * se), 256, 0, st>>>(dpre, q.B, G, se, q.causal);
+  BW_TRY(gemm(st, C, s, e, (int)BG, V, op(e, 1, (long long)C * e), dpre, op(1, e, se),
+              StoreF32{dKl, s, 1, (long long)C * s, 1.f, 0}));
+  BW_TRY(gemm(st, C, e, s, (int)BG, Kl, op(s, 1, (long long)C * s), dpre, op(e, 1, se),
+              StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
+  // ---- heads
+  zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dgamma, 4 * s);
+  zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dbeta, 4 * s);
+  const int rows = 64;
+  heads_grad<<<(unsigned)((M + rows - 1) / rows), 128, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
+                                                                q.dbeta, M, s, rows);
+  // ---- input side
+  pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, dU, dV, dZ, M, e, s);
+  BW_TRY(gemm(st, (int)M, d, N, 1, (const float *)pre, op(N, 1), Wuvz, op(1, N),
+              StoreIo<T>{(T *)q.dX, d}));
+  BW_TRY(gemm(st, d, N, (int)M, 1, X, op(1, d), (const float *)pre, op(N, 1),
+              StoreF32{q.dW_uvz, N, 1, 0, 1.f, 0}));
+#undef BW_TRY
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t backward_f32(const BackwardProblem &q) { return run<float>(q); }
+cudaError_t backward_bf16(const BackwardProblem &q) { return run<__nv_bfloat16>(q); }
+
+}  // namespace flashgau

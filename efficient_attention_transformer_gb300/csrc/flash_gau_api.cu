@@ -102,6 +102,49 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   return FLASH_GAU_OK;
 }
 
+// ---- backward workspace ----------------------------------------------------
+// fp32 buffers, each 256-byte aligned; with base == nullptr only the size.
+int backward_layout(int B, int T, int C, int d, int e, int s, int causal, char *base,
+                    BackwardLayout *L, size_t *total) {
+  if (B <= 0 || T <= 0 || C <= 0 || d <= 0 || e <= 0 || s <= 0) return FLASH_GAU_EINVAL;
+  if (T % C != 0) return FLASH_GAU_EINVAL;
+  const long long M = (long long)B * T, G = T / C;
+  // grid limits of the GEMM and the reductions: rows / 64 and B * G batches
+  // in gridDim.y / z, 2C - 1 bias blocks
+  if (M > 65535LL * 64 || (long long)B * G > 65535 || C > 4096 || s > (1 << 16) ||
+      e > (1 << 16) || d > (1 << 16))
+    return FLASH_GAU_ENOTSUP;
+  const size_t f = sizeof(float), N = 2 * (size_t)e + s, se = (size_t)s * e;
+  size_t off = 0;
+  auto take = [&](float **p, size_t n) {
+    if (p) *p = base ? reinterpret_cast<float *>(base + off) : nullptr;
+    off = align_up(off + n * f);
+  };
+  BackwardLayout dummy;
+  BackwardLayout &l = L ? *L : dummy;
+  take(&l.pre, M * N);
+  take(&l.U, M * e);
+  take(&l.V, M * e);
+  take(&l.Z, M * s);
+  take(&l.H, 4 * M * s);
+  take(&l.S, B * G * C * C);
+  take(&l.P, B * G * C * C);
+  take(&l.Vh, M * e);
+  take(&l.A, M * e);
+  take(&l.state, B * G * se);
+  take(&l.prefix, (causal ? B * G : B) * se);
+  take(&l.dA, M * e);
+  take(&l.dU, M * e);
+  take(&l.dVh, M * e);
+  take(&l.dV, M * e);
+  take(&l.dP, B * G * C * C);
+  take(&l.dH, 4 * M * s);
+  take(&l.dprefix, B * G * se);
+  take(&l.dZ, M * s);
+  *total = off;
+  return FLASH_GAU_OK;
+}
+
 // ---- stage schedules ------------------------------------------------------
 const Stage kStagesF32[] = {
     {"projection", simt_projection_f32},
@@ -304,6 +347,60 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w, const fla
   if (!blk) return FLASH_GAU_EINVAL;
   return run_forward(X, w, blk, B, T, C, causal, dtype, out, workspace, workspace_bytes, stream,
                      nullptr, 0);
+}
+
+size_t flash_gau_backward_workspace_bytes(int B, int T, int C, const flash_gau_weights *w,
+                                          int causal, int dtype) {
+  if (!w || (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16)) return 0;
+  size_t total = 0;
+  if (backward_layout(B, T, C, w->d, w->e, w->s, causal ? 1 : 0, nullptr, nullptr, &total) !=
+      FLASH_GAU_OK)
+    return 0;
+  return total;
+}
+
+int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w, int B, int T,
+                       int C, int causal, int dtype, const flash_gau_grads *g, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  if (!X || !dO || !w || !g || !workspace) return FLASH_GAU_EINVAL;
+  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos) return FLASH_GAU_EINVAL;
+  if (!g->dX || !g->dW_uvz || !g->dW_o || !g->dgamma || !g->dbeta || !g->drelpos)
+    return FLASH_GAU_EINVAL;
+  if (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16) return FLASH_GAU_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLASH_GAU_EWORKSPACE;
+  causal = causal ? 1 : 0;
+  BackwardProblem q;
+  size_t total = 0;
+  int st = backward_layout(B, T, C, w->d, w->e, w->s, causal, static_cast<char *>(workspace),
+                           &q.L, &total);
+  if (st != FLASH_GAU_OK) return st;
+  if (workspace_bytes < total) return FLASH_GAU_EWORKSPACE;
+  q.B = B;
+  q.T = T;
+  q.C = C;
+  q.G = T / C;
+  q.d = w->d;
+  q.e = w->e;
+  q.s = w->s;
+  q.causal = causal;
+  q.M = (long long)B * T;
+  q.lin_scale = w->lin_scale;
+  q.X = X;
+  q.dO = dO;
+  q.W_uvz = w->W_uvz;
+  q.W_o = w->W_o;
+  q.gamma = w->gamma;
+  q.beta = w->beta;
+  q.relpos = w->relpos;
+  q.dX = g->dX;
+  q.dW_uvz = g->dW_uvz;
+  q.dW_o = g->dW_o;
+  q.dgamma = g->dgamma;
+  q.dbeta = g->dbeta;
+  q.drelpos = g->drelpos;
+  q.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t err = dtype == FLASH_GAU_BF16 ? backward_bf16(q) : backward_f32(q);
+  return err == cudaSuccess ? FLASH_GAU_OK : record_cuda(err);
 }
 
 int flash_gau_forward(const void *X, const flash_gau_weights *w, int B, int T, int C, int causal,

@@ -85,6 +85,36 @@ __host__ __device__ inline long long rb64_row(long long r, long long c, long lon
 constexpr int kGridBarrierWord = 17;
 
 
+// Backward pass (backward.cu): fp32 work buffers in the caller's workspace.
+struct BackwardLayout {
+  float *pre;     // [M, 2e+s] X W_uvz, then its gradient
+  float *U, *V;   // [M, e]
+  float *Z;       // [M, s]
+  float *H;       // [4, M, s] Q_quad, K_quad, Q_lin, K_lin
+  float *S, *P;   // [B*G, C, C] scores, relu^2 weights
+  float *Vh, *A;  // [M, e] V_quad + V_lin, the gated product
+  float *state;   // [B*G, s, e]
+  float *prefix;  // [B*G or B, s, e], lin_scale included
+  float *dA, *dU, *dVh, *dV;  // [M, e]
+  float *dP;      // [B*G, C, C], then dS
+  float *dH;      // [4, M, s]
+  float *dprefix; // [B*G, s, e], then dState
+  float *dZ;      // [M, s]
+};
+struct BackwardProblem {
+  int B, T, C, G, d, e, s, causal;
+  long long M;
+  float lin_scale;
+  const void *X, *dO, *W_uvz, *W_o;
+  const float *gamma, *beta, *relpos;
+  void *dX;
+  float *dW_uvz, *dW_o, *dgamma, *dbeta, *drelpos;
+  BackwardLayout L;
+  cudaStream_t stream;
+};
+cudaError_t backward_f32(const BackwardProblem &q);
+cudaError_t backward_bf16(const BackwardProblem &q);
+
 using StageFn = cudaError_t (*)(const Problem &);
 
 // Launches `kernel` on the problem's stream with programmatic stream

@@ -209,6 +209,38 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
                             int causal, int dtype, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* ---- backward pass ------------------------------------------------------ */
+/* Gradients of L = sum(dO * O), O = flash_gau_forward(X, ...), with respect
+ * to X and every parameter, by the chain rule through the forward's steps
+ * (eq. 5, eq. 7, eq. 8 and the display after it): the backward the pages'
+ * training workloads need.  The call recomputes the forward's
+ * intermediates itself (it needs no earlier forward) and works in fp32 on
+ * the CUDA cores for both io types.  Gradients are written, not added.    */
+typedef struct flash_gau_grads {
+  void *dX;          /* device [B, T, d], io type                           */
+  float *dW_uvz;     /* device [d, 2e+s] fp32, columns as in W_uvz          */
+  float *dW_o;       /* device [e, d] fp32                                  */
+  float *dgamma;     /* device [4, s] fp32                                  */
+  float *dbeta;      /* device [4, s] fp32                                  */
+  float *drelpos;    /* device [2C-1] fp32                                  */
+} flash_gau_grads;
+
+/* fp32 work-buffer bytes flash_gau_backward needs, or 0 when the arguments
+ * are invalid or unsupported (B*T > 65535*64, B*T/C > 65535, C > 4096).   */
+size_t flash_gau_backward_workspace_bytes(int B, int T, int C,
+                                          const flash_gau_weights *w,
+                                          int causal, int dtype);
+
+/* X and dO: device [B, T, d], io type; w as for the forward (lin_scale
+ * included); g: host pointer to the gradient outputs; workspace: device,
+ * 256-byte aligned, >= flash_gau_backward_workspace_bytes.  Enqueued on
+ * `stream`, no synchronisation.  Returns FLASH_GAU_OK, FLASH_GAU_EINVAL,
+ * FLASH_GAU_ENOTSUP, FLASH_GAU_EWORKSPACE or FLASH_GAU_ECUDA.            */
+int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w,
+                       int B, int T, int C, int causal, int dtype,
+                       const flash_gau_grads *g, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
 /* ---- RoPE construction of the relative position bias ------------------- */
 /* Appendix D, Code 4 of "Transformer Quality in Linear Time" builds the bias
  * of windows of 512 positions and more from two learned vectors a, b of
