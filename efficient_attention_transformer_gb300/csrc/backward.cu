@@ -19,7 +19,10 @@
 //
 // The contractions run on one batched, strided GEMM kernel (64 x 64 tiles,
 // 4 x 4 per thread), so transposed views cost no copies; the rest are
-// elementwise or column-reduction kernels.
+// elementwise or column-reduction kernels.  For bf16 io, when the shapes
+// tile, the five large contractions (Pre, dW_o, dA, dX, dW_uvz) run on the
+// tensor cores instead (tc_gemm_any.cu), with the gated product and dPre
+// rounded to bf16 as their operands.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -175,12 +178,15 @@ __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
   }
 }
 
-// A = U * Vh
+// A = U * Vh (and its bf16 copy when A_io is set)
 __global__ void gate(const float *__restrict__ U, const float *__restrict__ Vh,
-                     float *__restrict__ A, long long n) {
+                     float *__restrict__ A, __nv_bfloat16 *__restrict__ A_io, long long n) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x)
-    A[i] = U[i] * Vh[i];
+       i += (long long)gridDim.x * blockDim.x) {
+    const float a = U[i] * Vh[i];
+    A[i] = a;
+    if (A_io) A_io[i] = __float2bfloat16_rn(a);
+  }
 }
 
 // dU = dA * Vh, dVh = dA * U
@@ -293,18 +299,44 @@ __global__ void heads_grad(const float *__restrict__ dH, const float *__restrict
   }
 }
 
-// dPre = d(U | V | Z) * swish'(Pre), in place over Pre
-__global__ void pre_grad(float *__restrict__ pre, const float *__restrict__ dU,
-                         const float *__restrict__ dV, const float *__restrict__ dZ, long long M,
-                         int e, int s) {
+// dPre = d(U | V | Z) * swish'(Pre), in place over Pre (and its bf16 copy
+// when pre_io is set)
+__global__ void pre_grad(float *__restrict__ pre, __nv_bfloat16 *__restrict__ pre_io,
+                         const float *__restrict__ dU, const float *__restrict__ dV,
+                         const float *__restrict__ dZ, long long M, int e, int s) {
   const int N = 2 * e + s;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
        i += (long long)gridDim.x * blockDim.x) {
     const long long m = i / N;
     const int c = (int)(i - m * N);
     const float g = c < e ? dU[m * e + c] : c < 2 * e ? dV[m * e + c - e] : dZ[m * s + c - 2 * e];
-    pre[i] = g * swish_grad(pre[i]);
+    const float v = g * swish_grad(pre[i]);
+    pre[i] = v;
+    if (pre_io) pre_io[i] = __float2bfloat16_rn(v);
   }
+}
+
+// a tensor-core contraction of the backward (bf16 operands)
+GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int a_mn,
+                    const void *B, long long ldb, int b_km, void *C, int c_bf16, int M, int N,
+                    int K, int allow_split) {
+  GemmAnyArgs g;
+  g.A = A;
+  g.lda = lda;
+  g.a_mn = a_mn;
+  g.B = B;
+  g.ldb = ldb;
+  g.b_km = b_km;
+  g.C = C;
+  g.c_bf16 = c_bf16;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.accumulate = 0;
+  g.allow_split = allow_split;
+  g.num_sms = q.num_sms;
+  g.status = q.L.status;
+  return g;
 }
 
 __global__ void zero_f32(float *p, int n) {
@@ -331,10 +363,21 @@ cudaError_t run(const BackwardProblem &q) {
   float *dVh = L.dVh, *dV = L.dV, *dP = L.dP, *dH = L.dH, *dpre = L.dprefix, *dZ = L.dZ;
   const long long Ms = M * s;
   cudaError_t err;
-#define BW_TRY(x)                         \
-  if ((err = (x)) != cudaSuccess) return err
+#define BW_TRY(x)                          \
+  do {                                     \
+    if ((err = (x)) != cudaSuccess) return err; \
+  } while (0)
+  // the five large contractions on the tensor cores: bf16 io, shapes that
+  // tile 128 x 64 (rows of every output, depths) and 64-wide columns
+  const bool tc = sizeof(T) == 2 && M % 128 == 0 && d % 128 == 0 && e % 128 == 0 &&
+                  N % 64 == 0 && L.A_io && L.dpre_io;
+  __nv_bfloat16 *A_io = tc ? (__nv_bfloat16 *)L.A_io : nullptr;
+  __nv_bfloat16 *dpre_io = tc ? (__nv_bfloat16 *)L.dpre_io : nullptr;
   // ---- recompute the forward
-  BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
+  if (tc)
+    BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, pre, 0, (int)M, N, d, 0), st));
+  else
+    BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
   act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s);
   const float *Qq = H, *Kq = H + Ms, *Ql = H + 2 * Ms, *Kl = H + 3 * Ms;
   // per chunk z: rows z*C .. of the [M, *] matrices
@@ -350,10 +393,18 @@ cudaError_t run(const BackwardProblem &q) {
   const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
   BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
               StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
-  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, M * e);
+  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, A_io, M * e);
   // ---- output projection and gate
-  BW_TRY(gemm(st, e, d, (int)M, 1, Ag, op(1, e), dO, op(d, 1), StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
-  BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
+  if (tc) {
+    // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
+    BW_TRY(tc_gemm_any(tc_args(q, A_io, e, 1, dO, d, 0, q.dW_o, 0, e, d, (int)M, 1), st));
+    // dA = dO W_o^T: B the transpose of the stored [e, d] W_o
+    BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, 0, (int)M, e, d, 0), st));
+  } else {
+    BW_TRY(gemm(st, e, d, (int)M, 1, Ag, op(1, e), dO, op(d, 1),
+                StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
+    BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
+  }
   gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e);
   // ---- local part
   BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
@@ -385,11 +436,17 @@ cudaError_t run(const BackwardProblem &q) {
   heads_grad<<<(unsigned)((M + rows - 1) / rows), 128, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows);
   // ---- input side
-  pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, dU, dV, dZ, M, e, s);
-  BW_TRY(gemm(st, (int)M, d, N, 1, (const float *)pre, op(N, 1), Wuvz, op(1, N),
-              StoreIo<T>{(T *)q.dX, d}));
-  BW_TRY(gemm(st, d, N, (int)M, 1, X, op(1, d), (const float *)pre, op(N, 1),
-              StoreF32{q.dW_uvz, N, 1, 0, 1.f, 0}));
+  pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, dpre_io, dU, dV, dZ, M, e, s);
+  if (tc) {
+    // dX = dPre W_uvz^T (bf16 out); dW_uvz = X^T dPre
+    BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
+    BW_TRY(tc_gemm_any(tc_args(q, X, d, 1, dpre_io, N, 0, q.dW_uvz, 0, d, N, (int)M, 1), st));
+  } else {
+    BW_TRY(gemm(st, (int)M, d, N, 1, (const float *)pre, op(N, 1), Wuvz, op(1, N),
+                StoreIo<T>{(T *)q.dX, d}));
+    BW_TRY(gemm(st, d, N, (int)M, 1, X, op(1, d), (const float *)pre, op(N, 1),
+                StoreF32{q.dW_uvz, N, 1, 0, 1.f, 0}));
+  }
 #undef BW_TRY
   return cudaGetLastError();
 }

@@ -104,7 +104,7 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
 
 // ---- backward workspace ----------------------------------------------------
 // fp32 buffers, each 256-byte aligned; with base == nullptr only the size.
-int backward_layout(int B, int T, int C, int d, int e, int s, int causal, char *base,
+int backward_layout(int B, int T, int C, int d, int e, int s, int causal, int dtype, char *base,
                     BackwardLayout *L, size_t *total) {
   if (B <= 0 || T <= 0 || C <= 0 || d <= 0 || e <= 0 || s <= 0) return FLASH_GAU_EINVAL;
   if (T % C != 0) return FLASH_GAU_EINVAL;
@@ -122,6 +122,8 @@ int backward_layout(int B, int T, int C, int d, int e, int s, int causal, char *
   };
   BackwardLayout dummy;
   BackwardLayout &l = L ? *L : dummy;
+  l.status = base ? reinterpret_cast<int *>(base) : nullptr;
+  off = kAlign;
   take(&l.pre, M * N);
   take(&l.U, M * e);
   take(&l.V, M * e);
@@ -141,6 +143,13 @@ int backward_layout(int B, int T, int C, int d, int e, int s, int causal, char *
   take(&l.dH, 4 * M * s);
   take(&l.dprefix, B * G * se);
   take(&l.dZ, M * s);
+  // bf16 operand copies for the tensor-core contractions (2 bytes each)
+  float *a_io = nullptr, *dpre_io = nullptr;
+  const size_t io_n = dtype == FLASH_GAU_BF16 ? 1 : 0;
+  take(&a_io, io_n * (M * e + 1) / 2);
+  take(&dpre_io, io_n * (M * N + 1) / 2);
+  l.A_io = a_io;
+  l.dpre_io = dpre_io;
   *total = off;
   return FLASH_GAU_OK;
 }
@@ -353,7 +362,8 @@ size_t flash_gau_backward_workspace_bytes(int B, int T, int C, const flash_gau_w
                                           int causal, int dtype) {
   if (!w || (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16)) return 0;
   size_t total = 0;
-  if (backward_layout(B, T, C, w->d, w->e, w->s, causal ? 1 : 0, nullptr, nullptr, &total) !=
+  if (backward_layout(B, T, C, w->d, w->e, w->s, causal ? 1 : 0, dtype, nullptr, nullptr,
+                      &total) !=
       FLASH_GAU_OK)
     return 0;
   return total;
@@ -371,8 +381,8 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
   causal = causal ? 1 : 0;
   BackwardProblem q;
   size_t total = 0;
-  int st = backward_layout(B, T, C, w->d, w->e, w->s, causal, static_cast<char *>(workspace),
-                           &q.L, &total);
+  int st = backward_layout(B, T, C, w->d, w->e, w->s, causal, dtype,
+                           static_cast<char *>(workspace), &q.L, &total);
   if (st != FLASH_GAU_OK) return st;
   if (workspace_bytes < total) return FLASH_GAU_EWORKSPACE;
   q.B = B;
@@ -399,6 +409,11 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
   q.dbeta = g->dbeta;
   q.drelpos = g->drelpos;
   q.stream = static_cast<cudaStream_t>(stream);
+  st = device_info(&q.num_sms);
+  if (st != FLASH_GAU_OK) return st;
+  // the status word of this workspace, read by flash_gau_workspace_status
+  cudaError_t zerr = cudaMemsetAsync(workspace, 0, sizeof(int), q.stream);
+  if (zerr != cudaSuccess) return record_cuda(zerr);
   const cudaError_t err = dtype == FLASH_GAU_BF16 ? backward_bf16(q) : backward_f32(q);
   return err == cudaSuccess ? FLASH_GAU_OK : record_cuda(err);
 }

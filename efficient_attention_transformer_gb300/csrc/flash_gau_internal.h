@@ -85,8 +85,27 @@ __host__ __device__ inline long long rb64_row(long long r, long long c, long lon
 constexpr int kGridBarrierWord = 17;
 
 
+// General tcgen05 GEMM (tc_gemm_any.cu): C[M, N] = A B, bf16 operands.
+struct GemmAnyArgs {
+  const void *A;
+  long long lda;
+  int a_mn;  // A is the transpose of a row-major [K, M] matrix
+  const void *B;
+  long long ldb;
+  int b_km;  // B is the transpose of a row-major [N, K] matrix
+  void *C;   // row-major [M, N], leading dimension N
+  int c_bf16;
+  int M, N, K;
+  int accumulate;   // fp32: add into C
+  int allow_split;  // fp32: split K across CTAs when the tiles are few
+  int num_sms;
+  int *status;
+};
+cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
+
 // Backward pass (backward.cu): fp32 work buffers in the caller's workspace.
 struct BackwardLayout {
+  int *status;    // the workspace's first slot: FLASH_GAU_ETIMEOUT on a timed-out wait
   float *pre;     // [M, 2e+s] X W_uvz, then its gradient
   float *U, *V;   // [M, e]
   float *Z;       // [M, s]
@@ -100,6 +119,8 @@ struct BackwardLayout {
   float *dH;      // [4, M, s]
   float *dprefix; // [B*G, s, e], then dState
   float *dZ;      // [M, s]
+  void *A_io;     // [M, e] bf16 copy of the gated product (tensor-core path)
+  void *dpre_io;  // [M, 2e+s] bf16 copy of dPre (tensor-core path)
 };
 struct BackwardProblem {
   int B, T, C, G, d, e, s, causal;
@@ -111,6 +132,7 @@ struct BackwardProblem {
   float *dW_uvz, *dW_o, *dgamma, *dbeta, *drelpos;
   BackwardLayout L;
   cudaStream_t stream;
+  int num_sms;
 };
 cudaError_t backward_f32(const BackwardProblem &q);
 cudaError_t backward_bf16(const BackwardProblem &q);

@@ -1,0 +1,361 @@
+// General tcgen05 GEMM for the large contractions of the backward pass,
+//   C[M, N] = A[M, K] B[K, N],  bf16 operands, fp32 accumulation in TMEM,
+// with either operand stored either way round:
+//   A_MN = false: A is a row-major [M, K] matrix (K-major); true: A is the
+//                 transpose of a row-major [K, M] matrix (M-major);
+//   B_KM = false: B is a row-major [K, N] matrix (N-major); true: B is the
+//                 transpose of a row-major [N, K] matrix (K-major).
+// fp32 results are stored, or added with vector atomics (split-K: several
+// CTAs sum into one zeroed tile); bf16 results go out through TMA stores.
+//
+// One persistent CTA per SM over 128 x 256 output tiles (x split), static
+// round robin.  Warp 0 streams 64-deep k-blocks of A and B into a 4-stage
+// ring of 128-byte-swizzled boxes with TMA; one thread of warp 1 issues
+// tcgen05.mma (M = 128, N = 256, K = 16) into one of two TMEM accumulators;
+// warps 2-5 drain the other with tcgen05.ld (one TMEM lane quarter each).
+#include <cuda_bf16.h>
+
+#include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace flashgau {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_BYTES = BN * BK * 2;       // 32 KB
+constexpr int BOX_BYTES = 64 * 64 * 2;     // one 64 x 64 box, 8 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 2 * ACC_COLS;
+constexpr int NUM_THREADS = 192;
+constexpr int STG_BYTES = 32 * 128;  // one 32-row x 128-byte store box per epilogue warp
+constexpr int STG_OFF = STAGES * STAGE_BYTES;
+constexpr int TILE_BYTES = STG_OFF + 4 * STG_BYTES;
+constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+struct AnyParams {
+  int M, N, K;
+  int m_tiles, n_tiles, splits, total;
+  int kb_split;  // k-blocks per split
+  float *Cf;     // fp32 output, row-major with leading dimension N
+  int atomic;    // fp32: add into C (zeroed by the caller) instead of storing
+  int *status;
+};
+
+struct Smem {
+  uint64_t full[STAGES], empty[STAGES];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ void raise_timeout(Smem *sm, int *status) {
+  sm->abort_flag = 1;
+  atomicExch(status, FLASH_GAU_ETIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+struct Tile {
+  int mt, nt, kb0, kb1;
+};
+__device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
+  Tile x;
+  const int split = t % p.splits, rem = t / p.splits;
+  x.nt = rem % p.n_tiles;
+  x.mt = rem / p.n_tiles;
+  const int kblocks = p.K / BK;
+  x.kb0 = split * p.kb_split;
+  x.kb1 = min(kblocks, x.kb0 + p.kb_split);
+  return x;
+}
+
+template <bool A_MN, bool B_KM, bool OUT_BF16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const AnyParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem *sm = reinterpret_cast<Smem *>(tiles + TILE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&sm->full[i]), 1);
+      mbar_init(smem_u32(&sm->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm->acc_full[i]), 1);
+      mbar_init(smem_u32(&sm->acc_empty[i]), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    sm->abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x) {
+        const Tile x = tile_of(p, t);
+        const int m0 = x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
+        for (int kb = x.kb0; kb < x.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
+            raise_timeout(sm, p.status);
+            break;
+          }
+          const uint32_t full = smem_u32(&sm->full[stage]);
+          uint8_t *sA = tiles + stage * STAGE_BYTES;
+          uint8_t *sB = sA + A_BYTES;
+          // a K-major B box is 256 rows whatever the tile's width (rows past
+          // N are zero-filled and counted)
+          const uint32_t b_bytes = B_KM ? (uint32_t)B_BYTES : (uint32_t)(nsz / 64) * BOX_BYTES;
+          mbar_arrive_expect_tx(full, A_BYTES + b_bytes);
+          if (A_MN) {
+            // [K, M] storage: 64 k-rows of two 64-column blocks of M
+            tma_load_2d(smem_u32(sA), &tmA, full, m0, kb * BK);
+            tma_load_2d(smem_u32(sA + BOX_BYTES), &tmA, full, m0 + 64, kb * BK);
+          } else {
+            tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, m0);
+          }
+          if (B_KM) {
+            tma_load_2d(smem_u32(sB), &tmB, full, kb * BK, n0);
+          } else {
+            for (int j = 0; j < nsz / 64; ++j)
+              tma_load_2d(smem_u32(sB + j * BOX_BYTES), &tmB, full, n0 + j * 64, kb * BK);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (elect_one()) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x, ++local) {
+        const Tile x = tile_of(p, t);
+        const int nsz = min(BN, p.N - x.nt * BN);
+        const int acc = local & 1;
+        if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), ((local >> 1) & 1) ^ 1, &sm->abort_flag)) {
+          raise_timeout(sm, p.status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+        const uint32_t idesc = idesc_bf16_f32(BM, nsz, A_MN ? 1 : 0, B_KM ? 0 : 1);
+        bool ok = true;
+        for (int kb = x.kb0; kb < x.kb1; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, &sm->abort_flag)) {
+            raise_timeout(sm, p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
+          // K-major: 16 elements (32 B) per step inside the swizzle atom;
+          // MN-major: 16 k-rows of 128 B per step, 64-wide blocks 8 KB apart
+          const uint64_t da = A_MN ? sw128_desc(sA, BOX_BYTES, 1024) : sw128_desc(sA, 16, 1024);
+          const uint64_t db = B_KM ? sw128_desc(sA + A_BYTES, 16, 1024)
+                                   : sw128_desc(sA + A_BYTES, BOX_BYTES, 1024);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_f16_ss(d_tmem, desc_advance(da, k * (A_MN ? 2048 : 32)),
+                       desc_advance(db, k * (B_KM ? 32 : 2048)), idesc, kb != x.kb0 || k != 0);
+          mma_commit(smem_u32(&sm->empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&sm->acc_full[acc]));
+      }
+      // every MMA this thread issued has completed once `drain` flips
+      mma_commit(smem_u32(&sm->drain));
+      if (!mbar_wait(smem_u32(&sm->drain), 0)) raise_timeout(sm, p.status);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    uint8_t *stg = tiles + STG_OFF + (warp - 2) * STG_BYTES;
+    int local = 0;
+    for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x, ++local) {
+      const Tile x = tile_of(p, t);
+      const int m0 = x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
+      const int acc = local & 1;
+      if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
+        raise_timeout(sm, p.status);
+        break;
+      }
+      tc_fence_after();
+      const int row0 = m0 + quarter * 32;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+      for (int c0 = 0; c0 < nsz; c0 += 64) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(taddr + c0, ra);
+        tmem_ld32(taddr + c0 + 32, rb);
+        tmem_ld_wait();
+        if (c0 + 64 >= nsz) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty[acc]));
+        }
+        if constexpr (OUT_BF16) {
+          // this row's 64 columns into the swizzled box, then one TMA store
+          if (lane == 0) tma_store_wait_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t *v = q < 4 ? &ra[8 * q] : &rb[8 * (q - 4)];
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            w.y = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            w.z = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            w.w = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            *reinterpret_cast<uint4 *>(stg + sw128_offset(lane, q)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, smem_u32(stg), n0 + c0, row0);
+            tma_store_commit();
+          }
+        } else {
+          float *crow = p.Cf + (size_t)(row0 + lane) * p.N + n0 + c0;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t *v = q < 8 ? &ra[4 * q] : &rb[4 * (q - 8)];
+            const float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
+            const float c = __uint_as_float(v[2]), d = __uint_as_float(v[3]);
+            if (p.atomic) red_add_v4(crow + 4 * q, a, b, c, d);
+            else *reinterpret_cast<float4 *>(crow + 4 * q) = make_float4(a, b, c, d);
+          }
+        }
+      }
+    }
+    if (OUT_BF16 && lane == 0) tma_store_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <bool A_MN, bool B_KM, bool OUT_BF16>
+cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                   const AnyParams &p, int num_sms, cudaStream_t stream) {
+  static unsigned long long configured = 0;  // one bit per device ordinal
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  auto kernel = tc_gemm_any_kernel<A_MN, B_KM, OUT_BF16>;
+  if (dev < 64 && !(configured & (1ull << dev))) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    configured |= 1ull << dev;
+  }
+  const int grid = p.total < num_sms ? p.total : num_sms;
+  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
+  if (g.M % BM != 0 || g.N % 64 != 0 || g.K % BK != 0 || g.M <= 0 || g.N <= 0 || g.K <= 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tmC;
+  cudaError_t err;
+  // A: K-major [M, K] in 64 x 128 boxes, or M-major [K, M] in 64 x 64 boxes
+  if (g.a_mn) err = make_tmap_bf16_2d(&tmA, g.A, g.K, g.M, g.lda, 64, 64);
+  else err = make_tmap_bf16_2d(&tmA, g.A, g.M, g.K, g.lda, BM, 64);
+  if (err != cudaSuccess) return err;
+  // B: N-major [K, N] in 64 x 64 boxes, or K-major [N, K] in 256-row boxes
+  if (g.b_km) err = make_tmap_bf16_2d(&tmB, g.B, g.N, g.K, g.ldb, BN, 64);
+  else err = make_tmap_bf16_2d(&tmB, g.B, g.K, g.N, g.ldb, 64, 64);
+  if (err != cudaSuccess) return err;
+  if (g.c_bf16) {
+    if ((err = make_tmap_bf16_2d(&tmC, g.C, g.M, g.N, g.N, 32, 64)) != cudaSuccess) return err;
+  } else {
+    tmC = tmA;  // unused
+  }
+  AnyParams p = {};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.m_tiles = g.M / BM;
+  p.n_tiles = (g.N + BN - 1) / BN;
+  const int kblocks = g.K / BK;
+  // split K when the output tiles would leave SMs idle (fp32 atomic output
+  // only); at least 8 k-blocks a split
+  int splits = 1;
+  const int out_tiles = p.m_tiles * p.n_tiles;
+  if (!g.c_bf16 && g.allow_split && out_tiles < g.num_sms) {
+    splits = (2 * g.num_sms + out_tiles - 1) / out_tiles;
+    const int max_splits = kblocks / 8 > 1 ? kblocks / 8 : 1;
+    if (splits > max_splits) splits = max_splits;
+  }
+  p.kb_split = (kblocks + splits - 1) / splits;
+  p.splits = (kblocks + p.kb_split - 1) / p.kb_split;
+  p.total = out_tiles * p.splits;
+  p.Cf = (float *)g.C;
+  p.atomic = p.splits > 1 || g.accumulate;
+  p.status = g.status;
+  if (p.atomic && !g.accumulate) {
+    // the split partial sums add into a zeroed output
+    if ((err = cudaMemsetAsync(g.C, 0, (size_t)g.M * g.N * sizeof(float), stream)) != cudaSuccess)
+      return err;
+  }
+  const int key = (g.a_mn ? 4 : 0) | (g.b_km ? 2 : 0) | (g.c_bf16 ? 1 : 0);
+  switch (key) {
+    case 0: return launch<false, false, false>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 1: return launch<false, false, true>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 2: return launch<false, true, false>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 3: return launch<false, true, true>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 4: return launch<true, false, false>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 5: return launch<true, false, true>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 6: return launch<true, true, false>(tmA, tmB, tmC, p, g.num_sms, stream);
+    default: return launch<true, true, true>(tmA, tmB, tmC, p, g.num_sms, stream);
+  }
+}
+
+}  // namespace flashgau

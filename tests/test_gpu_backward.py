@@ -2,10 +2,11 @@
 oracle's chain-rule gradients (oracle.flash_gau_backward, itself pinned by
 finite differences), on the same seeded inputs.
 
-Both sides see the same io-typed inputs (bf16-rounded for bf16 io).  The
-GPU computes in fp32, so the parameter gradients (fp32 outputs) get 1e-3 of
-their maximum for bf16 io and 1e-4 for fp32 io; dX, stored in the io type,
-gets 1e-2 for bf16 (its rounding alone is 2^-9)."""
+Both sides see the same io-typed inputs (bf16-rounded for bf16 io).  For
+fp32 io the GPU computes in fp32 throughout: every gradient gets 1e-4 of its
+maximum.  For bf16 io the large contractions run on the tensor cores with
+bf16 operands (the gated product and dPre rounded to bf16, 2^-9 each), so
+every gradient gets 1e-2, the bar of the layer's own bf16 intermediates."""
 
 import numpy as np
 import pytest
@@ -18,7 +19,7 @@ from oracle import flash_gau_backward
 
 pytestmark = pytest.mark.gpu
 
-TOL_W = {"fp32": 1e-4, "bf16": 1e-3}
+TOL_W = {"fp32": 1e-4, "bf16": 1e-2}
 TOL_X = {"fp32": 1e-4, "bf16": 1e-2}
 
 
@@ -67,6 +68,8 @@ def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed):
     ((1, 256, 64, 128, 32, 64), True, "fp32", 1.0),
     ((2, 256, 64, 128, 32, 64), False, "fp32", 0.25),
     ((2, 512, 128, 256, 128, 128), True, "bf16", 1.0 / 128),
+    ((1, 1024, 256, 512, 128, 256), True, "bf16", 1.0),
+    ((2, 512, 128, 384, 64, 128), False, "bf16", 0.5),
     ((1, 384, 96, 160, 64, 128), False, "bf16", 1.0),
     ((1, 256, 64, 128, 32, 256), True, "fp32", 0.0),
 ])
