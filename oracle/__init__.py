@@ -20,3 +20,4 @@ from .flash_gau import (  # noqa: F401
     algorithmic_flops_per_token,
 )
 from .backward import swish_grad, flash_gau_backward  # noqa: F401,E402
+from .decode import DecodeState  # noqa: F401,E402

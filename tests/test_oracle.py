@@ -436,6 +436,7 @@ def test_block_is_residual_around_the_layer_of_the_normalised_input():
 
 # ---------------------------------------------------------------- RoPE-Toeplitz bias
 import oracle as O  # noqa: E402
+import oracle as O_  # noqa: E402
 def test_rope_toeplitz_golden_worked_example():
     """Hand-worked 3 x 3 bias from a = (1, 0), b = (0, 1) (tests/golden)."""
     with open(os.path.join(GOLDEN, "rope_toeplitz_m2_n3.txt")) as f:
@@ -521,3 +522,44 @@ def test_swish_grad_against_library_derivative():
     sg = scipy.special.expit(x)
     want = sg + x * sg * (1 - sg)
     assert np.allclose(O.swish_grad(x), want, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("C,T,lin_scale", [(4, 11, 1.0), (8, 24, 0.5), (1, 5, 1.0), (16, 7, 0.0)])
+def test_decode_steps_equal_causal_forward_rows(C, T, lin_scale):
+    """By causality, the decode step's output for token t is row t of the
+    causal forward over any sequence that starts with the same t + 1
+    tokens (the rest zero-padded to a multiple of C)."""
+    rng = np.random.default_rng(70 + C)
+    d, e, s = 6, 10, 4
+    W_u, W_v = rng.normal(size=(d, e)) / 2, rng.normal(size=(d, e)) / 2
+    W_z, W_o = rng.normal(size=(d, s)) / 2, rng.normal(size=(e, d)) / 2
+    gamma, beta = rng.normal(1.0, 0.3, (4, s)), rng.normal(0.0, 0.3, (4, s))
+    relpos = rng.normal(0.0, 0.5, 2 * C - 1)
+    X = rng.normal(size=(T, d))
+    Tp = -(-T // C) * C
+    Xp = np.zeros((1, Tp, d))
+    Xp[0, :T] = X
+    O, _ = flash_gau(Xp, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, True, lin_scale)
+    st = O_.DecodeState(W_u, W_v, W_z, W_o, gamma, beta, relpos, C, lin_scale)
+    for t in range(T):
+        o = st.step(X[t])
+        assert np.allclose(o, O[0, t], rtol=1e-12, atol=1e-12), t
+
+
+def test_decode_prefix_is_completed_chunks_sum():
+    """After k full chunks the linear cache is the sum of their K_lin^T V,
+    and the chunk cache is empty."""
+    rng = np.random.default_rng(77)
+    d, e, s, C = 5, 7, 4, 3
+    W = [rng.normal(size=sh) for sh in ((d, e), (d, e), (d, s), (e, d))]
+    gamma, beta = rng.normal(1.0, 0.3, (4, s)), rng.normal(0.0, 0.3, (4, s))
+    st = O_.DecodeState(*W, gamma, beta, rng.normal(size=2 * C - 1), C)
+    X = rng.normal(size=(2 * C, d))
+    for x in X:
+        st.step(x)
+    Z = swish(X @ W[2])
+    Kl = Z * gamma[3] + beta[3]
+    V = swish(X @ W[1])
+    assert np.allclose(st.prefix, Kl.T @ V, rtol=1e-12, atol=1e-12)
+    assert st.kq == [] and st.t == 2 * C
