@@ -332,6 +332,55 @@ def run_ours(args, rank, world, local_rank):
     backward_ms = be0.elapsed_time(be1) / bn
     del bws
 
+    # ---- next row: autoregressive decode at the workload's widths, B
+    # sequences one token each per step, over two chunks (two folds of the
+    # linear cache); plain calls and one step replayed as a CUDA graph
+    decode = {}
+    drng = np.random.default_rng(4000 + w["seed"])
+    io_bytes = 2 if tdt == torch.bfloat16 else 4
+    for Bd in (1, 16, 64):
+        dec = bd.Decoder(weights, Bd, C)
+        xs = torch.tensor(drng.normal(size=(Bd, d)), dtype=tdt, device=dev)
+        od = torch.empty_like(xs)
+        nsteps = 2 * C
+        for _ in range(8):
+            dec.step(xs, out=od, stream=stream)
+        dec.reset()
+        de0, de1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        de0.record(stream)
+        for _ in range(nsteps):
+            dec.step(xs, out=od, stream=stream)
+        de1.record(stream)
+        torch.cuda.synchronize()
+        plain_us = de0.elapsed_time(de1) * 1e3 / nsteps
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            dec.step(xs, out=od, stream=cap)
+        stream.wait_stream(cap)
+        dec.reset()
+        torch.cuda.synchronize()
+        de0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(nsteps):
+                graph.replay()
+        de1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = de0.elapsed_time(de1) * 1e3 / nsteps
+        # bytes a step must move: both weight matrices once, and per
+        # sequence the linear cache and on average half a chunk of cached
+        # K_quad and V rows (fp32), plus the fold's share
+        wbytes = io_bytes * (d * (2 * e + s) + e * d)
+        sbytes = Bd * 4 * (s * e + (C // 2) * (s + e) + (C * (s + e) + 2 * s * e) // C)
+        best = min(plain_us, graph_us)
+        decode["B%d" % Bd] = {"us_per_step_plain": round(plain_us, 2),
+                              "us_per_step_graph": round(graph_us, 2),
+                              "tokens_per_s": round(Bd / (best * 1e-6), 1),
+                              "gbs": round((wbytes + sbytes) / (best * 1e-6) / 1e9, 1)}
+        del dec, graph
+
     if rank != 0:
         return None
     peaks = _peaks()
@@ -415,6 +464,11 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_tflops": round(2 * total_flops / (backward_ms * 1e-3) / 1e12, 2),
                 "executed_tflops": round(3 * total_flops / (backward_ms * 1e-3) / 1e12, 2),
                 "fp32_core_peak_tflops": round(FP32_CORE_PEAK_TFLOPS, 1)},
+            "decode": dict(
+                what="autoregressive decode step at the workload's widths (C = 256, causal): "
+                     "B sequences, one token each per step, 2C steps; four kernels per step "
+                     "(projection, chunk attention with the linear cache, output, cache fold)",
+                **decode),
             "rope_toeplitz_bias": {
                 "what": "relative-position table of the RoPE bias construction, C = 512, "
                         "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",

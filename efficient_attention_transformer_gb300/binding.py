@@ -44,6 +44,8 @@ EXPORTED = (
     "flash_gau_rope_toeplitz_bias",
     "flash_gau_backward_workspace_bytes",
     "flash_gau_backward",
+    "flash_gau_decode_state_bytes",
+    "flash_gau_decode_step",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -135,6 +137,10 @@ def lib():
         L.flash_gau_backward.argtypes = [p, p, ctypes.POINTER(Weights), i, i, i, i, i,
                                          ctypes.POINTER(Grads), p, sz, p]
         L.flash_gau_backward.restype = i
+        L.flash_gau_decode_state_bytes.argtypes = [i, i, ctypes.POINTER(Weights), i]
+        L.flash_gau_decode_state_bytes.restype = sz
+        L.flash_gau_decode_step.argtypes = [p, ctypes.POINTER(Weights), i, i, i, p, sz, p, p]
+        L.flash_gau_decode_step.restype = i
         _lib = L
     return _lib
 
@@ -361,3 +367,34 @@ def backward(X, dO, weights, C, causal, workspace=None, stream=None):
         int(bool(causal)), weights.dtype, ctypes.byref(g), _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), stream.cuda_stream))
     return out
+
+
+class Decoder:
+    """B sequences decoded one token per call through flash_gau_decode_step;
+    the state lives on the weights' device and starts all sequences at
+    position 0."""
+
+    def __init__(self, weights, B, C):
+        self.weights, self.B, self.C = weights, int(B), int(C)
+        n = lib().flash_gau_decode_state_bytes(self.B, self.C, ctypes.byref(weights.c),
+                                               weights.dtype)
+        if n == 0:
+            raise FlashGauError(EINVAL, "invalid or unsupported decode problem")
+        self.state = torch.zeros(n, dtype=torch.uint8, device=weights.W_uvz.device)
+
+    def reset(self):
+        self.state.zero_()
+
+    def step(self, x, out=None, stream=None):
+        """x: [B, d] in the io type; returns the [B, d] outputs."""
+        if tuple(x.shape) != (self.B, self.weights.d) or x.dtype != self.weights.W_uvz.dtype:
+            raise ValueError("x must be [B, d] in the weights' type")
+        if out is None:
+            out = torch.empty_like(x)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        _check(lib().flash_gau_decode_step(
+            _dev_ptr(x, "x", x.dtype), ctypes.byref(self.weights.c), self.B, self.C,
+            self.weights.dtype, _dev_ptr(self.state, "state"), self.state.numel(),
+            _dev_ptr(out, "out", x.dtype), stream.cuda_stream))
+        return out

@@ -1,0 +1,283 @@
+// Autoregressive decode step of the FLASH GAU layer: one new token for each
+// of B sequences, in constant work per token ("Transformer Quality in
+// Linear Time", §3.2.1: "the linear cache is one matrix and the local
+// attention is limited to one chunk").  Per sequence the state holds
+//   pos      tokens consumed so far (the new one sits at i = pos mod C of
+//            its chunk)
+//   Prefix   [s, e] fp32, the sum of K_lin^T V over completed chunks
+//   caches   the current chunk's K_quad, K_lin [C, s] and V [C, e] rows
+// and a step runs four launches, chained by programmatic dependent launch:
+//   project  x W_uvz in depth slices (pos += 1)
+//   attend   u, v, z = swish(sum of the slices), the four heads;
+//            a_j = relu(q_quad . k_quad_j / C + relpos[j - i + C - 1])^2
+//            (j <= i), vhat = sum_j a_j v_j + lin_scale q_lin Prefix,
+//            gated = u * vhat; the token's rows go into the caches
+//   output   gated W_o in depth slices
+//   finish   out = the slices' sum; at a chunk's last token
+//            Prefix += K_lin,chunk^T V_chunk
+// The projections stream the weights once per step for all B sequences
+// (split-K matrix-vector products on the CUDA cores with 16-byte weight
+// loads); everything is fp32 inside.
+#include <cuda_bf16.h>
+
+#include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace flashgau {
+namespace {
+
+using ptx::griddep_launch_dependents;
+using ptx::griddep_wait;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float swish(float x) { return x / (1.0f + expf(-x)); }
+
+constexpr int kGroup = 8;       // sequences per pass of a matrix-vector kernel
+constexpr int kWarps = 8;
+constexpr int kTileN = 256;     // output columns per block: 8 per lane
+// dynamic shared memory of the matrix-vector kernel: the group's input rows
+// and the warps' partial sums
+constexpr size_t kGemvSmem = sizeof(float) * (kGroup * 128 + kWarps * kGroup * (kTileN + 4));
+
+// 8 consecutive weights of row k from column c (c % 8 == 0), as floats
+__device__ __forceinline__ void load8(const __nv_bfloat16 *W, long long o, float (&w)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4 *>(W + o);
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    w[2 * i] = f.x;
+    w[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float *W, long long o, float (&w)[8]) {
+  const float4 a = *reinterpret_cast<const float4 *>(W + o);
+  const float4 b = *reinterpret_cast<const float4 *>(W + o + 4);
+  w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+}
+
+// Split-K matrix-vector products: part[slice][b][c] = sum over the slice's
+// ks rows k of x[b][k] W[k][c], for all B sequences.  Block (column tile,
+// slice); a lane owns 8 consecutive columns (16-byte loads of a weight row,
+// 512 coalesced bytes per warp), the warps share the slice's rows, and the
+// warps' sums meet in shared memory.  Consumers add the slices in a fixed
+// order, so the results do not depend on scheduling.
+template <typename Tx, typename Tw>
+__global__ void __launch_bounds__(256)
+gemv_splitk(const Tx *__restrict__ x, int B, const Tw *__restrict__ W, int K, int N, int ks,
+            float *__restrict__ part, int *pos) {
+  extern __shared__ float dsm[];
+  float(*sx)[128] = reinterpret_cast<float(*)[128]>(dsm);
+  float(*red)[kGroup][kTileN + 4] =
+      reinterpret_cast<float(*)[kGroup][kTileN + 4]>(dsm + kGroup * 128);
+  griddep_launch_dependents();
+  griddep_wait();  // x comes from the kernel before (or the step before)
+  if (pos && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) pos[b] += 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = blockIdx.x * kTileN + lane * 8;
+  const int k0 = blockIdx.y * ks, k1 = min(K, k0 + ks);
+  const int rows = (k1 - k0 + kWarps - 1) / kWarps;  // rows per warp
+  for (int b0 = 0; b0 < B; b0 += kGroup) {
+    const int nb = min(kGroup, B - b0);
+    for (int i = threadIdx.x; i < kGroup * ks; i += blockDim.x) {
+      const int b = i / ks, k = i - b * ks;
+      sx[b][k] = (b < nb && k0 + k < k1) ? to_f(x[(long long)(b0 + b) * K + k0 + k]) : 0.f;
+    }
+    __syncthreads();
+    float acc[kGroup][8];
+#pragma unroll
+    for (int b = 0; b < kGroup; ++b)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[b][j] = 0.f;
+    if (c < N) {
+      const int kw0 = k0 + warp * rows, kw1 = min(k1, kw0 + rows);
+#pragma unroll 4
+      for (int k = kw0; k < kw1; ++k) {
+        float w[8];
+        load8(W, (long long)k * N + c, w);
+#pragma unroll
+        for (int b = 0; b < kGroup; ++b) {
+          const float xv = sx[b][k - k0];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[b][j] = fmaf(xv, w[j], acc[b][j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kGroup; ++b)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) red[warp][b][lane * 8 + j] = acc[b][j];
+    __syncthreads();
+    for (int o = threadIdx.x; o < nb * kTileN; o += blockDim.x) {
+      const int b = o / kTileN, cc = o - b * kTileN;
+      const int col = blockIdx.x * kTileN + cc;
+      if (col >= N) continue;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += red[w][b][cc];
+      part[((long long)blockIdx.y * B + b0 + b) * N + col] = v;
+    }
+    __syncthreads();
+  }
+}
+
+// one block per (32 value columns, sequence), 8 warps: gathers the
+// projection's slices into the heads and this block's U and V columns, then
+// (warp w taking keys j = w, w + 8, .. and linear-cache rows k = w, w + 8, ..;
+// lanes the columns) the chunk-local weights, their sum over the cached V
+// rows, the linear term and the gate; the warps' sums meet in a fixed order
+constexpr int kAttW = 8;
+__global__ void __launch_bounds__(32 * kAttW)
+decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__restrict__ beta,
+              const float *__restrict__ relpos, int B, int C, int e, int s, int slices,
+              float lin_scale) {
+  extern __shared__ float dsm[];
+  float *sh = dsm, *sa = dsm + 4 * s, *red = sa + C;  // heads [4][s], weights [C], [8][32]
+  griddep_launch_dependents();
+  griddep_wait();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.y, c = blockIdx.x * 32 + lane;
+  const int N = 2 * e + s;
+  const int i = (L.pos[b] - 1) % C;
+  const float *yp = L.proj + (long long)b * N;
+  const long long sstride = (long long)B * N;  // between slices
+  for (int k = threadIdx.x; k < s; k += blockDim.x) {
+    float pz = 0.f;
+    for (int q = 0; q < slices; ++q) pz += yp[q * sstride + 2 * e + k];
+    const float z = swish(pz);
+    for (int h = 0; h < 4; ++h) sh[h * s + k] = fmaf(z, gamma[h * s + k], beta[h * s + k]);
+  }
+  __syncthreads();
+  const float *qq = sh, *kq_new = sh + s, *ql = sh + 2 * s, *kl_new = sh + 3 * s;
+  float *kq_c = L.kq + (long long)b * C * s, *kl_c = L.kl + (long long)b * C * s;
+  float *v_c = L.vc + (long long)b * C * e;
+  // weights of the chunk's keys 0 .. i (key i is the new token's): one key
+  // per warp at a time, the lanes splitting its s products
+  const float inv_c = 1.0f / (float)C;
+  for (int j = warp; j <= i; j += kAttW) {
+    const float *kr = j < i ? kq_c + (long long)j * s : kq_new;
+    float dot = 0.f;
+    for (int k = lane; k < s; k += 32) dot = fmaf(qq[k], kr[k], dot);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) {
+      const float r = fmaxf(fmaf(dot, inv_c, relpos[j - i + C - 1]), 0.f);
+      sa[j] = r * r;
+    }
+  }
+  __syncthreads();
+  float pu = 0.f, pv = 0.f;
+  if (c < e)
+    for (int q = 0; q < slices; ++q) {
+      pu += yp[q * sstride + c];
+      pv += yp[q * sstride + e + c];
+    }
+  const float u = swish(pu), vnew = swish(pv);
+  float acc = 0.f;
+  if (c < e) {
+#pragma unroll 4
+    for (int j = warp; j < i; j += kAttW) acc = fmaf(sa[j], v_c[(long long)j * e + c], acc);
+    if (i % kAttW == warp) acc = fmaf(sa[i], vnew, acc);
+    float lin = 0.f;
+    const float *pre = L.prefix + (long long)b * s * e + c;
+#pragma unroll 4
+    for (int k = warp; k < s; k += kAttW) lin = fmaf(ql[k], pre[(long long)k * e], lin);
+    acc = fmaf(lin_scale, lin, acc);
+  }
+  red[warp * 32 + lane] = acc;
+  __syncthreads();
+  if (warp == 0 && c < e) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttW; ++w) v += red[w * 32 + lane];
+    L.gated[(long long)b * e + c] = u * v;
+    v_c[(long long)i * e + c] = vnew;  // the token's row, for the chunk's later keys
+  }
+  if (blockIdx.x == 0)
+    for (int k = threadIdx.x; k < s; k += blockDim.x) {
+      kq_c[(long long)i * s + k] = kq_new[k];
+      kl_c[(long long)i * s + k] = kl_new[k];
+    }
+}
+
+// the output's slices into out (io type): blocks with blockIdx.y == 0, one
+// thread per column; and, at a chunk's last token,
+// Prefix += K_lin,chunk^T V_chunk: one thread per (k, c) element, blocks
+// (256 columns, k, sequence)
+template <typename T>
+__global__ void __launch_bounds__(256)
+decode_finish(DecodeLayout L, T *__restrict__ out, int B, int C, int d, int e, int s, int slices) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int b = blockIdx.z, k = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k == 0 && c < d) {
+    float v = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < slices; ++q) v += L.outp[((long long)q * B + b) * d + c];
+    out[(long long)b * d + c] = from_f<T>(v);
+  }
+  if ((L.pos[b] - 1) % C != C - 1 || c >= e) return;
+  const float *kl_c = L.kl + (long long)b * C * s, *v_c = L.vc + (long long)b * C * e;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int j = 0; j < C; ++j) acc = fmaf(kl_c[(long long)j * s + k], v_c[(long long)j * e + c], acc);
+  L.prefix[((long long)b * s + k) * e + c] += acc;
+}
+
+template <typename T>
+cudaError_t step(const DecodeProblem &q) {
+  cudaError_t err;
+  const int N = 2 * q.e + q.s;
+  const int sp = decode_slices(q.d, N), so = decode_slices(q.e, q.d);
+  const int ksp = (q.d + sp - 1) / sp, kso = (q.e + so - 1) / so;
+  const size_t smem_a = sizeof(float) * (4 * (size_t)q.s + q.C + 32 * kAttW);
+  static unsigned long long configured = 0;  // shared-memory ceilings, per device
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured & (1ull << dev))) {
+    if ((err = cudaFuncSetAttribute(decode_attend, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(sizeof(float) * (4 * 256 + 4096 + 32 * kAttW)))) !=
+            cudaSuccess ||
+        (err = cudaFuncSetAttribute(gemv_splitk<T, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kGemvSmem)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(gemv_splitk<float, T>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kGemvSmem)) != cudaSuccess)
+      return err;
+    configured |= 1ull << dev;
+  }
+  if ((err = launch_pdl(gemv_splitk<T, T>, dim3((N + kTileN - 1) / kTileN, sp), dim3(256),
+                        kGemvSmem,
+                        q.stream, (const T *)q.x, q.B, (const T *)q.W_uvz, q.d, N, ksp, q.L.proj,
+                        q.L.pos)) != cudaSuccess)
+    return err;
+  if ((err = launch_pdl(decode_attend, dim3((q.e + 31) / 32, q.B), dim3(32 * kAttW), smem_a, q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
+                        q.lin_scale)) != cudaSuccess)
+    return err;
+  if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so), dim3(256),
+                        kGemvSmem, q.stream, (const float *)q.L.gated, q.B, (const T *)q.W_o, q.e, q.d,
+                        kso, q.L.outp, (int *)nullptr)) != cudaSuccess)
+    return err;
+  const int fx = ((q.e > q.d ? q.e : q.d) + 255) / 256;
+  return launch_pdl(decode_finish<T>, dim3(fx, q.s, q.B), dim3(256), 0, q.stream,
+                    q.L, (T *)q.out, q.B, q.C, q.d, q.e, q.s, so);
+}
+
+}  // namespace
+
+cudaError_t decode_step_f32(const DecodeProblem &q) { return step<float>(q); }
+cudaError_t decode_step_bf16(const DecodeProblem &q) { return step<__nv_bfloat16>(q); }
+
+}  // namespace flashgau

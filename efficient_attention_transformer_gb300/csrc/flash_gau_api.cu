@@ -154,6 +154,46 @@ int backward_layout(int B, int T, int C, int d, int e, int s, int causal, int dt
   return FLASH_GAU_OK;
 }
 
+// ---- decode state ----------------------------------------------------------
+int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L, size_t *total) {
+  if (B <= 0 || C <= 0 || d <= 0 || e <= 0 || s <= 0) return FLASH_GAU_EINVAL;
+  // grid rows (sequences), the chunk's weights in shared memory, and the
+  // 8-column (16-byte) weight loads
+  if (B > 65535 || C > 4096 || s > 256 || d > 16384 || e > 16384) return FLASH_GAU_ENOTSUP;
+  if (d % 8 != 0 || e % 8 != 0 || s % 8 != 0) return FLASH_GAU_ENOTSUP;
+  const size_t N = 2 * (size_t)e + s;
+  const size_t sp = decode_slices(d, (int)N), so = decode_slices(e, d);
+  size_t off = 0;
+  auto take = [&](void **p, size_t bytes) {
+    *p = base ? base + off : nullptr;
+    off = align_up(off + bytes);
+  };
+  void *st, *pos, *pre, *kq, *kl, *vc, *proj, *g, *outp;
+  const size_t f = sizeof(float);
+  take(&st, sizeof(int));
+  take(&pos, (size_t)B * sizeof(int));
+  take(&pre, (size_t)B * s * e * f);
+  take(&kq, (size_t)B * C * s * f);
+  take(&kl, (size_t)B * C * s * f);
+  take(&vc, (size_t)B * C * e * f);
+  take(&proj, sp * B * N * f);
+  take(&g, (size_t)B * e * f);
+  take(&outp, so * B * d * f);
+  if (L) {
+    L->status = (int *)st;
+    L->pos = (int *)pos;
+    L->prefix = (float *)pre;
+    L->kq = (float *)kq;
+    L->kl = (float *)kl;
+    L->vc = (float *)vc;
+    L->proj = (float *)proj;
+    L->gated = (float *)g;
+    L->outp = (float *)outp;
+  }
+  *total = off;
+  return FLASH_GAU_OK;
+}
+
 // ---- stage schedules ------------------------------------------------------
 const Stage kStagesF32[] = {
     {"projection", simt_projection_f32},
@@ -415,6 +455,44 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
   cudaError_t zerr = cudaMemsetAsync(workspace, 0, sizeof(int), q.stream);
   if (zerr != cudaSuccess) return record_cuda(zerr);
   const cudaError_t err = dtype == FLASH_GAU_BF16 ? backward_bf16(q) : backward_f32(q);
+  return err == cudaSuccess ? FLASH_GAU_OK : record_cuda(err);
+}
+
+size_t flash_gau_decode_state_bytes(int B, int C, const flash_gau_weights *w, int dtype) {
+  if (!w || (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16)) return 0;
+  size_t total = 0;
+  if (decode_layout(B, C, w->d, w->e, w->s, nullptr, nullptr, &total) != FLASH_GAU_OK) return 0;
+  return total;
+}
+
+int flash_gau_decode_step(const void *x, const flash_gau_weights *w, int B, int C, int dtype,
+                          void *state, size_t state_bytes, void *out, void *stream) {
+  if (!x || !w || !state || !out) return FLASH_GAU_EINVAL;
+  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos) return FLASH_GAU_EINVAL;
+  if (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16) return FLASH_GAU_EINVAL;
+  if (reinterpret_cast<uintptr_t>(state) % kAlign != 0) return FLASH_GAU_EWORKSPACE;
+  DecodeProblem q;
+  size_t total = 0;
+  int st = decode_layout(B, C, w->d, w->e, w->s, static_cast<char *>(state), &q.L, &total);
+  if (st != FLASH_GAU_OK) return st;
+  if (state_bytes < total) return FLASH_GAU_EWORKSPACE;
+  int num_sms = 0;
+  if ((st = device_info(&num_sms)) != FLASH_GAU_OK) return st;
+  q.B = B;
+  q.C = C;
+  q.d = w->d;
+  q.e = w->e;
+  q.s = w->s;
+  q.lin_scale = w->lin_scale;
+  q.x = x;
+  q.W_uvz = w->W_uvz;
+  q.W_o = w->W_o;
+  q.gamma = w->gamma;
+  q.beta = w->beta;
+  q.relpos = w->relpos;
+  q.out = out;
+  q.stream = static_cast<cudaStream_t>(stream);
+  const cudaError_t err = dtype == FLASH_GAU_BF16 ? decode_step_bf16(q) : decode_step_f32(q);
   return err == cudaSuccess ? FLASH_GAU_OK : record_cuda(err);
 }
 

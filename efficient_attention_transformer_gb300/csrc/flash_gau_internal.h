@@ -103,6 +103,40 @@ struct GemmAnyArgs {
 };
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 
+// Decode step (decode.cu): the per-sequence state, all fp32 but pos.
+struct DecodeLayout {
+  int *status;     // the state's first slot
+  int *pos;        // [B] tokens consumed
+  float *prefix;   // [B, s, e] sum of completed chunks' K_lin^T V
+  float *kq, *kl;  // [B, C, s] the current chunk's K_quad, K_lin rows
+  float *vc;       // [B, C, e] the current chunk's V rows
+  float *proj;     // [slices, B, 2e+s] this step's x W_uvz, by depth slice
+  float *gated;    // [B, e]
+  float *outp;     // [slices, B, d] this step's gated W_o, by depth slice
+};
+// Depth slices of the decode step's split-K matrix-vector product with a
+// [K, N] weight: about 150 blocks of 256 columns x one slice, at most 128
+// rows a slice.
+inline int decode_slices(int K, int N) {
+  const int tiles = (N + 255) / 256;
+  int sl = (150 + tiles - 1) / tiles;
+  const int lo = (K + 127) / 128, hi = (K + 7) / 8;
+  if (sl < lo) sl = lo;
+  if (sl > hi) sl = hi;
+  return sl < 1 ? 1 : sl;
+}
+struct DecodeProblem {
+  int B, C, d, e, s;
+  float lin_scale;
+  const void *x, *W_uvz, *W_o;
+  const float *gamma, *beta, *relpos;
+  void *out;
+  DecodeLayout L;
+  cudaStream_t stream;
+};
+cudaError_t decode_step_f32(const DecodeProblem &q);
+cudaError_t decode_step_bf16(const DecodeProblem &q);
+
 // Backward pass (backward.cu): fp32 work buffers in the caller's workspace.
 struct BackwardLayout {
   int *status;    // the workspace's first slot: FLASH_GAU_ETIMEOUT on a timed-out wait

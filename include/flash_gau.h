@@ -241,6 +241,32 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
                        const flash_gau_grads *g, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/* ---- autoregressive decode ---------------------------------------------- */
+/* One new token for each of B sequences, in constant work per token ("the
+ * linear cache is one matrix and the local attention is limited to one
+ * chunk", Transformer Quality in Linear Time §3.2.1).  The state, one
+ * buffer per batch of sequences, keeps per sequence the number of tokens
+ * consumed, the linear cache (the sum of K_lin^T V over its completed
+ * chunks, fp32 [s, e]) and the current chunk's K_quad, K_lin and V rows
+ * (fp32).  A zeroed state starts B new sequences at position 0; each call
+ * consumes token x[b] of every sequence and writes its output, the row the
+ * causal forward would give it.  Each call enqueues four kernels on
+ * `stream` and does not synchronise.                                       */
+
+/* State bytes for B sequences, or 0 when the arguments are invalid or
+ * unsupported (B <= 65535, C <= 4096, s <= 256, d and e <= 16384, d, e and
+ * s multiples of 8).                                                       */
+size_t flash_gau_decode_state_bytes(int B, int C, const flash_gau_weights *w,
+                                    int dtype);
+
+/* x, out: device [B, d], io type; state: device, 256-byte aligned,
+ * >= flash_gau_decode_state_bytes; w as for the forward (causal).  Returns
+ * FLASH_GAU_OK, FLASH_GAU_EINVAL, FLASH_GAU_ENOTSUP, FLASH_GAU_EWORKSPACE
+ * or FLASH_GAU_ECUDA.                                                      */
+int flash_gau_decode_step(const void *x, const flash_gau_weights *w, int B, int C,
+                          int dtype, void *state, size_t state_bytes, void *out,
+                          void *stream);
+
 /* ---- RoPE construction of the relative position bias ------------------- */
 /* Appendix D, Code 4 of "Transformer Quality in Linear Time" builds the bias
  * of windows of 512 positions and more from two learned vectors a, b of
