@@ -10,8 +10,9 @@ calculus, written out step by step:
 
   O = A W_o,  A = U * Vh,  Vh = Vq + Vl
       dW_o = A^T dO,  dA = dO W_o^T,  dU = dA * Vh,  dVh = dA * U
-  Vq_g = P_g V_g,  P = relu(S)^2 (masked),  S = Qq Kq^T / C + b
-      dP = dVh_g V_g^T,  dV_g += P^T dVh_g,  dS = 2 relu(S) dP (masked)
+  Vq_g = l P_g V_g,  P = relu(S)^2 (masked),  S = Qq Kq^T / C + b,
+  l = local_scale
+      dP = l dVh_g V_g^T,  dV_g += l P^T dVh_g,  dS = 2 relu(S) dP (masked)
       dQq_g = dS Kq_g / C,  dKq_g = dS^T Qq_g / C,
       drelpos[j - i + C - 1] += dS[i, j]
   Vl_g = lin_scale Ql_g Prefix_g,  Prefix_g = sum_{h<g} State_h (causal) or
@@ -43,7 +44,7 @@ def swish_grad(x):
 
 
 def flash_gau_backward(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal, dO,
-                       lin_scale=1.0):
+                       lin_scale=1.0, local_scale=1.0):
     """Gradients of sum(dO * flash_gau(...)) (same arguments as ``flash_gau``
     without RoPE; dO: [B, T, d]).  Returns a dict with dX [B, T, d], dW_u,
     dW_v [d, e], dW_z [d, s], dW_o [e, d], dgamma, dbeta [4, s] and
@@ -71,7 +72,7 @@ def flash_gau_backward(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal, dO
             r = slice(g * C, (g + 1) * C)
             S[b, g] = Qq[b, r] @ Kq[b, r].T / C + bias
             P = np.maximum(S[b, g], 0.0) ** 2 * mask
-            Vq[b, r] = P @ V[b, r]
+            Vq[b, r] = local_scale * (P @ V[b, r])
             state[b, g] = Kl[b, r].T @ V[b, r]
     prefix = np.zeros((B, G, s, e))
     for b in range(B):
@@ -101,8 +102,8 @@ def flash_gau_backward(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal, dO
             r = slice(g * C, (g + 1) * C)
             relu = np.maximum(S[b, g], 0.0)
             P = relu ** 2 * mask
-            dP = dVh[b, r] @ V[b, r].T
-            dV[b, r] += P.T @ dVh[b, r]
+            dP = local_scale * (dVh[b, r] @ V[b, r].T)
+            dV[b, r] += local_scale * (P.T @ dVh[b, r])
             dS = 2.0 * relu * dP * mask
             dQq[b, r] = dS @ Kq[b, r] / C
             dKq[b, r] = dS.T @ Qq[b, r] / C

@@ -13,7 +13,7 @@ reading, written out here for one sequence:
             q_quad, k_quad, q_lin, k_lin = z * gamma_k + beta_k
             append k_quad, k_lin, v to the chunk cache (row i)
             a_j = relu(q_quad . k_quad_j / C + relpos[j - i + C - 1])^2, j <= i
-            o = [u * (sum_j a_j v_j + lin_scale * q_lin Prefix)] W_o
+            o = [u * (local_scale sum_j a_j v_j + lin_scale q_lin Prefix)] W_o
   chunk end (i = C - 1): Prefix += K_lin,chunk^T V_chunk; empty the cache
 
 By causality the output for token t equals row t of the forward pass over
@@ -31,11 +31,12 @@ __all__ = ["DecodeState"]
 class DecodeState:
     """One sequence's decode state (float64)."""
 
-    def __init__(self, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, lin_scale=1.0):
+    def __init__(self, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, lin_scale=1.0,
+                 local_scale=1.0):
         f = lambda a: np.asarray(a, dtype=np.float64)  # noqa: E731
         self.W_u, self.W_v, self.W_z, self.W_o = f(W_u), f(W_v), f(W_z), f(W_o)
         self.gamma, self.beta, self.relpos = f(gamma), f(beta), f(relpos)
-        self.C, self.lin_scale = int(C), float(lin_scale)
+        self.C, self.lin_scale, self.local_scale = int(C), float(lin_scale), float(local_scale)
         self.e, self.s = self.W_u.shape[1], self.W_z.shape[1]
         self.prefix = np.zeros((self.s, self.e))
         self.kq, self.kl, self.v = [], [], []
@@ -55,7 +56,7 @@ class DecodeState:
         Vc = np.array(self.v)        # [i + 1, e]
         j = np.arange(i + 1)
         a = np.maximum(K @ qq / C + self.relpos[j - i + C - 1], 0.0) ** 2
-        vhat = a @ Vc + self.lin_scale * (ql @ self.prefix)
+        vhat = self.local_scale * (a @ Vc) + self.lin_scale * (ql @ self.prefix)
         o = (u * vhat) @ self.W_o
         if i == C - 1:
             self.prefix = self.prefix + np.array(self.kl).T @ Vc

@@ -23,7 +23,9 @@ Readings taken where the pages disagree or are silent:
     is the same rule at C = T);
   * the global term is the plain sum of chunk states of eq. 7 / eq. 8, times
     a caller-chosen ``lin_scale`` (1 = eq. 7/8, 1/C = the listing's division,
-    0 = the LocalOnly ablation);
+    0 = the LocalOnly ablation); the local term is likewise multiplied by
+    ``local_scale`` (1 = as written, 0 = the GlobalOnly ablation of [TQLT]
+    §4.4, which keeps only the global part);
   * b[i, j] = relpos[j - i + C - 1], the Toeplitz matrix the Code 4 listing
     builds from 2C-1 weights, used for every C;
   * the causal mask keeps the diagonal (j <= i) and is applied after relu^2;
@@ -203,14 +205,15 @@ def toeplitz_relpos(T):
 
 
 def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
-              lin_scale=1.0, positions=None, rope_base=10000.0):
+              lin_scale=1.0, positions=None, rope_base=10000.0, local_scale=1.0):
     """FLASH GAU layer forward with mixed chunk attention, in float64.
 
     Steps ([TQLT] Method and flash_block; [FLASH-blog] "Mixed Chunking"):
       1. U = swish(X W_u), V = swish(X W_v), Z = swish(X W_z).
       2. Q_quad, K_quad, Q_lin, K_lin = Z * gamma_h + beta_h.
-      3. Per chunk g of C tokens: Vq_g = relu^2(Q_quad,g K_quad,g^T / C + b) V_g
-         (upper triangle zeroed when causal).
+      3. Per chunk g of C tokens: Vq_g = local_scale *
+         relu^2(Q_quad,g K_quad,g^T / C + b) V_g (upper triangle zeroed when
+         causal).
       4. State_g = K_lin,g^T V_g.
       5. Prefix_g = sum_{h<g} State_h if causal (eq. 8), else sum_h State_h
          (eq. 7).
@@ -249,7 +252,7 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
         for g in range(G):
             rows = slice(g * C, (g + 1) * C)
             a = chunk_scores(Qq[b, rows], Kq[b, rows], bias, C, causal)
-            Vq[b, rows] = a @ V[b, rows]
+            Vq[b, rows] = local_scale * (a @ V[b, rows])
             state[b, g] = Kl[b, rows].T @ V[b, rows]
 
     prefix = np.zeros((B, G, s, e))
@@ -277,6 +280,7 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
 
 def flash_block(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
                 lin_scale=1.0, norm="layer", norm_g=None, norm_b=None, norm_eps=1e-5,
+                local_scale=1.0,
                 rope_on=True, rope_base=10000.0, pos_offset=0):
     """The pages' FLASH block around the layer ([TQLT] flash_block
     pseudocode): shortcut = x; x = norm(x); the GAU of ``flash_gau`` with
@@ -298,7 +302,8 @@ def flash_block(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
     T = X.shape[1]
     positions = np.arange(T) + pos_offset if rope_on else None
     O, inter = flash_gau(Xn, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
-                         lin_scale, positions=positions, rope_base=rope_base)
+                         lin_scale, positions=positions, rope_base=rope_base,
+                         local_scale=local_scale)
     inter["Xn"] = Xn
     return O + X, inter
 

@@ -477,9 +477,10 @@ def test_toeplitz_relpos_round_trip():
 
 
 # ---------------------------------------------------------------- backward
-@pytest.mark.parametrize("causal,lin_scale,C", [(True, 1.0, 4), (False, 1.0, 4),
-                                                (True, 0.25, 2), (False, 0.0, 8)])
-def test_backward_matches_finite_differences(causal, lin_scale, C):
+@pytest.mark.parametrize("causal,lin_scale,C,local_scale", [
+    (True, 1.0, 4, 1.0), (False, 1.0, 4, 1.0), (True, 0.25, 2, 0.5), (False, 0.0, 8, 1.0),
+    (True, 1.0, 4, 0.0)])
+def test_backward_matches_finite_differences(causal, lin_scale, C, local_scale):
     """Every gradient entry of L = sum(dO * O) against central differences of
     the forward oracle (step 1e-6, float64), on a problem small enough to
     perturb each input and parameter once."""
@@ -494,12 +495,12 @@ def test_backward_matches_finite_differences(causal, lin_scale, C):
 
     def loss(a):
         O, _ = flash_gau(a["X"], a["W_u"], a["W_v"], a["W_z"], a["W_o"], a["gamma"],
-                         a["beta"], a["relpos"], C, causal, lin_scale)
+                         a["beta"], a["relpos"], C, causal, lin_scale, local_scale=local_scale)
         return float(np.sum(dO * O))
 
     grads = O.flash_gau_backward(args["X"], args["W_u"], args["W_v"], args["W_z"], args["W_o"],
                                  args["gamma"], args["beta"], args["relpos"], C, causal, dO,
-                                 lin_scale)
+                                 lin_scale, local_scale)
     h = 1e-6
     for name in args:
         g = grads["d" + name]
@@ -525,8 +526,9 @@ def test_swish_grad_against_library_derivative():
 
 
 # ---------------------------------------------------------------- decode
-@pytest.mark.parametrize("C,T,lin_scale", [(4, 11, 1.0), (8, 24, 0.5), (1, 5, 1.0), (16, 7, 0.0)])
-def test_decode_steps_equal_causal_forward_rows(C, T, lin_scale):
+@pytest.mark.parametrize("C,T,lin_scale,local_scale", [
+    (4, 11, 1.0, 1.0), (8, 24, 0.5, 1.0), (1, 5, 1.0, 1.0), (16, 7, 0.0, 1.0), (4, 13, 1.0, 0.0)])
+def test_decode_steps_equal_causal_forward_rows(C, T, lin_scale, local_scale):
     """By causality, the decode step's output for token t is row t of the
     causal forward over any sequence that starts with the same t + 1
     tokens (the rest zero-padded to a multiple of C)."""
@@ -540,8 +542,9 @@ def test_decode_steps_equal_causal_forward_rows(C, T, lin_scale):
     Tp = -(-T // C) * C
     Xp = np.zeros((1, Tp, d))
     Xp[0, :T] = X
-    O, _ = flash_gau(Xp, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, True, lin_scale)
-    st = O_.DecodeState(W_u, W_v, W_z, W_o, gamma, beta, relpos, C, lin_scale)
+    O, _ = flash_gau(Xp, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, True, lin_scale,
+                     local_scale=local_scale)
+    st = O_.DecodeState(W_u, W_v, W_z, W_o, gamma, beta, relpos, C, lin_scale, local_scale)
     for t in range(T):
         o = st.step(X[t])
         assert np.allclose(o, O[0, t], rtol=1e-12, atol=1e-12), t
@@ -563,3 +566,53 @@ def test_decode_prefix_is_completed_chunks_sum():
     V = swish(X @ W[1])
     assert np.allclose(st.prefix, Kl.T @ V, rtol=1e-12, atol=1e-12)
     assert st.kq == [] and st.t == 2 * C
+
+
+# ---------------------------------------------------------------- GlobalOnly
+def test_global_only_noncausal_is_full_linear_attention():
+    """local_scale = 0, non-causal: only the global term, the total of all
+    chunk states, remains; by associativity it is the full-length linear
+    attention U * (Q_lin K_lin^T V), computed here with the T x T matrix."""
+    rng = np.random.default_rng(80)
+    B, T, d, e, s, C = 2, 12, 5, 7, 4, 4
+    W_u, W_v = rng.normal(size=(d, e)), rng.normal(size=(d, e))
+    W_z, W_o = rng.normal(size=(d, s)), rng.normal(size=(e, d))
+    gamma, beta = rng.normal(1, 0.3, (4, s)), rng.normal(0, 0.3, (4, s))
+    X = rng.normal(size=(B, T, d))
+    O, _ = flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, rng.normal(size=2 * C - 1), C, False,
+                     lin_scale=0.7, local_scale=0.0)
+    U, V, Z = swish(X @ W_u), swish(X @ W_v), swish(X @ W_z)
+    Ql, Kl = Z * gamma[2] + beta[2], Z * gamma[3] + beta[3]
+    want = np.stack([(U[b] * (0.7 * (Ql[b] @ Kl[b].T) @ V[b])) @ W_o for b in range(B)])
+    assert np.allclose(O, want, rtol=1e-12, atol=1e-10)
+
+
+def test_global_only_causal_c1_is_strictly_causal_linear_attention():
+    """local_scale = 0, causal, C = 1: token t sees the states of tokens
+    t' < t only (a brute-force sum over earlier tokens)."""
+    rng = np.random.default_rng(81)
+    T, d, e, s = 9, 4, 6, 4
+    W_u, W_v = rng.normal(size=(d, e)), rng.normal(size=(d, e))
+    W_z, W_o = rng.normal(size=(d, s)), rng.normal(size=(e, d))
+    gamma, beta = rng.normal(1, 0.3, (4, s)), rng.normal(0, 0.3, (4, s))
+    X = rng.normal(size=(1, T, d))
+    O, _ = flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, np.array([0.3]), 1, True,
+                     local_scale=0.0)
+    U, V, Z = swish(X[0] @ W_u), swish(X[0] @ W_v), swish(X[0] @ W_z)
+    Ql, Kl = Z * gamma[2] + beta[2], Z * gamma[3] + beta[3]
+    for t in range(T):
+        acc = sum((Ql[t] @ Kl[h]) * V[h] for h in range(t)) if t else np.zeros(e)
+        assert np.allclose(O[0, t], (U[t] * acc) @ W_o, rtol=1e-12, atol=1e-12)
+
+
+def test_output_is_affine_in_local_scale():
+    """O(l) = O(0) + l (O(1) - O(0)): the local term enters linearly."""
+    rng = np.random.default_rng(82)
+    B, T, d, e, s, C = 1, 8, 4, 6, 4, 4
+    args = [rng.normal(size=(B, T, d)), rng.normal(size=(d, e)), rng.normal(size=(d, e)),
+            rng.normal(size=(d, s)), rng.normal(size=(e, d)), rng.normal(1, 0.3, (4, s)),
+            rng.normal(0, 0.3, (4, s)), rng.normal(size=2 * C - 1), C, True]
+    O0 = flash_gau(*args, local_scale=0.0)[0]
+    O1 = flash_gau(*args, local_scale=1.0)[0]
+    O25 = flash_gau(*args, local_scale=2.5)[0]
+    assert np.allclose(O25, O0 + 2.5 * (O1 - O0), rtol=1e-12, atol=1e-10)
