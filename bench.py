@@ -297,6 +297,33 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         block_ms = float(t[0])
 
+    # ---- next row: the two ablations of the mixed chunk attention on the
+    # same workload and weights: GlobalOnly (local term off: no chunk scores
+    # are formed) and LocalOnly (global term off)
+    ablations = {}
+    for name, lin_sc, loc_sc in (("global_only", 1.0, 0.0), ("local_only", 0.0, 1.0)):
+        wv = fg.GauWeights(weights.W_uvz, weights.W_o, weights.gamma, weights.beta,
+                           weights.relpos, d, e, s, lin_sc, loc_sc)
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            bd.forward(X, wv, C, causal, out=out, workspace=ws, stream=stream)
+        a0 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+        a1 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+        torch.cuda.synchronize()
+        for k in range(blk_steps):
+            flush.fill_(1.0)
+            a0[k].record(stream)
+            bd.forward(X, wv, C, causal, out=out, workspace=ws, stream=stream)
+            a1[k].record(stream)
+        torch.cuda.synchronize()
+        ab_ms = sum(x.elapsed_time(y) for x, y in zip(a0, a1)) / blk_steps
+        if bd.workspace_status(ws) != 0:
+            raise RuntimeError("kernel status after the %s runs" % name)
+        ablations[name] = {"ms_per_step": round(ab_ms, 5),
+                           "value": round(B * T * world / (ab_ms * 1e-3), 1),
+                           "unit": "tokens/s"}
+        del wv
+
     # ---- next row: the RoPE construction of the relative-position table
     # (windows of 512 and more), 128-wide learned vectors, C = 512
     trng = np.random.default_rng(2000 + w["seed"])
@@ -469,6 +496,13 @@ def run_ours(args, rank, world, local_rank):
                      "B sequences, one token each per step, 2C steps; four kernels per step "
                      "(projection, chunk attention with the linear cache, output, cache fold)",
                 **decode),
+            "global_only": dict(
+                what="the layer with the local term switched off (local_scale = 0): "
+                     "projection, chunk states, scan, Q_lin Prefix and the gate, output",
+                **ablations["global_only"]),
+            "local_only": dict(
+                what="the layer with the global term switched off (lin_scale = 0)",
+                **ablations["local_only"]),
             "rope_toeplitz_bias": {
                 "what": "relative-position table of the RoPE bias construction, C = 512, "
                         "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",

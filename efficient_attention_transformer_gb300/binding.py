@@ -63,6 +63,7 @@ class Weights(ctypes.Structure):
         ("e", ctypes.c_int),
         ("s", ctypes.c_int),
         ("lin_scale", ctypes.c_float),
+        ("local_scale", ctypes.c_float),
     ]
 
 
@@ -198,17 +199,18 @@ class Grads(ctypes.Structure):
 class GauWeights:
     """Device-resident layer parameters in the layout the library expects."""
 
-    def __init__(self, W_uvz, W_o, gamma, beta, relpos, d, e, s, lin_scale=1.0):
+    def __init__(self, W_uvz, W_o, gamma, beta, relpos, d, e, s, lin_scale=1.0,
+                 local_scale=1.0):
         self.W_uvz, self.W_o = W_uvz, W_o
         self.gamma, self.beta, self.relpos = gamma, beta, relpos
         self.d, self.e, self.s = int(d), int(e), int(s)
-        self.lin_scale = float(lin_scale)
+        self.lin_scale, self.local_scale = float(lin_scale), float(local_scale)
         self.dtype = dtype_code(W_uvz.dtype)
         f32 = torch.float32
         self.c = Weights(_dev_ptr(W_uvz, "W_uvz", W_uvz.dtype), _dev_ptr(W_o, "W_o", W_uvz.dtype),
                          _dev_ptr(gamma, "gamma", f32), _dev_ptr(beta, "beta", f32),
                          _dev_ptr(relpos, "relpos", f32), self.d, self.e, self.s,
-                         self.lin_scale)
+                         self.lin_scale, self.local_scale)
         if tuple(W_uvz.shape) != (d, 2 * e + s) or tuple(W_o.shape) != (e, d):
             raise ValueError("weight shapes do not match d, e, s")
         if tuple(gamma.shape) != (4, s) or tuple(beta.shape) != (4, s):

@@ -6,9 +6,10 @@
 //
 //   recompute  Pre = X W_uvz;  U, V, Z = swish(Pre);  heads = Z gamma + beta
 //              S = Qq Kq^T / C + b,  P = relu(S)^2 (masked)      per chunk
-//              Vh = P V + lin_scale Q_lin Prefix_g,  A = U * Vh
+//              Vh = l P V + lin_scale Q_lin Prefix_g,  A = U * Vh
+//              (l = local_scale)
 //   output     dW_o = A^T dO,  dA = dO W_o^T,  dU = dA * Vh,  dVh = dA * U
-//   local      dP = dVh V^T,  dV = P^T dVh,  dS = 2 relu(S) dP (masked),
+//   local      dP = l dVh V^T,  dV = l P^T dVh,  dS = 2 relu(S) dP (masked),
 //              dQq = dS Kq / C,  dKq = dS^T Qq / C,  db[j-i] += dS[i, j]
 //   global     dQl = lin_scale dVh Prefix^T,  dPrefix = lin_scale Ql^T dVh,
 //              dState_h = sum_{g>h} dPrefix_g (or the total),
@@ -384,7 +385,7 @@ cudaError_t run(const BackwardProblem &q) {
   BW_TRY(gemm(st, C, C, s, (int)BG, Qq, op(s, 1, (long long)C * s), Kq,
               op(1, s, (long long)C * s), ScoreEpi{S, P, q.relpos, C, q.causal, 1.f / C}));
   BW_TRY(gemm(st, C, e, C, (int)BG, P, op(C, 1, (long long)C * C), V, op(e, 1, (long long)C * e),
-              StoreF32{Vh, e, 1, (long long)C * e, 1.f, 0}));
+              StoreF32{Vh, e, 1, (long long)C * e, q.local_scale, 0}));
   BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
               op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
   scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, prefix, q.B, G, se, q.causal,
@@ -408,9 +409,9 @@ cudaError_t run(const BackwardProblem &q) {
   gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e);
   // ---- local part
   BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
-              op(1, e, (long long)C * e), StoreF32{dP, C, 1, (long long)C * C, 1.f, 0}));
+              op(1, e, (long long)C * e), StoreF32{dP, C, 1, (long long)C * C, q.local_scale, 0}));
   BW_TRY(gemm(st, C, e, C, (int)BG, P, op(1, C, (long long)C * C), dVh,
-              op(e, 1, (long long)C * e), StoreF32{dV, e, 1, (long long)C * e, 1.f, 0}));
+              op(e, 1, (long long)C * e), StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   score_grad<<<blocks_for(BG * C * C), 256, 0, st>>>(S, dP, BG, C, q.causal);
   relpos_grad<<<2 * C - 1, 256, 0, st>>>(dP, q.drelpos, BG, C);
   float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;

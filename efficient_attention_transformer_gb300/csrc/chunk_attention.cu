@@ -36,6 +36,11 @@
 // Two accumulators alternate between units, so while the epilogue warps
 // drain one, the MMAs of the next unit already fill the other.
 //
+// The local term carries a factor local_scale (1 as written).  Any other
+// non-zero value multiplies P in the relu^2 warps; 0 (global term only)
+// gives every unit zero key blocks, so no Q_quad/K_quad/V tile is loaded
+// and no score is formed: a unit is then acc = Q_lin Prefix and the gate.
+//
 // Shared memory (224 KB): Q_lin 32 KB, one ring of 8 x 16 KB stages for
 // Q_quad and K_quad atoms and V / prefix half-blocks, epilogue boxes
 // 8 warps x 2 x 4 KB.  TMEM: accumulators
@@ -102,6 +107,7 @@ struct AttnParams {
   int g_split;      // first chunk of the single-tile units
   int total;
   float inv_c;
+  float local_scale;  // factor on P; 0: no key blocks at all
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
@@ -138,7 +144,7 @@ __device__ __forceinline__ Unit unit_of(const AttnParams &p, int u) {
   x.chunk = chunk0 + u / (per_qt * p.n_qt);
   x.b = x.chunk / p.G;
   x.tok0 = (long long)x.chunk * p.C;
-  x.nkb = p.causal ? x.qt + 1 : p.C / KB;
+  x.nkb = p.local_scale == 0.f ? 0 : p.causal ? x.qt + 1 : p.C / KB;
   x.q_per_block = 4 * (x.nkb - 1) + 1 >= RING;
   return x;
 }
@@ -172,7 +178,9 @@ struct Ring {
 // columns (fp32) at sbuf + 64*half, writes P = relu^2(S/C + b) as 32 packed
 // bf16 columns over the start of those same columns.  The bias table holds
 // -inf at the causally masked offsets, so the mask costs nothing here.  All
-// 64 S values are in registers before the first store lands.
+// 64 S values are in registers before the first store lands.  SCALED: P is
+// multiplied by local_scale.
+template <bool SCALED>
 __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, int kb, int qt,
                                            int r, int half) {
   const int i = qt * QT + r;
@@ -193,6 +201,10 @@ __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, i
     x1 = fmaxf(x1, 0.f);
     x0 *= x0;
     x1 *= x1;
+    if (SCALED) {
+      x0 *= p.local_scale;
+      x1 *= p.local_scale;
+    }
     if (j < 32) lo[j / 2] = pack_bf16(x0, x1);
     else hi[(j - 32) / 2] = pack_bf16(x0, x1);
   }
@@ -304,7 +316,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
         const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
-        ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
+        if (x.nkb > 0) ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
         for (int t = 0; ok && t < x.ng; ++t) {
           const int col = (x.et0 + t) * ET;
           for (int kb = 0; ok && kb < x.nkb; ++kb) {
@@ -419,7 +431,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         }
         const Unit x = unit_of(p, u);
         const int n0 = n;
-        ok = issue_s(true, x.q_per_block || x.nkb == 1);
+        if (x.nkb > 0) ok = issue_s(true, x.q_per_block || x.nkb == 1);
         // P of the unit's key blocks stays in TMEM for all its value tiles
         for (int t = 0; ok && t < x.ng; ++t, ++v) {
           const bool last_t = t + 1 == x.ng;
@@ -447,7 +459,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
             if (ok) tc_fence_after();
           }
-          ok = ok && issue_b_smem(sQL, false) && issue_b_smem(sQL + ATOM_BYTES, false);
+          // with no key blocks the global term opens the accumulator
+          ok = ok && issue_b_smem(sQL, x.nkb == 0) && issue_b_smem(sQL + ATOM_BYTES, false);
           if (!ok) break;
           if (last_t) mma_commit(smem_u32(&bar->ql_empty));
           mma_commit(smem_u32(&bar->acc_full[v & 1]));
@@ -480,7 +493,10 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           break;
         }
         tc_fence_after();
-        relu2_half(tmem + lane_off + TM_S + sb * KB, p, kb, x.qt, r, half);
+        if (p.local_scale == 1.f)
+          relu2_half<false>(tmem + lane_off + TM_S + sb * KB, p, kb, x.qt, r, half);
+        else
+          relu2_half<true>(tmem + lane_off + TM_S + sb * KB, p, kb, x.qt, r, half);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar->p_full[sb]));
@@ -648,6 +664,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.n_grouped = p.g_split * p.n_qt * p.n_vg;
   p.total = p.n_grouped + singles * per_chunk;
   p.inv_c = 1.0f / (float)pr.C;
+  p.local_scale = pr.local_scale;
   p.bias = pr.bias;
   p.status = pr.status;
   p.next_unit = pr.status + kNextUnitWord;

@@ -140,7 +140,7 @@ constexpr int kAttW = 8;
 __global__ void __launch_bounds__(32 * kAttW)
 decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__restrict__ beta,
               const float *__restrict__ relpos, int B, int C, int e, int s, int slices,
-              float lin_scale) {
+              float lin_scale, float local_scale) {
   extern __shared__ float dsm[];
   float *sh = dsm, *sa = dsm + 4 * s, *red = sa + C;  // heads [4][s], weights [C], [8][32]
   griddep_launch_dependents();
@@ -172,7 +172,7 @@ decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__re
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     if (lane == 0) {
       const float r = fmaxf(fmaf(dot, inv_c, relpos[j - i + C - 1]), 0.f);
-      sa[j] = r * r;
+      sa[j] = local_scale * r * r;
     }
   }
   __syncthreads();
@@ -264,7 +264,7 @@ cudaError_t step(const DecodeProblem &q) {
                         q.L.pos)) != cudaSuccess)
     return err;
   if ((err = launch_pdl(decode_attend, dim3((q.e + 31) / 32, q.B), dim3(32 * kAttW), smem_a, q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
-                        q.lin_scale)) != cudaSuccess)
+                        q.lin_scale, q.local_scale)) != cudaSuccess)
     return err;
   if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so), dim3(256),
                         kGemvSmem, q.stream, (const float *)q.L.gated, q.B, (const T *)q.W_o, q.e, q.d,

@@ -1,5 +1,6 @@
 // C ABI of libflashgau: argument validation, workspace layout and the stage
 // schedule of one forward pass.  Every launch happens on the caller's stream.
+#include <math.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -240,6 +241,12 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
+// The two term factors: finite values only (an infinite factor would turn
+// the masked zeros of the local term into NaN).
+bool scales_finite(const flash_gau_weights *w) {
+  return isfinite(w->lin_scale) && isfinite(w->local_scale);
+}
+
 int check_block(const flash_gau_block *blk, int s) {
   if (!blk) return FLASH_GAU_OK;
   if (blk->norm < FLASH_GAU_NORM_NONE || blk->norm > FLASH_GAU_NORM_SCALE) return FLASH_GAU_EINVAL;
@@ -256,7 +263,7 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
                 size_t workspace_bytes, void *stream, void *const *stage_events,
                 int n_events) {
   if (!X || !w || !out || !workspace || !w->W_uvz || !w->W_o || !w->gamma || !w->beta ||
-      !w->relpos)
+      !w->relpos || !scales_finite(w))
     return FLASH_GAU_EINVAL;
   if (n_events < 0 || (n_events > 0 && !stage_events)) return FLASH_GAU_EINVAL;
   causal = causal ? 1 : 0;
@@ -286,6 +293,7 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.dtype = dtype;
   p.M = (long long)B * T;
   p.lin_scale = w->lin_scale;
+  p.local_scale = w->local_scale;
   p.X = X;
   p.W_uvz = w->W_uvz;
   p.W_o = w->W_o;
@@ -413,7 +421,8 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
                        int C, int causal, int dtype, const flash_gau_grads *g, void *workspace,
                        size_t workspace_bytes, void *stream) {
   if (!X || !dO || !w || !g || !workspace) return FLASH_GAU_EINVAL;
-  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos) return FLASH_GAU_EINVAL;
+  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos || !scales_finite(w))
+    return FLASH_GAU_EINVAL;
   if (!g->dX || !g->dW_uvz || !g->dW_o || !g->dgamma || !g->dbeta || !g->drelpos)
     return FLASH_GAU_EINVAL;
   if (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16) return FLASH_GAU_EINVAL;
@@ -435,6 +444,7 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
   q.causal = causal;
   q.M = (long long)B * T;
   q.lin_scale = w->lin_scale;
+  q.local_scale = w->local_scale;
   q.X = X;
   q.dO = dO;
   q.W_uvz = w->W_uvz;
@@ -468,7 +478,8 @@ size_t flash_gau_decode_state_bytes(int B, int C, const flash_gau_weights *w, in
 int flash_gau_decode_step(const void *x, const flash_gau_weights *w, int B, int C, int dtype,
                           void *state, size_t state_bytes, void *out, void *stream) {
   if (!x || !w || !state || !out) return FLASH_GAU_EINVAL;
-  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos) return FLASH_GAU_EINVAL;
+  if (!w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos || !scales_finite(w))
+    return FLASH_GAU_EINVAL;
   if (dtype != FLASH_GAU_FP32 && dtype != FLASH_GAU_BF16) return FLASH_GAU_EINVAL;
   if (reinterpret_cast<uintptr_t>(state) % kAlign != 0) return FLASH_GAU_EWORKSPACE;
   DecodeProblem q;
@@ -484,6 +495,7 @@ int flash_gau_decode_step(const void *x, const flash_gau_weights *w, int B, int 
   q.e = w->e;
   q.s = w->s;
   q.lin_scale = w->lin_scale;
+  q.local_scale = w->local_scale;
   q.x = x;
   q.W_uvz = w->W_uvz;
   q.W_o = w->W_o;
@@ -533,6 +545,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 104; }
+int flash_gau_version(void) { return 106; }
 
 }  // extern "C"

@@ -34,6 +34,7 @@ struct Problem {
   int B, T, C, G, d, e, s, causal, dtype;
   long long M;  // B * T tokens
   float lin_scale;
+  float local_scale;  // factor on the local term; 0 = global term only
   const void *X;
   const void *W_uvz;
   const void *W_o;
@@ -127,7 +128,7 @@ inline int decode_slices(int K, int N) {
 }
 struct DecodeProblem {
   int B, C, d, e, s;
-  float lin_scale;
+  float lin_scale, local_scale;
   const void *x, *W_uvz, *W_o;
   const float *gamma, *beta, *relpos;
   void *out;
@@ -159,7 +160,7 @@ struct BackwardLayout {
 struct BackwardProblem {
   int B, T, C, G, d, e, s, causal;
   long long M;
-  float lin_scale;
+  float lin_scale, local_scale;
   const void *X, *dO, *W_uvz, *W_o;
   const float *gamma, *beta, *relpos;
   void *dX;

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256)
 simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
                      const T *__restrict__ heads, const T *__restrict__ prefix,
                      const float *__restrict__ relpos, T *__restrict__ gated,
-                     long long M, int C, int G, int e, int s, int causal) {
+                     long long M, int C, int G, int e, int s, int causal, float local_scale) {
   extern __shared__ float sm[];
   const int sp = s + 1;
   float *q = sm;                          // [32][s+1]
@@ -187,7 +187,8 @@ simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
     q[rr * sp + k] = (i0 + rr < C) ? to_f(Qq[(tok0 + i0 + rr) * s + k]) : 0.f;
   }
   const float inv_c = 1.0f / (float)C;
-  const int key_end = causal ? min(C, i0 + kAttRows) : C;
+  // no keys at all when the local term is switched off
+  const int key_end = local_scale == 0.f ? 0 : causal ? min(C, i0 + kAttRows) : C;
   for (int j0 = 0; j0 < key_end; j0 += kAttKeys) {
     __syncthreads();
     for (int idx = tid; idx < kAttKeys * s; idx += 256) {
@@ -210,7 +211,7 @@ simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
       if (i < C && j < C && !(causal && j > i)) {
         float x = fmaf(sc, inv_c, relpos[j - i + C - 1]);
         x = fmaxf(x, 0.f);
-        a = x * x;
+        a = local_scale * x * x;
       }
       pw[rr * (kAttKeys + 1) + jj] = a;
     }
@@ -300,7 +301,7 @@ cudaError_t chunk_attention(const Problem &p) {
   dim3 grid(cdiv(p.e, kAttCols), cdiv(p.C, kAttRows), p.B * p.G);
   simt_chunk_attention<T><<<grid, 256, smem, p.stream>>>(
       (const T *)p.U, (const T *)p.V, (const T *)p.heads, (const T *)p.prefix, p.relpos,
-      (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal);
+      (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal, p.local_scale);
   return cudaGetLastError();
 }
 

@@ -10,7 +10,8 @@
  *   [U | V | Z] = swish(X [W_u | W_v | W_z])               swish(x) = x*sigmoid(x)
  *   Q_quad, K_quad, Q_lin, K_lin = Z * gamma_h + beta_h     (per-dimension heads)
  *   for every chunk g of C consecutive tokens (G = T / C chunks):
- *     Vq_g   = relu^2(Q_quad,g K_quad,g^T / C + b) V_g      b[i][j] = relpos[j-i+C-1]
+ *     Vq_g   = local_scale * relu^2(Q_quad,g K_quad,g^T / C + b) V_g
+ *                                                          b[i][j] = relpos[j-i+C-1]
  *              (entries with j > i are zero when causal; diagonal kept)
  *     P_g    = sum_{h<g} K_lin,h^T V_h   (causal, eq. 8; zero for g = 0)
  *            = sum_{h}   K_lin,h^T V_h   (non-causal, eq. 7)
@@ -20,7 +21,8 @@
  * Readings where the pages differ: scores are divided by C before the bias
  * (flash_block pseudocode); the chunk states are summed plainly (eq. 7/8),
  * lin_scale = 1 reproduces that, 1/C the appendix listing, 0 the LocalOnly
- * ablation; the Toeplitz bias of appendix D Code 4 (2C-1 weights) is used for
+ * ablation; local_scale = 1 is the layer as written, 0 the GlobalOnly
+ * ablation (section 4.4: only the global, linear part); the Toeplitz bias of appendix D Code 4 (2C-1 weights) is used for
  * every C.  No projection biases, norm, RoPE or residual are applied.
  *
  * Conventions for every entry point:
@@ -75,6 +77,8 @@ typedef struct flash_gau_weights {
   int e;                /* expansion width (U, V)                           */
   int s;                /* shared head width (Z)                            */
   float lin_scale;      /* factor on the global (linear) term               */
+  float local_scale;    /* factor on the local (quadratic) term: 1 as
+                           written; 0 skips the chunk scores entirely       */
 } flash_gau_weights;
 
 /* Byte offsets of the intermediates inside a workspace (all from its start).

@@ -23,9 +23,10 @@ class Case:
     """One problem instance on the GPU plus its float64 oracle result."""
 
     def __init__(self, B, T, d, e, s, C, causal, dtype, seed, lin_scale=1.0, inputs=None,
-                 device="cuda"):
+                 device="cuda", local_scale=1.0):
         self.B, self.T, self.d, self.e, self.s, self.C = B, T, d, e, s, C
         self.causal, self.dtype, self.lin_scale = causal, dtype, lin_scale
+        self.local_scale = local_scale
         self.inp = inputs or make_inputs(B, T, d, e, s, C, dtype, seed)
         tdt = torch_dtype(dtype)
         i = self.inp
@@ -38,7 +39,7 @@ class Case:
             torch.tensor(i["gamma"], dtype=torch.float32, device=dev),
             torch.tensor(i["beta"], dtype=torch.float32, device=dev),
             torch.tensor(i["relpos"], dtype=torch.float32, device=dev),
-            d, e, s, lin_scale)
+            d, e, s, lin_scale, local_scale)
         self.workspace = self.weights.new_workspace(B, T, C, causal, dev)
         self.out = torch.empty_like(self.X)
         self.layout = bd.workspace_layout(B, T, C, d, e, s, causal, self.weights.dtype)
@@ -52,7 +53,8 @@ class Case:
     def reference(self):
         i = self.inp
         return flash_gau(i["X"], i["W_u"], i["W_v"], i["W_z"], i["W_o"], i["gamma"],
-                         i["beta"], i["relpos"], self.C, self.causal, self.lin_scale)
+                         i["beta"], i["relpos"], self.C, self.causal, self.lin_scale,
+                         local_scale=self.local_scale)
 
     def intermediate(self, name):
         """An intermediate read back from the workspace, as float64, in its

@@ -78,7 +78,7 @@ def test_layout_rejects(L, args, code):
 
 
 def test_forward_rejects_before_any_launch(L):
-    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 32, 1.0)  # fake non-null pointers
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 32, 1.0, 1.0)  # fake non-null pointers
     ws = 1 << 20
     # null X
     assert L.flash_gau_forward(None, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 8, 256 * 64,
@@ -103,7 +103,7 @@ def test_forward_rejects_before_any_launch(L):
 
 
 def test_workspace_bytes_matches_layout(L):
-    w = bd.Weights(1, 2, 3, 4, 5, 768, 1536, 128, 1.0)
+    w = bd.Weights(1, 2, 3, 4, 5, 768, 1536, 128, 1.0, 1.0)
     n = L.flash_gau_workspace_bytes(8, 1024, 256, ctypes.byref(w), 1, bd.BF16)
     assert n == bd.workspace_layout(8, 1024, 256, 768, 1536, 128, True, bd.BF16)["total_bytes"]
     assert L.flash_gau_workspace_bytes(8, 1000, 256, ctypes.byref(w), 1, bd.BF16) == 0
@@ -124,7 +124,7 @@ def test_stage_names(L):
     dict(pos_offset=-1),                            # negative position
 ])
 def test_block_forward_rejects_bad_options_before_any_launch(L, opts):
-    w = bd.Weights(1, 2, 3, 4, 5, 128, 256, 128, 1.0)
+    w = bd.Weights(1, 2, 3, 4, 5, 128, 256, 128, 1.0, 1.0)
     base = dict(norm=bd.NORM_LAYER, norm_g=6, norm_b=None, norm_eps=1e-5, rope=1,
                 rope_base=10000.0, pos_offset=0, residual=1)
     base.update(opts)
@@ -138,8 +138,24 @@ def test_block_forward_rejects_bad_options_before_any_launch(L, opts):
 
 
 def test_block_forward_rejects_rope_with_odd_head_width(L):
-    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 33, 1.0)
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 33, 1.0, 1.0)
     blk = bd.Block(bd.NORM_NONE, None, None, 1e-5, 1, 10000.0, 0, 1)
     n = bd.workspace_layout(1, 256, 64, 64, 128, 33, True, bd.FP32)["total_bytes"]
     assert L.flash_gau_block_forward(16, ctypes.byref(w), ctypes.byref(blk), 1, 256, 64, 1,
                                      bd.FP32, 1 << 40, 256, n, None) == bd.EINVAL
+
+
+@pytest.mark.parametrize("lin,loc", [(float("inf"), 1.0), (1.0, float("nan")),
+                                     (1.0, float("-inf"))])
+def test_non_finite_term_factors_rejected_before_any_launch(L, lin, loc):
+    """An infinite or NaN factor on either term is refused on the host by the
+    forward, the backward and the decode step."""
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 32, lin, loc)
+    ws = 1 << 20
+    assert L.flash_gau_forward(16, ctypes.byref(w), 1, 256, 64, 1, bd.FP32, 1 << 40, 256,
+                               ws, None) == bd.EINVAL
+    g = bd.Grads(1, 2, 3, 4, 5, 6)
+    assert L.flash_gau_backward(16, 32, ctypes.byref(w), 1, 256, 64, 1, bd.FP32,
+                                ctypes.byref(g), 256, ws, None) == bd.EINVAL
+    assert L.flash_gau_decode_step(16, ctypes.byref(w), 1, 64, bd.FP32, 256, ws, 1 << 40,
+                                   None) == bd.EINVAL

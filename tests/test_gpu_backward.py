@@ -31,7 +31,7 @@ def _built():
     build()
 
 
-def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed):
+def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed, local_scale=1.0):
     inp = make_inputs(B, T, d, e, s, C, dtype, seed)
     tdt = torch_dtype(dtype)
     dev = torch.device("cuda")
@@ -44,13 +44,13 @@ def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed):
                       torch.tensor(inp["gamma"], dtype=torch.float32, device=dev),
                       torch.tensor(inp["beta"], dtype=torch.float32, device=dev),
                       torch.tensor(inp["relpos"], dtype=torch.float32, device=dev),
-                      d, e, s, lin_scale)
+                      d, e, s, lin_scale, local_scale)
     X = torch.tensor(inp["X"], dtype=tdt, device=dev)
     got = bd.backward(X, dO, w, C, causal)
     torch.cuda.synchronize()
     ref = flash_gau_backward(inp["X"], inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"],
                              inp["gamma"], inp["beta"], inp["relpos"], C, causal, dO64,
-                             lin_scale)
+                             lin_scale, local_scale)
     g = {k: v.double().cpu().numpy() for k, v in got.items()}
     errs = {
         "dX": rel_err(g["dX"], ref["dX"].reshape(B, T, d)),
@@ -96,3 +96,19 @@ def test_backward_rejects_bad_arguments():
                               bd.FP32, ctypes.byref(g), X.data_ptr(), 0,
                               torch.cuda.current_stream().cuda_stream)
     assert st == bd.EINVAL  # null gradient pointers
+
+
+@pytest.mark.parametrize("shape,causal,dtype,local_scale", [
+    ((1, 256, 64, 128, 32, 64), True, "fp32", 0.0),       # GlobalOnly
+    ((2, 256, 64, 128, 32, 64), False, "fp32", -0.5),
+    ((2, 512, 128, 256, 128, 128), True, "bf16", 0.0),
+    ((1, 512, 128, 256, 128, 256), False, "bf16", 2.0),
+])
+def test_backward_with_scaled_local_term(shape, causal, dtype, local_scale):
+    """The local term times local_scale (0: the GlobalOnly ablation, whose
+    relpos gradient is then exactly zero)."""
+    B, T, d, e, s, C = shape
+    errs = _run(B, T, d, e, s, C, causal, dtype, 1.0, seed=71 + T, local_scale=local_scale)
+    print(dtype, causal, local_scale, {k: "%.2e" % v for k, v in errs.items()})
+    for k, v in errs.items():
+        assert v <= (TOL_X if k == "dX" else TOL_W)[dtype], (k, errs)

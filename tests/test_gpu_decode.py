@@ -27,19 +27,22 @@ def _built():
     build()
 
 
-@pytest.mark.parametrize("B,steps,d,e,s,C,dtype,lin_scale", [
-    (3, 40, 64, 128, 32, 16, "fp32", 1.0),
-    (2, 70, 96, 160, 64, 32, "fp32", 0.5),
-    (4, 300, 768, 1536, 128, 256, "bf16", 1.0 / 256),
-    (17, 20, 128, 256, 128, 8, "bf16", 1.0),
+@pytest.mark.parametrize("B,steps,d,e,s,C,dtype,lin_scale,local_scale", [
+    (3, 40, 64, 128, 32, 16, "fp32", 1.0, 1.0),
+    (2, 70, 96, 160, 64, 32, "fp32", 0.5, 1.0),
+    (4, 300, 768, 1536, 128, 256, "bf16", 1.0 / 256, 1.0),
+    (17, 20, 128, 256, 128, 8, "bf16", 1.0, 1.0),
+    (2, 50, 64, 128, 32, 16, "fp32", 1.0, 0.0),    # GlobalOnly
+    (3, 40, 128, 256, 128, 16, "bf16", 1.0, 0.5),
 ])
-def test_decode_matches_causal_forward(B, steps, d, e, s, C, dtype, lin_scale):
+def test_decode_matches_causal_forward(B, steps, d, e, s, C, dtype, lin_scale, local_scale):
     T = -(-steps // C) * C
     inp = make_inputs(B, T, d, e, s, C, dtype, 90 + C)
     X = inp["X"].copy()
     X[:, steps:] = 0.0
     ref, _ = flash_gau(X, inp["W_u"], inp["W_v"], inp["W_z"], inp["W_o"], inp["gamma"],
-                       inp["beta"], inp["relpos"], C, True, lin_scale)
+                       inp["beta"], inp["relpos"], C, True, lin_scale,
+                       local_scale=local_scale)
     tdt = torch_dtype(dtype)
     dev = torch.device("cuda")
     W_uvz = np.concatenate([inp["W_u"], inp["W_v"], inp["W_z"]], axis=1)
@@ -48,7 +51,7 @@ def test_decode_matches_causal_forward(B, steps, d, e, s, C, dtype, lin_scale):
                       torch.tensor(inp["gamma"], dtype=torch.float32, device=dev),
                       torch.tensor(inp["beta"], dtype=torch.float32, device=dev),
                       torch.tensor(inp["relpos"], dtype=torch.float32, device=dev),
-                      d, e, s, lin_scale)
+                      d, e, s, lin_scale, local_scale)
     dec = bd.Decoder(w, B, C)
     Xd = torch.tensor(X, dtype=tdt, device=dev)
     outs = [dec.step(Xd[:, t].contiguous()).double().cpu().numpy() for t in range(steps)]

@@ -80,3 +80,39 @@ def test_rope_toeplitz_rejects_bad_arguments():
                                           out.data_ptr(), s) == bd.EINVAL  # base <= 1
     assert L.flash_gau_rope_toeplitz_bias(None, a.data_ptr(), 2, 8, 10000.0,
                                           out.data_ptr(), s) == bd.EINVAL
+
+
+# ---------------------------------------------------------------- GlobalOnly
+# The local term times local_scale ("Transformer Quality in Linear Time",
+# section 4.4, the ablation that keeps only the global, linear part, is
+# local_scale = 0).  For bf16 io with local_scale = 0 the attention kernel
+# forms no scores at all; other values scale P in its relu^2 warps.
+@pytest.mark.parametrize("shape,causal,dtype,local_scale", [
+    ((2, 1024, 256, 512, 128, 256), True, "bf16", 0.0),
+    ((2, 1024, 256, 512, 128, 256), False, "bf16", 0.0),
+    ((1, 512, 128, 768, 128, 128), True, "bf16", 0.0),
+    ((1, 1024, 256, 512, 128, 256), True, "bf16", 0.5),
+    ((1, 512, 128, 256, 128, 512), False, "bf16", -1.5),
+    ((2, 200, 48, 72, 40, 40), True, "fp32", 0.0),
+    ((1, 192, 64, 96, 32, 64), False, "fp32", 0.0),
+    ((2, 200, 48, 72, 40, 40), True, "fp32", 0.25),
+])
+def test_forward_with_scaled_local_term(shape, causal, dtype, local_scale):
+    B, T, d, e, s, C = shape
+    case = Case(B, T, d, e, s, C, causal, dtype, seed=51 + C, local_scale=local_scale)
+    O = case.run()
+    ref, _ = case.reference()
+    assert rel_err(O, ref) <= TOL[dtype], rel_err(O, ref)
+    assert case.status() == 0
+
+
+def test_global_only_does_not_depend_on_the_local_inputs():
+    """local_scale = 0 (bf16, tensor-core path): changing the relative
+    position bias, which enters only the local term, leaves the output
+    bit-identical."""
+    B, T, d, e, s, C = 1, 512, 128, 256, 128, 256
+    case = Case(B, T, d, e, s, C, True, "bf16", seed=77, local_scale=0.0)
+    O1 = case.run()
+    case.weights.relpos.normal_()
+    O2 = case.run()
+    assert np.array_equal(O1, O2)
