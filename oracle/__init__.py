@@ -10,6 +10,7 @@ from .flash_gau import (  # noqa: F401
     scale_offset,
     relpos_bias,
     chunk_scores,
+    chunk_mask,
     layer_norm,
     scale_norm,
     rope,

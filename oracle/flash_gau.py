@@ -30,6 +30,10 @@ Readings taken where the pages disagree or are silent:
     builds from 2C-1 weights, used for every C;
   * the causal mask keeps the diagonal (j <= i) and is applied after relu^2;
   * the causal global term of the first chunk is the empty sum, i.e. zero;
+  * segment masks (packed text) act on the global term only, at chunk
+    granularity: a segment is a maximal run of consecutive chunks with one
+    id, and the optional row normalisation makes the global term the mean
+    of the visible chunk states (``chunk_mask``);
   * no bias terms, norm, RoPE or residual in ``flash_gau`` (the layer as
     eq. 3-8 write it); ``flash_block`` adds the pre-norm, RoPE on the four
     heads over global token positions and the residual of the pages'
@@ -204,8 +208,37 @@ def toeplitz_relpos(T):
     return out
 
 
+def chunk_mask(G, causal, segment_ids=None, average=False):
+    """The G x G chunk mask of the global term ([TQLT] Paper vs code, the
+    segment-mask item: a chunk mask built from segment ids, applied to the
+    chunk summaries in the linear part only, each row optionally normalised
+    to sum to one with empty rows left at zero).
+
+    M[g, h] = 1 when chunk g sees chunk h: h < g if causal (eq. 8), every h
+    otherwise (eq. 7), and g and h lie in one segment.  Reading: a segment
+    is a maximal run of consecutive chunks with equal id (packed text puts
+    each document in one run); segment_ids=None is one segment.  With
+    ``average`` each non-empty row is divided by its number of ones, so the
+    global term becomes the mean of the visible chunk states."""
+    M = np.zeros((G, G))
+    for g in range(G):
+        for h in range(G):
+            if causal and h >= g:
+                continue
+            if segment_ids is not None:
+                lo, hi = min(g, h), max(g, h)
+                if any(segment_ids[k] != segment_ids[g] for k in range(lo, hi + 1)):
+                    continue
+            M[g, h] = 1.0
+    if average:
+        n = M.sum(axis=1, keepdims=True)
+        M = np.divide(M, n, out=np.zeros_like(M), where=n > 0)
+    return M
+
+
 def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
-              lin_scale=1.0, positions=None, rope_base=10000.0, local_scale=1.0):
+              lin_scale=1.0, positions=None, rope_base=10000.0, local_scale=1.0,
+              segment_ids=None, chunk_average=False):
     """FLASH GAU layer forward with mixed chunk attention, in float64.
 
     Steps ([TQLT] Method and flash_block; [FLASH-blog] "Mixed Chunking"):
@@ -225,6 +258,8 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
     ([FLASH-blog] "Mixed Chunking" assumes divisibility).  With
     ``positions`` ([T]) the four heads are rotated by ``rope`` after step 2
     (the flash_block reading); the default keeps eq. 3-8 as written.
+    With ``segment_ids`` ([B, G] chunk ids) or ``chunk_average``, step 5
+    weighs the states by ``chunk_mask``: Prefix_g = sum_h M[g, h] State_h.
 
     Returns (O, inter) with O: [B, T, d] float64 and ``inter`` a dict of the
     intermediates U, V, Z, heads [4, B, T, s], state [B, G, s, e],
@@ -256,14 +291,23 @@ def flash_gau(X, W_u, W_v, W_z, W_o, gamma, beta, relpos, C, causal,
             state[b, g] = Kl[b, rows].T @ V[b, rows]
 
     prefix = np.zeros((B, G, s, e))
-    for b in range(B):
-        total = np.zeros((s, e))
-        for g in range(G):
-            if causal:
-                prefix[b, g] = total  # strictly earlier chunks only
-            total = total + state[b, g]
-        if not causal:
-            prefix[b, :] = total
+    if segment_ids is None and not chunk_average:
+        for b in range(B):
+            total = np.zeros((s, e))
+            for g in range(G):
+                if causal:
+                    prefix[b, g] = total  # strictly earlier chunks only
+                total = total + state[b, g]
+            if not causal:
+                prefix[b, :] = total
+    else:
+        for b in range(B):
+            seg = None if segment_ids is None else np.asarray(segment_ids)[b]
+            M = chunk_mask(G, causal, seg, chunk_average)
+            for g in range(G):
+                for h in range(G):
+                    if M[g, h] != 0.0:
+                        prefix[b, g] += M[g, h] * state[b, h]
 
     Vl = np.zeros((B, T, e))
     for b in range(B):

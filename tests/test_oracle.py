@@ -616,3 +616,93 @@ def test_output_is_affine_in_local_scale():
     O1 = flash_gau(*args, local_scale=1.0)[0]
     O25 = flash_gau(*args, local_scale=2.5)[0]
     assert np.allclose(O25, O0 + 2.5 * (O1 - O0), rtol=1e-12, atol=1e-10)
+
+
+# ---------------------------------------------------------- segment masks
+def _layer_args(rng, B, T, d, e, s, C):
+    return dict(X=rng.normal(size=(B, T, d)), W_u=rng.normal(size=(d, e)) / np.sqrt(d),
+                W_v=rng.normal(size=(d, e)) / np.sqrt(d), W_z=rng.normal(size=(d, s)) / np.sqrt(d),
+                W_o=rng.normal(size=(e, d)) / np.sqrt(e), gamma=rng.normal(1, 0.3, (4, s)),
+                beta=rng.normal(0, 0.3, (4, s)), relpos=rng.normal(size=2 * C - 1))
+
+
+def _call(a, C, causal, **kw):
+    return flash_gau(a["X"], a["W_u"], a["W_v"], a["W_z"], a["W_o"], a["gamma"], a["beta"],
+                     a["relpos"], C, causal, **kw)[0]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_documents_equal_separate_runs(causal):
+    """Two documents packed into one sequence, each a whole number of chunks,
+    with one segment id per document: the output on each document's tokens
+    equals the layer run on that document alone (the local part never
+    crosses a chunk, the masked global part never crosses the boundary)."""
+    rng = np.random.default_rng(90)
+    d, e, s, C = 6, 8, 4, 4
+    a = _layer_args(rng, 1, 5 * C, d, e, s, C)
+    seg = np.array([[7, 7, 7, 2, 2]])
+    O = _call(a, C, causal, segment_ids=seg)
+    for lo, hi in ((0, 3 * C), (3 * C, 5 * C)):
+        part = dict(a, X=a["X"][:, lo:hi])
+        assert np.allclose(O[:, lo:hi], _call(part, C, causal), rtol=1e-12, atol=1e-12)
+
+
+def test_one_segment_is_the_unsegmented_layer():
+    rng = np.random.default_rng(91)
+    a = _layer_args(rng, 2, 12, 5, 6, 4, 3)
+    for causal in (True, False):
+        O = _call(a, 3, causal, segment_ids=np.full((2, 4), 5))
+        assert np.allclose(O, _call(a, 3, causal), rtol=1e-12, atol=1e-12)
+
+
+def test_distinct_segments_leave_only_the_chunk_itself():
+    """Every chunk its own segment: causal, no earlier chunk is visible, so
+    the global term vanishes (the LocalOnly output); non-causal, each chunk
+    sees exactly itself."""
+    rng = np.random.default_rng(92)
+    B, T, d, e, s, C = 1, 12, 5, 6, 4, 4
+    a = _layer_args(rng, B, T, d, e, s, C)
+    seg = np.array([[0, 1, 2]])
+    assert np.allclose(_call(a, C, True, segment_ids=seg), _call(a, C, True, lin_scale=0.0),
+                       rtol=1e-12, atol=1e-12)
+    # non-causal, each chunk alone is the layer run on that chunk
+    O = _call(a, C, False, segment_ids=seg)
+    for g in range(3):
+        part = dict(a, X=a["X"][:, g * C:(g + 1) * C])
+        assert np.allclose(O[:, g * C:(g + 1) * C], _call(part, C, False), rtol=1e-12,
+                           atol=1e-12)
+
+
+def test_repeated_id_after_a_gap_starts_a_new_segment():
+    """Ids 3, 3, 4, 3: the last chunk is a new run, so causally it sees no
+    earlier chunk (the mask row is empty)."""
+    M = O.chunk_mask(4, True, [3, 3, 4, 3])
+    assert M.tolist() == [[0, 0, 0, 0], [1, 0, 0, 0], [0, 0, 0, 0], [0, 0, 0, 0]]
+    M = O.chunk_mask(4, False, [3, 3, 4, 3], average=True)
+    assert np.allclose(M, [[.5, .5, 0, 0], [.5, .5, 0, 0], [0, 0, 1, 0], [0, 0, 0, 1]])
+
+
+def test_chunk_average_matches_token_level_brute_force():
+    """Row-normalised mask: the global term of token t is Q_lin,t times the
+    mean over the visible chunks of their states, each state summed token by
+    token (K_lin,tau^T V_tau) rather than as a matrix product."""
+    rng = np.random.default_rng(93)
+    B, T, d, e, s, C = 1, 15, 4, 5, 3, 3
+    a = _layer_args(rng, B, T, d, e, s, C)
+    seg = np.array([[1, 1, 1, 2, 2]])
+    for causal in (True, False):
+        O_ = _call(a, C, causal, segment_ids=seg, chunk_average=True, local_scale=0.0)
+        U = swish(a["X"][0] @ a["W_u"])
+        V = swish(a["X"][0] @ a["W_v"])
+        Z = swish(a["X"][0] @ a["W_z"])
+        Ql, Kl = Z * a["gamma"][2] + a["beta"][2], Z * a["gamma"][3] + a["beta"][3]
+        for t in range(T):
+            g = t // C
+            vis = [h for h in range(5) if seg[0, h] == seg[0, g] and (h < g or not causal)]
+            acc = np.zeros(e)
+            for h in vis:
+                for tau in range(h * C, (h + 1) * C):
+                    acc += (Ql[t] @ Kl[tau]) * V[tau]
+            if vis:
+                acc /= len(vis)
+            assert np.allclose(O_[0, t], (U[t] * acc) @ a["W_o"], rtol=1e-12, atol=1e-12)
