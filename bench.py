@@ -324,6 +324,33 @@ def run_ours(args, rank, world, local_rank):
                            "unit": "tokens/s"}
         del wv
 
+    # ---- next row: packed text, the chunk-masked global term: each batch
+    # row holds four documents of G/4 chunks (ids 0..3), mean of the visible
+    # chunk states
+    G = T // C
+    seg_ids = torch.tensor(np.repeat(np.arange(4), -(-G // 4))[:G][None, :].repeat(B, 0),
+                           dtype=torch.int32, device=dev)
+
+    def seg_step():
+        bd.forward_segmented(X, weights, C, causal, seg_ids, True, out=out, workspace=ws,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        seg_step()
+    s0 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+    s1 = [torch.cuda.Event(enable_timing=True) for _ in range(blk_steps)]
+    torch.cuda.synchronize()
+    for k in range(blk_steps):
+        flush.fill_(1.0)
+        s0[k].record(stream)
+        seg_step()
+        s1[k].record(stream)
+    torch.cuda.synchronize()
+    seg_ms = sum(x.elapsed_time(y) for x, y in zip(s0, s1)) / blk_steps
+    if bd.workspace_status(ws) != 0:
+        raise RuntimeError("kernel status after the segmented runs")
+
     # ---- next row: the RoPE construction of the relative-position table
     # (windows of 512 and more), 128-wide learned vectors, C = 512
     trng = np.random.default_rng(2000 + w["seed"])
@@ -503,6 +530,11 @@ def run_ours(args, rank, world, local_rank):
             "local_only": dict(
                 what="the layer with the global term switched off (lin_scale = 0)",
                 **ablations["local_only"]),
+            "segmented": {
+                "what": "packed text: four documents per batch row (segment ids per chunk), "
+                        "global term = mean of the visible chunk states of the document",
+                "ms_per_step": round(seg_ms, 5),
+                "value": round(tokens / (seg_ms * 1e-3), 1), "unit": "tokens/s"},
             "rope_toeplitz_bias": {
                 "what": "relative-position table of the RoPE bias construction, C = 512, "
                         "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",

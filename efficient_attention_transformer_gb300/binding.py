@@ -46,10 +46,15 @@ EXPORTED = (
     "flash_gau_backward",
     "flash_gau_decode_state_bytes",
     "flash_gau_decode_step",
+    "flash_gau_forward_segmented",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+class Segments(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("average", ctypes.c_int)]
 
 
 class Weights(ctypes.Structure):
@@ -131,6 +136,10 @@ def lib():
         L.flash_gau_block_forward.argtypes = [p, ctypes.POINTER(Weights), ctypes.POINTER(Block),
                                               i, i, i, i, i, p, p, sz, p]
         L.flash_gau_block_forward.restype = i
+        L.flash_gau_forward_segmented.argtypes = [p, ctypes.POINTER(Weights),
+                                                  ctypes.POINTER(Segments), i, i, i, i, i, p,
+                                                  p, sz, p]
+        L.flash_gau_forward_segmented.restype = i
         L.flash_gau_rope_toeplitz_bias.argtypes = [p, p, i, i, ctypes.c_float, p, p]
         L.flash_gau_rope_toeplitz_bias.restype = i
         L.flash_gau_backward_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights), i, i]
@@ -260,6 +269,37 @@ def forward(X, weights, C, causal, out=None, workspace=None, stream=None,
     else:
         st = lib().flash_gau_forward(*args)
     _check(st)
+    return out
+
+
+def forward_segmented(X, weights, C, causal, segment_ids=None, average=False, out=None,
+                      workspace=None, stream=None):
+    """O = FLASH-GAU(X) with a chunk mask on the global term, through
+    flash_gau_forward_segmented.  segment_ids: int32 CUDA tensor [B, T / C]
+    (one id per chunk; a change of id starts a segment) or None; average:
+    the mean of the visible chunk states instead of their sum."""
+    if X.dim() != 3:
+        raise ValueError("X must be [B, T, d]")
+    B, T, d = X.shape
+    if d != weights.d or X.dtype != weights.W_uvz.dtype:
+        raise ValueError("X does not match the weights")
+    ids = None
+    if segment_ids is not None:
+        if T % C != 0 or tuple(segment_ids.shape) != (B, T // C):
+            raise ValueError("segment_ids must be [B, T / C]")
+        ids = _dev_ptr(segment_ids, "segment_ids", torch.int32)
+    seg = Segments(ids, int(bool(average)))
+    if out is None:
+        out = torch.empty_like(X)
+    if workspace is None:
+        workspace = weights.new_workspace(B, T, C, causal, X.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(X.device)
+    _check(lib().flash_gau_forward_segmented(
+        _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), ctypes.byref(seg), B, T, C,
+        int(bool(causal)), weights.dtype, _dev_ptr(out, "out", X.dtype),
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        stream.cuda_stream))
     return out
 
 

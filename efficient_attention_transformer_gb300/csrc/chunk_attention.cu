@@ -108,6 +108,7 @@ struct AttnParams {
   int total;
   float inv_c;
   float local_scale;  // factor on P; 0: no key blocks at all
+  int per_chunk;      // a prefix state per chunk (else one per batch row)
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
@@ -314,7 +315,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         if (!ok || u < 0) break;
         const Unit x = unit_of(p, u);
         const long long qrow = x.tok0 + x.qt * QT;
-        const long long pre_row0 = (long long)(p.causal ? x.chunk : x.b) * SD;
+        const long long pre_row0 = (long long)(p.per_chunk ? x.chunk : x.b) * SD;
         const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
         if (x.nkb > 0) ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
         for (int t = 0; ok && t < x.ng; ++t) {
@@ -624,7 +625,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
     return err;
   if ((err = make_tmap_bf16_2d(&tU, pr.U, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tG, pr.gated, pr.M, pr.e, pr.e, 32, 64)) != cudaSuccess) return err;
-  const long long pre_rows = (long long)(pr.causal ? pr.B * pr.G : pr.B) * pr.s;
+  const long long pre_rows = (long long)(pr.per_chunk ? pr.B * pr.G : pr.B) * pr.s;
   if ((err = make_tmap_bf16_2d(&tPre, pr.prefix, pre_rows * pr.e / 64, 64, 64, 128, 64)) !=
       cudaSuccess)
     return err;
@@ -665,6 +666,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.total = p.n_grouped + singles * per_chunk;
   p.inv_c = 1.0f / (float)pr.C;
   p.local_scale = pr.local_scale;
+  p.per_chunk = pr.per_chunk;
   p.bias = pr.bias;
   p.status = pr.status;
   p.next_unit = pr.status + kNextUnitWord;

@@ -90,7 +90,7 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   L->state = off;
   off = align_up(off + (size_t)B * G * s * e * io);
   L->prefix = off;
-  off = align_up(off + (causal ? (size_t)B * G : (size_t)B) * s * e * io);
+  off = align_up(off + (size_t)B * G * s * e * io);  // per chunk when segmented
   L->gated = off;
   off = align_up(off + M * e * io);
   L->bias = off;
@@ -261,7 +261,7 @@ int check_block(const flash_gau_block *blk, int s) {
 int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block *blk, int B,
                 int T, int C, int causal, int dtype, void *out, void *workspace,
                 size_t workspace_bytes, void *stream, void *const *stage_events,
-                int n_events) {
+                int n_events, const flash_gau_segments *seg = nullptr) {
   if (!X || !w || !out || !workspace || !w->W_uvz || !w->W_o || !w->gamma || !w->beta ||
       !w->relpos || !scales_finite(w))
     return FLASH_GAU_EINVAL;
@@ -294,6 +294,9 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.M = (long long)B * T;
   p.lin_scale = w->lin_scale;
   p.local_scale = w->local_scale;
+  p.seg_ids = seg ? seg->ids : nullptr;
+  p.chunk_average = (seg && seg->average) ? 1 : 0;
+  p.per_chunk = (causal || p.seg_ids) ? 1 : 0;
   p.X = X;
   p.W_uvz = w->W_uvz;
   p.W_o = w->W_o;
@@ -404,6 +407,14 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w, const fla
   if (!blk) return FLASH_GAU_EINVAL;
   return run_forward(X, w, blk, B, T, C, causal, dtype, out, workspace, workspace_bytes, stream,
                      nullptr, 0);
+}
+
+int flash_gau_forward_segmented(const void *X, const flash_gau_weights *w,
+                                const flash_gau_segments *seg, int B, int T, int C, int causal,
+                                int dtype, void *out, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  return run_forward(X, w, nullptr, B, T, C, causal, dtype, out, workspace, workspace_bytes,
+                     stream, nullptr, 0, seg);
 }
 
 size_t flash_gau_backward_workspace_bytes(int B, int T, int C, const flash_gau_weights *w,
@@ -545,6 +556,6 @@ const char *flash_gau_strerror(int status) {
   }
 }
 
-int flash_gau_version(void) { return 106; }
+int flash_gau_version(void) { return 107; }
 
 }  // extern "C"

@@ -35,6 +35,11 @@ struct Problem {
   long long M;  // B * T tokens
   float lin_scale;
   float local_scale;  // factor on the local term; 0 = global term only
+  // chunk mask of the global term: segment ids [B, G] (null: one segment)
+  // and row normalisation; per_chunk: a prefix state per chunk (causal or
+  // segmented), else one per batch row
+  const int *seg_ids;
+  int chunk_average, per_chunk;
   const void *X;
   const void *W_uvz;
   const void *W_o;

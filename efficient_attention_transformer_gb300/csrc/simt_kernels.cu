@@ -129,25 +129,44 @@ struct StoreEpi {
 
 // ---------------------------------------------------------- prefix scan ----
 // One thread per (b, s*e element): the G-step running sum of chunk states.
+// With segment ids (a change of id between neighbouring chunks starts a
+// segment) the sums restart at each segment, and a non-causal prefix is the
+// segment's total, one per chunk; `average` divides each sum by its number
+// of chunks (an empty sum stays zero).
 template <typename T>
 __global__ void simt_prefix_scan(const T *__restrict__ state, T *__restrict__ prefix,
-                                 int B, int G, long long se, int causal, float lin_scale) {
+                                 int B, int G, long long se, int causal, float lin_scale,
+                                 const int *__restrict__ seg_ids, int average, int per_chunk) {
   griddep_wait();
   griddep_launch_dependents();
   long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   if (idx >= B * se) return;
   long long b = idx / se, r = idx % se;
   const T *st = state + b * G * se + r;
+  const int *seg = seg_ids ? seg_ids + b * G : nullptr;
+  T *pre = prefix + (per_chunk ? b * G * se : b * se) + r;
   float run = 0.f;
-  if (causal) {
-    T *pre = prefix + b * G * se + r;
-    for (int g = 0; g < G; ++g) {
-      pre[g * se] = from_f<T>(lin_scale * run);
-      run += to_f(st[g * se]);
+  int start = 0;
+  auto write_total = [&](int end) {
+    const float v = (average ? lin_scale / (float)(end - start) : lin_scale) * run;
+    for (int h = start; h < end; ++h) pre[h * se] = from_f<T>(v);
+  };
+  for (int g = 0; g < G; ++g) {
+    if (seg && g > 0 && seg[g] != seg[g - 1]) {
+      if (!causal) write_total(g);
+      run = 0.f;
+      start = g;
     }
-  } else {
-    for (int g = 0; g < G; ++g) run += to_f(st[g * se]);
-    prefix[b * se + r] = from_f<T>(lin_scale * run);
+    if (causal) {
+      const int n = g - start;
+      const float sc = average ? (n > 0 ? lin_scale / (float)n : 0.f) : lin_scale;
+      pre[g * se] = from_f<T>(sc * run);
+    }
+    run += to_f(st[g * se]);
+  }
+  if (!causal) {
+    if (per_chunk) write_total(G);
+    else pre[0] = from_f<T>((average ? lin_scale / (float)G : lin_scale) * run);
   }
 }
 
@@ -164,7 +183,8 @@ __global__ void __launch_bounds__(256)
 simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
                      const T *__restrict__ heads, const T *__restrict__ prefix,
                      const float *__restrict__ relpos, T *__restrict__ gated,
-                     long long M, int C, int G, int e, int s, int causal, float local_scale) {
+                     long long M, int C, int G, int e, int s, int causal, float local_scale,
+                     int per_chunk) {
   extern __shared__ float sm[];
   const int sp = s + 1;
   float *q = sm;                          // [32][s+1]
@@ -230,7 +250,7 @@ simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
     q[rr * sp + k] = (i0 + rr < C) ? to_f(Ql[(tok0 + i0 + rr) * s + k]) : 0.f;
   }
   const long long se = (long long)s * e;
-  const T *pre = prefix + (causal ? (long long)chunk * se : (long long)(chunk / G) * se);
+  const T *pre = prefix + (per_chunk ? (long long)chunk * se : (long long)(chunk / G) * se);
   (void)g;
   for (int k0 = 0; k0 < s; k0 += kAttKeys) {
     __syncthreads();
@@ -286,7 +306,8 @@ template <typename T>
 cudaError_t prefix_scan(const Problem &p) {
   long long se = (long long)p.s * p.e;
   return launch_pdl(simt_prefix_scan<T>, dim3(cdiv(p.B * se, 256)), dim3(256), 0, p.stream,
-                    (const T *)p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale);
+                    (const T *)p.state, (T *)p.prefix, p.B, p.G, se, p.causal, p.lin_scale,
+                    p.seg_ids, p.chunk_average, p.per_chunk);
 }
 
 template <typename T>
@@ -301,7 +322,7 @@ cudaError_t chunk_attention(const Problem &p) {
   dim3 grid(cdiv(p.e, kAttCols), cdiv(p.C, kAttRows), p.B * p.G);
   simt_chunk_attention<T><<<grid, 256, smem, p.stream>>>(
       (const T *)p.U, (const T *)p.V, (const T *)p.heads, (const T *)p.prefix, p.relpos,
-      (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal, p.local_scale);
+      (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal, p.local_scale, p.per_chunk);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,8 @@
 // Chunk states of mixed chunk attention and their prefix sums, one kernel:
 //   State_g  = K_lin,g^T V_g   for every chunk g of C tokens
 //   Prefix_g = lin_scale * sum_{h<g} State_h   (causal; else the total once)
+// or, with a chunk mask (segment ids, row normalisation), lin_scale times
+// the sum (or mean) of the states of the chunk's segment that it sees
 // ("Transformer Quality in Linear Time", eq. 7 and eq. 8, the summands of
 // the global term and their cumulative sum), bf16 operands, fp32
 // accumulation in TMEM, bf16 states; the sums run in fp32.
@@ -61,6 +63,9 @@ struct GemmParams {
   int B, G, causal;
   long long se8;
   float lin_scale;
+  const int *seg;   // [B, G] segment ids or null; a change of id starts a segment
+  int average;      // divide each sum by the number of chunks in it
+  int per_chunk;    // one prefix per chunk (causal or segmented)
 };
 
 struct Smem {
@@ -180,14 +185,35 @@ __device__ bool scan_states(const GemmParams &p, uint8_t *buf, int buf_bytes, Sm
     if (threadIdx.x == 0 && !mbar_wait(bar, phase, &sm->abort_flag)) raise_timeout(sm, p.status);
     __syncthreads();
     if (sm->abort_flag) return false;
-    uint4 *pre = p.prefix8 + (p.causal ? b * p.G * p.se8 : b * p.se8) + r0;
+    uint4 *pre = p.prefix8 + (p.per_chunk ? b * p.G * p.se8 : b * p.se8) + r0;
+    const int *seg = p.seg ? p.seg + b * p.G : nullptr;
     for (int c = threadIdx.x; c < wc; c += blockDim.x) {
       float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      int start = 0;  // first chunk of the current segment
+      // non-causal: the segment's total for each of its chunks [start, end)
+      auto write_total = [&](int end) {
+        const float sc = p.average ? p.lin_scale / (float)(end - start) : p.lin_scale;
+        const uint4 v = scaled8(run, sc);
+        for (int h = start; h < end; ++h) pre[(long long)h * p.se8 + c] = v;
+      };
       for (int g = 0; g < p.G; ++g) {
-        if (p.causal) pre[(long long)g * p.se8 + c] = scaled8(run, p.lin_scale);
+        if (seg && g > 0 && __ldg(seg + g) != __ldg(seg + g - 1)) {
+          if (!p.causal) write_total(g);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) run[k] = 0.f;
+          start = g;
+        }
+        if (p.causal) {
+          const int n = g - start;  // chunks this one sees
+          const float sc = p.average ? (n > 0 ? p.lin_scale / (float)n : 0.f) : p.lin_scale;
+          pre[(long long)g * p.se8 + c] = scaled8(run, sc);
+        }
         add8(run, sbuf[g * wc + c]);
       }
-      if (!p.causal) pre[c] = scaled8(run, p.lin_scale);
+      if (!p.causal) {
+        if (p.per_chunk) write_total(p.G);
+        else pre[c] = scaled8(run, p.average ? p.lin_scale / (float)p.G : p.lin_scale);
+      }
     }
     __syncthreads();  // the buffer is refilled by the next item
   }
@@ -455,6 +481,9 @@ cudaError_t tc_chunk_state_scan_bf16(const Problem &pr) {
   p.causal = pr.causal;
   p.se8 = (long long)pr.s * pr.e / 8;  // s == 128
   p.lin_scale = pr.lin_scale;
+  p.seg = pr.seg_ids;
+  p.average = pr.chunk_average;
+  p.per_chunk = pr.per_chunk;
   return launch<true>(tmA, tmB, tS, p, pr);
 }
 

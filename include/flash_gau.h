@@ -92,9 +92,10 @@ typedef struct flash_gau_workspace_layout {
   size_t V;             /* [B*T, e] io: swish(X W_v)                 (*)    */
   size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
   size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk   (*)    */
-  size_t prefix;        /* causal [B, G, s, e], non-causal [B, s, e], io:
-                           lin_scale * (exclusive / total) chunk-state sum
-                                                                      (*)   */
+  size_t prefix;        /* [B, G, s, e] io: lin_scale * (exclusive / total)
+                           chunk-state sum of each chunk; a non-causal
+                           forward without segments writes only the first
+                           [B, s, e] (one total per batch row)        (*)   */
   size_t gated;         /* [B*T, e] io: U * (Vq + Vl)                       */
   size_t bias;          /* [2C-1] fp32: relpos as the bf16 attention kernel
                            reads it; causal: the entries of offset j-i >= 1
@@ -212,6 +213,34 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
                             const flash_gau_block *blk, int B, int T, int C,
                             int causal, int dtype, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/* ---- segment masks (packed text) -------------------------------------- */
+/* The global term with a chunk mask ("Transformer Quality in Linear Time",
+ * Paper vs code, the segment-mask item; Pitfalls, the same item): segment
+ * ids mask the chunk summaries in the linear part only (the local part is
+ * unchanged), and each row of the mask may be normalised to sum to one, so
+ * the global term becomes the mean of the visible chunk states:
+ *   Prefix_g = lin_scale * sum_h M[g, h] State_h
+ *   M[g, h]  = 1 when h is visible from g (h < g causal, any h otherwise)
+ *              and g, h lie in one segment; rows divided by their count
+ *              when `average` (an empty row stays zero).
+ * Reading: a segment is a maximal run of consecutive chunks with one id (a
+ * change of id between neighbouring chunks starts a new segment; packed
+ * text gives each document one run, whole chunks each).                   */
+typedef struct flash_gau_segments {
+  const int *ids;  /* device [B, G] int32 chunk segment ids, or NULL (the
+                      whole sequence is one segment)                       */
+  int average;     /* nonzero: row-normalised mask (mean of the states)    */
+} flash_gau_segments;
+
+/* flash_gau_forward with the chunk mask of `seg` (a host pointer, read
+ * during the call; NULL = no mask, the plain sums of eq. 7/8).  Arguments
+ * and workspace as for flash_gau_forward.                                  */
+int flash_gau_forward_segmented(const void *X, const flash_gau_weights *w,
+                                const flash_gau_segments *seg, int B, int T,
+                                int C, int causal, int dtype, void *out,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
 
 /* ---- backward pass ------------------------------------------------------ */
 /* Gradients of L = sum(dO * O), O = flash_gau_forward(X, ...), with respect
