@@ -187,7 +187,16 @@ __device__ bool scan_states(const GemmParams &p, uint8_t *buf, int buf_bytes, Sm
     if (sm->abort_flag) return false;
     uint4 *pre = p.prefix8 + (p.per_chunk ? b * p.G * p.se8 : b * p.se8) + r0;
     const int *seg = p.seg ? p.seg + b * p.G : nullptr;
-    for (int c = threadIdx.x; c < wc; c += blockDim.x) {
+    const bool plain = !seg && !p.average;  // eq. 7/8 as written: the short loop
+    for (int c = threadIdx.x; plain && c < wc; c += blockDim.x) {
+      float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int g = 0; g < p.G; ++g) {
+        if (p.causal) pre[(long long)g * p.se8 + c] = scaled8(run, p.lin_scale);
+        add8(run, sbuf[g * wc + c]);
+      }
+      if (!p.causal) pre[c] = scaled8(run, p.lin_scale);
+    }
+    for (int c = threadIdx.x; !plain && c < wc; c += blockDim.x) {
       float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       int start = 0;  // first chunk of the current segment
       // non-causal: the segment's total for each of its chunks [start, end)
