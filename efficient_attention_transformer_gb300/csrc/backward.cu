@@ -21,9 +21,12 @@
 // The contractions run on one batched, strided GEMM kernel (64 x 64 tiles,
 // 4 x 4 per thread), so transposed views cost no copies; the rest are
 // elementwise or column-reduction kernels.  For bf16 io, when the shapes
-// tile, the five large contractions (Pre, dW_o, dA, dX, dW_uvz) run on the
-// tensor cores instead (tc_gemm_any.cu), with the gated product and dPre
-// rounded to bf16 as their operands.
+// tile, every contraction runs on the tensor cores instead (tc_gemm_any.cu):
+// the five large ones (Pre, dW_o, dA, dX, dW_uvz) and, batched over the
+// chunks, the chunk-level ones, with their operands (the gated product,
+// dPre, V, the heads, P, dS, dVh, the prefix states and their gradients)
+// rounded to bf16 by the kernels that produce them; sums, scans and the
+// elementwise steps stay fp32.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -157,10 +160,12 @@ Operand op(long long sm, long long sk, long long sb = 0, int div = 1) { return {
 
 // ------------------------------------------------------------ elementwise --
 // U, V, Z = swish(Pre) and the four heads Z gamma_k + beta_k
+// (and bf16 copies of V and the heads when V_io / H_io are set)
 __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
                           float *__restrict__ V, float *__restrict__ Z, float *__restrict__ H,
                           const float *__restrict__ gamma, const float *__restrict__ beta,
-                          long long M, int e, int s) {
+                          long long M, int e, int s, __nv_bfloat16 *__restrict__ V_io,
+                          __nv_bfloat16 *__restrict__ H_io) {
   const int N = 2 * e + s;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
        i += (long long)gridDim.x * blockDim.x) {
@@ -171,10 +176,15 @@ __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
       U[m * e + c] = y;
     } else if (c < 2 * e) {
       V[m * e + c - e] = y;
+      if (V_io) V_io[m * e + c - e] = __float2bfloat16_rn(y);
     } else {
       const int k = c - 2 * e;
       Z[m * s + k] = y;
-      for (int h = 0; h < 4; ++h) H[(h * M + m) * s + k] = fmaf(y, gamma[h * s + k], beta[h * s + k]);
+      for (int h = 0; h < 4; ++h) {
+        const float v = fmaf(y, gamma[h * s + k], beta[h * s + k]);
+        H[(h * M + m) * s + k] = v;
+        if (H_io) H_io[(h * M + m) * s + k] = __float2bfloat16_rn(v);
+      }
     }
   }
 }
@@ -193,22 +203,44 @@ __global__ void gate(const float *__restrict__ U, const float *__restrict__ Vh,
 // dU = dA * Vh, dVh = dA * U
 __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict__ U,
                           const float *__restrict__ Vh, float *__restrict__ dU,
-                          float *__restrict__ dVh, long long n) {
+                          float *__restrict__ dVh, long long n,
+                          __nv_bfloat16 *__restrict__ dVh_io) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     dU[i] = dA[i] * Vh[i];
-    dVh[i] = dA[i] * U[i];
+    const float g = dA[i] * U[i];
+    dVh[i] = g;
+    if (dVh_io) dVh_io[i] = __float2bfloat16_rn(g);
+  }
+}
+
+// the scores from the raw products R = Qq Kq^T of chunk z (in place):
+// S = R / C + relpos[j - i + C - 1], and P = relu(S)^2 (zero above the
+// diagonal when causal) as a bf16 operand
+__global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_io,
+                          const float *__restrict__ relpos, long long chunks, int C, int causal,
+                          float inv_c) {
+  const long long n = chunks * C * C;
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n;
+       o += (long long)gridDim.x * blockDim.x) {
+    const int j = (int)(o % C), i = (int)((o / C) % C);
+    const float v = fmaf(S[o], inv_c, relpos[j - i + C - 1]);
+    S[o] = v;
+    const float r = fmaxf(v, 0.f);
+    P_io[o] = __float2bfloat16_rn((causal && j > i) ? 0.f : r * r);
   }
 }
 
 // dS = 2 relu(S) dP, zero above the diagonal when causal (in place over dP)
 __global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, long long chunks,
-                           int C, int causal) {
+                           int C, int causal, __nv_bfloat16 *__restrict__ dS_io) {
   const long long n = chunks * C * C;
   for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n;
        o += (long long)gridDim.x * blockDim.x) {
     const int j = (int)(o % C), i = (int)((o / C) % C);
-    dP[o] = (causal && j > i) ? 0.f : 2.f * fmaxf(S[o], 0.f) * dP[o];
+    const float v = (causal && j > i) ? 0.f : 2.f * fmaxf(S[o], 0.f) * dP[o];
+    dP[o] = v;
+    if (dS_io) dS_io[o] = __float2bfloat16_rn(v);
   }
 }
 
@@ -236,37 +268,50 @@ __global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ dr
 
 // prefix[b][g] = lin_scale * (exclusive sum over chunks, or the total)
 __global__ void scan_forward(const float *__restrict__ state, float *__restrict__ prefix, int B,
-                             int G, long long se, int causal, float lin_scale) {
+                             int G, long long se, int causal, float lin_scale,
+                             __nv_bfloat16 *__restrict__ prefix_io) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
        i += (long long)gridDim.x * blockDim.x) {
     const long long b = i / se, r = i - b * se;
     float run = 0.f;
     for (int g = 0; g < G; ++g) {
-      if (causal) prefix[(b * G + g) * se + r] = lin_scale * run;
+      if (causal) {
+        const long long o = (b * G + g) * se + r;
+        prefix[o] = lin_scale * run;
+        if (prefix_io) prefix_io[o] = __float2bfloat16_rn(lin_scale * run);
+      }
       run += state[(b * G + g) * se + r];
     }
-    if (!causal) prefix[b * se + r] = lin_scale * run;
+    if (!causal) {
+      prefix[b * se + r] = lin_scale * run;
+      if (prefix_io) prefix_io[b * se + r] = __float2bfloat16_rn(lin_scale * run);
+    }
   }
 }
 
 // dState_h = sum_{g>h} dPrefix_g (causal) or the total (in place), with the
 // lin_scale factor already inside dPrefix
-__global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long se, int causal) {
+__global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long se, int causal,
+                              __nv_bfloat16 *__restrict__ dstate_io) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
        i += (long long)gridDim.x * blockDim.x) {
     const long long b = i / se, r = i - b * se;
     if (causal) {
       float run = 0.f;
       for (int g = G - 1; g >= 0; --g) {
-        float *p = dpre + (b * G + g) * se + r;
-        const float v = *p;
-        *p = run;
+        const long long o = (b * G + g) * se + r;
+        const float v = dpre[o];
+        dpre[o] = run;
+        if (dstate_io) dstate_io[o] = __float2bfloat16_rn(run);
         run += v;
       }
     } else {
       float tot = 0.f;
       for (int g = 0; g < G; ++g) tot += dpre[(b * G + g) * se + r];
-      for (int g = 0; g < G; ++g) dpre[(b * G + g) * se + r] = tot;
+      for (int g = 0; g < G; ++g) {
+        dpre[(b * G + g) * se + r] = tot;
+        if (dstate_io) dstate_io[(b * G + g) * se + r] = __float2bfloat16_rn(tot);
+      }
     }
   }
 }
@@ -374,26 +419,61 @@ cudaError_t run(const BackwardProblem &q) {
                   N % 64 == 0 && L.A_io && L.dpre_io;
   __nv_bfloat16 *A_io = tc ? (__nv_bfloat16 *)L.A_io : nullptr;
   __nv_bfloat16 *dpre_io = tc ? (__nv_bfloat16 *)L.dpre_io : nullptr;
+  // the chunk-level contractions on the tensor cores too, batched over the
+  // chunks: chunks and heads of whole 128-row tiles
+  const bool tcc = tc && C % 128 == 0 && s % 128 == 0 && L.H_io && L.V_io && L.P_io &&
+                   L.prefix_io && L.dVh_io && L.dS_io && L.dstate_io;
+  typedef __nv_bfloat16 bf;
+  bf *H_io = tcc ? (bf *)L.H_io : nullptr, *V_io = tcc ? (bf *)L.V_io : nullptr;
+  bf *P_io = (bf *)L.P_io, *pre_io = tcc ? (bf *)L.prefix_io : nullptr;
+  bf *dVh_io = tcc ? (bf *)L.dVh_io : nullptr, *dS_io = tcc ? (bf *)L.dS_io : nullptr;
+  bf *dst_io = tcc ? (bf *)L.dstate_io : nullptr;
+  const bf *Qq_io = H_io, *Kq_io = H_io + (tcc ? Ms : 0), *Ql_io = H_io + (tcc ? 2 * Ms : 0);
+  const bf *Kl_io = H_io + (tcc ? 3 * Ms : 0);
+  // C[z] (+)= alpha A[z] B[z / b_div] for the BG chunks z
+  auto bt = [&](const void *A, long long lda, int a_mn, const void *Bm, long long ldb, int b_km,
+                float *Cm, int m, int n, int k, int b_div, float alpha, int acc) {
+    GemmAnyArgs g = tc_args(q, A, lda, a_mn, Bm, ldb, b_km, Cm, 0, m, n, k, 0);
+    g.batches = (int)BG;
+    g.b_div = b_div;
+    g.alpha = alpha;
+    g.accumulate = acc;
+    return tc_gemm_any(g, st);
+  };
+  const int pdiv = q.causal ? 1 : G;  // chunks sharing one prefix state
   // ---- recompute the forward
   if (tc)
     BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, pre, 0, (int)M, N, d, 0), st));
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
-  act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s);
+  act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s, V_io,
+                                               H_io);
   const float *Qq = H, *Kq = H + Ms, *Ql = H + 2 * Ms, *Kl = H + 3 * Ms;
   // per chunk z: rows z*C .. of the [M, *] matrices
-  BW_TRY(gemm(st, C, C, s, (int)BG, Qq, op(s, 1, (long long)C * s), Kq,
-              op(1, s, (long long)C * s), ScoreEpi{S, P, q.relpos, C, q.causal, 1.f / C}));
-  BW_TRY(gemm(st, C, e, C, (int)BG, P, op(C, 1, (long long)C * C), V, op(e, 1, (long long)C * e),
-              StoreF32{Vh, e, 1, (long long)C * e, q.local_scale, 0}));
-  BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
-              op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
+  if (tcc) {
+    BW_TRY(bt(Qq_io, s, 0, Kq_io, s, 1, S, C, C, s, 1, 1.f, 0));  // raw Qq Kq^T
+    score_act<<<blocks_for(BG * C * C), 256, 0, st>>>(S, P_io, q.relpos, BG, C, q.causal,
+                                                       1.f / C);
+    BW_TRY(bt(P_io, C, 0, V_io, e, 0, Vh, C, e, C, 1, q.local_scale, 0));
+    BW_TRY(bt(Kl_io, s, 1, V_io, e, 0, state, s, e, C, 1, 1.f, 0));
+  } else {
+    BW_TRY(gemm(st, C, C, s, (int)BG, Qq, op(s, 1, (long long)C * s), Kq,
+                op(1, s, (long long)C * s), ScoreEpi{S, P, q.relpos, C, q.causal, 1.f / C}));
+    BW_TRY(gemm(st, C, e, C, (int)BG, P, op(C, 1, (long long)C * C), V,
+                op(e, 1, (long long)C * e), StoreF32{Vh, e, 1, (long long)C * e, q.local_scale, 0}));
+    BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
+                op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
+  }
   scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, prefix, q.B, G, se, q.causal,
-                                                      q.lin_scale);
+                                                      q.lin_scale, pre_io);
   // Vh += Q_lin Prefix (a chunk's prefix, or its batch row's total)
-  const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
-  BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
-              StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
+  if (tcc) {
+    BW_TRY(bt(Ql_io, s, 0, pre_io, e, 0, Vh, C, e, s, pdiv, 1.f, 1));
+  } else {
+    const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
+    BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
+                StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
+  }
   gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, A_io, M * e);
   // ---- output projection and gate
   if (tc) {
@@ -406,30 +486,52 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
-  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e);
+  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e, dVh_io);
   // ---- local part
-  BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
-              op(1, e, (long long)C * e), StoreF32{dP, C, 1, (long long)C * C, q.local_scale, 0}));
-  BW_TRY(gemm(st, C, e, C, (int)BG, P, op(1, C, (long long)C * C), dVh,
-              op(e, 1, (long long)C * e), StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
-  score_grad<<<blocks_for(BG * C * C), 256, 0, st>>>(S, dP, BG, C, q.causal);
+  if (tcc) {
+    BW_TRY(bt(dVh_io, e, 0, V_io, e, 1, dP, C, C, e, 1, q.local_scale, 0));
+    BW_TRY(bt(P_io, C, 1, dVh_io, e, 0, dV, C, e, C, 1, q.local_scale, 0));
+  } else {
+    BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
+                op(1, e, (long long)C * e),
+                StoreF32{dP, C, 1, (long long)C * C, q.local_scale, 0}));
+    BW_TRY(gemm(st, C, e, C, (int)BG, P, op(1, C, (long long)C * C), dVh,
+                op(e, 1, (long long)C * e),
+                StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
+  }
+  score_grad<<<blocks_for(BG * C * C), 256, 0, st>>>(S, dP, BG, C, q.causal, dS_io);
   relpos_grad<<<2 * C - 1, 256, 0, st>>>(dP, q.drelpos, BG, C);
   float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;
-  BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(C, 1, (long long)C * C), Kq,
-              op(s, 1, (long long)C * s), StoreF32{dQq, s, 1, (long long)C * s, 1.f / C, 0}));
-  BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(1, C, (long long)C * C), Qq,
-              op(s, 1, (long long)C * s), StoreF32{dKq, s, 1, (long long)C * s, 1.f / C, 0}));
+  if (tcc) {
+    BW_TRY(bt(dS_io, C, 0, Kq_io, s, 0, dQq, C, s, C, 1, 1.f / C, 0));
+    BW_TRY(bt(dS_io, C, 1, Qq_io, s, 0, dKq, C, s, C, 1, 1.f / C, 0));
+  } else {
+    BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(C, 1, (long long)C * C), Kq,
+                op(s, 1, (long long)C * s), StoreF32{dQq, s, 1, (long long)C * s, 1.f / C, 0}));
+    BW_TRY(gemm(st, C, s, C, (int)BG, dP, op(1, C, (long long)C * C), Qq,
+                op(s, 1, (long long)C * s), StoreF32{dKq, s, 1, (long long)C * s, 1.f / C, 0}));
+  }
   // ---- global part
-  const Operand opreT = q.causal ? op(1, e, se) : op(1, e, se, G);
-  BW_TRY(gemm(st, C, s, e, (int)BG, dVh, op(e, 1, (long long)C * e), prefix, opreT,
-              StoreF32{dQl, s, 1, (long long)C * s, 1.f, 0}));
-  BW_TRY(gemm(st, s, e, C, (int)BG, Ql, op(1, s, (long long)C * s), dVh,
-              op(e, 1, (long long)C * e), StoreF32{dpre, e, 1, se, q.lin_scale, 0}));
-  scan_backward<<<blocks_for(q.B * se), 256, 0, st>>>(dpre, q.B, G, se, q.causal);
-  BW_TRY(gemm(st, C, s, e, (int)BG, V, op(e, 1, (long long)C * e), dpre, op(1, e, se),
-              StoreF32{dKl, s, 1, (long long)C * s, 1.f, 0}));
-  BW_TRY(gemm(st, C, e, s, (int)BG, Kl, op(s, 1, (long long)C * s), dpre, op(e, 1, se),
-              StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
+  if (tcc) {
+    BW_TRY(bt(dVh_io, e, 0, pre_io, e, 1, dQl, C, s, e, pdiv, 1.f, 0));
+    BW_TRY(bt(Ql_io, s, 1, dVh_io, e, 0, dpre, s, e, C, 1, q.lin_scale, 0));
+  } else {
+    const Operand opreT = q.causal ? op(1, e, se) : op(1, e, se, G);
+    BW_TRY(gemm(st, C, s, e, (int)BG, dVh, op(e, 1, (long long)C * e), prefix, opreT,
+                StoreF32{dQl, s, 1, (long long)C * s, 1.f, 0}));
+    BW_TRY(gemm(st, s, e, C, (int)BG, Ql, op(1, s, (long long)C * s), dVh,
+                op(e, 1, (long long)C * e), StoreF32{dpre, e, 1, se, q.lin_scale, 0}));
+  }
+  scan_backward<<<blocks_for(q.B * se), 256, 0, st>>>(dpre, q.B, G, se, q.causal, dst_io);
+  if (tcc) {
+    BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
+    BW_TRY(bt(Kl_io, s, 0, dst_io, e, 0, dV, C, e, s, 1, 1.f, 1));
+  } else {
+    BW_TRY(gemm(st, C, s, e, (int)BG, V, op(e, 1, (long long)C * e), dpre, op(1, e, se),
+                StoreF32{dKl, s, 1, (long long)C * s, 1.f, 0}));
+    BW_TRY(gemm(st, C, e, s, (int)BG, Kl, op(s, 1, (long long)C * s), dpre, op(e, 1, se),
+                StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
+  }
   // ---- heads
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dgamma, 4 * s);
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dbeta, 4 * s);

@@ -151,6 +151,22 @@ int backward_layout(int B, int T, int C, int d, int e, int s, int causal, int dt
   take(&dpre_io, io_n * (M * N + 1) / 2);
   l.A_io = a_io;
   l.dpre_io = dpre_io;
+  float *h_io = nullptr, *v_io = nullptr, *p_io = nullptr, *pre_io = nullptr;
+  float *dvh_io = nullptr, *ds_io = nullptr, *dst_io = nullptr;
+  take(&h_io, io_n * (4 * M * s + 1) / 2);
+  take(&v_io, io_n * (M * e + 1) / 2);
+  take(&p_io, io_n * (B * G * C * C + 1) / 2);
+  take(&pre_io, io_n * ((causal ? B * G : B) * se + 1) / 2);
+  take(&dvh_io, io_n * (M * e + 1) / 2);
+  take(&ds_io, io_n * (B * G * C * C + 1) / 2);
+  take(&dst_io, io_n * (B * G * se + 1) / 2);
+  l.H_io = h_io;
+  l.V_io = v_io;
+  l.P_io = p_io;
+  l.prefix_io = pre_io;
+  l.dVh_io = dvh_io;
+  l.dS_io = ds_io;
+  l.dstate_io = dst_io;
   *total = off;
   return FLASH_GAU_OK;
 }

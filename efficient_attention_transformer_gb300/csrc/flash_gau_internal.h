@@ -106,6 +106,12 @@ struct GemmAnyArgs {
   int allow_split;  // fp32: split K across CTAs when the tiles are few
   int num_sms;
   int *status;
+  // batched: `batches` independent products, each operand's batch z stored
+  // right after batch z-1 (A: M or K rows, B: K or N rows, C: M rows, as
+  // the operand is stored); B's batch is z / b_div (a shared operand)
+  int batches = 1;
+  int b_div = 1;
+  float alpha = 1.f;  // fp32 output: C (+)= alpha * A B
 };
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 
@@ -161,6 +167,14 @@ struct BackwardLayout {
   float *dZ;      // [M, s]
   void *A_io;     // [M, e] bf16 copy of the gated product (tensor-core path)
   void *dpre_io;  // [M, 2e+s] bf16 copy of dPre (tensor-core path)
+  // bf16 operand copies of the chunk-level contractions (tensor-core path)
+  void *H_io;       // [4, M, s]
+  void *V_io;       // [M, e]
+  void *P_io;       // [B*G, C, C]
+  void *prefix_io;  // [B*G or B, s, e]
+  void *dVh_io;     // [M, e]
+  void *dS_io;      // [B*G, C, C]
+  void *dstate_io;  // [B*G, s, e]
 };
 struct BackwardProblem {
   int B, T, C, G, d, e, s, causal;

@@ -8,6 +8,10 @@
 // fp32 results are stored, or added with vector atomics (split-K: several
 // CTAs sum into one zeroed tile); bf16 results go out through TMA stores.
 //
+// Batched form: independent products stacked along the stored rows of each
+// operand (a batch never shares a 128-row tile or a 64-deep k-block with
+// the next), one tile list over all of them.
+//
 // One persistent CTA per SM over 128 x 256 output tiles (x split), static
 // round robin.  Warp 0 streams 64-deep k-blocks of A and B into a 4-stage
 // ring of 128-byte-swizzled boxes with TMA; one thread of warp 1 issues
@@ -43,6 +47,9 @@ struct AnyParams {
   int kb_split;  // k-blocks per split
   float *Cf;     // fp32 output, row-major with leading dimension N
   int atomic;    // fp32: add into C (zeroed by the caller) instead of storing
+  float alpha;   // fp32 output scale
+  int b_div;     // B's batch = the tile's batch / b_div
+  int kbox_rows; // rows of a K-major B box: min(256, N)
   int *status;
 };
 
@@ -71,13 +78,14 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
 }
 
 struct Tile {
-  int mt, nt, kb0, kb1;
+  int z, mt, nt, kb0, kb1;
 };
 __device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
   Tile x;
   const int split = t % p.splits, rem = t / p.splits;
   x.nt = rem % p.n_tiles;
-  x.mt = rem / p.n_tiles;
+  x.mt = (rem / p.n_tiles) % p.m_tiles;
+  x.z = rem / (p.n_tiles * p.m_tiles);
   const int kblocks = p.K / BK;
   x.kb0 = split * p.kb_split;
   x.kb1 = min(kblocks, x.kb0 + p.kb_split);
@@ -129,6 +137,9 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x) {
         const Tile x = tile_of(p, t);
         const int m0 = x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
+        // this batch's first stored row of A and of B
+        const int za = x.z * (A_MN ? p.K : p.M);
+        const int zb = (x.z / p.b_div) * (B_KM ? p.N : p.K);
         for (int kb = x.kb0; kb < x.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
@@ -139,20 +150,21 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           uint8_t *sB = sA + A_BYTES;
           // a K-major B box is 256 rows whatever the tile's width (rows past
           // N are zero-filled and counted)
-          const uint32_t b_bytes = B_KM ? (uint32_t)B_BYTES : (uint32_t)(nsz / 64) * BOX_BYTES;
+          const uint32_t b_bytes =
+              B_KM ? (uint32_t)p.kbox_rows * 128u : (uint32_t)(nsz / 64) * BOX_BYTES;
           mbar_arrive_expect_tx(full, A_BYTES + b_bytes);
           if (A_MN) {
             // [K, M] storage: 64 k-rows of two 64-column blocks of M
-            tma_load_2d(smem_u32(sA), &tmA, full, m0, kb * BK);
-            tma_load_2d(smem_u32(sA + BOX_BYTES), &tmA, full, m0 + 64, kb * BK);
+            tma_load_2d(smem_u32(sA), &tmA, full, m0, za + kb * BK);
+            tma_load_2d(smem_u32(sA + BOX_BYTES), &tmA, full, m0 + 64, za + kb * BK);
           } else {
-            tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, m0);
+            tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, za + m0);
           }
           if (B_KM) {
-            tma_load_2d(smem_u32(sB), &tmB, full, kb * BK, n0);
+            tma_load_2d(smem_u32(sB), &tmB, full, kb * BK, zb + n0);
           } else {
             for (int j = 0; j < nsz / 64; ++j)
-              tma_load_2d(smem_u32(sB + j * BOX_BYTES), &tmB, full, n0 + j * 64, kb * BK);
+              tma_load_2d(smem_u32(sB + j * BOX_BYTES), &tmB, full, n0 + j * 64, zb + kb * BK);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -216,7 +228,7 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     int local = 0;
     for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x, ++local) {
       const Tile x = tile_of(p, t);
-      const int m0 = x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
+      const int m0 = x.z * p.M + x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
       const int acc = local & 1;
       if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
         raise_timeout(sm, p.status);
@@ -260,8 +272,8 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const uint32_t *v = q < 8 ? &ra[4 * q] : &rb[4 * (q - 8)];
-            const float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
-            const float c = __uint_as_float(v[2]), d = __uint_as_float(v[3]);
+            const float a = p.alpha * __uint_as_float(v[0]), b = p.alpha * __uint_as_float(v[1]);
+            const float c = p.alpha * __uint_as_float(v[2]), d = p.alpha * __uint_as_float(v[3]);
             if (p.atomic) red_add_v4(crow + 4 * q, a, b, c, d);
             else *reinterpret_cast<float4 *>(crow + 4 * q) = make_float4(a, b, c, d);
           }
@@ -301,20 +313,25 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
 }  // namespace
 
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
-  if (g.M % BM != 0 || g.N % 64 != 0 || g.K % BK != 0 || g.M <= 0 || g.N <= 0 || g.K <= 0)
+  if (g.M % BM != 0 || g.N % 64 != 0 || g.K % BK != 0 || g.M <= 0 || g.N <= 0 || g.K <= 0 ||
+      g.batches <= 0 || g.b_div <= 0)
     return cudaErrorInvalidValue;
+  const long long Z = g.batches, ZB = (g.batches + g.b_div - 1) / g.b_div;
+  const int kbox = g.N < BN ? g.N : BN;
   CUtensorMap tmA, tmB, tmC;
   cudaError_t err;
   // A: K-major [M, K] in 64 x 128 boxes, or M-major [K, M] in 64 x 64 boxes
-  if (g.a_mn) err = make_tmap_bf16_2d(&tmA, g.A, g.K, g.M, g.lda, 64, 64);
-  else err = make_tmap_bf16_2d(&tmA, g.A, g.M, g.K, g.lda, BM, 64);
+  if (g.a_mn) err = make_tmap_bf16_2d(&tmA, g.A, Z * g.K, g.M, g.lda, 64, 64);
+  else err = make_tmap_bf16_2d(&tmA, g.A, Z * g.M, g.K, g.lda, BM, 64);
   if (err != cudaSuccess) return err;
-  // B: N-major [K, N] in 64 x 64 boxes, or K-major [N, K] in 256-row boxes
-  if (g.b_km) err = make_tmap_bf16_2d(&tmB, g.B, g.N, g.K, g.ldb, BN, 64);
-  else err = make_tmap_bf16_2d(&tmB, g.B, g.K, g.N, g.ldb, 64, 64);
+  // B: N-major [K, N] in 64 x 64 boxes, or K-major [N, K] in boxes of
+  // min(256, N) rows
+  if (g.b_km) err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.N, g.K, g.ldb, kbox, 64);
+  else err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.K, g.N, g.ldb, 64, 64);
   if (err != cudaSuccess) return err;
   if (g.c_bf16) {
-    if ((err = make_tmap_bf16_2d(&tmC, g.C, g.M, g.N, g.N, 32, 64)) != cudaSuccess) return err;
+    if ((err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64)) != cudaSuccess)
+      return err;
   } else {
     tmC = tmA;  // unused
   }
@@ -328,7 +345,7 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   // split K when the output tiles would leave SMs idle (fp32 atomic output
   // only); at least 8 k-blocks a split
   int splits = 1;
-  const int out_tiles = p.m_tiles * p.n_tiles;
+  const int out_tiles = (int)Z * p.m_tiles * p.n_tiles;
   if (!g.c_bf16 && g.allow_split && out_tiles < g.num_sms) {
     splits = (2 * g.num_sms + out_tiles - 1) / out_tiles;
     const int max_splits = kblocks / 8 > 1 ? kblocks / 8 : 1;
@@ -338,11 +355,15 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   p.splits = (kblocks + p.kb_split - 1) / p.kb_split;
   p.total = out_tiles * p.splits;
   p.Cf = (float *)g.C;
+  p.alpha = g.alpha;
+  p.b_div = g.b_div;
+  p.kbox_rows = kbox;
   p.atomic = p.splits > 1 || g.accumulate;
   p.status = g.status;
   if (p.atomic && !g.accumulate) {
     // the split partial sums add into a zeroed output
-    if ((err = cudaMemsetAsync(g.C, 0, (size_t)g.M * g.N * sizeof(float), stream)) != cudaSuccess)
+    if ((err = cudaMemsetAsync(g.C, 0, (size_t)Z * g.M * g.N * sizeof(float), stream)) !=
+        cudaSuccess)
       return err;
   }
   const int key = (g.a_mn ? 4 : 0) | (g.b_km ? 2 : 0) | (g.c_bf16 ? 1 : 0);

@@ -72,6 +72,10 @@ def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed, local_scale=1.0):
     ((2, 512, 128, 384, 64, 128), False, "bf16", 0.5),
     ((1, 384, 96, 160, 64, 128), False, "bf16", 1.0),
     ((1, 256, 64, 128, 32, 256), True, "fp32", 0.0),
+    # chunk-level contractions on the tensor cores: value width with a
+    # 128-column tile tail, several chunks non-causal
+    ((2, 512, 128, 384, 128, 128), True, "bf16", 1.0),
+    ((1, 1024, 256, 512, 128, 256), False, "bf16", 1.0 / 256),
 ])
 def test_backward_matches_oracle(shape, causal, dtype, lin_scale):
     B, T, d, e, s, C = shape
