@@ -159,8 +159,9 @@ cudaError_t gemm(cudaStream_t st, int M, int N, int K, int batches, const TA *A,
 Operand op(long long sm, long long sk, long long sb = 0, int div = 1) { return {sm, sk, sb, div}; }
 
 // ------------------------------------------------------------ elementwise --
-// U, V, Z = swish(Pre) and the four heads Z gamma_k + beta_k
-// (and bf16 copies of V and the heads when V_io / H_io are set)
+// U, V, Z = swish(Pre) and the four heads Z gamma_k + beta_k (CUDA-core
+// path: fp32 Pre, any widths).  V and H are written in fp32 when given, and
+// as bf16 copies when V_io / H_io are.
 __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
                           float *__restrict__ V, float *__restrict__ Z, float *__restrict__ H,
                           const float *__restrict__ gamma, const float *__restrict__ beta,
@@ -175,32 +176,32 @@ __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
     if (c < e) {
       U[m * e + c] = y;
     } else if (c < 2 * e) {
-      V[m * e + c - e] = y;
+      if (V) V[m * e + c - e] = y;
       if (V_io) V_io[m * e + c - e] = __float2bfloat16_rn(y);
     } else {
       const int k = c - 2 * e;
       Z[m * s + k] = y;
       for (int h = 0; h < 4; ++h) {
         const float v = fmaf(y, gamma[h * s + k], beta[h * s + k]);
-        H[(h * M + m) * s + k] = v;
+        if (H) H[(h * M + m) * s + k] = v;
         if (H_io) H_io[(h * M + m) * s + k] = __float2bfloat16_rn(v);
       }
     }
   }
 }
 
-// A = U * Vh (and its bf16 copy when A_io is set)
+// A = U * Vh (fp32 when A is set, a bf16 copy when A_io is)
 __global__ void gate(const float *__restrict__ U, const float *__restrict__ Vh,
                      float *__restrict__ A, __nv_bfloat16 *__restrict__ A_io, long long n) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const float a = U[i] * Vh[i];
-    A[i] = a;
+    if (A) A[i] = a;
     if (A_io) A_io[i] = __float2bfloat16_rn(a);
   }
 }
 
-// dU = dA * Vh, dVh = dA * U
+// dU = dA * Vh, dVh = dA * U (fp32 when dVh is set, a bf16 copy when dVh_io is)
 __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict__ U,
                           const float *__restrict__ Vh, float *__restrict__ dU,
                           float *__restrict__ dVh, long long n,
@@ -209,7 +210,7 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
        i += (long long)gridDim.x * blockDim.x) {
     dU[i] = dA[i] * Vh[i];
     const float g = dA[i] * U[i];
-    dVh[i] = g;
+    if (dVh) dVh[i] = g;
     if (dVh_io) dVh_io[i] = __float2bfloat16_rn(g);
   }
 }
@@ -217,53 +218,58 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
 // the scores from the raw products R = Qq Kq^T of chunk z (in place):
 // S = R / C + relpos[j - i + C - 1], and P = relu(S)^2 (zero above the
 // diagonal when causal) as a bf16 operand
+// (blocks along y take the rows z*C + i of the [B*G*C, C] score matrices)
 __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_io,
-                          const float *__restrict__ relpos, long long chunks, int C, int causal,
+                          const float *__restrict__ relpos, long long rows, int C, int causal,
                           float inv_c) {
-  const long long n = chunks * C * C;
-  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n;
-       o += (long long)gridDim.x * blockDim.x) {
-    const int j = (int)(o % C), i = (int)((o / C) % C);
-    const float v = fmaf(S[o], inv_c, relpos[j - i + C - 1]);
+  for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
+  const int i = (int)(row % C);
+  const float *rp = relpos + C - 1 - i;  // + j
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < C; j += gridDim.x * blockDim.x) {
+    const long long o = row * C + j;
+    const float v = fmaf(S[o], inv_c, rp[j]);
     S[o] = v;
     const float r = fmaxf(v, 0.f);
     P_io[o] = __float2bfloat16_rn((causal && j > i) ? 0.f : r * r);
   }
+  }
 }
 
 // dS = 2 relu(S) dP, zero above the diagonal when causal (in place over dP)
-__global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, long long chunks,
+// (blocks along y take the rows of the score matrices)
+__global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, long long rows,
                            int C, int causal, __nv_bfloat16 *__restrict__ dS_io) {
-  const long long n = chunks * C * C;
-  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < n;
-       o += (long long)gridDim.x * blockDim.x) {
-    const int j = (int)(o % C), i = (int)((o / C) % C);
+  for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
+  const int i = (int)(row % C);
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < C; j += gridDim.x * blockDim.x) {
+    const long long o = row * C + j;
     const float v = (causal && j > i) ? 0.f : 2.f * fmaxf(S[o], 0.f) * dP[o];
     dP[o] = v;
     if (dS_io) dS_io[o] = __float2bfloat16_rn(v);
   }
+  }
 }
 
-// drelpos[k] = sum over chunks and over (i, j) with j - i = k - (C - 1)
+// drelpos[k] = sum over chunks and over (i, j) with j - i = k - (C - 1).
+// A block takes kRelRows consecutive rows of the [B*G*C, C] matrix dS, reads
+// them along j (coalesced) into 2C - 1 shared bins by offset, then adds its
+// bins to drelpos (zeroed first) with one atomic per bin.
+constexpr int kRelRows = 32;
 __global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ drelpos,
-                            long long chunks, int C) {
-  const int k = blockIdx.x;  // 0 .. 2C - 2
-  const int off = k - (C - 1);
-  const int i0 = off < 0 ? -off : 0, n = C - (off < 0 ? -off : off);
-  float acc = 0.f;
-  for (long long t = threadIdx.x; t < chunks * n; t += blockDim.x) {
-    const long long z = t / n;
-    const int i = i0 + (int)(t - z * n);
-    acc += dS[(z * C + i) * C + i + off];
-  }
-  __shared__ float red[256];
-  red[threadIdx.x] = acc;
+                            long long rows, int C) {
+  extern __shared__ float bins[];  // [2C - 1]
+  for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x) bins[k] = 0.f;
   __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w /= 2) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
+  const long long r0 = (long long)blockIdx.x * kRelRows;
+  for (int rr = 0; rr < kRelRows && r0 + rr < rows; ++rr) {
+    const long long row = r0 + rr;
+    const int i = (int)(row % C);
+    for (int j = threadIdx.x; j < C; j += blockDim.x)
+      atomicAdd(&bins[j - i + C - 1], dS[row * C + j]);
   }
-  if (threadIdx.x == 0) drelpos[k] = red[0];
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x)
+    if (bins[k] != 0.f) atomicAdd(drelpos + k, bins[k]);
 }
 
 // prefix[b][g] = lin_scale * (exclusive sum over chunks, or the total)
@@ -291,26 +297,37 @@ __global__ void scan_forward(const float *__restrict__ state, float *__restrict_
 
 // dState_h = sum_{g>h} dPrefix_g (causal) or the total (in place), with the
 // lin_scale factor already inside dPrefix
+// (with dstate_io set, dState goes only there, as bf16, and dPrefix is left
+// as it is)
 __global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long se, int causal,
                               __nv_bfloat16 *__restrict__ dstate_io) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
        i += (long long)gridDim.x * blockDim.x) {
     const long long b = i / se, r = i - b * se;
     if (causal) {
+      // groups of 8 chunks, last first: the 8 loads issue together
       float run = 0.f;
-      for (int g = G - 1; g >= 0; --g) {
-        const long long o = (b * G + g) * se + r;
-        const float v = dpre[o];
-        dpre[o] = run;
-        if (dstate_io) dstate_io[o] = __float2bfloat16_rn(run);
-        run += v;
+      for (int g1 = G; g1 > 0; g1 -= 8) {
+        const int g0 = g1 - 8 > 0 ? g1 - 8 : 0;
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (g0 + k < g1) v[k] = dpre[(b * G + g0 + k) * se + r];
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+          if (g0 + k >= g1) continue;
+          const long long o = (b * G + g0 + k) * se + r;
+          if (dstate_io) dstate_io[o] = __float2bfloat16_rn(run);
+          else dpre[o] = run;
+          run += v[k];
+        }
       }
     } else {
       float tot = 0.f;
       for (int g = 0; g < G; ++g) tot += dpre[(b * G + g) * se + r];
       for (int g = 0; g < G; ++g) {
-        dpre[(b * G + g) * se + r] = tot;
         if (dstate_io) dstate_io[(b * G + g) * se + r] = __float2bfloat16_rn(tot);
+        else dpre[(b * G + g) * se + r] = tot;
       }
     }
   }
@@ -362,6 +379,94 @@ __global__ void pre_grad(float *__restrict__ pre, __nv_bfloat16 *__restrict__ pr
   }
 }
 
+// act_heads with a bf16 Pre (tensor-core recompute, CUDA-core chunk path)
+__global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__restrict__ U,
+                               float *__restrict__ V, float *__restrict__ Z,
+                               float *__restrict__ H, const float *__restrict__ gamma,
+                               const float *__restrict__ beta, long long M, int e, int s) {
+  const int N = 2 * e + s;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / N;
+    const int c = (int)(i - m * N);
+    const float y = swish(__bfloat162float(pre[i]));
+    if (c < e) {
+      U[m * e + c] = y;
+    } else if (c < 2 * e) {
+      V[m * e + c - e] = y;
+    } else {
+      const int k = c - 2 * e;
+      Z[m * s + k] = y;
+      for (int h = 0; h < 4; ++h) H[(h * M + m) * s + k] = fmaf(y, gamma[h * s + k], beta[h * s + k]);
+    }
+  }
+}
+
+// The tensor-core path's forms of the two kernels above: Pre comes as bf16
+// (the recompute GEMM's output, in the dPre buffer), four columns per
+// thread (e and s multiples of 4), and only the bf16 operands that the
+// tensor-core contractions read are written besides U and Z.
+struct Bf4 {
+  __nv_bfloat162 a, b;
+};
+__device__ __forceinline__ float4 load_bf4(const __nv_bfloat16 *p) {
+  const Bf4 v = *reinterpret_cast<const Bf4 *>(p);
+  const float2 x = __bfloat1622float2(v.a), y = __bfloat1622float2(v.b);
+  return make_float4(x.x, x.y, y.x, y.y);
+}
+__device__ __forceinline__ void store_bf4(__nv_bfloat16 *p, float a, float b, float c, float d) {
+  Bf4 v;
+  v.a = __floats2bfloat162_rn(a, b);
+  v.b = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<Bf4 *>(p) = v;
+}
+
+__global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__restrict__ U,
+                             float *__restrict__ Z, const float *__restrict__ gamma,
+                             const float *__restrict__ beta, long long M, int e, int s,
+                             __nv_bfloat16 *__restrict__ V_io, __nv_bfloat16 *__restrict__ H_io) {
+  const int N4 = (2 * e + s) / 4, e4 = e / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / N4;
+    const int c4 = (int)(i - m * N4);
+    const float4 x = load_bf4(pre + 4 * i);
+    const float4 y = make_float4(swish(x.x), swish(x.y), swish(x.z), swish(x.w));
+    if (c4 < e4) {
+      reinterpret_cast<float4 *>(U)[m * e4 + c4] = y;
+    } else if (c4 < 2 * e4) {
+      store_bf4(V_io + m * e + 4 * (c4 - e4), y.x, y.y, y.z, y.w);
+    } else {
+      const int k = 4 * (c4 - 2 * e4);
+      reinterpret_cast<float4 *>(Z + m * s)[k / 4] = y;
+      for (int h = 0; h < 4; ++h) {
+        const float *g = gamma + h * s + k, *b = beta + h * s + k;
+        store_bf4(H_io + (h * M + m) * s + k, fmaf(y.x, __ldg(g), __ldg(b)),
+                  fmaf(y.y, __ldg(g + 1), __ldg(b + 1)), fmaf(y.z, __ldg(g + 2), __ldg(b + 2)),
+                  fmaf(y.w, __ldg(g + 3), __ldg(b + 3)));
+      }
+    }
+  }
+}
+
+// dPre = d(U | V | Z) * swish'(Pre), bf16, in place over the bf16 Pre
+__global__ void pre_grad_v4(__nv_bfloat16 *__restrict__ pre_io, const float *__restrict__ dU,
+                            const float *__restrict__ dV, const float *__restrict__ dZ,
+                            long long M, int e, int s) {
+  const int N4 = (2 * e + s) / 4, e4 = e / 4, s4 = s / 4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / N4;
+    const int c4 = (int)(i - m * N4);
+    const float4 g = c4 < e4       ? reinterpret_cast<const float4 *>(dU)[m * e4 + c4]
+                     : c4 < 2 * e4 ? reinterpret_cast<const float4 *>(dV)[m * e4 + c4 - e4]
+                                   : reinterpret_cast<const float4 *>(dZ)[m * s4 + c4 - 2 * e4];
+    const float4 x = load_bf4(pre_io + 4 * i);
+    store_bf4(pre_io + 4 * i, g.x * swish_grad(x.x), g.y * swish_grad(x.y),
+              g.z * swish_grad(x.z), g.w * swish_grad(x.w));
+  }
+}
+
 // a tensor-core contraction of the backward (bf16 operands)
 GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int a_mn,
                     const void *B, long long ldb, int b_km, void *C, int c_bf16, int M, int N,
@@ -388,6 +493,13 @@ GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int 
 __global__ void zero_f32(float *p, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0.f;
+}
+
+// blocks of 256 threads over the columns of a row, each block looping over
+// rows: at most 2048 blocks along y
+dim3 rows_grid(int cols, long long rows) {
+  const int bx = (cols + 255) / 256;
+  return dim3(bx < 8 ? bx : 8, (unsigned)(rows < 2048 ? rows : 2048));
 }
 
 unsigned blocks_for(long long n) {
@@ -442,18 +554,26 @@ cudaError_t run(const BackwardProblem &q) {
   };
   const int pdiv = q.causal ? 1 : G;  // chunks sharing one prefix state
   // ---- recompute the forward
+  // (the tensor-core path keeps Pre in bf16, in the buffer of dPre)
   if (tc)
-    BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, pre, 0, (int)M, N, d, 0), st));
+    BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, dpre_io, 1, (int)M, N, d, 0), st));
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
-  act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s, V_io,
-                                               H_io);
+  if (tcc)
+    act_heads_v4<<<blocks_for(M * N / 4), 256, 0, st>>>(dpre_io, U, Z, q.gamma, q.beta, M, e, s,
+                                                         V_io, H_io);
+  else if (tc)  // bf16 Pre, fp32 heads and V for the CUDA-core chunk contractions
+    act_heads_bf16<<<blocks_for(M * N), 256, 0, st>>>(dpre_io, U, V, Z, H, q.gamma, q.beta, M, e,
+                                                      s);
+  else
+    act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s,
+                                                 nullptr, nullptr);
   const float *Qq = H, *Kq = H + Ms, *Ql = H + 2 * Ms, *Kl = H + 3 * Ms;
   // per chunk z: rows z*C .. of the [M, *] matrices
   if (tcc) {
     BW_TRY(bt(Qq_io, s, 0, Kq_io, s, 1, S, C, C, s, 1, 1.f, 0));  // raw Qq Kq^T
-    score_act<<<blocks_for(BG * C * C), 256, 0, st>>>(S, P_io, q.relpos, BG, C, q.causal,
-                                                       1.f / C);
+    score_act<<<rows_grid(C, BG * C), 256, 0, st>>>(S, P_io, q.relpos, BG * C, C, q.causal,
+                                                     1.f / C);
     BW_TRY(bt(P_io, C, 0, V_io, e, 0, Vh, C, e, C, 1, q.local_scale, 0));
     BW_TRY(bt(Kl_io, s, 1, V_io, e, 0, state, s, e, C, 1, 1.f, 0));
   } else {
@@ -474,7 +594,7 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
-  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, A_io, M * e);
+  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, tc ? nullptr : Ag, A_io, M * e);
   // ---- output projection and gate
   if (tc) {
     // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
@@ -486,7 +606,8 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
-  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e, dVh_io);
+  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, tcc ? nullptr : dVh, M * e,
+                                               dVh_io);
   // ---- local part
   if (tcc) {
     BW_TRY(bt(dVh_io, e, 0, V_io, e, 1, dP, C, C, e, 1, q.local_scale, 0));
@@ -499,8 +620,10 @@ cudaError_t run(const BackwardProblem &q) {
                 op(e, 1, (long long)C * e),
                 StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   }
-  score_grad<<<blocks_for(BG * C * C), 256, 0, st>>>(S, dP, BG, C, q.causal, dS_io);
-  relpos_grad<<<2 * C - 1, 256, 0, st>>>(dP, q.drelpos, BG, C);
+  score_grad<<<rows_grid(C, BG * C), 256, 0, st>>>(S, dP, BG * C, C, q.causal, dS_io);
+  zero_f32<<<(2 * C - 1 + 255) / 256, 256, 0, st>>>(q.drelpos, 2 * C - 1);
+  relpos_grad<<<(unsigned)((BG * C + kRelRows - 1) / kRelRows), 256,
+                (2 * C - 1) * sizeof(float), st>>>(dP, q.drelpos, BG * C, C);
   float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;
   if (tcc) {
     BW_TRY(bt(dS_io, C, 0, Kq_io, s, 0, dQq, C, s, C, 1, 1.f / C, 0));
@@ -535,11 +658,14 @@ cudaError_t run(const BackwardProblem &q) {
   // ---- heads
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dgamma, 4 * s);
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dbeta, 4 * s);
-  const int rows = 64;
+  const int rows = 16;
   heads_grad<<<(unsigned)((M + rows - 1) / rows), 128, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows);
   // ---- input side
-  pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, dpre_io, dU, dV, dZ, M, e, s);
+  if (tc)
+    pre_grad_v4<<<blocks_for(M * N / 4), 256, 0, st>>>(dpre_io, dU, dV, dZ, M, e, s);
+  else
+    pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, nullptr, dU, dV, dZ, M, e, s);
   if (tc) {
     // dX = dPre W_uvz^T (bf16 out); dW_uvz = X^T dPre
     BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
