@@ -205,6 +205,14 @@ __device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src
       "r"(src), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
+// Element-wise add of a shared-memory box into global memory (fp32 maps).
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

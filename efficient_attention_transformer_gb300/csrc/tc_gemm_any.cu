@@ -5,8 +5,9 @@
 //                 transpose of a row-major [K, M] matrix (M-major);
 //   B_KM = false: B is a row-major [K, N] matrix (N-major); true: B is the
 //                 transpose of a row-major [N, K] matrix (K-major).
-// fp32 results are stored, or added with vector atomics (split-K: several
-// CTAs sum into one zeroed tile); bf16 results go out through TMA stores.
+// Results leave through TMA from per-warp swizzled staging boxes: bf16 as
+// stores; fp32 as stores, or as TMA reduce-adds when accumulating into C or
+// when several CTAs split K and sum into one zeroed tile.
 //
 // Batched form: independent products stacked along the stored rows of each
 // operand (a batch never shares a 128-row tile or a 64-deep k-block with
@@ -36,16 +37,15 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int NUM_THREADS = 192;
-constexpr int STG_BYTES = 32 * 128;  // one 32-row x 128-byte store box per epilogue warp
-constexpr int STG_OFF = STAGES * STAGE_BYTES;
-constexpr int TILE_BYTES = STG_OFF + 4 * STG_BYTES;
+constexpr int STG_BYTES = 32 * 128;  // one 32-row x 128-byte store box
+constexpr int STG_OFF = STAGES * STAGE_BYTES;  // two boxes per epilogue warp
+constexpr int TILE_BYTES = STG_OFF + 4 * 2 * STG_BYTES;
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct AnyParams {
   int M, N, K;
   int m_tiles, n_tiles, splits, total;
   int kb_split;  // k-blocks per split
-  float *Cf;     // fp32 output, row-major with leading dimension N
   int atomic;    // fp32: add into C (zeroed by the caller) instead of storing
   float alpha;   // fp32 output scale
   int b_div;     // B's batch = the tile's batch / b_div
@@ -69,12 +69,6 @@ __device__ __forceinline__ void raise_timeout(Smem *sm, int *status) {
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
 }
 
 struct Tile {
@@ -224,8 +218,8 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   } else {
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    uint8_t *stg = tiles + STG_OFF + (warp - 2) * STG_BYTES;
-    int local = 0;
+    uint8_t *stg = tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES;
+    int local = 0, nbox = 0;
     for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x, ++local) {
       const Tile x = tile_of(p, t);
       const int m0 = x.z * p.M + x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
@@ -268,19 +262,34 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             tma_store_commit();
           }
         } else {
-          float *crow = p.Cf + (size_t)(row0 + lane) * p.N + n0 + c0;
+          // two 32-column fp32 boxes, alternating between the warp's two
+          // staging buffers
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const uint32_t *v = q < 8 ? &ra[4 * q] : &rb[4 * (q - 8)];
-            const float a = p.alpha * __uint_as_float(v[0]), b = p.alpha * __uint_as_float(v[1]);
-            const float c = p.alpha * __uint_as_float(v[2]), d = p.alpha * __uint_as_float(v[3]);
-            if (p.atomic) red_add_v4(crow + 4 * q, a, b, c, d);
-            else *reinterpret_cast<float4 *>(crow + 4 * q) = make_float4(a, b, c, d);
+          for (int h = 0; h < 2; ++h, ++nbox) {
+            uint8_t *box = stg + (nbox & 1) * STG_BYTES;
+            if (lane == 0) tma_store_wait_read<1>();
+            __syncwarp();
+            const uint32_t *v = h == 0 ? ra : rb;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 w = make_float4(p.alpha * __uint_as_float(v[4 * q]),
+                                     p.alpha * __uint_as_float(v[4 * q + 1]),
+                                     p.alpha * __uint_as_float(v[4 * q + 2]),
+                                     p.alpha * __uint_as_float(v[4 * q + 3]));
+              *reinterpret_cast<float4 *>(box + sw128_offset(lane, q)) = w;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (p.atomic) tma_reduce_add_2d(&tmC, smem_u32(box), n0 + c0 + 32 * h, row0);
+              else tma_store_2d(&tmC, smem_u32(box), n0 + c0 + 32 * h, row0);
+              tma_store_commit();
+            }
           }
         }
       }
     }
-    if (OUT_BF16 && lane == 0) tma_store_wait<0>();
+    if (lane == 0) tma_store_wait<0>();
     __syncwarp();
   }
 
@@ -329,12 +338,9 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   if (g.b_km) err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.N, g.K, g.ldb, kbox, 64);
   else err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.K, g.N, g.ldb, 64, 64);
   if (err != cudaSuccess) return err;
-  if (g.c_bf16) {
-    if ((err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64)) != cudaSuccess)
-      return err;
-  } else {
-    tmC = tmA;  // unused
-  }
+  if (g.c_bf16) err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64);
+  else err = make_tmap_f32_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 32);
+  if (err != cudaSuccess) return err;
   AnyParams p = {};
   p.M = g.M;
   p.N = g.N;
@@ -354,7 +360,6 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   p.kb_split = (kblocks + splits - 1) / splits;
   p.splits = (kblocks + p.kb_split - 1) / p.kb_split;
   p.total = out_tiles * p.splits;
-  p.Cf = (float *)g.C;
   p.alpha = g.alpha;
   p.b_div = g.b_div;
   p.kbox_rows = kbox;
