@@ -404,8 +404,16 @@ __global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__r
 
 // The tensor-core path's forms of the two kernels above: Pre comes as bf16
 // (the recompute GEMM's output, in the dPre buffer), four columns per
-// thread (e and s multiples of 4), and only the bf16 operands that the
-// tensor-core contractions read are written besides U and Z.
+// thread (e and s multiples of 4), the sigmoid from the fast exponential
+// and reciprocal (their errors are far below the bf16 rounding of Pre),
+// and only the bf16 operands that the tensor-core contractions read are
+// written besides U and Z.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x); }
+__device__ __forceinline__ float swish_grad_fast(float x) {
+  const float sg = sigmoid_fast(x);
+  return sg * (1.0f + x * (1.0f - sg));
+}
 struct Bf4 {
   __nv_bfloat162 a, b;
 };
@@ -426,12 +434,16 @@ __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__res
                              const float *__restrict__ beta, long long M, int e, int s,
                              __nv_bfloat16 *__restrict__ V_io, __nv_bfloat16 *__restrict__ H_io) {
   const int N4 = (2 * e + s) / 4, e4 = e / 4;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N4;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long m = i / N4;
-    const int c4 = (int)(i - m * N4);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  // (row, column group) of element i, advanced by the stride without a divide
+  long long m = i0 / N4;
+  int c4 = (int)(i0 - m * N4);
+  const long long dm = stride / N4;
+  const int dc = (int)(stride - dm * N4);
+  for (long long i = i0; i < M * N4; i += stride) {
     const float4 x = load_bf4(pre + 4 * i);
-    const float4 y = make_float4(swish(x.x), swish(x.y), swish(x.z), swish(x.w));
+    const float4 y = make_float4(swish_fast(x.x), swish_fast(x.y), swish_fast(x.z), swish_fast(x.w));
     if (c4 < e4) {
       reinterpret_cast<float4 *>(U)[m * e4 + c4] = y;
     } else if (c4 < 2 * e4) {
@@ -446,6 +458,37 @@ __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__res
                   fmaf(y.w, __ldg(g + 3), __ldg(b + 3)));
       }
     }
+    m += dm;
+    c4 += dc;
+    if (c4 >= N4) {
+      c4 -= N4;
+      ++m;
+    }
+  }
+}
+
+// A = U * Vh as bf16 only; n4 = elements / 4
+__global__ void gate_v4(const float4 *__restrict__ U, const float4 *__restrict__ Vh,
+                        __nv_bfloat16 *__restrict__ A_io, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 u = U[i], v = Vh[i];
+    store_bf4(A_io + 4 * i, u.x * v.x, u.y * v.y, u.z * v.z, u.w * v.w);
+  }
+}
+
+// dU = dA * Vh (fp32), dVh = dA * U (bf16 only, or also fp32 when dVh is set)
+__global__ void gate_grad_v4(const float4 *__restrict__ dA, const float4 *__restrict__ U,
+                             const float4 *__restrict__ Vh, float4 *__restrict__ dU,
+                             float4 *__restrict__ dVh, __nv_bfloat16 *__restrict__ dVh_io,
+                             long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 a = dA[i], u = U[i], v = Vh[i];
+    dU[i] = make_float4(a.x * v.x, a.y * v.y, a.z * v.z, a.w * v.w);
+    const float4 g = make_float4(a.x * u.x, a.y * u.y, a.z * u.z, a.w * u.w);
+    if (dVh) dVh[i] = g;
+    store_bf4(dVh_io + 4 * i, g.x, g.y, g.z, g.w);
   }
 }
 
@@ -454,16 +497,25 @@ __global__ void pre_grad_v4(__nv_bfloat16 *__restrict__ pre_io, const float *__r
                             const float *__restrict__ dV, const float *__restrict__ dZ,
                             long long M, int e, int s) {
   const int N4 = (2 * e + s) / 4, e4 = e / 4, s4 = s / 4;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N4;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long m = i / N4;
-    const int c4 = (int)(i - m * N4);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  long long m = i0 / N4;
+  int c4 = (int)(i0 - m * N4);
+  const long long dm = stride / N4;
+  const int dc = (int)(stride - dm * N4);
+  for (long long i = i0; i < M * N4; i += stride) {
     const float4 g = c4 < e4       ? reinterpret_cast<const float4 *>(dU)[m * e4 + c4]
                      : c4 < 2 * e4 ? reinterpret_cast<const float4 *>(dV)[m * e4 + c4 - e4]
                                    : reinterpret_cast<const float4 *>(dZ)[m * s4 + c4 - 2 * e4];
     const float4 x = load_bf4(pre_io + 4 * i);
-    store_bf4(pre_io + 4 * i, g.x * swish_grad(x.x), g.y * swish_grad(x.y),
-              g.z * swish_grad(x.z), g.w * swish_grad(x.w));
+    store_bf4(pre_io + 4 * i, g.x * swish_grad_fast(x.x), g.y * swish_grad_fast(x.y),
+              g.z * swish_grad_fast(x.z), g.w * swish_grad_fast(x.w));
+    m += dm;
+    c4 += dc;
+    if (c4 >= N4) {
+      c4 -= N4;
+      ++m;
+    }
   }
 }
 
@@ -594,7 +646,11 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
-  gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, tc ? nullptr : Ag, A_io, M * e);
+  if (tc)
+    gate_v4<<<blocks_for(M * e / 4), 256, 0, st>>>((const float4 *)U, (const float4 *)Vh, A_io,
+                                                    M * e / 4);
+  else
+    gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, nullptr, M * e);
   // ---- output projection and gate
   if (tc) {
     // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
@@ -606,8 +662,12 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
-  gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, tcc ? nullptr : dVh, M * e,
-                                               dVh_io);
+  if (tcc)
+    gate_grad_v4<<<blocks_for(M * e / 4), 256, 0, st>>>(
+        (const float4 *)dA, (const float4 *)U, (const float4 *)Vh, (float4 *)dU, nullptr, dVh_io,
+        M * e / 4);
+  else
+    gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e, nullptr);
   // ---- local part
   if (tcc) {
     BW_TRY(bt(dVh_io, e, 0, V_io, e, 1, dP, C, C, e, 1, q.local_scale, 0));
