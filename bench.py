@@ -509,9 +509,10 @@ def run_ours(args, rank, world, local_rank):
             "extra_ms_over_layer": round(block_ms - step_ms, 5)},
             "backward": {
                 "what": "gradients of sum(dO * O) for X, W_uvz, W_o, gamma, beta, relpos "
-                        "(recomputes the forward's intermediates); the five large "
-                        "contractions on the tensor cores (bf16 operands, fp32 "
-                        "accumulation), the chunk-level ones on the CUDA cores in fp32",
+                        "(recomputes the forward's intermediates); every contraction on "
+                        "the tensor cores (bf16 operands, fp32 accumulation; the chunk-level "
+                        "ones batched over the chunks), sums, scans and elementwise steps "
+                        "in fp32",
                 "ms_per_call": round(backward_ms, 3),
                 "value": round(tokens / (backward_ms * 1e-3), 1), "unit": "tokens/s",
                 # two contractions per forward contraction, plus the recompute
