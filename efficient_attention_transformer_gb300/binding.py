@@ -47,6 +47,8 @@ EXPORTED = (
     "flash_gau_decode_state_bytes",
     "flash_gau_decode_step",
     "flash_gau_forward_segmented",
+    "flash_gau_forward_host_workspace_bytes",
+    "flash_gau_forward_host",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -140,6 +142,12 @@ def lib():
                                                   ctypes.POINTER(Segments), i, i, i, i, i, p,
                                                   p, sz, p]
         L.flash_gau_forward_segmented.restype = i
+        L.flash_gau_forward_host_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights),
+                                                             i, i]
+        L.flash_gau_forward_host_workspace_bytes.restype = sz
+        L.flash_gau_forward_host.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p,
+                                             sz, p]
+        L.flash_gau_forward_host.restype = i
         L.flash_gau_rope_toeplitz_bias.argtypes = [p, p, i, i, ctypes.c_float, p, p]
         L.flash_gau_rope_toeplitz_bias.restype = i
         L.flash_gau_backward_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights), i, i]
@@ -300,6 +308,39 @@ def forward_segmented(X, weights, C, causal, segment_ids=None, average=False, ou
         int(bool(causal)), weights.dtype, _dev_ptr(out, "out", X.dtype),
         _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         stream.cuda_stream))
+    return out
+
+
+def forward_host(X, weights, C, causal, out=None, workspace=None, stream=None):
+    """O = FLASH-GAU(X) on host tensors through flash_gau_forward_host: X is
+    a CPU tensor [B, T, d] (pinned for overlapped copies), the result goes to
+    `out` (a CPU tensor like X; allocated pinned when None).  The call
+    returns once the work is queued on `stream`; synchronise it before
+    reading `out`."""
+    if X.dim() != 3 or X.is_cuda:
+        raise ValueError("X must be a CPU tensor [B, T, d]")
+    if not X.is_contiguous():
+        raise ValueError("X must be contiguous")
+    B, T, d = X.shape
+    if d != weights.d or X.dtype != weights.W_uvz.dtype:
+        raise ValueError("X does not match the weights")
+    if out is None:
+        out = torch.empty_like(X).pin_memory()
+    if out.is_cuda or out.shape != X.shape or out.dtype != X.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU tensor like X")
+    dev = weights.W_uvz.device
+    if workspace is None:
+        n = lib().flash_gau_forward_host_workspace_bytes(B, T, C, ctypes.byref(weights.c),
+                                                         int(bool(causal)), weights.dtype)
+        if n == 0:
+            raise FlashGauError(EINVAL, "invalid or unsupported problem")
+        workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    _check(lib().flash_gau_forward_host(
+        X.data_ptr(), ctypes.byref(weights.c), B, T, C, int(bool(causal)), weights.dtype,
+        out.data_ptr(), _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), stream.cuda_stream))
     return out
 
 

@@ -214,6 +214,31 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
                             int causal, int dtype, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* ---- host buffers ----------------------------------------------------- */
+/* The forward pass on host memory: X_host [B, T, d] is copied to the
+ * device, the layer runs, and O is copied back to out_host [B, T, d] (both
+ * io type, host pointers; page-locked memory lets the copies run
+ * asynchronously and overlap, pageable memory works but copies
+ * synchronously).  Batch rows are independent, so the batch is cut into up
+ * to four parts: the input copy of one part, the layer on another and the
+ * output copy of a third run at the same time.  The copies run on two
+ * streams that the library creates once per device (no device memory) and
+ * shares between calls; the layer runs on `stream`, which is made to wait
+ * for the last output copy before the call returns, and whose earlier work
+ * comes first.  Synchronise `stream` before reading out_host.  Calls on
+ * one device are serialised while they enqueue.
+ *   workspace  device, >= flash_gau_forward_host_workspace_bytes(...)
+ *              bytes, 256-byte aligned: device copies of X and O, then the
+ *              layer's workspace for one part of the batch
+ * Other arguments and return values as for flash_gau_forward.             */
+size_t flash_gau_forward_host_workspace_bytes(int B, int T, int C,
+                                              const flash_gau_weights *w,
+                                              int causal, int dtype);
+int flash_gau_forward_host(const void *X_host, const flash_gau_weights *w,
+                           int B, int T, int C, int causal, int dtype,
+                           void *out_host, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
 /* ---- segment masks (packed text) -------------------------------------- */
 /* The global term with a chunk mask ("Transformer Quality in Linear Time",
  * Paper vs code, the segment-mask item; Pitfalls, the same item): segment
