@@ -528,8 +528,9 @@ def run_ours(args, rank, world, local_rank):
                 "fp32_core_peak_tflops": round(FP32_CORE_PEAK_TFLOPS, 1)},
             "decode": dict(
                 what="autoregressive decode step at the workload's widths (C = 256, causal): "
-                     "B sequences, one token each per step, 2C steps; four kernels per step "
-                     "(projection, chunk attention with the linear cache, output, cache fold)",
+                     "B sequences, one token each per step, 2C steps; five kernels per step "
+                     "(projection, chunk weights, chunk attention with the linear cache, "
+                     "output, cache fold)",
                 **decode),
             "global_only": dict(
                 what="the layer with the local term switched off (local_scale = 0): "

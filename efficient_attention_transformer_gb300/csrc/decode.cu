@@ -1,23 +1,27 @@
 // Autoregressive decode step of the FLASH GAU layer: one new token for each
 // of B sequences, in constant work per token ("Transformer Quality in
-// Linear Time", §3.2.1: "the linear cache is one matrix and the local
-// attention is limited to one chunk").  Per sequence the state holds
+// Linear Time", §3.2.1: decoding keeps the global term as a single running
+// matrix and attends locally within the current chunk only).  Per sequence
+// the state holds
 //   pos      tokens consumed so far (the new one sits at i = pos mod C of
 //            its chunk)
 //   Prefix   [s, e] fp32, the sum of K_lin^T V over completed chunks
 //   caches   the current chunk's K_quad, K_lin [C, s] and V [C, e] rows
-// and a step runs four launches, chained by programmatic dependent launch:
+// and a step runs five launches, chained by programmatic dependent launch:
 //   project  x W_uvz in depth slices (pos += 1)
-//   attend   u, v, z = swish(sum of the slices), the four heads;
+//   scores   z = swish(sum of the Z slices), the four heads, and
 //            a_j = relu(q_quad . k_quad_j / C + relpos[j - i + C - 1])^2
-//            (j <= i), vhat = sum_j a_j v_j + lin_scale q_lin Prefix,
-//            gated = u * vhat; the token's rows go into the caches
+//            (j <= i), once per sequence
+//   attend   u, v = swish(sum of the slices); vhat = sum_j a_j v_j +
+//            lin_scale q_lin Prefix, gated = u * vhat; the token's rows go
+//            into the caches
 //   output   gated W_o in depth slices
 //   finish   out = the slices' sum; at a chunk's last token
 //            Prefix += K_lin,chunk^T V_chunk
 // The projections stream the weights once per step for all B sequences
 // (split-K matrix-vector products on the CUDA cores with 16-byte weight
-// loads); everything is fp32 inside.
+// loads); everything is fp32 inside.  The step is latency-bound: the
+// kernels keep several independent loads in flight per thread.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
@@ -131,18 +135,83 @@ gemv_splitk(const Tx *__restrict__ x, int B, const Tw *__restrict__ W, int K, in
   }
 }
 
+// The chunk weights of the new token, once per sequence: block (32-key
+// tile, sequence), 8 warps of 4 keys each.  Each block forms z = swish of
+// the projection's Z slices and the two quadratic heads it needs; block 0
+// of a sequence also stores all four heads for the attend kernel.  A warp
+// issues the loads of its 4 cached key rows together, then reduces the 4
+// dot products; a_j = local_scale relu(q_quad . k_quad_j / C +
+// relpos[j - i + C - 1])^2 for j <= i (key i is the new token's own).
+constexpr int kKeyTile = 32;
+constexpr int kMaxS = 256;
+__global__ void __launch_bounds__(256)
+decode_scores(DecodeLayout L, const float *__restrict__ gamma, const float *__restrict__ beta,
+              const float *__restrict__ relpos, int B, int C, int e, int s, int slices,
+              float local_scale) {
+  __shared__ float qq[kMaxS], kq_new[kMaxS];
+  griddep_launch_dependents();
+  griddep_wait();
+  const int b = blockIdx.y, j0 = blockIdx.x * kKeyTile;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int N = 2 * e + s;
+  const int i = (L.pos[b] - 1) % C;
+  if (j0 > i && blockIdx.x != 0) return;
+  const float *yp = L.proj + (long long)b * N;
+  const long long sstride = (long long)B * N;
+  for (int k = threadIdx.x; k < s; k += blockDim.x) {
+    float pz = 0.f;
+    for (int q = 0; q < slices; ++q) pz += yp[q * sstride + 2 * e + k];
+    const float z = swish(pz);
+    qq[k] = fmaf(z, gamma[k], beta[k]);
+    kq_new[k] = fmaf(z, gamma[s + k], beta[s + k]);
+    if (blockIdx.x == 0)
+      for (int h = 0; h < 4; ++h)
+        L.heads[((long long)b * 4 + h) * s + k] = fmaf(z, gamma[h * s + k], beta[h * s + k]);
+  }
+  __syncthreads();
+  if (j0 > i) return;
+  const float *kq_c = L.kq + (long long)b * C * s;
+  const float inv_c = 1.0f / (float)C;
+  constexpr int KW = kKeyTile / 8;  // keys per warp
+  constexpr int MS = kMaxS / 32;    // key elements per lane
+  float kv[KW][MS];
+#pragma unroll
+  for (int t = 0; t < KW; ++t) {
+    const int j = j0 + warp * KW + t;
+#pragma unroll
+    for (int m = 0; m < MS; ++m) {
+      const int k = lane + 32 * m;
+      kv[t][m] = 0.f;
+      if (j <= i && k < s) kv[t][m] = j < i ? kq_c[(long long)j * s + k] : kq_new[k];
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < KW; ++t) {
+    const int j = j0 + warp * KW + t;
+    float dot = 0.f;
+#pragma unroll
+    for (int m = 0; m < MS; ++m) {
+      const int k = lane + 32 * m;
+      if (k < s) dot = fmaf(qq[k], kv[t][m], dot);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0 && j <= i) {
+      const float r = fmaxf(fmaf(dot, inv_c, relpos[j - i + C - 1]), 0.f);
+      L.score[(long long)b * C + j] = local_scale * r * r;
+    }
+  }
+}
+
 // one block per (32 value columns, sequence), 8 warps: gathers the
-// projection's slices into the heads and this block's U and V columns, then
-// (warp w taking keys j = w, w + 8, .. and linear-cache rows k = w, w + 8, ..;
-// lanes the columns) the chunk-local weights, their sum over the cached V
-// rows, the linear term and the gate; the warps' sums meet in a fixed order
+// projection's slices into this block's U and V columns, then (warp w
+// taking keys j = w, w + 8, .. and linear-cache rows k = w, w + 8, ..;
+// lanes the columns) the weighted sum of the cached V rows, the linear
+// term and the gate; the warps' sums meet in a fixed order
 constexpr int kAttW = 8;
 __global__ void __launch_bounds__(32 * kAttW)
-decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__restrict__ beta,
-              const float *__restrict__ relpos, int B, int C, int e, int s, int slices,
-              float lin_scale, float local_scale) {
-  extern __shared__ float dsm[];
-  float *sh = dsm, *sa = dsm + 4 * s, *red = sa + C;  // heads [4][s], weights [C], [8][32]
+decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_scale) {
+  __shared__ float red[kAttW * 32];
   griddep_launch_dependents();
   griddep_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -150,32 +219,10 @@ decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__re
   const int N = 2 * e + s;
   const int i = (L.pos[b] - 1) % C;
   const float *yp = L.proj + (long long)b * N;
-  const long long sstride = (long long)B * N;  // between slices
-  for (int k = threadIdx.x; k < s; k += blockDim.x) {
-    float pz = 0.f;
-    for (int q = 0; q < slices; ++q) pz += yp[q * sstride + 2 * e + k];
-    const float z = swish(pz);
-    for (int h = 0; h < 4; ++h) sh[h * s + k] = fmaf(z, gamma[h * s + k], beta[h * s + k]);
-  }
-  __syncthreads();
-  const float *qq = sh, *kq_new = sh + s, *ql = sh + 2 * s, *kl_new = sh + 3 * s;
-  float *kq_c = L.kq + (long long)b * C * s, *kl_c = L.kl + (long long)b * C * s;
+  const long long sstride = (long long)B * N;
+  const float *ql = L.heads + ((long long)b * 4 + 2) * s;
+  const float *sa = L.score + (long long)b * C;
   float *v_c = L.vc + (long long)b * C * e;
-  // weights of the chunk's keys 0 .. i (key i is the new token's): one key
-  // per warp at a time, the lanes splitting its s products
-  const float inv_c = 1.0f / (float)C;
-  for (int j = warp; j <= i; j += kAttW) {
-    const float *kr = j < i ? kq_c + (long long)j * s : kq_new;
-    float dot = 0.f;
-    for (int k = lane; k < s; k += 32) dot = fmaf(qq[k], kr[k], dot);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (lane == 0) {
-      const float r = fmaxf(fmaf(dot, inv_c, relpos[j - i + C - 1]), 0.f);
-      sa[j] = local_scale * r * r;
-    }
-  }
-  __syncthreads();
   float pu = 0.f, pv = 0.f;
   if (c < e)
     for (int q = 0; q < slices; ++q) {
@@ -185,14 +232,32 @@ decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__re
   const float u = swish(pu), vnew = swish(pv);
   float acc = 0.f;
   if (c < e) {
-#pragma unroll 4
-    for (int j = warp; j < i; j += kAttW) acc = fmaf(sa[j], v_c[(long long)j * e + c], acc);
-    if (i % kAttW == warp) acc = fmaf(sa[i], vnew, acc);
-    float lin = 0.f;
+    // eight independent loads in flight per lane, one accumulator each
+    float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j0 = warp; j0 < i; j0 += 8 * kAttW) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kAttW;
+        if (j < i) a8[u] = fmaf(sa[j], v_c[(long long)j * e + c], a8[u]);
+      }
+    }
+    if (i % kAttW == warp) a8[0] = fmaf(sa[i], vnew, a8[0]);
+    float lin[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const float *pre = L.prefix + (long long)b * s * e + c;
-#pragma unroll 4
-    for (int k = warp; k < s; k += kAttW) lin = fmaf(ql[k], pre[(long long)k * e], lin);
-    acc = fmaf(lin_scale, lin, acc);
+    for (int k0 = warp; k0 < s; k0 += 8 * kAttW) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * kAttW;
+        if (k < s) lin[u] = fmaf(ql[k], pre[(long long)k * e], lin[u]);
+      }
+    }
+    float l = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      acc += a8[t];
+      l += lin[t];
+    }
+    acc = fmaf(lin_scale, l, acc);
   }
   red[warp * 32 + lane] = acc;
   __syncthreads();
@@ -203,25 +268,30 @@ decode_attend(DecodeLayout L, const float *__restrict__ gamma, const float *__re
     L.gated[(long long)b * e + c] = u * v;
     v_c[(long long)i * e + c] = vnew;  // the token's row, for the chunk's later keys
   }
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
+    const float *h = L.heads + (long long)b * 4 * s;
+    float *kq_c = L.kq + (long long)b * C * s, *kl_c = L.kl + (long long)b * C * s;
     for (int k = threadIdx.x; k < s; k += blockDim.x) {
-      kq_c[(long long)i * s + k] = kq_new[k];
-      kl_c[(long long)i * s + k] = kl_new[k];
+      kq_c[(long long)i * s + k] = h[s + k];
+      kl_c[(long long)i * s + k] = h[3 * s + k];
     }
+  }
 }
 
 // the output's slices into out (io type): blocks with blockIdx.y == 0, one
 // thread per column; and, at a chunk's last token,
-// Prefix += K_lin,chunk^T V_chunk: one thread per (k, c) element, blocks
-// (256 columns, k, sequence)
+// Prefix += K_lin,chunk^T V_chunk: one thread per column c for kFoldRows
+// rows k, blocks (256 columns, row group, sequence).  Away from a chunk's
+// end the row-group blocks return at once, so there are few of them.
+constexpr int kFoldRows = 16;
 template <typename T>
 __global__ void __launch_bounds__(256)
 decode_finish(DecodeLayout L, T *__restrict__ out, int B, int C, int d, int e, int s, int slices) {
   griddep_launch_dependents();
   griddep_wait();
-  const int b = blockIdx.z, k = blockIdx.y;
+  const int b = blockIdx.z, k0 = blockIdx.y * kFoldRows;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k == 0 && c < d) {
+  if (blockIdx.y == 0 && c < d) {
     float v = 0.f;
 #pragma unroll 4
     for (int q = 0; q < slices; ++q) v += L.outp[((long long)q * B + b) * d + c];
@@ -229,10 +299,19 @@ decode_finish(DecodeLayout L, T *__restrict__ out, int B, int C, int d, int e, i
   }
   if ((L.pos[b] - 1) % C != C - 1 || c >= e) return;
   const float *kl_c = L.kl + (long long)b * C * s, *v_c = L.vc + (long long)b * C * e;
-  float acc = 0.f;
-#pragma unroll 4
-  for (int j = 0; j < C; ++j) acc = fmaf(kl_c[(long long)j * s + k], v_c[(long long)j * e + c], acc);
-  L.prefix[((long long)b * s + k) * e + c] += acc;
+  const int k1 = k0 + kFoldRows < s ? k0 + kFoldRows : s;
+  float acc[kFoldRows];
+#pragma unroll
+  for (int t = 0; t < kFoldRows; ++t) acc[t] = 0.f;
+  for (int j = 0; j < C; ++j) {
+    const float v = v_c[(long long)j * e + c];
+#pragma unroll
+    for (int t = 0; t < kFoldRows; ++t)
+      if (k0 + t < k1) acc[t] = fmaf(kl_c[(long long)j * s + k0 + t], v, acc[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < kFoldRows; ++t)
+    if (k0 + t < k1) L.prefix[((long long)b * s + k0 + t) * e + c] += acc[t];
 }
 
 template <typename T>
@@ -241,16 +320,13 @@ cudaError_t step(const DecodeProblem &q) {
   const int N = 2 * q.e + q.s;
   const int sp = decode_slices(q.d, N), so = decode_slices(q.e, q.d);
   const int ksp = (q.d + sp - 1) / sp, kso = (q.e + so - 1) / so;
-  const size_t smem_a = sizeof(float) * (4 * (size_t)q.s + q.C + 32 * kAttW);
+
   static unsigned long long configured = 0;  // shared-memory ceilings, per device
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev >= 64) return cudaErrorInvalidDevice;
   if (!(configured & (1ull << dev))) {
-    if ((err = cudaFuncSetAttribute(decode_attend, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(sizeof(float) * (4 * 256 + 4096 + 32 * kAttW)))) !=
-            cudaSuccess ||
-        (err = cudaFuncSetAttribute(gemv_splitk<T, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((err = cudaFuncSetAttribute(gemv_splitk<T, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kGemvSmem)) != cudaSuccess ||
         (err = cudaFuncSetAttribute(gemv_splitk<float, T>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -263,15 +339,20 @@ cudaError_t step(const DecodeProblem &q) {
                         q.stream, (const T *)q.x, q.B, (const T *)q.W_uvz, q.d, N, ksp, q.L.proj,
                         q.L.pos)) != cudaSuccess)
     return err;
-  if ((err = launch_pdl(decode_attend, dim3((q.e + 31) / 32, q.B), dim3(32 * kAttW), smem_a, q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
-                        q.lin_scale, q.local_scale)) != cudaSuccess)
+  if ((err = launch_pdl(decode_scores, dim3((q.C + kKeyTile - 1) / kKeyTile, q.B), dim3(256), 0,
+                        q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
+                        q.local_scale)) != cudaSuccess)
+    return err;
+  if ((err = launch_pdl(decode_attend, dim3((q.e + 31) / 32, q.B), dim3(32 * kAttW), 0, q.stream,
+                        q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale)) != cudaSuccess)
     return err;
   if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so), dim3(256),
                         kGemvSmem, q.stream, (const float *)q.L.gated, q.B, (const T *)q.W_o, q.e, q.d,
                         kso, q.L.outp, (int *)nullptr)) != cudaSuccess)
     return err;
   const int fx = ((q.e > q.d ? q.e : q.d) + 255) / 256;
-  return launch_pdl(decode_finish<T>, dim3(fx, q.s, q.B), dim3(256), 0, q.stream,
+  return launch_pdl(decode_finish<T>, dim3(fx, (q.s + kFoldRows - 1) / kFoldRows, q.B),
+                    dim3(256), 0, q.stream,
                     q.L, (T *)q.out, q.B, q.C, q.d, q.e, q.s, so);
 }
 

@@ -185,7 +185,7 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
     *p = base ? base + off : nullptr;
     off = align_up(off + bytes);
   };
-  void *st, *pos, *pre, *kq, *kl, *vc, *proj, *g, *outp;
+  void *st, *pos, *pre, *kq, *kl, *vc, *proj, *g, *outp, *hd, *sc;
   const size_t f = sizeof(float);
   take(&st, sizeof(int));
   take(&pos, (size_t)B * sizeof(int));
@@ -196,6 +196,8 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
   take(&proj, sp * B * N * f);
   take(&g, (size_t)B * e * f);
   take(&outp, so * B * d * f);
+  take(&hd, (size_t)B * 4 * s * f);
+  take(&sc, (size_t)B * C * f);
   if (L) {
     L->status = (int *)st;
     L->pos = (int *)pos;
@@ -206,6 +208,8 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
     L->proj = (float *)proj;
     L->gated = (float *)g;
     L->outp = (float *)outp;
+    L->heads = (float *)hd;
+    L->score = (float *)sc;
   }
   *total = off;
   return FLASH_GAU_OK;

@@ -125,6 +125,8 @@ struct DecodeLayout {
   float *proj;     // [slices, B, 2e+s] this step's x W_uvz, by depth slice
   float *gated;    // [B, e]
   float *outp;     // [slices, B, d] this step's gated W_o, by depth slice
+  float *heads;    // [B, 4, s] this step's four heads
+  float *score;    // [B, C] this step's chunk weights a_j (local_scale included)
 };
 // Depth slices of the decode step's split-K matrix-vector product with a
 // [K, N] weight: about 150 blocks of 256 columns x one slice, at most 128
