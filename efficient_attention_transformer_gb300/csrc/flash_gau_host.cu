@@ -91,7 +91,7 @@ int flash_gau_forward_host(const void *X_host, const flash_gau_weights *w, int B
   size_t xb = 0, fwd = 0;
   const size_t need = host_bytes(B, T, C, w, causal, dtype, &xb, &fwd);
   if (need == 0) {
-    // the same verdict as the device-buffer forward for these arguments
+    // the same status as the device-buffer forward for these arguments
     flash_gau_workspace_layout L;
     const int st = flash_gau_workspace_layout_query(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
     return st != FLASH_GAU_OK ? st : FLASH_GAU_EINVAL;

@@ -181,7 +181,7 @@ __device__ bool scan_states(const GemmParams &p, uint8_t *buf, int buf_bytes, Sm
         bulk_load(smem_u32(buf + (size_t)g * wc * 16), p.state8 + (b * p.G + g) * p.se8 + r0,
                   (uint32_t)(wc * 16), bar);
     }
-    // one thread waits; every thread sees its verdict after the barrier
+    // one thread waits; every thread sees the outcome after the barrier
     if (threadIdx.x == 0 && !mbar_wait(bar, phase, &sm->abort_flag)) raise_timeout(sm, p.status);
     __syncthreads();
     if (sm->abort_flag) return false;

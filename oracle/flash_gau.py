@@ -157,8 +157,8 @@ def rope(h, positions, base=10000.0):
     """Rotary position embedding of the last axis (s even): the pair
     (h[2i], h[2i+1]) of the vector at position p is rotated by the angle
     p * base^(-2i/s).  [TQLT] flash_block pseudocode: RoPE on the four heads,
-    "over the whole sequence, not restarted per chunk"; [FLASH-blog]: the
-    models use RoPE.
+    with positions counted along the whole sequence rather than from the
+    start of each chunk; [FLASH-blog]: the models use RoPE.
 
     h: [..., T, s]; positions: [T] (one position per row of h)."""
     h = np.asarray(h, dtype=np.float64)
