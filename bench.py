@@ -158,6 +158,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of each rank's floats over the process group (the
+    slowest rank sets a job's time); the values themselves when no group of
+    more than one rank is running."""
+    import torch
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: the tokens every rank processed over the
+    slowest rank's time (ms)."""
+    return tokens_per_rank * world / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import efficient_attention_transformer_gb300 as fg
@@ -236,10 +255,7 @@ def run_ours(args, rank, world, local_rank):
         split_ms += evs[k][0].elapsed_time(evs[k][nst])
     per_stage /= args.steps
     split_ms /= args.steps
-    if world > 1:
-        t = torch.tensor([step_ms, wall], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms, wall = float(t[0]), float(t[1])
+    step_ms, wall = max_over_ranks([step_ms, wall], dev)
 
     # ---- end to end: pinned host X in, O out, through the host-buffer entry
     # point (flash_gau_forward_host: its copies of one part of the batch
@@ -267,10 +283,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
 
     # ---- next row: the flash_block wrapper (LayerNorm, RoPE on the four heads,
     # residual) around the same layer on the same workload, timed the same way
@@ -299,10 +312,7 @@ def run_ours(args, rank, world, local_rank):
     block_ms = sum(a.elapsed_time(b) for a, b in zip(b0, b1)) / blk_steps
     if bd.workspace_status(ws) != 0:
         raise RuntimeError("kernel status after the flash_block runs")
-    if world > 1:
-        t = torch.tensor([block_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        block_ms = float(t[0])
+    (block_ms,) = max_over_ranks([block_ms], dev)
 
     # ---- next row: the two ablations of the mixed chunk attention on the
     # same workload and weights: GlobalOnly (local term off: no chunk scores
@@ -323,11 +333,12 @@ def run_ours(args, rank, world, local_rank):
             bd.forward(X, wv, C, causal, out=out, workspace=ws, stream=stream)
             a1[k].record(stream)
         torch.cuda.synchronize()
-        ab_ms = sum(x.elapsed_time(y) for x, y in zip(a0, a1)) / blk_steps
+        (ab_ms,) = max_over_ranks([sum(x.elapsed_time(y) for x, y in zip(a0, a1)) / blk_steps],
+                                  dev)
         if bd.workspace_status(ws) != 0:
             raise RuntimeError("kernel status after the %s runs" % name)
         ablations[name] = {"ms_per_step": round(ab_ms, 5),
-                           "value": round(B * T * world / (ab_ms * 1e-3), 1),
+                           "value": round(job_tokens_per_s(B * T, world, ab_ms), 1),
                            "unit": "tokens/s"}
         del wv
 
@@ -354,7 +365,7 @@ def run_ours(args, rank, world, local_rank):
         seg_step()
         s1[k].record(stream)
     torch.cuda.synchronize()
-    seg_ms = sum(x.elapsed_time(y) for x, y in zip(s0, s1)) / blk_steps
+    (seg_ms,) = max_over_ranks([sum(x.elapsed_time(y) for x, y in zip(s0, s1)) / blk_steps], dev)
     if bd.workspace_status(ws) != 0:
         raise RuntimeError("kernel status after the segmented runs")
 
@@ -390,7 +401,7 @@ def run_ours(args, rank, world, local_rank):
         bd.backward(X, dO, weights, C, causal, workspace=bws, stream=stream)
     be1.record(stream)
     torch.cuda.synchronize()
-    backward_ms = be0.elapsed_time(be1) / bn
+    (backward_ms,) = max_over_ranks([be0.elapsed_time(be1) / bn], dev)
     del bws
 
     # ---- next row: autoregressive decode at the workload's widths, B
@@ -475,7 +486,7 @@ def run_ours(args, rank, world, local_rank):
     layer_tflops = total_flops / (step_ms * 1e-3) / 1e12
     res = {
         "metric": METRIC,
-        "value": round(tokens / (step_ms * 1e-3), 1),
+        "value": round(job_tokens_per_s(B * T, world, step_ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -503,7 +514,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": nst * args.steps,
         "wall_ms_per_step_incl_flush": round(wall * 1e3 / args.steps, 4),
         "ms_per_step_with_stage_events": round(split_ms, 5),
-        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(B * T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(X.numel() * X.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
                 "ms_per_step": round(e2e_ms, 5)},
