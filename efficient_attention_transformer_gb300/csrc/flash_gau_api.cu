@@ -518,7 +518,7 @@ int flash_gau_decode_step(const void *x, const flash_gau_weights *w, int B, int 
   int st = decode_layout(B, C, w->d, w->e, w->s, static_cast<char *>(state), &q.L, &total);
   if (st != FLASH_GAU_OK) return st;
   if (state_bytes < total) return FLASH_GAU_EWORKSPACE;
-  int num_sms = 0;
+  int num_sms = 0;  // the device check
   if ((st = device_info(&num_sms)) != FLASH_GAU_OK) return st;
   q.B = B;
   q.C = C;
