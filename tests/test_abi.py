@@ -160,3 +160,35 @@ def test_non_finite_term_factors_rejected_before_any_launch(L, lin, loc):
                                 ctypes.byref(g), 256, ws, None) == bd.EINVAL
     assert L.flash_gau_decode_step(16, ctypes.byref(w), 1, 64, bd.FP32, 256, ws, 1 << 40,
                                    None) == bd.EINVAL
+
+
+def test_product_and_oracle_share_no_code():
+    """The CUDA path never imports the oracle, and the oracle never imports
+    the package: the two sides share only the seeded input generator."""
+    pkg = os.path.join(ROOT, "efficient_attention_transformer_gb300")
+    pat = re.compile(r"^\s*(from\s+oracle\b|import\s+oracle\b)", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f), errors="replace").read()
+                assert not pat.search(text), f
+                assert "oracle/" not in text, f
+    opat = re.compile(r"efficient_attention_transformer_gb300\.(?!synthetic)")
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith(".py"):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert not opat.search(text), f
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without the built library every entry point raises; nothing falls
+    back to a CPU computation."""
+    import torch
+    monkeypatch.setattr(bd, "_LIB_PATH", os.path.join(ROOT, "no_such_dir", "libflashgau.so"))
+    monkeypatch.setattr(bd, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        bd.lib()
+    # host tensors are refused as weights: there is no CPU path to take them
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        bd.GauWeights(torch.zeros(64, 288), torch.zeros(128, 64), torch.zeros(4, 32),
+                      torch.zeros(4, 32), torch.zeros(127), 64, 128, 32)
