@@ -44,6 +44,22 @@ __device__ __forceinline__ float swish_grad(float x) {
   return sg * (1.0f + x * (1.0f - sg));
 }
 
+// four bf16 values as floats, and back (8-byte accesses)
+struct Bf4 {
+  __nv_bfloat162 a, b;
+};
+__device__ __forceinline__ float4 load_bf4(const __nv_bfloat16 *p) {
+  const Bf4 v = *reinterpret_cast<const Bf4 *>(p);
+  const float2 x = __bfloat1622float2(v.a), y = __bfloat1622float2(v.b);
+  return make_float4(x.x, x.y, y.x, y.y);
+}
+__device__ __forceinline__ void store_bf4(__nv_bfloat16 *p, float a, float b, float c, float d) {
+  Bf4 v;
+  v.a = __floats2bfloat162_rn(a, b);
+  v.b = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<Bf4 *>(p) = v;
+}
+
 // ------------------------------------------------------------------ GEMM --
 // C[z](m, n) = sum_k A[z / adiv](m, k) B[z / bdiv](k, n), handed to the
 // epilogue per element.  Element strides: A(m, k) at m * sam + k * sak, B(k,
@@ -218,20 +234,28 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
 // the scores from the raw products R = Qq Kq^T of chunk z (in place):
 // S = R / C + relpos[j - i + C - 1], and P = relu(S)^2 (zero above the
 // diagonal when causal) as a bf16 operand
-// (blocks along y take the rows z*C + i of the [B*G*C, C] score matrices)
+// Four columns per thread (C a multiple of 4), over the rows z*C + i of the
+// [B*G*C, C] score matrices.
 __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_io,
                           const float *__restrict__ relpos, long long rows, int C, int causal,
                           float inv_c) {
-  for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
-  const int i = (int)(row % C);
-  const float *rp = relpos + C - 1 - i;  // + j
-  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < C; j += gridDim.x * blockDim.x) {
-    const long long o = row * C + j;
-    const float v = fmaf(S[o], inv_c, rp[j]);
-    S[o] = v;
-    const float r = fmaxf(v, 0.f);
-    P_io[o] = __float2bfloat16_rn((causal && j > i) ? 0.f : r * r);
-  }
+  const int C4 = C / 4;
+  for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < rows * C4;
+       q += (long long)gridDim.x * blockDim.x) {
+    const long long row = q / C4;
+    const int j = 4 * (int)(q - row * C4), i = (int)(row % C);
+    float4 v = reinterpret_cast<float4 *>(S)[q];
+    const float *rp = relpos + C - 1 - i + j;
+    v.x = fmaf(v.x, inv_c, rp[0]);
+    v.y = fmaf(v.y, inv_c, rp[1]);
+    v.z = fmaf(v.z, inv_c, rp[2]);
+    v.w = fmaf(v.w, inv_c, rp[3]);
+    reinterpret_cast<float4 *>(S)[q] = v;
+    const float r0 = fmaxf(v.x, 0.f), r1 = fmaxf(v.y, 0.f), r2 = fmaxf(v.z, 0.f),
+                r3 = fmaxf(v.w, 0.f);
+    const bool m = causal != 0;
+    store_bf4(P_io + 4LL * q, (m && j > i) ? 0.f : r0 * r0, (m && j + 1 > i) ? 0.f : r1 * r1,
+              (m && j + 2 > i) ? 0.f : r2 * r2, (m && j + 3 > i) ? 0.f : r3 * r3);
   }
 }
 
@@ -272,7 +296,8 @@ __global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ dr
     if (bins[k] != 0.f) atomicAdd(drelpos + k, bins[k]);
 }
 
-// prefix[b][g] = lin_scale * (exclusive sum over chunks, or the total)
+// prefix[b][g] = lin_scale * (exclusive sum over chunks, or the total), in
+// fp32 when prefix is set and as bf16 when prefix_io is
 __global__ void scan_forward(const float *__restrict__ state, float *__restrict__ prefix, int B,
                              int G, long long se, int causal, float lin_scale,
                              __nv_bfloat16 *__restrict__ prefix_io) {
@@ -283,13 +308,13 @@ __global__ void scan_forward(const float *__restrict__ state, float *__restrict_
     for (int g = 0; g < G; ++g) {
       if (causal) {
         const long long o = (b * G + g) * se + r;
-        prefix[o] = lin_scale * run;
+        if (prefix) prefix[o] = lin_scale * run;
         if (prefix_io) prefix_io[o] = __float2bfloat16_rn(lin_scale * run);
       }
       run += state[(b * G + g) * se + r];
     }
     if (!causal) {
-      prefix[b * se + r] = lin_scale * run;
+      if (prefix) prefix[b * se + r] = lin_scale * run;
       if (prefix_io) prefix_io[b * se + r] = __float2bfloat16_rn(lin_scale * run);
     }
   }
@@ -334,31 +359,48 @@ __global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long 
 }
 
 // dZ = sum_k dH_k * gamma_k; dgamma, dbeta as column sums of dH_k * Z, dH_k
-// (per block partial sums over its rows, added atomically)
-__global__ void heads_grad(const float *__restrict__ dH, const float *__restrict__ Z,
-                           const float *__restrict__ gamma, float *__restrict__ dZ,
-                           float *__restrict__ dgamma, float *__restrict__ dbeta, long long M,
-                           int s, int rows_per_block) {
+// (per block partial sums over its rows, added atomically; 256 threads)
+__global__ void __launch_bounds__(256)
+heads_grad(const float *__restrict__ dH, const float *__restrict__ Z,
+           const float *__restrict__ gamma, float *__restrict__ dZ, float *__restrict__ dgamma,
+           float *__restrict__ dbeta, long long M, int s, int rows_per_block) {
+  // two row parities x 128 columns; the parities meet in shared memory
+  __shared__ float red[8][128];
+  const int par = threadIdx.x / 128, cl = threadIdx.x % 128;
   const long long r0 = (long long)blockIdx.x * rows_per_block;
   const long long r1 = r0 + rows_per_block < M ? r0 + rows_per_block : M;
-  for (int c = threadIdx.x; c < s; c += blockDim.x) {
-    float g[4], bsum[4] = {0.f, 0.f, 0.f, 0.f}, gsum[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < 4; ++k) g[k] = gamma[k * s + c];
-    for (long long m = r0; m < r1; ++m) {
-      const float z = Z[m * s + c];
-      float dz = 0.f;
-      for (int k = 0; k < 4; ++k) {
-        const float dh = dH[((long long)k * M + m) * s + c];
-        dz = fmaf(dh, g[k], dz);
-        gsum[k] = fmaf(dh, z, gsum[k]);
-        bsum[k] += dh;
+  for (int c0 = 0; c0 < s; c0 += 128) {
+    const int c = c0 + cl;
+    float bsum[4] = {0.f, 0.f, 0.f, 0.f}, gsum[4] = {0.f, 0.f, 0.f, 0.f};
+    if (c < s) {
+      float g[4];
+      for (int k = 0; k < 4; ++k) g[k] = gamma[k * s + c];
+#pragma unroll 4
+      for (long long m = r0 + par; m < r1; m += 2) {
+        const float z = Z[m * s + c];
+        float dz = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float dh = dH[((long long)k * M + m) * s + c];
+          dz = fmaf(dh, g[k], dz);
+          gsum[k] = fmaf(dh, z, gsum[k]);
+          bsum[k] += dh;
+        }
+        dZ[m * s + c] = dz;
       }
-      dZ[m * s + c] = dz;
     }
-    for (int k = 0; k < 4; ++k) {
-      atomicAdd(dgamma + k * s + c, gsum[k]);
-      atomicAdd(dbeta + k * s + c, bsum[k]);
-    }
+    if (par == 1)
+      for (int k = 0; k < 4; ++k) {
+        red[k][cl] = gsum[k];
+        red[4 + k][cl] = bsum[k];
+      }
+    __syncthreads();
+    if (par == 0 && c < s)
+      for (int k = 0; k < 4; ++k) {
+        atomicAdd(dgamma + k * s + c, gsum[k] + red[k][cl]);
+        atomicAdd(dbeta + k * s + c, bsum[k] + red[4 + k][cl]);
+      }
+    __syncthreads();
   }
 }
 
@@ -413,20 +455,6 @@ __device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x
 __device__ __forceinline__ float swish_grad_fast(float x) {
   const float sg = sigmoid_fast(x);
   return sg * (1.0f + x * (1.0f - sg));
-}
-struct Bf4 {
-  __nv_bfloat162 a, b;
-};
-__device__ __forceinline__ float4 load_bf4(const __nv_bfloat16 *p) {
-  const Bf4 v = *reinterpret_cast<const Bf4 *>(p);
-  const float2 x = __bfloat1622float2(v.a), y = __bfloat1622float2(v.b);
-  return make_float4(x.x, x.y, y.x, y.y);
-}
-__device__ __forceinline__ void store_bf4(__nv_bfloat16 *p, float a, float b, float c, float d) {
-  Bf4 v;
-  v.a = __floats2bfloat162_rn(a, b);
-  v.b = __floats2bfloat162_rn(c, d);
-  *reinterpret_cast<Bf4 *>(p) = v;
 }
 
 __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__restrict__ U,
@@ -624,8 +652,8 @@ cudaError_t run(const BackwardProblem &q) {
   // per chunk z: rows z*C .. of the [M, *] matrices
   if (tcc) {
     BW_TRY(bt(Qq_io, s, 0, Kq_io, s, 1, S, C, C, s, 1, 1.f, 0));  // raw Qq Kq^T
-    score_act<<<rows_grid(C, BG * C), 256, 0, st>>>(S, P_io, q.relpos, BG * C, C, q.causal,
-                                                     1.f / C);
+    score_act<<<blocks_for(BG * C * C / 4), 256, 0, st>>>(S, P_io, q.relpos, BG * C, C, q.causal,
+                                                           1.f / C);
     BW_TRY(bt(P_io, C, 0, V_io, e, 0, Vh, C, e, C, 1, q.local_scale, 0));
     BW_TRY(bt(Kl_io, s, 1, V_io, e, 0, state, s, e, C, 1, 1.f, 0));
   } else {
@@ -636,8 +664,8 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
                 op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
   }
-  scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, prefix, q.B, G, se, q.causal,
-                                                      q.lin_scale, pre_io);
+  scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, tcc ? nullptr : prefix, q.B, G, se,
+                                                      q.causal, q.lin_scale, pre_io);
   // Vh += Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
     BW_TRY(bt(Ql_io, s, 0, pre_io, e, 0, Vh, C, e, s, pdiv, 1.f, 1));
@@ -718,8 +746,8 @@ cudaError_t run(const BackwardProblem &q) {
   // ---- heads
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dgamma, 4 * s);
   zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dbeta, 4 * s);
-  const int rows = 16;
-  heads_grad<<<(unsigned)((M + rows - 1) / rows), 128, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
+  const int rows = 128;
+  heads_grad<<<(unsigned)((M + rows - 1) / rows), 256, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows);
   // ---- input side
   if (tc)
