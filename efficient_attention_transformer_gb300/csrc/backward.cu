@@ -274,6 +274,43 @@ __global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, 
   }
 }
 
+// Tensor-core path: dS = 2 relu(S) dP (zero above the diagonal when causal)
+// as the bf16 operand of the next contractions, and its diagonal sums
+// drelpos[j - i + C - 1] (zeroed first) in one pass.  Four columns per
+// thread (C a multiple of 4); a block takes a contiguous range of rows,
+// bins its values by offset in shared memory and adds its bins to drelpos.
+__global__ void __launch_bounds__(256)
+score_grad_relpos(const float *__restrict__ S, const float *__restrict__ dP,
+                  __nv_bfloat16 *__restrict__ dS_io, float *__restrict__ drelpos, long long rows,
+                  int C, int causal, long long rows_per_block) {
+  extern __shared__ float bins[];  // [2C - 1]
+  for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x) bins[k] = 0.f;
+  __syncthreads();
+  const int C4 = C / 4;
+  const long long r0 = blockIdx.x * rows_per_block;
+  const long long r1 = r0 + rows_per_block < rows ? r0 + rows_per_block : rows;
+  for (long long q = r0 * C4 + threadIdx.x; q < r1 * C4; q += blockDim.x) {
+    const long long row = q / C4;
+    const int j = 4 * (int)(q - row * C4), i = (int)(row % C);
+    const float4 sv = reinterpret_cast<const float4 *>(S)[q];
+    const float4 pv = reinterpret_cast<const float4 *>(dP)[q];
+    const bool m = causal != 0;
+    const float d0 = (m && j > i) ? 0.f : 2.f * fmaxf(sv.x, 0.f) * pv.x;
+    const float d1 = (m && j + 1 > i) ? 0.f : 2.f * fmaxf(sv.y, 0.f) * pv.y;
+    const float d2 = (m && j + 2 > i) ? 0.f : 2.f * fmaxf(sv.z, 0.f) * pv.z;
+    const float d3 = (m && j + 3 > i) ? 0.f : 2.f * fmaxf(sv.w, 0.f) * pv.w;
+    store_bf4(dS_io + 4 * q, d0, d1, d2, d3);
+    float *bk = bins + (j - i + C - 1);
+    if (d0 != 0.f) atomicAdd(bk, d0);
+    if (d1 != 0.f) atomicAdd(bk + 1, d1);
+    if (d2 != 0.f) atomicAdd(bk + 2, d2);
+    if (d3 != 0.f) atomicAdd(bk + 3, d3);
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x)
+    if (bins[k] != 0.f) atomicAdd(drelpos + k, bins[k]);
+}
+
 // drelpos[k] = sum over chunks and over (i, j) with j - i = k - (C - 1).
 // A block takes kRelRows consecutive rows of the [B*G*C, C] matrix dS, reads
 // them along j (coalesced) into 2C - 1 shared bins by offset, then adds its
@@ -708,10 +745,16 @@ cudaError_t run(const BackwardProblem &q) {
                 op(e, 1, (long long)C * e),
                 StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   }
-  score_grad<<<rows_grid(C, BG * C), 256, 0, st>>>(S, dP, BG * C, C, q.causal, dS_io);
   zero_f32<<<(2 * C - 1 + 255) / 256, 256, 0, st>>>(q.drelpos, 2 * C - 1);
-  relpos_grad<<<(unsigned)((BG * C + kRelRows - 1) / kRelRows), 256,
-                (2 * C - 1) * sizeof(float), st>>>(dP, q.drelpos, BG * C, C);
+  if (tcc) {
+    const long long rpb = 32;  // rows per block
+    score_grad_relpos<<<(unsigned)((BG * C + rpb - 1) / rpb), 256, (2 * C - 1) * sizeof(float),
+                        st>>>(S, dP, dS_io, q.drelpos, BG * C, C, q.causal, rpb);
+  } else {
+    score_grad<<<rows_grid(C, BG * C), 256, 0, st>>>(S, dP, BG * C, C, q.causal, nullptr);
+    relpos_grad<<<(unsigned)((BG * C + kRelRows - 1) / kRelRows), 256,
+                  (2 * C - 1) * sizeof(float), st>>>(dP, q.drelpos, BG * C, C);
+  }
   float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;
   if (tcc) {
     BW_TRY(bt(dS_io, C, 0, Kq_io, s, 0, dQq, C, s, C, 1, 1.f / C, 0));
