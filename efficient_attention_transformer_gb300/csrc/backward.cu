@@ -484,10 +484,11 @@ __global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__r
 // The tensor-core path's forms of the two kernels above: Pre comes as bf16
 // (the recompute GEMM's output, in the dPre buffer), four columns per
 // thread (e and s multiples of 4), the sigmoid from the fast exponential
-// and reciprocal (their errors are far below the bf16 rounding of Pre),
+// and division intrinsics (their errors are far below the bf16 rounding of
+// Pre),
 // and only the bf16 operands that the tensor-core contractions read are
 // written besides U and Z.
-__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x); }
 __device__ __forceinline__ float swish_grad_fast(float x) {
   const float sg = sigmoid_fast(x);
