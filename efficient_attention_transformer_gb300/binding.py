@@ -49,6 +49,7 @@ EXPORTED = (
     "flash_gau_forward_segmented",
     "flash_gau_forward_host_workspace_bytes",
     "flash_gau_forward_host",
+    "flash_gau_selftest_bounded_wait",
 )
 
 # Capacity of the static scratch behind flash_gau_forward_noalloc.
@@ -148,6 +149,8 @@ def lib():
         L.flash_gau_forward_host.argtypes = [p, ctypes.POINTER(Weights), i, i, i, i, i, p, p,
                                              sz, p]
         L.flash_gau_forward_host.restype = i
+        L.flash_gau_selftest_bounded_wait.argtypes = [i, p, p]
+        L.flash_gau_selftest_bounded_wait.restype = i
         L.flash_gau_rope_toeplitz_bias.argtypes = [p, p, i, i, ctypes.c_float, p, p]
         L.flash_gau_rope_toeplitz_bias.restype = i
         L.flash_gau_backward_workspace_bytes.argtypes = [i, i, i, ctypes.POINTER(Weights), i, i]

@@ -214,6 +214,18 @@ int flash_gau_block_forward(const void *X, const flash_gau_weights *w,
                             int causal, int dtype, void *out, void *workspace,
                             size_t workspace_bytes, void *stream);
 
+/* ---- diagnostics -------------------------------------------------------- */
+/* Checks that a wait the library's kernels make gives up instead of hanging:
+ * one kernel waits on something that nothing signals, then records
+ * FLASH_GAU_ETIMEOUT.  which = 0 waits on a shared-memory mbarrier (the form
+ * of the TMA and tensor-core pipelines), 1 on a flag in global memory (the
+ * form of the chunk-state kernel's grid barrier).  words: device int[2],
+ * zeroed by the caller; once the stream has run the kernel (about two
+ * seconds, the library's wait limit) words[0] holds FLASH_GAU_ETIMEOUT and
+ * the context stays usable.  Returns FLASH_GAU_OK once queued, or
+ * FLASH_GAU_EINVAL.                                                        */
+int flash_gau_selftest_bounded_wait(int which, int *words, void *stream);
+
 /* ---- host buffers ----------------------------------------------------- */
 /* The forward pass on host memory: X_host [B, T, d] is copied to the
  * device, the layer runs, and O is copied back to out_host [B, T, d] (both
