@@ -453,9 +453,60 @@ def run_ours(args, rank, world, local_rank):
                               "gbs": round((wbytes + sbytes) / (best * 1e-6) / 1e9, 1)}
         del dec, graph
 
+    # ---- the other workloads of the scope table, timed the same way (each
+    # is also a parity case of the GPU tests)
+    others = {}
+    for wname in WORKLOADS:
+        if wname == args.workload:
+            continue
+        ow = dict(WORKLOADS[wname])
+        oi = make_inputs(**ow)
+        otdt = torch.bfloat16 if ow["dtype"] == "bf16" else torch.float32
+        owt = fg.GauWeights(
+            torch.tensor(np.concatenate([oi["W_u"], oi["W_v"], oi["W_z"]], axis=1), dtype=otdt,
+                         device=dev),
+            torch.tensor(oi["W_o"], dtype=otdt, device=dev),
+            torch.tensor(oi["gamma"], dtype=torch.float32, device=dev),
+            torch.tensor(oi["beta"], dtype=torch.float32, device=dev),
+            torch.tensor(oi["relpos"], dtype=torch.float32, device=dev),
+            ow["d"], ow["e"], ow["s"])
+        oX = torch.tensor(oi["X"], dtype=otdt, device=dev)
+        oout = torch.empty_like(oX)
+        ows = owt.new_workspace(ow["B"], ow["T"], ow["C"], ow["causal"], dev)
+        for _ in range(3):
+            flush.fill_(1.0)
+            bd.forward(oX, owt, ow["C"], ow["causal"], out=oout, workspace=ows, stream=stream)
+        on = 20
+        o0 = [torch.cuda.Event(enable_timing=True) for _ in range(on)]
+        o1 = [torch.cuda.Event(enable_timing=True) for _ in range(on)]
+        torch.cuda.synchronize()
+        for k in range(on):
+            flush.fill_(1.0)
+            o0[k].record(stream)
+            bd.forward(oX, owt, ow["C"], ow["causal"], out=oout, workspace=ows, stream=stream)
+            o1[k].record(stream)
+        torch.cuda.synchronize()
+        (oms,) = max_over_ranks([sum(a.elapsed_time(b) for a, b in zip(o0, o1)) / on], dev)
+        if bd.workspace_status(ows) != 0:
+            raise RuntimeError("kernel status after the %s runs" % wname)
+        owork = stage_work(ow)
+        onames = bd.stage_names(owt.dtype, ow["causal"])
+        oflops = sum(owork[n][0] for n in onames)
+        otf = oflops / (oms * 1e-3) / 1e12
+        others[wname] = {"ms_per_step": round(oms, 5),
+                         "value": round(job_tokens_per_s(ow["B"] * ow["T"], world, oms), 1),
+                         "unit": "tokens/s", "tflops": round(otf, 2)}
+        del owt, oX, oout, ows
+
     if rank != 0:
         return None
     peaks = _peaks()
+    for wname, rec in others.items():
+        # fp32 runs on the CUDA cores, bf16 on the tensor cores
+        if WORKLOADS[wname]["dtype"] == "fp32":
+            rec["frac_of_fp32_core_peak"] = round(rec["tflops"] / FP32_CORE_PEAK_TFLOPS, 4)
+        else:
+            rec["frac_of_bf16_peak"] = round(rec["tflops"] / peaks["bf16_tflops"], 4)
     work = stage_work(w)
     tokens = B * T * world
     # the stages this schedule runs (the table also lists the other dtype's)
@@ -555,6 +606,11 @@ def run_ours(args, rank, world, local_rank):
                         "global term = mean of the visible chunk states of the document",
                 "ms_per_step": round(seg_ms, 5),
                 "value": round(tokens / (seg_ms * 1e-3), 1), "unit": "tokens/s"},
+            "other_workloads": dict(
+                what="the scope table's other workloads, same timing (L2 flushed, 20 steps); "
+                     "algorithmic TFLOP/s against the bf16 tensor-core peak, or the fp32 "
+                     "CUDA-core peak for the fp32 one",
+                **others),
             "rope_toeplitz_bias": {
                 "what": "relative-position table of the RoPE bias construction, C = 512, "
                         "128-wide vectors (1023 entries x 64 pairs), back-to-back launches",

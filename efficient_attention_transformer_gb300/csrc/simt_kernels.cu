@@ -51,16 +51,32 @@ simt_gemm(int M, int N, int K, const Tin *__restrict__ A, long long sam,
   A += batch * sab;
   Bm += batch * sbb;
   float acc[4][4] = {};
+  // each thread's share of a k-tile (4 A and 4 B elements), loaded into
+  // registers one k-tile ahead so the loads overlap the products
+  constexpr int kPer = kTile * kTileK / 256;
+  float ra[kPer], rb[kPer];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int idx = threadIdx.x + t * 256;
+      const int kk = idx % kTileK, mm = idx / kTileK;
+      const int gm = m0 + mm, gk = k0 + kk;
+      ra[t] = (gm < M && gk < K) ? to_f(A[gm * sam + gk * sak]) : 0.f;
+      const int nn = idx % kTile, kb = idx / kTile;
+      const int gn = n0 + nn, gk2 = k0 + kb;
+      rb[t] = (gn < N && gk2 < K) ? to_f(Bm[gk2 * sbk + gn * sbn]) : 0.f;
+    }
+  };
+  fetch(0);
   for (int k0 = 0; k0 < K; k0 += kTileK) {
-    for (int idx = threadIdx.x; idx < kTile * kTileK; idx += 256) {
-      int kk = idx % kTileK, mm = idx / kTileK;
-      int gm = m0 + mm, gk = k0 + kk;
-      As[kk][mm] = (gm < M && gk < K) ? to_f(A[gm * sam + gk * sak]) : 0.f;
-      int nn = idx % kTile, kb = idx / kTile;
-      int gn = n0 + nn, gk2 = k0 + kb;
-      Bs[kb][nn] = (gn < N && gk2 < K) ? to_f(Bm[gk2 * sbk + gn * sbn]) : 0.f;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int idx = threadIdx.x + t * 256;
+      As[idx % kTileK][idx / kTileK] = ra[t];
+      Bs[idx / kTile][idx % kTile] = rb[t];
     }
     __syncthreads();
+    if (k0 + kTileK < K) fetch(k0 + kTileK);
 #pragma unroll
     for (int kk = 0; kk < kTileK; ++kk) {
       float a[4], b[4];
@@ -310,15 +326,27 @@ cudaError_t prefix_scan(const Problem &p) {
                     p.seg_ids, p.chunk_average, p.per_chunk);
 }
 
+size_t attention_smem(int s) {
+  const size_t sp = (size_t)s + 1;
+  return sizeof(float) * (kAttRows * sp + kAttKeys * sp + (size_t)kAttRows * (kAttKeys + 1) +
+                          (size_t)kAttKeys * (kAttCols + 1));
+}
+
 template <typename T>
 cudaError_t chunk_attention(const Problem &p) {
-  const int sp = p.s + 1;
-  size_t smem = sizeof(float) * ((size_t)kAttRows * sp + (size_t)kAttKeys * sp +
-                                 (size_t)kAttRows * (kAttKeys + 1) +
-                                 (size_t)kAttKeys * (kAttCols + 1));
-  cudaError_t err = cudaFuncSetAttribute(simt_chunk_attention<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = attention_smem(p.s);
+  // the shared-memory ceiling for the widest head (s = 128), once per device
+  static unsigned long long configured = 0;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured & (1ull << dev))) {
+    err = cudaFuncSetAttribute(simt_chunk_attention<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)attention_smem(128));
+    if (err != cudaSuccess) return err;
+    configured |= 1ull << dev;
+  }
   dim3 grid(cdiv(p.e, kAttCols), cdiv(p.C, kAttRows), p.B * p.G);
   simt_chunk_attention<T><<<grid, 256, smem, p.stream>>>(
       (const T *)p.U, (const T *)p.V, (const T *)p.heads, (const T *)p.prefix, p.relpos,
