@@ -203,19 +203,29 @@ decode_scores(DecodeLayout L, const float *__restrict__ gamma, const float *__re
   }
 }
 
-// one block per (32 value columns, sequence), 8 warps: gathers the
+// one block per (128 value columns, sequence), 8 warps: gathers the
 // projection's slices into this block's U and V columns, then (warp w
 // taking keys j = w, w + 8, .. and linear-cache rows k = w, w + 8, ..;
-// lanes the columns) the weighted sum of the cached V rows, the linear
-// term and the gate; the warps' sums meet in a fixed order
+// each lane 4 consecutive columns, 16-byte loads) the weighted sum of the
+// cached V rows, the linear term and the gate; the warps' sums meet in a
+// fixed order
 constexpr int kAttW = 8;
+constexpr int kAttCols = 128;  // value columns per block: 4 per lane
+__device__ __forceinline__ float4 fma4(float a, float4 v, float4 acc) {
+  return make_float4(fmaf(a, v.x, acc.x), fmaf(a, v.y, acc.y), fmaf(a, v.z, acc.z),
+                     fmaf(a, v.w, acc.w));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 __global__ void __launch_bounds__(32 * kAttW)
 decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_scale) {
-  __shared__ float red[kAttW * 32];
+  __shared__ float4 red[kAttW][32];
   griddep_launch_dependents();
   griddep_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int b = blockIdx.y, c = blockIdx.x * 32 + lane;
+  const int b = blockIdx.y, c = blockIdx.x * kAttCols + lane * 4;  // 4 columns a lane
   const int N = 2 * e + s;
   const int i = (L.pos[b] - 1) % C;
   const float *yp = L.proj + (long long)b * N;
@@ -223,50 +233,57 @@ decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_
   const float *ql = L.heads + ((long long)b * 4 + 2) * s;
   const float *sa = L.score + (long long)b * C;
   float *v_c = L.vc + (long long)b * C * e;
-  float pu = 0.f, pv = 0.f;
-  if (c < e)
+  const bool on = c < e;  // e is a multiple of 8: all 4 columns or none
+  float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pv = pu;
+  if (on)
     for (int q = 0; q < slices; ++q) {
-      pu += yp[q * sstride + c];
-      pv += yp[q * sstride + e + c];
+      pu = add4(pu, *reinterpret_cast<const float4 *>(yp + q * sstride + c));
+      pv = add4(pv, *reinterpret_cast<const float4 *>(yp + q * sstride + e + c));
     }
-  const float u = swish(pu), vnew = swish(pv);
-  float acc = 0.f;
-  if (c < e) {
-    // eight independent loads in flight per lane, one accumulator each
-    float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float4 u = make_float4(swish(pu.x), swish(pu.y), swish(pu.z), swish(pu.w));
+  const float4 vnew = make_float4(swish(pv.x), swish(pv.y), swish(pv.z), swish(pv.w));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (on) {
+    // eight independent 16-byte loads in flight per lane, one accumulator each
+    float4 a8[8], l8[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) a8[t] = l8[t] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = warp; j0 < i; j0 += 8 * kAttW) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u * kAttW;
-        if (j < i) a8[u] = fmaf(sa[j], v_c[(long long)j * e + c], a8[u]);
+      for (int t = 0; t < 8; ++t) {
+        const int j = j0 + t * kAttW;
+        if (j < i)
+          a8[t] = fma4(sa[j], *reinterpret_cast<const float4 *>(v_c + (long long)j * e + c), a8[t]);
       }
     }
-    if (i % kAttW == warp) a8[0] = fmaf(sa[i], vnew, a8[0]);
-    float lin[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (i % kAttW == warp) a8[0] = fma4(sa[i], vnew, a8[0]);
     const float *pre = L.prefix + (long long)b * s * e + c;
     for (int k0 = warp; k0 < s; k0 += 8 * kAttW) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * kAttW;
-        if (k < s) lin[u] = fmaf(ql[k], pre[(long long)k * e], lin[u]);
+      for (int t = 0; t < 8; ++t) {
+        const int k = k0 + t * kAttW;
+        if (k < s)
+          l8[t] = fma4(ql[k], *reinterpret_cast<const float4 *>(pre + (long long)k * e), l8[t]);
       }
     }
-    float l = 0.f;
+    float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-      acc += a8[t];
-      l += lin[t];
+      acc = add4(acc, a8[t]);
+      l = add4(l, l8[t]);
     }
-    acc = fmaf(lin_scale, l, acc);
+    acc = fma4(lin_scale, l, acc);
   }
-  red[warp * 32 + lane] = acc;
+  red[warp][lane] = acc;
   __syncthreads();
-  if (warp == 0 && c < e) {
-    float v = 0.f;
+  if (warp == 0 && on) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kAttW; ++w) v += red[w * 32 + lane];
-    L.gated[(long long)b * e + c] = u * v;
-    v_c[(long long)i * e + c] = vnew;  // the token's row, for the chunk's later keys
+    for (int w = 0; w < kAttW; ++w) v = add4(v, red[w][lane]);
+    *reinterpret_cast<float4 *>(L.gated + (long long)b * e + c) =
+        make_float4(u.x * v.x, u.y * v.y, u.z * v.z, u.w * v.w);
+    // the token's row, for the chunk's later keys
+    *reinterpret_cast<float4 *>(v_c + (long long)i * e + c) = vnew;
   }
   if (blockIdx.x == 0) {
     const float *h = L.heads + (long long)b * 4 * s;
@@ -343,7 +360,8 @@ cudaError_t step(const DecodeProblem &q) {
                         q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
                         q.local_scale)) != cudaSuccess)
     return err;
-  if ((err = launch_pdl(decode_attend, dim3((q.e + 31) / 32, q.B), dim3(32 * kAttW), 0, q.stream,
+  if ((err = launch_pdl(decode_attend, dim3((q.e + kAttCols - 1) / kAttCols, q.B), dim3(32 * kAttW),
+                        0, q.stream,
                         q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale)) != cudaSuccess)
     return err;
   if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so), dim3(256),
