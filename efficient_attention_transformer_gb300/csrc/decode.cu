@@ -71,7 +71,7 @@ __device__ __forceinline__ void load8(const float *W, long long o, float (&w)[8]
 
 // Split-K matrix-vector products: part[slice][b][c] = sum over the slice's
 // ks rows k of x[b][k] W[k][c], for all B sequences.  Block (column tile,
-// slice); a lane owns 8 consecutive columns (16-byte loads of a weight row,
+// slice, group of 8 sequences); a lane owns 8 consecutive columns (16-byte loads of a weight row,
 // 512 coalesced bytes per warp), the warps share the slice's rows, and the
 // warps' sums meet in shared memory.  Consumers add the slices in a fixed
 // order, so the results do not depend on scheduling.
@@ -85,13 +85,15 @@ gemv_splitk(const Tx *__restrict__ x, int B, const Tw *__restrict__ W, int K, in
       reinterpret_cast<float(*)[kGroup][kTileN + 4]>(dsm + kGroup * 128);
   griddep_launch_dependents();
   griddep_wait();  // x comes from the kernel before (or the step before)
-  if (pos && blockIdx.x == 0 && blockIdx.y == 0)
+  if (pos && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
     for (int b = threadIdx.x; b < B; b += blockDim.x) pos[b] += 1;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = blockIdx.x * kTileN + lane * 8;
   const int k0 = blockIdx.y * ks, k1 = min(K, k0 + ks);
   const int rows = (k1 - k0 + kWarps - 1) / kWarps;  // rows per warp
-  for (int b0 = 0; b0 < B; b0 += kGroup) {
+  // this block's group of up to kGroup sequences (the groups run in parallel)
+  {
+    const int b0 = blockIdx.z * kGroup;
     const int nb = min(kGroup, B - b0);
     for (int i = threadIdx.x; i < kGroup * ks; i += blockDim.x) {
       const int b = i / ks, k = i - b * ks;
@@ -351,7 +353,8 @@ cudaError_t step(const DecodeProblem &q) {
       return err;
     configured |= 1ull << dev;
   }
-  if ((err = launch_pdl(gemv_splitk<T, T>, dim3((N + kTileN - 1) / kTileN, sp), dim3(256),
+  const int groups = (q.B + kGroup - 1) / kGroup;
+  if ((err = launch_pdl(gemv_splitk<T, T>, dim3((N + kTileN - 1) / kTileN, sp, groups), dim3(256),
                         kGemvSmem,
                         q.stream, (const T *)q.x, q.B, (const T *)q.W_uvz, q.d, N, ksp, q.L.proj,
                         q.L.pos)) != cudaSuccess)
@@ -364,7 +367,8 @@ cudaError_t step(const DecodeProblem &q) {
                         0, q.stream,
                         q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale)) != cudaSuccess)
     return err;
-  if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so), dim3(256),
+  if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so, groups),
+                        dim3(256),
                         kGemvSmem, q.stream, (const float *)q.L.gated, q.B, (const T *)q.W_o, q.e, q.d,
                         kso, q.L.outp, (int *)nullptr)) != cudaSuccess)
     return err;
