@@ -312,15 +312,16 @@ int flash_gau_backward(const void *X, const void *dO, const flash_gau_weights *w
                        size_t workspace_bytes, void *stream);
 
 /* ---- autoregressive decode ---------------------------------------------- */
-/* One new token for each of B sequences, in constant work per token ("the
- * linear cache is one matrix and the local attention is limited to one
- * chunk", Transformer Quality in Linear Time §3.2.1).  The state, one
+/* One new token for each of B sequences, in constant work per token
+ * (Transformer Quality in Linear Time §3.2.1: the global term is carried as
+ * one running matrix and the local attention reaches back within the
+ * current chunk only).  The state, one
  * buffer per batch of sequences, keeps per sequence the number of tokens
  * consumed, the linear cache (the sum of K_lin^T V over its completed
  * chunks, fp32 [s, e]) and the current chunk's K_quad, K_lin and V rows
  * (fp32).  A zeroed state starts B new sequences at position 0; each call
  * consumes token x[b] of every sequence and writes its output, the row the
- * causal forward would give it.  Each call enqueues four kernels on
+ * causal forward would give it.  Each call enqueues five kernels on
  * `stream` and does not synchronise.                                       */
 
 /* State bytes for B sequences, or 0 when the arguments are invalid or
