@@ -2,8 +2,9 @@
 INFRASTRUCTURE ONLY: the same import rule as ``oracle.flash_gau``).
 
 [TQLT] §3.2.1 ("Discussion"): decoding takes constant work per token,
-O(C d^2), "because the linear cache is one matrix and the local attention is
-limited to one chunk"; how that cache is kept is not stated.  The plainest
+O(C d^2), since the global term is carried as one running matrix and the
+local attention reaches back within the current chunk only; how that cache
+is kept is not stated.  The plainest
 reading, written out here for one sequence:
 
   state     Prefix = sum over completed chunks h of K_lin,h^T V_h  [s, e]
