@@ -69,3 +69,31 @@ def test_host_forward_workspace_checks():
     assert st == bd.EWORKSPACE
     assert L.flash_gau_forward_host_workspace_bytes(2, 250, 64, ctypes.byref(case.weights.c), 1,
                                                     bd.FP32) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_forward_replays_as_a_cuda_graph(dtype):
+    """The forward enqueues only kernels (tensor maps are built on the host
+    at capture), so it can be captured once and replayed; a replay on new
+    input data equals the eager call bit for bit."""
+    B, T, d, e, s, C = (2, 512, 128, 256, 128, 128) if dtype == "bf16" else (1, 192, 64, 96, 32, 64)
+    case = Case(B, T, d, e, s, C, True, dtype, seed=161)
+    ws, out = case.workspace, case.out
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):  # warm-up outside the capture
+        bd.forward(case.X, case.weights, C, True, out=out, workspace=ws, stream=cap)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        bd.forward(case.X, case.weights, C, True, out=out, workspace=ws, stream=cap)
+    torch.cuda.synchronize()
+    for seed in (1, 2):
+        torch.manual_seed(seed)
+        case.X.copy_(torch.randn_like(case.X) * (1 + seed))
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        eager = bd.forward(case.X, case.weights, C, True, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, eager)
