@@ -30,9 +30,19 @@
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace flashgau {
 namespace {
+
+// Every kernel of the backward is launched with programmatic dependent
+// launch: it may be scheduled while the previous one drains, waits for it
+// before touching memory, and lets the next one be scheduled at once.
+__device__ __forceinline__ void pdl_enter() {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+}
+
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -76,6 +86,7 @@ template <typename TA, typename TB, typename Epi>
 __global__ void __launch_bounds__(256)
 bw_gemm(int M, int N, int K, const TA *__restrict__ A, Operand oa, const TB *__restrict__ Bm,
         Operand ob, Epi epi) {
+  pdl_enter();
   __shared__ float As[kTileK][kTile + 1];
   __shared__ float Bs[kTileK][kTile + 1];
   const int z = blockIdx.z;
@@ -168,8 +179,7 @@ cudaError_t gemm(cudaStream_t st, int M, int N, int K, int batches, const TA *A,
                  const TB *Bm, Operand ob, Epi epi) {
   if (M <= 0 || N <= 0 || batches <= 0) return cudaSuccess;
   dim3 grid((N + kTile - 1) / kTile, (M + kTile - 1) / kTile, batches);
-  bw_gemm<TA, TB, Epi><<<grid, 256, 0, st>>>(M, N, K, A, oa, Bm, ob, epi);
-  return cudaGetLastError();
+  return launch_pdl(bw_gemm<TA, TB, Epi>, grid, dim3(256), 0, st, M, N, K, A, oa, Bm, ob, epi);
 }
 
 Operand op(long long sm, long long sk, long long sb = 0, int div = 1) { return {sm, sk, sb, div}; }
@@ -183,6 +193,7 @@ __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
                           const float *__restrict__ gamma, const float *__restrict__ beta,
                           long long M, int e, int s, __nv_bfloat16 *__restrict__ V_io,
                           __nv_bfloat16 *__restrict__ H_io) {
+  pdl_enter();
   const int N = 2 * e + s;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
        i += (long long)gridDim.x * blockDim.x) {
@@ -209,6 +220,7 @@ __global__ void act_heads(const float *__restrict__ pre, float *__restrict__ U,
 // A = U * Vh (fp32 when A is set, a bf16 copy when A_io is)
 __global__ void gate(const float *__restrict__ U, const float *__restrict__ Vh,
                      float *__restrict__ A, __nv_bfloat16 *__restrict__ A_io, long long n) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const float a = U[i] * Vh[i];
@@ -222,6 +234,7 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
                           const float *__restrict__ Vh, float *__restrict__ dU,
                           float *__restrict__ dVh, long long n,
                           __nv_bfloat16 *__restrict__ dVh_io) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     dU[i] = dA[i] * Vh[i];
@@ -239,6 +252,7 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
 __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_io,
                           const float *__restrict__ relpos, long long rows, int C, int causal,
                           float inv_c) {
+  pdl_enter();
   const int C4 = C / 4;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < rows * C4;
        q += (long long)gridDim.x * blockDim.x) {
@@ -263,6 +277,7 @@ __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_i
 // (blocks along y take the rows of the score matrices)
 __global__ void score_grad(const float *__restrict__ S, float *__restrict__ dP, long long rows,
                            int C, int causal, __nv_bfloat16 *__restrict__ dS_io) {
+  pdl_enter();
   for (long long row = blockIdx.y; row < rows; row += gridDim.y) {
   const int i = (int)(row % C);
   for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < C; j += gridDim.x * blockDim.x) {
@@ -283,6 +298,7 @@ __global__ void __launch_bounds__(256)
 score_grad_relpos(const float *__restrict__ S, const float *__restrict__ dP,
                   __nv_bfloat16 *__restrict__ dS_io, float *__restrict__ drelpos, long long rows,
                   int C, int causal, long long rows_per_block) {
+  pdl_enter();
   extern __shared__ float bins[];  // [2C - 1]
   for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x) bins[k] = 0.f;
   __syncthreads();
@@ -318,6 +334,7 @@ score_grad_relpos(const float *__restrict__ S, const float *__restrict__ dP,
 constexpr int kRelRows = 32;
 __global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ drelpos,
                             long long rows, int C) {
+  pdl_enter();
   extern __shared__ float bins[];  // [2C - 1]
   for (int k = threadIdx.x; k < 2 * C - 1; k += blockDim.x) bins[k] = 0.f;
   __syncthreads();
@@ -338,6 +355,7 @@ __global__ void relpos_grad(const float *__restrict__ dS, float *__restrict__ dr
 __global__ void scan_forward(const float *__restrict__ state, float *__restrict__ prefix, int B,
                              int G, long long se, int causal, float lin_scale,
                              __nv_bfloat16 *__restrict__ prefix_io) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
        i += (long long)gridDim.x * blockDim.x) {
     const long long b = i / se, r = i - b * se;
@@ -363,6 +381,7 @@ __global__ void scan_forward(const float *__restrict__ state, float *__restrict_
 // as it is)
 __global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long se, int causal,
                               __nv_bfloat16 *__restrict__ dstate_io) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se;
        i += (long long)gridDim.x * blockDim.x) {
     const long long b = i / se, r = i - b * se;
@@ -401,6 +420,7 @@ __global__ void __launch_bounds__(256)
 heads_grad(const float *__restrict__ dH, const float *__restrict__ Z,
            const float *__restrict__ gamma, float *__restrict__ dZ, float *__restrict__ dgamma,
            float *__restrict__ dbeta, long long M, int s, int rows_per_block) {
+  pdl_enter();
   // two row parities x 128 columns; the parities meet in shared memory
   __shared__ float red[8][128];
   const int par = threadIdx.x / 128, cl = threadIdx.x % 128;
@@ -446,6 +466,7 @@ heads_grad(const float *__restrict__ dH, const float *__restrict__ Z,
 __global__ void pre_grad(float *__restrict__ pre, __nv_bfloat16 *__restrict__ pre_io,
                          const float *__restrict__ dU, const float *__restrict__ dV,
                          const float *__restrict__ dZ, long long M, int e, int s) {
+  pdl_enter();
   const int N = 2 * e + s;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
        i += (long long)gridDim.x * blockDim.x) {
@@ -463,6 +484,7 @@ __global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__r
                                float *__restrict__ V, float *__restrict__ Z,
                                float *__restrict__ H, const float *__restrict__ gamma,
                                const float *__restrict__ beta, long long M, int e, int s) {
+  pdl_enter();
   const int N = 2 * e + s;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * N;
        i += (long long)gridDim.x * blockDim.x) {
@@ -499,6 +521,7 @@ __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__res
                              float *__restrict__ Z, const float *__restrict__ gamma,
                              const float *__restrict__ beta, long long M, int e, int s,
                              __nv_bfloat16 *__restrict__ V_io, __nv_bfloat16 *__restrict__ H_io) {
+  pdl_enter();
   const int N4 = (2 * e + s) / 4, e4 = e / 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -536,6 +559,7 @@ __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__res
 // A = U * Vh as bf16 only; n4 = elements / 4
 __global__ void gate_v4(const float4 *__restrict__ U, const float4 *__restrict__ Vh,
                         __nv_bfloat16 *__restrict__ A_io, long long n4) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 u = U[i], v = Vh[i];
@@ -548,6 +572,7 @@ __global__ void gate_grad_v4(const float4 *__restrict__ dA, const float4 *__rest
                              const float4 *__restrict__ Vh, float4 *__restrict__ dU,
                              float4 *__restrict__ dVh, __nv_bfloat16 *__restrict__ dVh_io,
                              long long n4) {
+  pdl_enter();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 a = dA[i], u = U[i], v = Vh[i];
@@ -562,6 +587,7 @@ __global__ void gate_grad_v4(const float4 *__restrict__ dA, const float4 *__rest
 __global__ void pre_grad_v4(__nv_bfloat16 *__restrict__ pre_io, const float *__restrict__ dU,
                             const float *__restrict__ dV, const float *__restrict__ dZ,
                             long long M, int e, int s) {
+  pdl_enter();
   const int N4 = (2 * e + s) / 4, e4 = e / 4, s4 = s / 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -609,6 +635,7 @@ GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int 
 }
 
 __global__ void zero_f32(float *p, int n) {
+  pdl_enter();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0.f;
 }
@@ -643,6 +670,7 @@ cudaError_t run(const BackwardProblem &q) {
   do {                                     \
     if ((err = (x)) != cudaSuccess) return err; \
   } while (0)
+#define LAUNCH(...) BW_TRY(launch_pdl(__VA_ARGS__));
   // the five large contractions on the tensor cores: bf16 io, shapes that
   // tile 128 x 64 (rows of every output, depths) and 64-wide columns
   const bool tc = sizeof(T) == 2 && M % 128 == 0 && d % 128 == 0 && e % 128 == 0 &&
@@ -678,20 +706,20 @@ cudaError_t run(const BackwardProblem &q) {
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
   if (tcc)
-    act_heads_v4<<<blocks_for(M * N / 4), 256, 0, st>>>(dpre_io, U, Z, q.gamma, q.beta, M, e, s,
-                                                         V_io, H_io);
+    LAUNCH(act_heads_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, U, Z, q.gamma, q.beta, M, e, s,
+                                                         V_io, H_io)
   else if (tc)  // bf16 Pre, fp32 heads and V for the CUDA-core chunk contractions
-    act_heads_bf16<<<blocks_for(M * N), 256, 0, st>>>(dpre_io, U, V, Z, H, q.gamma, q.beta, M, e,
-                                                      s);
+    LAUNCH(act_heads_bf16, blocks_for(M * N), 256, 0, st, dpre_io, U, V, Z, H, q.gamma, q.beta, M, e,
+                                                      s)
   else
-    act_heads<<<blocks_for(M * N), 256, 0, st>>>(pre, U, V, Z, H, q.gamma, q.beta, M, e, s,
-                                                 nullptr, nullptr);
+    LAUNCH(act_heads, blocks_for(M * N), 256, 0, st, pre, U, V, Z, H, q.gamma, q.beta, M, e, s,
+                                                 nullptr, nullptr)
   const float *Qq = H, *Kq = H + Ms, *Ql = H + 2 * Ms, *Kl = H + 3 * Ms;
   // per chunk z: rows z*C .. of the [M, *] matrices
   if (tcc) {
     BW_TRY(bt(Qq_io, s, 0, Kq_io, s, 1, S, C, C, s, 1, 1.f, 0));  // raw Qq Kq^T
-    score_act<<<blocks_for(BG * C * C / 4), 256, 0, st>>>(S, P_io, q.relpos, BG * C, C, q.causal,
-                                                           1.f / C);
+    LAUNCH(score_act, blocks_for(BG * C * C / 4), 256, 0, st, S, P_io, q.relpos, BG * C, C, q.causal,
+                                                           1.f / C)
     BW_TRY(bt(P_io, C, 0, V_io, e, 0, Vh, C, e, C, 1, q.local_scale, 0));
     BW_TRY(bt(Kl_io, s, 1, V_io, e, 0, state, s, e, C, 1, 1.f, 0));
   } else {
@@ -702,8 +730,8 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
                 op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
   }
-  scan_forward<<<blocks_for(q.B * se), 256, 0, st>>>(state, tcc ? nullptr : prefix, q.B, G, se,
-                                                      q.causal, q.lin_scale, pre_io);
+  LAUNCH(scan_forward, blocks_for(q.B * se), 256, 0, st, state, tcc ? nullptr : prefix, q.B, G, se,
+                                                      q.causal, q.lin_scale, pre_io)
   // Vh += Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
     BW_TRY(bt(Ql_io, s, 0, pre_io, e, 0, Vh, C, e, s, pdiv, 1.f, 1));
@@ -713,10 +741,10 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
   if (tc)
-    gate_v4<<<blocks_for(M * e / 4), 256, 0, st>>>((const float4 *)U, (const float4 *)Vh, A_io,
-                                                    M * e / 4);
+    LAUNCH(gate_v4, blocks_for(M * e / 4), 256, 0, st, (const float4 *)U, (const float4 *)Vh, A_io,
+                                                    M * e / 4)
   else
-    gate<<<blocks_for(M * e), 256, 0, st>>>(U, Vh, Ag, nullptr, M * e);
+    LAUNCH(gate, blocks_for(M * e), 256, 0, st, U, Vh, Ag, nullptr, M * e)
   // ---- output projection and gate
   if (tc) {
     // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
@@ -729,11 +757,11 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
   if (tcc)
-    gate_grad_v4<<<blocks_for(M * e / 4), 256, 0, st>>>(
+    LAUNCH(gate_grad_v4, blocks_for(M * e / 4), 256, 0, st, 
         (const float4 *)dA, (const float4 *)U, (const float4 *)Vh, (float4 *)dU, nullptr, dVh_io,
-        M * e / 4);
+        M * e / 4)
   else
-    gate_grad<<<blocks_for(M * e), 256, 0, st>>>(dA, U, Vh, dU, dVh, M * e, nullptr);
+    LAUNCH(gate_grad, blocks_for(M * e), 256, 0, st, dA, U, Vh, dU, dVh, M * e, nullptr)
   // ---- local part
   if (tcc) {
     BW_TRY(bt(dVh_io, e, 0, V_io, e, 1, dP, C, C, e, 1, q.local_scale, 0));
@@ -746,15 +774,13 @@ cudaError_t run(const BackwardProblem &q) {
                 op(e, 1, (long long)C * e),
                 StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   }
-  zero_f32<<<(2 * C - 1 + 255) / 256, 256, 0, st>>>(q.drelpos, 2 * C - 1);
+  LAUNCH(zero_f32, (2 * C - 1 + 255) / 256, 256, 0, st, q.drelpos, 2 * C - 1)
   if (tcc) {
     const long long rpb = 32;  // rows per block
-    score_grad_relpos<<<(unsigned)((BG * C + rpb - 1) / rpb), 256, (2 * C - 1) * sizeof(float),
-                        st>>>(S, dP, dS_io, q.drelpos, BG * C, C, q.causal, rpb);
+    LAUNCH(score_grad_relpos, (unsigned)((BG * C + rpb - 1) / rpb), 256, (2 * C - 1) * sizeof(float), st, S, dP, dS_io, q.drelpos, BG * C, C, q.causal, rpb)
   } else {
-    score_grad<<<rows_grid(C, BG * C), 256, 0, st>>>(S, dP, BG * C, C, q.causal, nullptr);
-    relpos_grad<<<(unsigned)((BG * C + kRelRows - 1) / kRelRows), 256,
-                  (2 * C - 1) * sizeof(float), st>>>(dP, q.drelpos, BG * C, C);
+    LAUNCH(score_grad, rows_grid(C, BG * C), 256, 0, st, S, dP, BG * C, C, q.causal, nullptr)
+    LAUNCH(relpos_grad, (unsigned)((BG * C + kRelRows - 1) / kRelRows), 256, (2 * C - 1) * sizeof(float), st, dP, q.drelpos, BG * C, C)
   }
   float *dQq = dH, *dKq = dH + Ms, *dQl = dH + 2 * Ms, *dKl = dH + 3 * Ms;
   if (tcc) {
@@ -777,7 +803,7 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, s, e, C, (int)BG, Ql, op(1, s, (long long)C * s), dVh,
                 op(e, 1, (long long)C * e), StoreF32{dpre, e, 1, se, q.lin_scale, 0}));
   }
-  scan_backward<<<blocks_for(q.B * se), 256, 0, st>>>(dpre, q.B, G, se, q.causal, dst_io);
+  LAUNCH(scan_backward, blocks_for(q.B * se), 256, 0, st, dpre, q.B, G, se, q.causal, dst_io)
   if (tcc) {
     BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
     BW_TRY(bt(Kl_io, s, 0, dst_io, e, 0, dV, C, e, s, 1, 1.f, 1));
@@ -788,16 +814,16 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
   }
   // ---- heads
-  zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dgamma, 4 * s);
-  zero_f32<<<(8 * s + 255) / 256, 256, 0, st>>>(q.dbeta, 4 * s);
+  LAUNCH(zero_f32, (8 * s + 255) / 256, 256, 0, st, q.dgamma, 4 * s)
+  LAUNCH(zero_f32, (8 * s + 255) / 256, 256, 0, st, q.dbeta, 4 * s)
   const int rows = 128;
-  heads_grad<<<(unsigned)((M + rows - 1) / rows), 256, 0, st>>>(dH, Z, q.gamma, dZ, q.dgamma,
-                                                                q.dbeta, M, s, rows);
+  LAUNCH(heads_grad, (unsigned)((M + rows - 1) / rows), 256, 0, st, dH, Z, q.gamma, dZ, q.dgamma,
+                                                                q.dbeta, M, s, rows)
   // ---- input side
   if (tc)
-    pre_grad_v4<<<blocks_for(M * N / 4), 256, 0, st>>>(dpre_io, dU, dV, dZ, M, e, s);
+    LAUNCH(pre_grad_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, dU, dV, dZ, M, e, s)
   else
-    pre_grad<<<blocks_for(M * N), 256, 0, st>>>(pre, nullptr, dU, dV, dZ, M, e, s);
+    LAUNCH(pre_grad, blocks_for(M * N), 256, 0, st, pre, nullptr, dU, dV, dZ, M, e, s)
   if (tc) {
     // dX = dPre W_uvz^T (bf16 out); dW_uvz = X^T dPre
     BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
@@ -808,6 +834,7 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, d, N, (int)M, 1, X, op(1, d), (const float *)pre, op(N, 1),
                 StoreF32{q.dW_uvz, N, 1, 0, 1.f, 0}));
   }
+#undef LAUNCH
 #undef BW_TRY
   return cudaGetLastError();
 }

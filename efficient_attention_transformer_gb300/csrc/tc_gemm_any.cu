@@ -122,6 +122,11 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
+  // launched with programmatic dependent launch: the setup above overlaps
+  // the previous kernel's tail; wait for it before any operand or output
+  // access, and let the next kernel be scheduled
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -315,8 +320,7 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
     configured |= 1ull << dev;
   }
   const int grid = p.total < num_sms ? p.total : num_sms;
-  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmC, p);
 }
 
 }  // namespace
