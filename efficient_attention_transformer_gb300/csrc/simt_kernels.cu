@@ -43,6 +43,9 @@ __global__ void __launch_bounds__(256)
 simt_gemm(int M, int N, int K, const Tin *__restrict__ A, long long sam,
           long long sak, long long sab, const Tin *__restrict__ Bm, long long sbk,
           long long sbn, long long sbb, Epi epi) {
+  // launched with programmatic dependent launch (see the stage functions)
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float As[kTileK][kTile + 1];
   __shared__ float Bs[kTileK][kTile + 1];
   const int batch = blockIdx.z;
@@ -201,6 +204,8 @@ simt_chunk_attention(const T *__restrict__ U, const T *__restrict__ V,
                      const float *__restrict__ relpos, T *__restrict__ gated,
                      long long M, int C, int G, int e, int s, int causal, float local_scale,
                      int per_chunk) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ float sm[];
   const int sp = s + 1;
   float *q = sm;                          // [32][s+1]
@@ -302,9 +307,9 @@ cudaError_t projection(const Problem &p) {
   const int N = 2 * p.e + p.s;
   dim3 grid(cdiv(N, kTile), cdiv(p.M, kTile), 1);
   ProjEpi<T> epi{(T *)p.U, (T *)p.V, (T *)p.heads, p.gamma, p.beta, p.M, p.e, p.s};
-  simt_gemm<T><<<grid, 256, 0, p.stream>>>((int)p.M, N, p.d, (const T *)p.A_in, p.d, 1, 0,
-                                           (const T *)p.W_uvz, N, 1, 0, epi);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm<T, ProjEpi<T>>, grid, dim3(256), 0, p.stream, (int)p.M, N, p.d,
+                    (const T *)p.A_in, (long long)p.d, 1LL, 0LL, (const T *)p.W_uvz, (long long)N,
+                    1LL, 0LL, epi);
 }
 
 template <typename T>
@@ -313,9 +318,9 @@ cudaError_t chunk_state(const Problem &p) {
   const T *Kl = (const T *)p.heads + 3 * p.M * p.s;
   dim3 grid(cdiv(p.e, kTile), cdiv(p.s, kTile), p.B * p.G);
   StateEpi<T> epi{(T *)p.state, p.s, p.e};
-  simt_gemm<T><<<grid, 256, 0, p.stream>>>(p.s, p.e, p.C, Kl, 1, p.s, (long long)p.C * p.s,
-                                           (const T *)p.V, p.e, 1, (long long)p.C * p.e, epi);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm<T, StateEpi<T>>, grid, dim3(256), 0, p.stream, p.s, p.e, p.C, Kl,
+                    1LL, (long long)p.s, (long long)p.C * p.s, (const T *)p.V, (long long)p.e, 1LL,
+                    (long long)p.C * p.e, epi);
 }
 
 template <typename T>
@@ -348,19 +353,19 @@ cudaError_t chunk_attention(const Problem &p) {
     configured |= 1ull << dev;
   }
   dim3 grid(cdiv(p.e, kAttCols), cdiv(p.C, kAttRows), p.B * p.G);
-  simt_chunk_attention<T><<<grid, 256, smem, p.stream>>>(
-      (const T *)p.U, (const T *)p.V, (const T *)p.heads, (const T *)p.prefix, p.relpos,
-      (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal, p.local_scale, p.per_chunk);
-  return cudaGetLastError();
+  return launch_pdl(simt_chunk_attention<T>, grid, dim3(256), smem, p.stream, (const T *)p.U,
+                    (const T *)p.V, (const T *)p.heads, (const T *)p.prefix, p.relpos,
+                    (T *)p.gated, p.M, p.C, p.G, p.e, p.s, p.causal, p.local_scale,
+                    p.per_chunk);
 }
 
 template <typename T>
 cudaError_t output(const Problem &p) {
   dim3 grid(cdiv(p.d, kTile), cdiv(p.M, kTile), 1);
   StoreEpi<T> epi{(T *)p.out, p.d, (const T *)p.residual};
-  simt_gemm<T><<<grid, 256, 0, p.stream>>>((int)p.M, p.d, p.e, (const T *)p.gated, p.e, 1, 0,
-                                           (const T *)p.W_o, p.d, 1, 0, epi);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm<T, StoreEpi<T>>, grid, dim3(256), 0, p.stream, (int)p.M, p.d, p.e,
+                    (const T *)p.gated, (long long)p.e, 1LL, 0LL, (const T *)p.W_o, (long long)p.d,
+                    1LL, 0LL, epi);
 }
 
 }  // namespace
