@@ -192,3 +192,26 @@ def test_missing_library_fails_loudly(monkeypatch):
     with pytest.raises(ValueError, match="CUDA tensor"):
         bd.GauWeights(torch.zeros(64, 288), torch.zeros(128, 64), torch.zeros(4, 32),
                       torch.zeros(4, 32), torch.zeros(127), 64, 128, 32)
+
+
+def test_host_forward_and_segmented_forward_reject_before_any_launch(L):
+    w = bd.Weights(1, 2, 3, 4, 5, 64, 128, 32, 1.0, 1.0)
+    n = L.flash_gau_forward_host_workspace_bytes(2, 256, 64, ctypes.byref(w), 1, bd.FP32)
+    assert n > 0
+    # ragged T: no workspace size, and the call refuses
+    assert L.flash_gau_forward_host_workspace_bytes(2, 250, 64, ctypes.byref(w), 1, bd.FP32) == 0
+    assert L.flash_gau_forward_host(16, ctypes.byref(w), 2, 250, 64, 1, bd.FP32, 32, 256, n,
+                                    None) == bd.EINVAL
+    # null host buffers, too small or misaligned workspace
+    assert L.flash_gau_forward_host(None, ctypes.byref(w), 2, 256, 64, 1, bd.FP32, 32, 256, n,
+                                    None) == bd.EINVAL
+    assert L.flash_gau_forward_host(16, ctypes.byref(w), 2, 256, 64, 1, bd.FP32, 32, 256, n - 1,
+                                    None) == bd.EWORKSPACE
+    assert L.flash_gau_forward_host(16, ctypes.byref(w), 2, 256, 64, 1, bd.FP32, 32, 257, n,
+                                    None) == bd.EWORKSPACE
+    # the segmented forward validates like the plain one
+    seg = bd.Segments(None, 1)
+    assert L.flash_gau_forward_segmented(None, ctypes.byref(w), ctypes.byref(seg), 1, 256, 64, 1,
+                                         bd.FP32, 1 << 40, 256, 1 << 20, None) == bd.EINVAL
+    assert L.flash_gau_forward_segmented(16, ctypes.byref(w), ctypes.byref(seg), 1, 250, 64, 1,
+                                         bd.FP32, 1 << 40, 256, 1 << 20, None) == bd.EINVAL
