@@ -129,11 +129,13 @@ struct DecodeLayout {
   float *score;    // [B, C] this step's chunk weights a_j (local_scale included)
 };
 // Depth slices of the decode step's split-K matrix-vector product with a
-// [K, N] weight: about 150 blocks of 256 columns x one slice, at most 128
+// [K, N] weight: about 150 blocks of 256 columns x one slice, but at most 16
+// slices (their consumers add the slices one after another), at most 128
 // rows a slice.
 inline int decode_slices(int K, int N) {
   const int tiles = (N + 255) / 256;
   int sl = (150 + tiles - 1) / tiles;
+  if (sl > 16) sl = 16;
   const int lo = (K + 127) / 128, hi = (K + 7) / 8;
   if (sl < lo) sl = lo;
   if (sl > hi) sl = hi;
