@@ -358,11 +358,13 @@ def forward_noalloc(X, weights, C, causal, out=None, stream=None):
         raise ValueError("X does not match the weights")
     if out is None:
         out = torch.empty_like(X)
-    if stream is None:
-        stream = torch.cuda.current_stream(X.device)
-    _check(lib().flash_gau_forward_noalloc(
-        _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), B, T, C, int(bool(causal)),
-        weights.dtype, _dev_ptr(out, "out", X.dtype), stream.cuda_stream))
+    # the library picks the scratch of the current device: make it X's
+    with torch.cuda.device(X.device):
+        if stream is None:
+            stream = torch.cuda.current_stream(X.device)
+        _check(lib().flash_gau_forward_noalloc(
+            _dev_ptr(X, "X", X.dtype), ctypes.byref(weights.c), B, T, C, int(bool(causal)),
+            weights.dtype, _dev_ptr(out, "out", X.dtype), stream.cuda_stream))
     return out
 
 

@@ -1,8 +1,10 @@
 // Backward pass of the FLASH GAU layer: the gradients of sum(dO * O) with
 // respect to X and every parameter ("Transformer Quality in Linear Time",
 // Method, eq. 5, eq. 7, eq. 8 and the display after it, differentiated by
-// the chain rule).  CUDA-core fp32 throughout, for both io types (bf16
-// operands are widened as they are loaded):
+// the chain rule).  For bf16 io whose shapes tile, every contraction runs
+// on the tcgen05 tensor cores (bf16 operands, fp32 accumulation); fp32 io
+// and bf16 shapes that do not tile run them on the CUDA cores in fp32
+// (bf16 operands widened as they are loaded):
 //
 //   recompute  Pre = X W_uvz;  U, V, Z = swish(Pre);  heads = Z gamma + beta
 //              S = Qq Kq^T / C + b,  P = relu(S)^2 (masked)      per chunk

@@ -2,8 +2,8 @@
 // fp32 accumulation ("Transformer Quality in Linear Time", Method: local
 // part, eq. 7/8 global part, display after eq. 8; flash_block pseudocode):
 //
-//   acc   = Q_lin Prefix_g                                      (global term)
-//   acc  += sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]    (local term)
+//   acc   = sum_kb relu^2(Q_quad K_quad[kb]^T / C + b) V[kb]    (local term)
+//   acc  += Q_lin Prefix_g                                      (global term)
 //   gated = U * acc
 //
 // Work unit: (chunk, 128-query tile, 128-column value tile).  One
@@ -20,8 +20,9 @@
 //   warp 0     TMA producer: Q_lin, and one ring carrying Q_quad, K_quad,
 //              V and prefix state tiles in the order the MMAs consume them;
 //   warp 1     MMA issuer: S = Q_quad K_quad^T into a 128-column TMEM
-//              buffer (two buffers), acc = Q_lin Prefix (smem A), acc += P V
-//              with P read from TMEM;
+//              buffer (two buffers), acc = P V with P read from TMEM, then
+//              acc += Q_lin Prefix (smem A), so that the prefix states, which
+//              the kernel launched before this one writes, are needed last;
 //   warps 2-9  relu^2, two per TMEM lane quarter, each for 64 of a block's
 //              128 keys: read S with tcgen05.ld, compute relu^2(S/C + b)
 //              (the bias table carries the causal mask as -inf, written by

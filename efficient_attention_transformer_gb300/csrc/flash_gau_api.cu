@@ -11,17 +11,19 @@
 using namespace flashgau;
 
 namespace {
-
-constexpr size_t kAlign = 256;
-constexpr int kMaxDevices = 64;
-
 thread_local char g_cuda_msg[256] = "no CUDA error recorded";
+}  // namespace
 
-int record_cuda(cudaError_t err) {
+int flashgau::record_cuda(cudaError_t err) {
   snprintf(g_cuda_msg, sizeof(g_cuda_msg), "CUDA error %d: %s", (int)err,
            cudaGetErrorString(err));
   return FLASH_GAU_ECUDA;
 }
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -277,28 +279,46 @@ int check_block(const flash_gau_block *blk, int s) {
   return FLASH_GAU_OK;
 }
 
+}  // namespace
+
+int flashgau::check_forward(const void *X, const flash_gau_weights *w, int B, int T, int C,
+                            int causal, int dtype, const void *out, const void *workspace,
+                            size_t workspace_bytes, flash_gau_workspace_layout *L,
+                            int *num_sms) {
+  if (!X || !w || !out || !w->W_uvz || !w->W_o || !w->gamma || !w->beta || !w->relpos ||
+      !scales_finite(w))
+    return FLASH_GAU_EINVAL;
+  int st = layout(B, T, C, w->d, w->e, w->s, causal ? 1 : 0, dtype, L);
+  if (st != FLASH_GAU_OK) return st;
+  const size_t io = dtype == FLASH_GAU_BF16 ? 2 : 4;
+  const size_t nx = (size_t)B * T * w->d * io;
+  if (overlaps(out, nx, X, nx)) return FLASH_GAU_EINVAL;
+  if (workspace) {
+    if (workspace_bytes < L->total_bytes || ((uintptr_t)workspace % kAlign) != 0)
+      return FLASH_GAU_EWORKSPACE;
+    if (overlaps(out, nx, workspace, L->total_bytes)) return FLASH_GAU_EINVAL;
+  }
+  return device_info(num_sms);
+}
+
+namespace {
+
 // One forward: the layer alone (blk == null) or the flash_block wrapper.
 int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block *blk, int B,
                 int T, int C, int causal, int dtype, void *out, void *workspace,
                 size_t workspace_bytes, void *stream, void *const *stage_events,
                 int n_events, const flash_gau_segments *seg = nullptr) {
-  if (!X || !w || !out || !workspace || !w->W_uvz || !w->W_o || !w->gamma || !w->beta ||
-      !w->relpos || !scales_finite(w))
-    return FLASH_GAU_EINVAL;
+  if (!workspace) return FLASH_GAU_EINVAL;
   if (n_events < 0 || (n_events > 0 && !stage_events)) return FLASH_GAU_EINVAL;
   causal = causal ? 1 : 0;
+  if (w) {
+    const int bst = check_block(blk, w->s);
+    if (bst != FLASH_GAU_OK) return bst;
+  }
   flash_gau_workspace_layout L;
-  int st = layout(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
-  if (st != FLASH_GAU_OK) return st;
-  if ((st = check_block(blk, w->s)) != FLASH_GAU_OK) return st;
-  if (workspace_bytes < L.total_bytes || ((uintptr_t)workspace % kAlign) != 0)
-    return FLASH_GAU_EWORKSPACE;
-  const size_t io = dtype == FLASH_GAU_BF16 ? 2 : 4;
-  const size_t nx = (size_t)B * T * w->d * io;
-  if (overlaps(out, nx, X, nx) || overlaps(out, nx, workspace, L.total_bytes))
-    return FLASH_GAU_EINVAL;
   int num_sms = 0;
-  st = device_info(&num_sms);
+  const int st = check_forward(X, w, B, T, C, causal, dtype, out, workspace, workspace_bytes,
+                               &L, &num_sms);
   if (st != FLASH_GAU_OK) return st;
 
   Problem p;

@@ -29,6 +29,18 @@ __device__ __forceinline__ void rope_sincos(float pos, float2 phi, float *sn, fl
 // Fills the table for head width s and the given base (host side).
 void rope_table(RopeTable *tab, int s, float base);
 
+// Keeps the message of a failed CUDA call for flash_gau_strerror and returns
+// FLASH_GAU_ECUDA.
+int record_cuda(cudaError_t err);
+
+// Every host-side check of one forward call before its first launch:
+// pointers and factors, the shape (filling *L with the workspace layout),
+// out against X, and the current device (filling *num_sms).  With a
+// non-null workspace, also its size, alignment and overlap with out.
+int check_forward(const void *X, const flash_gau_weights *w, int B, int T, int C, int causal,
+                  int dtype, const void *out, const void *workspace, size_t workspace_bytes,
+                  flash_gau_workspace_layout *L, int *num_sms);
+
 // One forward call, with every device pointer resolved.
 struct Problem {
   int B, T, C, G, d, e, s, causal, dtype;

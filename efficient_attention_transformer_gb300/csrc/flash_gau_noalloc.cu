@@ -6,6 +6,8 @@
 
 #include "flash_gau_internal.h"
 
+using namespace flashgau;
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -21,15 +23,18 @@ std::mutex g_scratch_mu;
 
 extern "C" int flash_gau_forward_noalloc(const void *X, const flash_gau_weights *w, int B, int T,
                                          int C, int causal, int dtype, void *out, void *stream) {
-  if (!X || !w || !out) return FLASH_GAU_EINVAL;
   causal = causal ? 1 : 0;
+  // Every argument check of flash_gau_forward comes first, so that a
+  // rejected call leaves the shared array (and its status word) untouched.
   flash_gau_workspace_layout L;
-  int st = flash_gau_workspace_layout_query(B, T, C, w->d, w->e, w->s, causal, dtype, &L);
+  int num_sms = 0;
+  int st = check_forward(X, w, B, T, C, causal, dtype, out, nullptr, 0, &L, &num_sms);
   if (st != FLASH_GAU_OK) return st;
   if (L.total_bytes > FLASH_GAU_NOALLOC_SCRATCH_BYTES) return FLASH_GAU_EWORKSPACE;
 
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FLASH_GAU_ECUDA;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return record_cuda(err);
   if (dev < 0 || dev >= kMaxDevices) return FLASH_GAU_EDEVICE;
   void *scratch = nullptr;
   {
@@ -37,17 +42,21 @@ extern "C" int flash_gau_forward_noalloc(const void *X, const flash_gau_weights 
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
       void *ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
-        return FLASH_GAU_ECUDA;
+      err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (err != cudaSuccess) return record_cuda(err);
+      if (!ptr) return FLASH_GAU_ECUDA;
       g_scratch_addr[dev] = ptr;
     }
     scratch = g_scratch_addr[dev];
   }
+  st = check_forward(X, w, B, T, C, causal, dtype, out, scratch, FLASH_GAU_NOALLOC_SCRATCH_BYTES,
+                     &L, &num_sms);
+  if (st != FLASH_GAU_OK) return st;
   // The status word is the only part of the workspace that must start at
   // zero; every intermediate is fully rewritten by the kernels.
-  if (cudaMemsetAsync(static_cast<char *>(scratch) + L.status, 0, sizeof(int),
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FLASH_GAU_ECUDA;
+  err = cudaMemsetAsync(static_cast<char *>(scratch) + L.status, 0, sizeof(int),
+                        static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return record_cuda(err);
   return flash_gau_forward(X, w, B, T, C, causal, dtype, out, scratch,
                            FLASH_GAU_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -118,8 +118,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// 2-D tiled load of one box into shared memory, completing on `bar`.
-// x is the innermost (contiguous) coordinate in elements, y the row.
 // Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte
 // aligned) from global memory into this CTA's shared memory, completing on
 // mbarrier `bar`.
@@ -132,6 +130,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
+// 2-D tiled load of one box into shared memory, completing on `bar`.
+// x is the innermost (contiguous) coordinate in elements, y the row.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y) {
   asm volatile(
@@ -161,17 +161,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(pol)
-      : "memory");
-}
-
-// Same load, written to the same shared-memory offset of every CTA of the
-// cluster in `mask` and signalling the mbarrier at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                               int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
       : "memory");
 }
 
@@ -297,16 +286,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA
-// of the cluster in `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
       : "memory");
 }
 

@@ -284,8 +284,14 @@ int flash_gau_forward_segmented(const void *X, const flash_gau_weights *w,
  * to X and every parameter, by the chain rule through the forward's steps
  * (eq. 5, eq. 7, eq. 8 and the display after it): the backward the pages'
  * training workloads need.  The call recomputes the forward's
- * intermediates itself (it needs no earlier forward) and works in fp32 on
- * the CUDA cores for both io types.  Gradients are written, not added.    */
+ * intermediates itself (it needs no earlier forward).  For bf16 io with
+ * B*T, d, e, C and s multiples of 128 every contraction runs on the
+ * tcgen05 tensor cores with bf16 operands and fp32 accumulation (with C or
+ * s not multiples of 128, the chunk-level ones run on the CUDA cores);
+ * fp32 io, and other bf16 shapes, run the contractions in fp32 on the
+ * CUDA cores.  Sums, scans and the
+ * elementwise steps are fp32 in both cases.  Gradients are written, not
+ * added.                                                                   */
 typedef struct flash_gau_grads {
   void *dX;          /* device [B, T, d], io type                           */
   float *dW_uvz;     /* device [d, 2e+s] fp32, columns as in W_uvz          */
@@ -375,10 +381,13 @@ int flash_gau_rope_toeplitz_bias(const float *a, const float *b, int m, int C,
  *   - Problems whose workspace (flash_gau_workspace_bytes) is larger than
  *     the scratch are rejected with FLASH_GAU_EWORKSPACE before anything is
  *     launched; other argument errors return the same codes as
- *     flash_gau_forward.
+ *     flash_gau_forward.  Every check runs before the array is touched, so
+ *     a rejected call leaves it (and its status word) as it was.
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make
- *     that first call before any stream capture on that device.
+ *     that first call before any stream capture on that device.  The
+ *     cached address is not looked up again, so resetting a device
+ *     (cudaDeviceReset) while the library stays loaded is not supported.
  *   - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  *     library routine.  It enqueues a 4-byte cudaMemsetAsync that clears
  *     the status word, then the same kernels as flash_gau_forward, on

@@ -76,6 +76,11 @@ def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed, local_scale=1.0):
     # 128-column tile tail, several chunks non-causal
     ((2, 512, 128, 384, 128, 128), True, "bf16", 1.0),
     ((1, 1024, 256, 512, 128, 256), False, "bf16", 1.0 / 256),
+    # the layer's full widths (d = 768, e = 1536): the weight gradients run
+    # split-K over 36 and 78 output tiles, and the persistent contractions
+    # take several rounds of tiles
+    ((1, 2048, 768, 1536, 128, 256), True, "bf16", 1.0),
+    ((2, 1024, 768, 1536, 128, 256), False, "bf16", 1.0),
 ])
 def test_backward_matches_oracle(shape, causal, dtype, lin_scale):
     B, T, d, e, s, C = shape
