@@ -122,8 +122,6 @@ struct Bars {
   volatile int abort_flag;
 };
 
-static_assert(sizeof(Bars) <= 512, "barriers exceed their shared-memory slot");
-
 struct AttnParams {
   int C, G, causal;
   int n_et, n_qt;   // value tiles (128 columns of e), query tiles per chunk
@@ -530,7 +528,6 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
       bool prefix_ready = p.n_pitems > 0;
       if (prefix_ready) griddep_wait();
-      int a = 0;  // attention units loaded so far: the Q_lin buffer's phase
       for (int i = 0;; ++i) {
         int u = atomicAdd(p.next_unit, 1);
         if (u >= p.n_pitems + p.total) u = -1;
@@ -570,7 +567,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
               griddep_wait();
               prefix_ready = true;
             }
-            ok = mbar_wait(smem_u32(&bar->ql_empty), (a & 1) ^ 1, abort);
+            ok = mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
             if (!ok) break;
             const uint32_t f = smem_u32(&bar->ql_full);
             mbar_arrive_expect_tx(f, Q_BYTES);
@@ -595,7 +592,6 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                load(&tmPre, 1, 0, rb64_row(pre_row0 + 64, col, ncb));
         }
         if (!ok) break;
-        ++a;
       }
       if (!ok) raise_timeout(bar, p.status);
     }
@@ -676,8 +672,8 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         return true;
       };
       const uint32_t idesc_st = idesc_bf16_f32(128, ET, 1, 1);
-      int pi = 0;  // prefix items issued so far
-      int a = 0;   // attention units issued so far: the Q_lin buffer's phase
+      int pi = 0;              // prefix items issued so far
+      bool attn_begun = false;  // an attention unit has been issued
       for (int i = 0; ok; ++i) {
         int u = pop(i);
         if (u < 0) {
@@ -720,13 +716,14 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           release(i);
           continue;
         }
-        if (a == 0) {
+        if (!attn_begun) {
           // the attention's TMEM buffers are the prefix slots
           if (pi > 0 && !mbar_wait(smem_u32(&bar->ps_free), (pi - 1) & 1, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          attn_begun = true;
         }
         u -= p.n_pitems;
         const Unit x = unit_of(p, u);
@@ -756,7 +753,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             if (ok && last_t) mma_commit(smem_u32(&bar->sb_free[sb]));
           }
           if (ok && t == 0) {
-            ok = mbar_wait(smem_u32(&bar->ql_full), a & 1, abort);
+            ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
             if (ok) tc_fence_after();
           }
           // with no key blocks the global term opens the accumulator
@@ -766,7 +763,6 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           mma_commit(smem_u32(&bar->acc_full[v & 1]));
         }
         if (!ok) break;
-        ++a;
         release(i);
       }
       if (!ok) raise_timeout(bar, p.status);
