@@ -73,13 +73,6 @@ def stage_work(w):
                              io * (M * s + M * e + 2 * B * G * s * e + pre_rows * s * e)),
         "chunk_attention": (2.0 * M * (cbar * s + cbar * e + s * e),
                             io * (2 * M * e + 3 * M * s + pre_rows * s * e + M * e)),
-        # bf16 without a chunk mask: the chunk states and their look-back
-        # scan inside the attention kernel (K_lin and V read for the states,
-        # the prefix states written and read back, no bf16 states)
-        "chunk_scan_attention": (2.0 * M * s * e + B * G * s * e
-                                 + 2.0 * M * (cbar * s + cbar * e + s * e),
-                                 io * (M * s + M * e + pre_rows * s * e)
-                                 + io * (2 * M * e + 3 * M * s + pre_rows * s * e + M * e)),
         "output": (2.0 * M * e * d, io * (M * e + e * d + M * d)),
     }
 

@@ -78,7 +78,7 @@ class Weights(ctypes.Structure):
 class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("total_bytes", "status", "U", "V", "heads", "state", "prefix", "gated",
-                 "bias", "xn", "rope", "scan")]
+                 "bias", "xn", "rope")]
 
 
 class Block(ctypes.Structure):

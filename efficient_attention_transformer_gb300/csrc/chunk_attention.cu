@@ -37,26 +37,6 @@
 // Two accumulators alternate between units, so while the epilogue warps
 // drain one, the MMAs of the next unit already fill the other.
 //
-// Chunk states and their prefix sums (eq. 7/8: State_g = K_lin,g^T V_g and
-// the exclusive, or total, sum over chunks) are computed here too, as the
-// first work items of the same counter, when no chunk mask applies.  A
-// prefix item is (batch row b, 128-column value tile, segment of L <= 4
-// consecutive chunks): the MMA thread puts the L chunk states into the four
-// 128-column TMEM slots (K_lin^T read M-major, V N-major, through the same
-// ring), then the sixteen relu^2 and epilogue warps scan them, each warp
-// owning 32 state rows x 32 columns of the tile: it sums its part over the
-// segment, publishes that aggregate, looks back over the earlier segments
-// of the same (b, tile) for their aggregates or inclusive sums (a
-// decoupled look-back: a segment's inclusive sum, once published, ends the
-// walk), publishes its own inclusive sum, then writes the segment's prefix
-// states (running sum, lin_scale applied, bf16) straight to global memory
-// and counts itself done for the item.  An attention unit's producer waits
-// for that count (16) before it loads the prefix state it needs.  Every
-// wait targets an item with a lower ticket, claimed earlier by a CTA that
-// is already running, so the order of tickets rules out a cycle; every
-// wait is bounded all the same.  With a chunk mask the prefix states come
-// from the kernel launched before this one, and there are no prefix items.
-//
 // The local term carries a factor local_scale (1 as written).  Any other
 // non-zero value multiplies P in the relu^2 warps; 0 (global term only)
 // gives every unit zero key blocks, so no Q_quad/K_quad/V tile is loaded
@@ -102,10 +82,6 @@ constexpr int TILE_BYTES = OFF_E + EPI_WARPS * 2 * E_BOX_BYTES;  // 224 KB
 constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 512;
 
 constexpr uint32_t TM_ACC = 0, TM_S = 256;
-// prefix items: chunk state k of the segment in TMEM columns 128 k
-constexpr int SLOTS = 4;
-constexpr int SCAN_WARPS = RELU_WARPS + EPI_WARPS;
-constexpr int PART = 32 * 32;  // fp32 values of one warp's part of a 128 x 128 tile
 
 struct Bars {
   uint64_t ql_full, ql_empty;
@@ -114,8 +90,6 @@ struct Bars {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t u_full[EPI_WARPS][2];
   uint64_t uq_full[4], uq_empty[4];  // unit-index queue
-  uint64_t ps_full[SLOTS];  // prefix item: chunk state k is in its TMEM slot
-  uint64_t ps_free;         // prefix item: every scan warp has read the slots
   volatile int unit_q[4];
   uint64_t drain;
   uint32_t tmem_base;
@@ -139,39 +113,7 @@ struct AttnParams {
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
-  // prefix items: n_pitems tickets before the attention units (0: the
-  // prefix states come from the kernel launched before this one)
-  int n_pitems;
-  int B, L, n_seg;  // batch rows, chunks per segment, segments per batch row
-  float lin_scale;
-  int *pflag;   // [n_pitems][16] per warp part: 1 aggregate, 2 inclusive sum published
-  int *pdone;   // [n_pitems] warps whose prefix rows are stored (zeroed by the projection)
-  float *pagg;  // [n_pitems][16][32 columns][32 rows] aggregates
-  float *pincl; // same layout: inclusive sums
-  __nv_bfloat16 *prefix;  // prefix states, 64 x 64 blocks (rows = state rows)
 };
-
-// A prefix item: batch row b, value tile jt, chunks g0 .. g0 + nL - 1 of the
-// row; tickets are segment-major, so earlier segments come first.
-struct PItem {
-  int b, jt, sigma, g0, nL, rem;  // rem: index of (b, jt) within a segment
-};
-__device__ __forceinline__ PItem pitem_of(const AttnParams &p, int t) {
-  const int per = p.B * p.n_et;
-  PItem x;
-  x.sigma = t / per;
-  x.rem = t % per;
-  x.b = x.rem / p.n_et;
-  x.jt = x.rem % p.n_et;
-  x.g0 = x.sigma * p.L;
-  x.nL = min(p.L, p.G - x.g0);
-  return x;
-}
-// The prefix item that writes the prefix state of chunk (b, g), value tile jt.
-__device__ __forceinline__ int pitem_for(const AttnParams &p, int b, int g, int jt) {
-  const int sigma = p.causal ? g / p.L : p.n_seg - 1;
-  return sigma * p.B * p.n_et + b * p.n_et + jt;
-}
 
 // Agents that consume each queued unit index: the MMA thread, the relu^2
 // warps and the epilogue warps (one arrival per warp).
@@ -272,158 +214,6 @@ __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, i
   tmem_st16(sbuf + c0 + 16, hi);
 }
 
-// Waits until every lane of the warp reads (acquire, device scope) a value
-// >= need at `flag`; *seen is the smallest value the lanes read, so every
-// lane has synchronised with the release that wrote it.  False after the
-// wait limit or once another role of the CTA has given up.
-__device__ __forceinline__ bool wait_flag_warp(const int *flag, int need, const volatile int *abort,
-                                               int *seen) {
-  uint64_t t0 = 0;
-  for (uint32_t n = 0;; ++n) {
-    const int v = ld_acquire_gpu(flag);
-    if (__all_sync(0xffffffffu, v >= need)) {
-      *seen = __reduce_min_sync(0xffffffffu, v);
-      return true;
-    }
-    if (n == 0) t0 = globaltimer();
-    bool quit = (n & 15u) == 15u && (*abort || globaltimer() - t0 > kWaitLimitNs);
-    if (__any_sync(0xffffffffu, quit)) return false;
-    __nanosleep(32);
-  }
-}
-
-// 32 consecutive prefix-state columns of one row, lin_scale applied, as
-// bf16 into the 64 x 64-blocked prefix buffer (64 contiguous bytes).
-__device__ __forceinline__ void store_prefix_row(const AttnParams &p, long long row, int col,
-                                                 const float (&v)[32]) {
-  const long long ncb = 2LL * p.n_et;
-  uint4 *dst = reinterpret_cast<uint4 *>(p.prefix + rb64_row(row, col, ncb) * 64 + (col & 63));
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 w;
-    w.x = pack_bf16(p.lin_scale * v[8 * q + 0], p.lin_scale * v[8 * q + 1]);
-    w.y = pack_bf16(p.lin_scale * v[8 * q + 2], p.lin_scale * v[8 * q + 3]);
-    w.z = pack_bf16(p.lin_scale * v[8 * q + 4], p.lin_scale * v[8 * q + 5]);
-    w.w = pack_bf16(p.lin_scale * v[8 * q + 6], p.lin_scale * v[8 * q + 7]);
-    dst[q] = w;
-  }
-}
-
-// acc[16 h + c] += column 16 h + c of TMEM slot k, this thread's row
-__device__ __forceinline__ void add_slot_half(uint32_t taddr, int k, int h, float (&acc)[32]) {
-  uint32_t v[16];
-  tmem_ld16(taddr + k * ET + 16 * h, v);
-  tmem_ld_wait();
-#pragma unroll
-  for (int c = 0; c < 16; ++c) acc[16 * h + c] += __uint_as_float(v[c]);
-}
-
-// One scan warp's share of prefix item t (the pi-th prefix item of this
-// CTA): state rows 32 * (warp % 4) + lane, value columns 32 * cg .. + 31 of
-// the item's tile, cg = (warp - 2) / 4.  The segment's chunk states are
-// read from TMEM more than once rather than held in registers.  Returns
-// false on a timed-out or aborted wait (the caller reports it).
-__device__ bool scan_item(const AttnParams &p, Bars *bar, uint32_t tmem, int t, int pi, int warp,
-                          int lane, const volatile int *abort) {
-  const PItem x = pitem_of(p, t);
-  const int quarter = warp & 3, part = warp - 2, cg = part >> 2;
-  const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + cg * 32;
-  const int per = p.B * p.n_et;
-  const size_t me = ((size_t)t * SCAN_WARPS + part) * PART + lane;  // column c at + 32 c
-  int *flag = p.pflag + (size_t)t * SCAN_WARPS + part;
-  float acc[32];
-#pragma unroll
-  for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-  // the segment's aggregate: the sum of its chunk states, slot by slot
-  for (int k = 0; k < x.nL; ++k) {
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar->ps_full[k]), pi & 1, abort)))
-      return false;
-    tc_fence_after();
-    add_slot_half(taddr, k, 0, acc);
-    add_slot_half(taddr, k, 1, acc);
-  }
-  if (x.sigma > 0) {
-#pragma unroll
-    for (int c = 0; c < 32; ++c) p.pagg[me + 32 * c] = acc[c];
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_gpu(flag, 1);
-    // acc becomes the sum of the earlier segments: look back over them,
-    // adding their aggregates until one has its inclusive sum published
-#pragma unroll
-    for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-    for (int sp = x.sigma - 1; sp >= 0; --sp) {
-      const size_t pt = (size_t)sp * per + x.rem;
-      int f = 0;
-      if (!wait_flag_warp(p.pflag + pt * SCAN_WARPS + part, 1, abort, &f)) return false;
-      const float *src = (f >= 2 ? p.pincl : p.pagg) + (pt * SCAN_WARPS + part) * PART + lane;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) acc[c] += __ldcg(src + 32 * c);
-      if (f >= 2) break;
-    }
-    // inclusive sum = earlier segments + this one's chunk states
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float in[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) in[c] = acc[16 * h + c];
-      for (int k = 0; k < x.nL; ++k) {
-        uint32_t v[16];
-        tmem_ld16(taddr + k * ET + 16 * h, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 16; ++c) in[c] += __uint_as_float(v[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) p.pincl[me + 32 * (16 * h + c)] = in[c];
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 32; ++c) p.pincl[me + 32 * c] = acc[c];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-  }
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) st_release_gpu(flag, 2);
-
-  // acc = sum of the earlier segments; the prefix states
-  const int row = quarter * 32 + lane;  // state row
-  const int col = x.jt * ET + cg * 32;
-  bool stored = false;
-  if (p.causal) {
-    // exclusive running sums: chunk g0 + k sees acc + slots 0 .. k-1
-    for (int k = 0; k < x.nL; ++k) {
-      store_prefix_row(p, (long long)(x.b * p.G + x.g0 + k) * SD + row, col, acc);
-      if (k + 1 < x.nL) {
-        add_slot_half(taddr, k, 0, acc);
-        add_slot_half(taddr, k, 1, acc);
-      }
-    }
-    stored = true;
-  } else if (x.sigma == p.n_seg - 1) {
-    // the total of the batch row, one prefix state for all its chunks
-    for (int k = 0; k < x.nL; ++k) {
-      add_slot_half(taddr, k, 0, acc);
-      add_slot_half(taddr, k, 1, acc);
-    }
-    store_prefix_row(p, (long long)x.b * SD + row, col, acc);
-    stored = true;
-  }
-  // every TMEM read above has completed: the slots are free
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&bar->ps_free));
-  if (stored) {
-    // the prefix rows are read next by other CTAs' TMA (async proxy) loads
-    fence_proxy_async_global();
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) red_release_gpu_add(p.pdone + t, 1);
-  }
-  return true;
-}
-
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                        const __grid_constant__ CUtensorMap tmKq,
@@ -431,8 +221,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmPre,
                        const __grid_constant__ CUtensorMap tmU,
-                       const __grid_constant__ CUtensorMap tmG,
-                       const __grid_constant__ CUtensorMap tmKl, const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tmG, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -459,8 +248,6 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
       mbar_init(smem_u32(&bar->uq_full[q]), 1);
       mbar_init(smem_u32(&bar->uq_empty[q]), QUEUE_AGENTS);
     }
-    for (int k = 0; k < SLOTS; ++k) mbar_init(smem_u32(&bar->ps_full[k]), 1);
-    mbar_init(smem_u32(&bar->ps_free), SCAN_WARPS);
     mbar_init(smem_u32(&bar->drain), 1);
     bar->abort_flag = 0;
     fence_mbar_init();
@@ -473,16 +260,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // This kernel may start while the kernel launched before it still runs.
-  // With prefix items that kernel is the projection, which writes
-  // everything read here (U, V, the heads, the bias table, the zeroed work
-  // counter and flags): the producer waits for it before taking its first
-  // ticket, and the other roles touch that data only for tickets the
-  // producer has handed them.  Without prefix items it is the chunk-state
-  // kernel: everything except the prefix states was written by the
-  // projection, which completed before any CTA of that kernel got past its
-  // own griddepcontrol.wait, and the producer waits for that kernel itself
-  // just before its first prefix load.
+  // This kernel may start while the chunk-state/scan kernel launched before
+  // it still runs: everything except the prefix states (U, V, the heads, the
+  // zeroed work counter) was written by the projection, which completed
+  // before any CTA of that kernel got past its own griddepcontrol.wait, and
+  // the producer waits for that kernel itself just before its first prefix
+  // load.
   griddep_launch_dependents();
   const uint32_t tmem = bar->tmem_base;
   // unit queue: entry q of this CTA's sequence sits in slot q & 3
@@ -525,31 +308,16 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         mbar_arrive(smem_u32(&bar->uq_full[q & 3]));
         return true;
       };
-      const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
-      bool prefix_ready = p.n_pitems > 0;
-      if (prefix_ready) griddep_wait();
+      bool prefix_ready = false;
       for (int i = 0;; ++i) {
         int u = atomicAdd(p.next_unit, 1);
-        if (u >= p.n_pitems + p.total) u = -1;
+        if (u >= p.total) u = -1;
         ok = push(i, u);
         if (!ok || u < 0) break;
-        if (u < p.n_pitems) {
-          // prefix item: per chunk of the segment, per 64 tokens, the
-          // K_lin^T atom pair (M-major) and the V rows of the value tile
-          const PItem x = pitem_of(p, u);
-          for (int k = 0; ok && k < x.nL; ++k) {
-            const long long tok0 = (long long)(x.b * p.G + x.g0 + k) * p.C;
-            for (int kb = 0; ok && kb < p.C / 64; ++kb)
-              ok = load(&tmKl, 2, 0, tok0 + kb * 64) &&
-                   load(&tmV, 1, 0, rb64_row(tok0 + kb * 64, x.jt * ET, ncb));
-          }
-          if (!ok) break;
-          continue;
-        }
-        u -= p.n_pitems;
         const Unit x = unit_of(p, u);
         const long long qrow = x.tok0 + x.qt * QT;
         const long long pre_row0 = (long long)(p.per_chunk ? x.chunk : x.b) * SD;
+        const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
         if (x.nkb > 0) ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
         for (int t = 0; ok && t < x.ng; ++t) {
           const int col = (x.et0 + t) * ET;
@@ -573,20 +341,6 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             mbar_arrive_expect_tx(f, Q_BYTES);
             tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
             tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
-          }
-          if (ok && p.n_pitems > 0) {
-            // the prefix item that writes this prefix state has stored it
-            const int *done = p.pdone + pitem_for(p, x.b, x.chunk - x.b * p.G, x.et0 + t);
-            const uint64_t t0 = globaltimer();
-            for (uint32_t n = 0; ld_acquire_gpu(done) < SCAN_WARPS; ++n) {
-              if ((n & 15u) == 15u && (*abort || globaltimer() - t0 > kWaitLimitNs)) {
-                ok = false;
-                break;
-              }
-              __nanosleep(64);
-            }
-            // its generic-proxy stores before this thread's TMA loads
-            fence_proxy_async_global();
           }
           ok = ok && load(&tmPre, 1, 0, rb64_row(pre_row0, col, ncb)) &&
                load(&tmPre, 1, 0, rb64_row(pre_row0 + 64, col, ncb));
@@ -671,61 +425,12 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         mma_commit(smem_u32(&bar->empty[st]));
         return true;
       };
-      const uint32_t idesc_st = idesc_bf16_f32(128, ET, 1, 1);
-      int pi = 0;              // prefix items issued so far
-      bool attn_begun = false;  // an attention unit has been issued
       for (int i = 0; ok; ++i) {
-        int u = pop(i);
+        const int u = pop(i);
         if (u < 0) {
           ok = u == -1;
           break;
         }
-        if (u < p.n_pitems) {
-          // prefix item: chunk state k of the segment into TMEM slot k,
-          // once the scan warps have read the previous item's slots
-          const PItem x = pitem_of(p, u);
-          if (pi > 0 && !mbar_wait(smem_u32(&bar->ps_free), (pi - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int k = 0; ok && k < SLOTS; ++k) {
-            for (int kb = 0; k < x.nL && kb < p.C / 64; ++kb) {
-              int sa, sb;
-              if (!(next_stage(sa) && next_stage(sb))) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // A = K_lin^T: two 64-wide M blocks 8 KB apart, 16 tokens a
-              // step; B = V: two 64-wide N blocks 8 KB apart
-              const uint64_t da = sw128_desc(stage_addr(sa), B_BOX_BYTES, 1024);
-              const uint64_t db = sw128_desc(stage_addr(sb), B_BOX_BYTES, 1024);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss(tmem + k * ET, desc_advance(da, kk * 2048), desc_advance(db, kk * 2048),
-                           idesc_st, (kb | kk) != 0);
-              mma_commit(smem_u32(&bar->empty[sa]));
-              mma_commit(smem_u32(&bar->empty[sb]));
-            }
-            // every slot completes once per item, used or not
-            if (ok) mma_commit(smem_u32(&bar->ps_full[k]));
-          }
-          if (!ok) break;
-          ++pi;
-          release(i);
-          continue;
-        }
-        if (!attn_begun) {
-          // the attention's TMEM buffers are the prefix slots
-          if (pi > 0 && !mbar_wait(smem_u32(&bar->ps_free), (pi - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          attn_begun = true;
-        }
-        u -= p.n_pitems;
         const Unit x = unit_of(p, u);
         const int n0 = n;
         if (x.nkb > 0) ok = issue_s(true, x.q_per_block || x.nkb == 1);
@@ -774,7 +479,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // row inside the query tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int n = 0, pi = 0;
+    int n = 0;
     bool ok = true;
     for (int q = 0; ok; ++q) {
       const int u = pop(q);
@@ -782,13 +487,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         ok = u == -1;
         break;
       }
-      if (u < p.n_pitems) {
-        ok = scan_item(p, bar, tmem, u, pi++, warp, lane, abort);
-        __syncwarp();
-        if (ok && lane == 0) release(q);
-        continue;
-      }
-      const Unit x = unit_of(p, u - p.n_pitems);
+      const Unit x = unit_of(p, u);
       for (int kb = 0; kb < x.nkb; ++kb, ++n) {
         const int sb = n & 1;
         if (!mbar_wait(smem_u32(&bar->s_full[sb]), (n >> 1) & 1, abort)) {
@@ -828,24 +527,11 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                   (int)(x.tok0 + x.qt * QT + quarter * 32));
     };
     bool ok = true;
-    int i0 = 0;
     int cur = pop(0);
     ok = cur != -2;
-    // prefix items first (they hold the lowest tickets)
-    for (int pi = 0; ok && cur >= 0 && cur < p.n_pitems; ++pi) {
-      ok = scan_item(p, bar, tmem, cur, pi, warp, lane, abort);
-      __syncwarp();
-      if (!ok) break;
-      if (lane == 0) release(i0);
-      cur = pop(++i0);
-      ok = cur != -2;
-    }
-    // attention units from here on: indices without the prefix items
-    auto unit_idx = [&](int t) { return t < 0 ? t : t - p.n_pitems; };
-    cur = unit_idx(cur);
-    if (ok) load_u(cur, 0, 0);
+    load_u(cur, 0, 0);
     int v = 0;
-    for (int i = i0; ok && cur >= 0; ++i) {
+    for (int i = 0; ok && cur >= 0; ++i) {
       const Unit x = unit_of(p, cur);
       const int grow = (int)(x.tok0 + x.qt * QT + quarter * 32);
       int nxt = -1;
@@ -855,7 +541,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         // later).  Not earlier: the producer announces it only after all of
         // this unit's loads, which need the earlier value tiles drained.
         if (t + 1 == x.ng) {
-          nxt = unit_idx(pop(i + 1));
+          nxt = pop(i + 1);
           if (nxt == -2) {
             ok = false;
             break;
@@ -924,19 +610,11 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
 
 }  // namespace
 
-namespace {
-
-// fused: the chunk states and their prefix sums as the kernel's first work
-// items (no chunk mask); else the prefix states come from the chunk-state
-// kernel launched just before.
-cudaError_t launch_attention(const Problem &pr, bool fused) {
+cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   const __nv_bfloat16 *heads = (const __nv_bfloat16 *)pr.heads;
   const long long Ms = pr.M * pr.s;
-  CUtensorMap tQq, tKq, tQl, tV, tPre, tU, tG, tKl;
+  CUtensorMap tQq, tKq, tQl, tV, tPre, tU, tG;
   cudaError_t err;
-  // K_lin in 64-token x 64-column boxes: two make one M-major A atom pair
-  if ((err = make_tmap_bf16_2d(&tKl, heads + 3 * Ms, pr.M, pr.s, pr.s, 64, 64)) != cudaSuccess)
-    return err;
   if ((err = make_tmap_bf16_2d(&tQq, heads, pr.M, pr.s, pr.s, QT, 64)) != cudaSuccess) return err;
   if ((err = make_tmap_bf16_2d(&tKq, heads + Ms, pr.M, pr.s, pr.s, KB, 64)) != cudaSuccess)
     return err;
@@ -993,35 +671,9 @@ cudaError_t launch_attention(const Problem &pr, bool fused) {
   p.bias = pr.bias;
   p.status = pr.status;
   p.next_unit = pr.status + kNextUnitWord;
-  p.B = pr.B;
-  p.lin_scale = pr.lin_scale;
-  p.n_pitems = 0;
-  p.L = 1;
-  p.n_seg = 1;
-  p.pflag = p.pdone = nullptr;
-  p.pagg = p.pincl = nullptr;
-  p.prefix = (__nv_bfloat16 *)pr.prefix;
-  if (fused) {
-    if (pr.s != SD || pr.e % ET != 0 || pr.C % 64 != 0 || !pr.scan_flags)
-      return cudaErrorInvalidValue;
-    long long items = 0;
-    scan_geometry(pr.B, pr.G, pr.e, &p.L, &p.n_seg, &items);
-    p.n_pitems = (int)items;
-    p.pflag = pr.scan_flags;
-    p.pdone = pr.scan_flags + items * SCAN_WARPS;
-    p.pagg = pr.scan_agg;
-    p.pincl = pr.scan_incl;
-  }
-  const int work = p.n_pitems + p.total;
-  const int grid = work < pr.num_sms ? work : pr.num_sms;
+  const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;
   return launch_pdl(chunk_attention_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
-                    tQq, tKq, tQl, tV, tPre, tU, tG, tKl, p);
+                    tQq, tKq, tQl, tV, tPre, tU, tG, p);
 }
-
-}  // namespace
-
-cudaError_t tc_chunk_attention_bf16(const Problem &pr) { return launch_attention(pr, false); }
-
-cudaError_t tc_scan_attention_bf16(const Problem &pr) { return launch_attention(pr, true); }
 
 }  // namespace flashgau

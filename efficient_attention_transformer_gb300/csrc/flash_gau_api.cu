@@ -101,14 +101,6 @@ int layout(int B, int T, int C, int d, int e, int s, int causal, int dtype,
   off = align_up(off + M * d * io);
   L->rope = off;
   off = align_up(off + (size_t)T * (s / 2) * 4);
-  L->scan = off;
-  if (dtype == FLASH_GAU_BF16) {
-    int sL = 0, nseg = 0;
-    long long items = 0;
-    scan_geometry(B, (int)G, e, &sL, &nseg, &items);
-    off = align_up(off + (size_t)items * kScanWordsPerItem * sizeof(int));
-    off = align_up(off + 2 * (size_t)items * kScanPartBytes);
-  }
   L->total_bytes = off;
   return FLASH_GAU_OK;
 }
@@ -233,29 +225,17 @@ const Stage kStagesF32[] = {
     {"chunk_attention", simt_chunk_attention_f32},
     {"output", simt_output_f32},
 };
-// bf16: the chunk states and their prefix sums inside the attention kernel
 const Stage kStagesBF16[] = {
-    {"projection", tc_projection_bf16},
-    {"chunk_scan_attention", tc_scan_attention_bf16},
-    {"output", tc_output_bf16},
-};
-// bf16 with a chunk mask (segments, averaging): a chunk-state kernel with
-// its own scan before the attention
-const Stage kStagesBF16Masked[] = {
     {"projection", tc_projection_bf16},
     {"chunk_state_scan", tc_chunk_state_scan_bf16},
     {"chunk_attention", tc_chunk_attention_bf16},
     {"output", tc_output_bf16},
 };
 
-const Stage *stages(int dtype, bool masked, int *n) {
+const Stage *stages(int dtype, int /*causal*/, int *n) {
   if (dtype == FLASH_GAU_FP32) {
     *n = (int)(sizeof(kStagesF32) / sizeof(kStagesF32[0]));
     return kStagesF32;
-  }
-  if (dtype == FLASH_GAU_BF16 && masked) {
-    *n = (int)(sizeof(kStagesBF16Masked) / sizeof(kStagesBF16Masked[0]));
-    return kStagesBF16Masked;
   }
   if (dtype == FLASH_GAU_BF16) {
     *n = (int)(sizeof(kStagesBF16) / sizeof(kStagesBF16[0]));
@@ -375,21 +355,6 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.bias = reinterpret_cast<float *>(ws + L.bias);
   p.xn = ws + L.xn;
   p.rope_cs = ws + L.rope;
-  p.scan_flags = nullptr;
-  p.n_scan_words = 0;
-  p.scan_agg = p.scan_incl = nullptr;
-  const bool masked = p.seg_ids || p.chunk_average;
-  if (dtype == FLASH_GAU_BF16 && !masked) {
-    int sL = 0, nseg = 0;
-    long long items = 0;
-    scan_geometry(B, p.G, p.e, &sL, &nseg, &items);
-    p.scan_flags = reinterpret_cast<int *>(ws + L.scan);
-    p.n_scan_words = (int)(items * kScanWordsPerItem);
-    p.scan_agg = reinterpret_cast<float *>(
-        ws + align_up(L.scan + (size_t)items * kScanWordsPerItem * sizeof(int)));
-    p.scan_incl = reinterpret_cast<float *>(reinterpret_cast<char *>(p.scan_agg) +
-                                            (size_t)items * kScanPartBytes);
-  }
   p.stream = (cudaStream_t)stream;
   p.num_sms = num_sms;
   p.norm = blk ? blk->norm : FLASH_GAU_NORM_NONE;
@@ -404,7 +369,7 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   if (p.rope) rope_table(&p.rope_tab, p.s, p.rope_base);
 
   int n = 0;
-  const Stage *sched = stages(dtype, masked, &n);
+  const Stage *sched = stages(dtype, causal, &n);
   Stage full[8];
   int nf = 0;
   if (p.norm != FLASH_GAU_NORM_NONE) full[nf++] = {"norm", block_norm};
@@ -445,15 +410,15 @@ size_t flash_gau_workspace_bytes(int B, int T, int C, const flash_gau_weights *w
   return L.total_bytes;
 }
 
-int flash_gau_num_stages(int dtype, int /*causal*/) {
+int flash_gau_num_stages(int dtype, int causal) {
   int n = 0;
-  stages(dtype, false, &n);
+  stages(dtype, causal, &n);
   return n;
 }
 
-const char *flash_gau_stage_name(int dtype, int /*causal*/, int k) {
+const char *flash_gau_stage_name(int dtype, int causal, int k) {
   int n = 0;
-  const Stage *st = stages(dtype, false, &n);
+  const Stage *st = stages(dtype, causal, &n);
   if (!st || k < 0 || k >= n) return nullptr;
   return st[k].name;
 }

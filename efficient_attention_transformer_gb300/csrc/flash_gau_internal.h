@@ -81,25 +81,9 @@ struct Problem {
   RopeTable rope_tab;  // filled when rope is set
   void *rope_cs;       // [s / 2][T] half2 (cos, sin), bf16 path
   const void *residual;
-  // bf16 forward without a chunk mask: the look-back scan of the chunk
-  // states inside the attention kernel (flags zeroed by the projection)
-  int *scan_flags;  // [items][17]: 16 per-warp look-back flags, then a done count
-  int n_scan_words;
-  float *scan_agg, *scan_incl;  // [items][16][32][32] fp32 each
   cudaStream_t stream;
   int num_sms;
 };
-
-// Geometry of the look-back scan of the chunk states: a work item is (batch
-// row, 128-column value tile, segment of L <= 4 consecutive chunks, which
-// fill the four 128-column TMEM slots of one SM).
-inline void scan_geometry(int B, int G, int e, int *L, int *n_seg, long long *items) {
-  *L = G < 4 ? G : 4;
-  *n_seg = (G + *L - 1) / *L;
-  *items = (long long)B * (e / 128) * *n_seg;
-}
-constexpr int kScanWordsPerItem = 17;
-constexpr size_t kScanPartBytes = 16 * 32 * 32 * 4;  // one item's aggregate (or inclusive sum)
 
 // The status word's 256-byte workspace slot also holds, at these int
 // offsets, the work counter of the chunk-attention kernel and the arrival
@@ -272,10 +256,7 @@ cudaError_t tc_projection_bf16(const Problem &p);
 cudaError_t tc_chunk_state_scan_bf16(const Problem &p);
 cudaError_t tc_output_bf16(const Problem &p);
 
-// bf16 tensor-core chunk attention (chunk_attention.cu): after the
-// chunk-state kernel, or with the chunk states and their look-back scan as
-// its first work items
+// bf16 tensor-core chunk attention (chunk_attention.cu)
 cudaError_t tc_chunk_attention_bf16(const Problem &p);
-cudaError_t tc_scan_attention_bf16(const Problem &p);
 
 }  // namespace flashgau

@@ -60,9 +60,6 @@ struct Params {
   int e, s;
   int *status;
   int *sched;  // projection: the scheduling words of the workspace, zeroed here
-  // projection: the attention kernel's look-back flags, zeroed here
-  int *scan_words;
-  int n_scan_words;
   // projection: the attention kernel's bias table, written here
   const float *relpos;
   float *bias;
@@ -188,16 +185,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   // setup above overlaps the previous kernel's tail; its outputs are read below
   griddep_wait();
   griddep_launch_dependents();
-  // The chunk-state kernel's grid barrier, the chunk-attention kernel's
-  // work counter and its look-back flags start from zero.  Those kernels
-  // touch them only after this grid has completed (after their own
-  // griddepcontrol.wait, or once every CTA of the chunk-state kernel has
-  // passed that wait), and the previous forward's kernels had all completed
-  // before this one got past its wait.
-  if (EPI != EPI_STORE)
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < p.n_scan_words;
-         k += gridDim.x * blockDim.x)
-      p.scan_words[k] = 0;
+  // The chunk-state kernel's grid barrier and the chunk-attention kernel's
+  // work counter start from zero.  Both kernels touch them only after this
+  // grid has completed (the first after its griddepcontrol.wait, the second
+  // once every CTA of the first has passed that wait), and the previous
+  // forward's kernels had all completed before this one got past its wait.
   if (EPI != EPI_STORE && blockIdx.x == 0) {
     if (threadIdx.x == 0) {
       p.sched[kNextUnitWord] = 0;
@@ -507,8 +499,6 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   p.gamma = pr.gamma;
   p.beta = pr.beta;
   p.sched = pr.status;
-  p.scan_words = pr.scan_flags;
-  p.n_scan_words = pr.scan_flags ? pr.n_scan_words : 0;
   p.T_seq = pr.T;
   p.rope_cs = (const uint32_t *)pr.rope_cs;
   p.relpos = pr.relpos;

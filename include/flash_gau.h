@@ -91,9 +91,7 @@ typedef struct flash_gau_workspace_layout {
   size_t U;             /* [B*T, e] io: swish(X W_u)                        */
   size_t V;             /* [B*T, e] io: swish(X W_v)                 (*)    */
   size_t heads;         /* [4, B*T, s] io: Q_quad, K_quad, Q_lin, K_lin      */
-  size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk   (*);
-                           written only by the FP32 forward and by a
-                           forward with a chunk mask (segments)             */
+  size_t state;         /* [B, G, s, e] io: K_lin,g^T V_g per chunk   (*)    */
   size_t prefix;        /* [B, G, s, e] io: lin_scale * (exclusive / total)
                            chunk-state sum of each chunk; a non-causal
                            forward without segments writes only the first
@@ -106,10 +104,6 @@ typedef struct flash_gau_workspace_layout {
                            flash_gau_block_forward (unused otherwise)       */
   size_t rope;          /* [s/2, T] fp16 (cos, sin) pairs: the RoPE table of
                            flash_gau_block_forward, bf16 (unused otherwise) */
-  size_t scan;          /* BF16 only (0 bytes for FP32): flags, per-segment
-                           aggregates and inclusive sums (fp32) of the
-                           look-back scan over the chunk states that the
-                           bf16 attention kernel runs without a chunk mask  */
 } flash_gau_workspace_layout;
 /* Intermediates are row-major, except those marked (*) for FLASH_GAU_BF16:
  * these, seen as [rows, e] matrices (rows = B*T, B*G*s or B*s), are stored
@@ -165,13 +159,8 @@ int flash_gau_forward_timed(const void *X, const flash_gau_weights *w, int B,
                             void *stream, void *const *stage_events,
                             int n_events);
 
-/* Number of kernel stages one forward (flash_gau_forward, without a chunk
- * mask) launches for this dtype / causality, and a static name for stage k
- * (NULL when out of range).  BF16: projection, chunk_scan_attention (the
- * chunk states, their prefix sums and the chunk attention in one kernel),
- * output.  A forward with a chunk mask (flash_gau_forward_segmented) runs
- * the chunk states and their scan as a kernel of their own before the
- * attention.                                                               */
+/* Number of kernel stages one forward launches for this dtype / causality,
+ * and a static name for stage k (NULL when out of range).                  */
 int flash_gau_num_stages(int dtype, int causal);
 const char *flash_gau_stage_name(int dtype, int causal, int k);
 

@@ -16,8 +16,7 @@ import bench  # noqa: E402
 from efficient_attention_transformer_gb300.synthetic import WORKLOADS  # noqa: E402
 from oracle import algorithmic_flops_per_token  # noqa: E402
 
-BF16_STAGES = ("projection", "chunk_scan_attention", "output")
-BF16_MASKED_STAGES = ("projection", "chunk_state_scan", "chunk_attention", "output")
+BF16_STAGES = ("projection", "chunk_state_scan", "chunk_attention", "output")
 FP32_STAGES = ("projection", "chunk_state", "prefix_scan", "chunk_attention", "output")
 
 
@@ -25,15 +24,14 @@ FP32_STAGES = ("projection", "chunk_state", "prefix_scan", "chunk_attention", "o
 def test_stage_flops_add_up_to_the_oracle_formula(name):
     w = WORKLOADS[name]
     work = bench.stage_work(w)
+    stages = BF16_STAGES if w["dtype"] == "bf16" else FP32_STAGES
+    total = sum(work[n][0] for n in stages)
     M = w["B"] * w["T"]
     want = M * algorithmic_flops_per_token(w["d"], w["e"], w["s"], w["C"], w["causal"])
     # the stages also count the scan's additions, B*G*s*e, which the
     # per-token formula leaves out
     extra = w["B"] * (w["T"] // w["C"]) * w["s"] * w["e"]
-    schedules = (BF16_STAGES, BF16_MASKED_STAGES) if w["dtype"] == "bf16" else (FP32_STAGES,)
-    for stages in schedules:
-        total = sum(work[n][0] for n in stages)
-        assert total == pytest.approx(want + extra, rel=1e-12), stages
+    assert total == pytest.approx(want + extra, rel=1e-12)
 
 
 def test_reference_arm_prints_the_contract_line():

@@ -33,10 +33,7 @@ def _check_all(case, O, ref, inter):
     errs["U"] = rel_err(case.intermediate("U"), inter["U"].reshape(M, -1))
     errs["V"] = rel_err(case.intermediate("V"), inter["V"].reshape(M, -1))
     errs["heads"] = rel_err(case.intermediate("heads"), inter["heads"].reshape(4, M, -1))
-    if case.dtype == "fp32":
-        # the bf16 forward scans the chunk states without storing them
-        errs["state"] = rel_err(case.intermediate("state"),
-                                inter["state"].reshape(-1, case.s, case.e))
+    errs["state"] = rel_err(case.intermediate("state"), inter["state"].reshape(-1, case.s, case.e))
     pre = inter["prefix"] * case.lin_scale
     if not case.causal:
         pre = pre[:, 0]
