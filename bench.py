@@ -177,6 +177,80 @@ def job_tokens_per_s(tokens_per_rank, world, ms):
     return tokens_per_rank * world / (ms * 1e-3)
 
 
+def run_part(args, dev):
+    """One component alone, a few calls, for profiling a kernel under ncu
+    without the rest of the bench: the layer, the flash_block wrapper, the
+    RoPE table, the backward, decode steps (B = 1, 16, 64), or the fp32
+    layer on the small workload.  Returns a short record."""
+    import torch
+    import efficient_attention_transformer_gb300 as fg
+    from efficient_attention_transformer_gb300 import binding as bd
+    from efficient_attention_transformer_gb300.synthetic import WORKLOADS, make_inputs
+    name = "tiny_causal_fp32_T256" if args.part == "fp32" else args.workload
+    w = dict(WORKLOADS[name])
+    B, T, d, e, s, C, causal = w["B"], w["T"], w["d"], w["e"], w["s"], w["C"], w["causal"]
+    tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    inp = make_inputs(**w)
+    W_uvz = np.concatenate([inp["W_u"], inp["W_v"], inp["W_z"]], axis=1)
+    weights = fg.GauWeights(torch.tensor(W_uvz, dtype=tdt, device=dev),
+                            torch.tensor(inp["W_o"], dtype=tdt, device=dev),
+                            torch.tensor(inp["gamma"], dtype=torch.float32, device=dev),
+                            torch.tensor(inp["beta"], dtype=torch.float32, device=dev),
+                            torch.tensor(inp["relpos"], dtype=torch.float32, device=dev),
+                            d, e, s)
+    X = torch.tensor(inp["X"], dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = args.warmup + args.steps
+    calls = 0
+    t0 = time.perf_counter()
+    if args.part in ("layer", "fp32", "block"):
+        ws = weights.new_workspace(B, T, C, causal, dev)
+        out = torch.empty_like(X)
+        g = torch.ones(d, dtype=torch.float32, device=dev)
+        for _ in range(n):
+            if args.part == "block":
+                bd.block_forward(X, weights, C, causal, norm=bd.NORM_LAYER, norm_g=g, norm_b=g,
+                                 out=out, workspace=ws, stream=stream)
+            else:
+                bd.forward(X, weights, C, causal, out=out, workspace=ws, stream=stream)
+            calls += 1
+        status = bd.workspace_status(ws)
+    elif args.part == "rope":
+        a = torch.ones(128, dtype=torch.float32, device=dev)
+        tout = torch.empty(2 * 512 - 1, dtype=torch.float32, device=dev)
+        for _ in range(n):
+            bd.rope_toeplitz_bias(a, a, 512, out=tout, stream=stream)
+            calls += 1
+        status = 0
+    elif args.part == "backward":
+        dO = torch.tensor(np.random.default_rng(3000 + w["seed"]).normal(size=(B, T, d)),
+                          dtype=tdt, device=dev)
+        bws = torch.empty(lib_backward_bytes(bd, weights, B, T, C, causal), dtype=torch.uint8,
+                          device=dev)
+        for _ in range(n):
+            bd.backward(X, dO, weights, C, causal, workspace=bws, stream=stream)
+            calls += 1
+        status = bd.workspace_status(bws)
+    elif args.part == "decode":
+        status = 0
+        for Bd in (1, 16, 64):
+            dec = bd.Decoder(weights, Bd, C)
+            xs = torch.tensor(np.random.default_rng(4000 + Bd).normal(size=(Bd, d)), dtype=tdt,
+                              device=dev)
+            od = torch.empty_like(xs)
+            for _ in range(n):
+                dec.step(xs, out=od, stream=stream)
+                calls += 1
+            del dec
+    else:
+        raise ValueError("unknown part %r" % args.part)
+    torch.cuda.synchronize()
+    if status != 0:
+        raise RuntimeError("kernel status %d in part %s" % (status, args.part))
+    return {"part": args.part, "workload": name, "calls": calls,
+            "wall_ms_per_call": round((time.perf_counter() - t0) * 1e3 / max(1, calls), 4)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import efficient_attention_transformer_gb300 as fg
@@ -187,6 +261,8 @@ def run_ours(args, rank, world, local_rank):
     build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    if args.part != "all":
+        return run_part(args, dev)
     w = dict(WORKLOADS[args.workload])
     B, T, d, e, s, C, causal = w["B"], w["T"], w["d"], w["e"], w["s"], w["C"], w["causal"]
     tdt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
@@ -741,6 +817,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", default="all",
+                    choices=["all", "layer", "block", "rope", "backward", "decode", "fp32"],
+                    help="run one component alone (a profiling aid; prints a short record)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
