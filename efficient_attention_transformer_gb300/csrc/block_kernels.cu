@@ -240,23 +240,26 @@ bool norm_fills_rope_table(const Problem &p) {
 // relpos[k] = rope(a)_i . rope(b)_j for any i, j with j - i = k - (C - 1):
 // rotating a by i and b by j leaves a . R(j - i) b, per pair
 // (a0 b0 + a1 b1) cos(delta) + (a1 b0 - a0 b1) sin(delta), delta = (j - i)
-// times the pair's frequency.  One thread per entry, fp32 sums over the
-// pairs, the angles from the same exact-turns method as the heads' RoPE.
+// times the pair's frequency.  One warp per entry, the lanes taking pairs
+// q = lane, lane + 32, ..., fp32 partial sums added by a butterfly; the
+// angles from the same exact-turns method as the heads' RoPE.
 __global__ void __launch_bounds__(256)
 rope_toeplitz_kernel(const float *__restrict__ a, const float *__restrict__ b, int pairs, int C,
                      const RopeTable phi, float *__restrict__ relpos) {
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  const int k = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
   if (k >= 2 * C - 1) return;
   const float off = (float)(k - (C - 1));  // exact: |off| < 2^24
   float acc = 0.f;
-  for (int q = 0; q < pairs; ++q) {
+  for (int q = lane; q < pairs; q += 32) {
     float sn, cs;
     rope_sincos(off, phi.phi[q], &sn, &cs);
     const float a0 = a[2 * q], a1 = a[2 * q + 1], b0 = b[2 * q], b1 = b[2 * q + 1];
     acc = fmaf(fmaf(a0, b0, a1 * b1), cs, acc);
     acc = fmaf(fmaf(a1, b0, -a0 * b1), sn, acc);
   }
-  relpos[k] = acc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) relpos[k] = acc;
 }
 
 }  // namespace
@@ -286,8 +289,8 @@ cudaError_t rope_toeplitz_bias(const float *a, const float *b, int m, int C, flo
                                float *relpos, cudaStream_t stream) {
   RopeTable phi;
   rope_table(&phi, m, base);
-  const unsigned n = (unsigned)(2 * C - 1);
-  rope_toeplitz_kernel<<<(n + 255) / 256, 256, 0, stream>>>(a, b, m / 2, C, phi, relpos);
+  const unsigned n = (unsigned)(2 * C - 1);  // entries, one warp each, 8 a block
+  rope_toeplitz_kernel<<<(n + 7) / 8, 256, 0, stream>>>(a, b, m / 2, C, phi, relpos);
   return cudaGetLastError();
 }
 

@@ -18,14 +18,20 @@
 //   output   gated W_o in depth slices
 //   finish   out = the slices' sum; at a chunk's last token
 //            Prefix += K_lin,chunk^T V_chunk
-// The projections stream the weights once per step for all B sequences
-// (split-K matrix-vector products on the CUDA cores with 16-byte weight
-// loads); everything is fp32 inside.  The step is latency-bound: the
-// kernels keep several independent loads in flight per thread.
+// The projections stream the weights once per step for all B sequences.
+// For bf16 io they run on the tcgen05 tensor cores: y^T = W^T x^T with 128
+// weight columns in the TMEM lanes and the sequences as the MMA's N (up to
+// 256), split over the depth in about 150 blocks, the weight tiles loaded by
+// TMA before the step's input is ready (programmatic dependent launch).  For
+// fp32 io they are split-K matrix-vector products on the CUDA cores with
+// 16-byte weight loads.  Sums, scores and caches are fp32.  The step is
+// latency-bound: the kernels keep several independent loads in flight per
+// thread.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"
 #include "sm103_ptx.cuh"
+#include "tma_host.h"
 
 namespace flashgau {
 namespace {
@@ -137,6 +143,116 @@ gemv_splitk(const Tx *__restrict__ x, int B, const Tw *__restrict__ W, int K, in
   }
 }
 
+// Split-K product on the tensor cores, bf16 operands, fp32 accumulation:
+// part[slice][b][c] = sum over the slice's rows k of x[b][k] W[k][c], as
+// y^T = W^T x^T.  Block (128 weight columns, depth slice of kbs 64-row
+// k-blocks): A = the W tile, two 64-column boxes per k-block read M-major;
+// B = the sequences' x rows (npad = B rounded up to 16, rows past B read as
+// zeros), K-major; D = [128 columns, npad sequences] fp32 in TMEM.  Thread 0
+// issues the weight loads before waiting for the kernel before (the weights
+// are inputs), then the x loads and the MMAs; each of the four warps drains
+// its 32 columns (thread = column, registers = sequences), so the stores of
+// one sequence's columns are coalesced.  Every wait is bounded.
+constexpr int kTcCols = 128;
+constexpr int kTcMaxKb = 4;
+constexpr int kTcW = 64 * 64 * 2;  // one 64 x 64 weight box
+__host__ __device__ constexpr size_t tc_stage_bytes(int npad) { return 2 * kTcW + (size_t)npad * 128; }
+
+__global__ void __launch_bounds__(128, 1)
+decode_tc_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+               int B, int npad, int K, int N, int kbs, float *__restrict__ part, int *pos,
+               int *status) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_w, bar_x, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n0 = blockIdx.x * kTcCols;
+  const int nkb_all = (K + 63) / 64, kb0 = blockIdx.y * kbs;
+  const int nkb = min(kbs, nkb_all - kb0);
+  const uint32_t tcols = npad <= 32 ? 32 : npad <= 64 ? 64 : npad <= 128 ? 128 : 256;
+  const size_t stage = tc_stage_bytes(npad);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar_w), 1);
+    mbar_init(smem_u32(&bar_x), 1);
+    mbar_init(smem_u32(&bar_mma), 1);
+    failed = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    // the weight tiles: inputs, loaded while the kernel before still runs
+    mbar_arrive_expect_tx(smem_u32(&bar_w), (uint32_t)(nkb * 2 * kTcW));
+    for (int k = 0; k < nkb; ++k)
+      for (int h = 0; h < 2; ++h)
+        tma_load_2d(smem_u32(tiles + k * stage + h * kTcW), &tmW, smem_u32(&bar_w), n0 + 64 * h,
+                    (kb0 + k) * 64);
+  }
+  griddep_launch_dependents();
+  griddep_wait();  // x comes from the kernel before
+  if (pos && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int b = threadIdx.x; b < B; b += blockDim.x) pos[b] += 1;
+  const uint32_t idesc = idesc_bf16_f32(kTcCols, npad, 1, 0);
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bar_x), (uint32_t)(nkb * npad * 128));
+    for (int k = 0; k < nkb; ++k)
+      tma_load_2d(smem_u32(tiles + k * stage + 2 * kTcW), &tmX, smem_u32(&bar_x), (kb0 + k) * 64, 0);
+    if (mbar_wait(smem_u32(&bar_w), 0) && mbar_wait(smem_u32(&bar_x), 0)) {
+      tc_fence_after();
+      for (int k = 0; k < nkb; ++k) {
+        // A: W^T, M-major, the two 64-column boxes 8 KB apart, 16 rows of
+        // 128 B per step; B: x rows, K-major, 32 B per step
+        const uint64_t da = sw128_desc(smem_u32(tiles + k * stage), kTcW, 1024);
+        const uint64_t db = sw128_desc(smem_u32(tiles + k * stage + 2 * kTcW), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_ss(tmem_base, desc_advance(da, kk * 2048), desc_advance(db, kk * 32), idesc,
+                     (k | kk) != 0);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    } else {
+      failed = 1;
+      atomicExch(status, FLASH_GAU_ETIMEOUT);
+    }
+  }
+  __syncthreads();
+  bool ok = !failed && mbar_wait(smem_u32(&bar_mma), 0);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+    tc_fence_after();
+    const int col = n0 + warp * 32 + lane;
+    const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
+    float *dst = part + (size_t)blockIdx.y * B * N + col;
+    for (int c0 = 0; c0 < npad; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(taddr + c0, v);
+      tmem_ld_wait();
+      if (col < N)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < B) dst[(size_t)(c0 + j) * N] = __uint_as_float(v[j]);
+    }
+  } else if (lane == 0) {
+    atomicExch(status, FLASH_GAU_ETIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tcols);
+  }
+}
+
 // The chunk weights of the new token, once per sequence: block (32-key
 // tile, sequence), 8 warps of 4 keys each.  Each block forms z = swish of
 // the projection's Z slices and the two quadratic heads it needs; block 0
@@ -222,7 +338,8 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 }
 
 __global__ void __launch_bounds__(32 * kAttW)
-decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_scale) {
+decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_scale,
+              __nv_bfloat16 *gated_io) {
   __shared__ float4 red[kAttW][32];
   griddep_launch_dependents();
   griddep_wait();
@@ -282,8 +399,14 @@ decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kAttW; ++w) v = add4(v, red[w][lane]);
-    *reinterpret_cast<float4 *>(L.gated + (long long)b * e + c) =
-        make_float4(u.x * v.x, u.y * v.y, u.z * v.z, u.w * v.w);
+    const float4 g = make_float4(u.x * v.x, u.y * v.y, u.z * v.z, u.w * v.w);
+    *reinterpret_cast<float4 *>(L.gated + (long long)b * e + c) = g;
+    if (gated_io) {
+      // bf16 copy: the tensor-core output projection's operand
+      __nv_bfloat162 h2[2] = {__floats2bfloat162_rn(g.x, g.y), __floats2bfloat162_rn(g.z, g.w)};
+      *reinterpret_cast<uint2 *>(gated_io + (long long)b * e + c) =
+          *reinterpret_cast<const uint2 *>(h2);
+    }
     // the token's row, for the chunk's later keys
     *reinterpret_cast<float4 *>(v_c + (long long)i * e + c) = vnew;
   }
@@ -333,11 +456,41 @@ decode_finish(DecodeLayout L, T *__restrict__ out, int B, int C, int d, int e, i
     if (k0 + t < k1) L.prefix[((long long)b * s + k0 + t) * e + c] += acc[t];
 }
 
+// One tensor-core split-K product: part[slices][B][N] from x [B, K] (bf16)
+// and W [K, N] (bf16); slices from decode_tc_slices.
+cudaError_t tc_product(const void *x, const void *W, int B, int K, int N, float *part, int *pos,
+                       int *status, cudaStream_t stream) {
+  const int npad = (B + 15) / 16 * 16;
+  int kbs = 0;
+  const int slices = decode_tc_slices(K, N, &kbs);
+  CUtensorMap tW, tX;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tW, W, K, N, N, 64, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tX, x, B, K, K, npad, 64)) != cudaSuccess) return err;
+  const size_t smem = kbs * tc_stage_bytes(npad) + 1024;
+  static unsigned long long configured = 0;  // shared-memory ceiling, per device
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  if (!(configured & (1ull << dev))) {
+    if ((err = cudaFuncSetAttribute(decode_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(kTcMaxKb * tc_stage_bytes(kDecodeTcMaxB) + 1024))) !=
+        cudaSuccess)
+      return err;
+    configured |= 1ull << dev;
+  }
+  return launch_pdl(decode_tc_gemm, dim3((N + kTcCols - 1) / kTcCols, slices), dim3(128), smem,
+                    stream, tW, tX, B, npad, K, N, kbs, part, pos, status);
+}
+
 template <typename T>
 cudaError_t step(const DecodeProblem &q) {
   cudaError_t err;
   const int N = 2 * q.e + q.s;
-  const int sp = decode_slices(q.d, N), so = decode_slices(q.e, q.d);
+  // bf16: the projections on the tensor cores
+  const bool tc = sizeof(T) == 2 && q.B <= kDecodeTcMaxB;
+  const int sp = tc ? decode_tc_slices(q.d, N, nullptr) : decode_slices(q.d, N);
+  const int so = tc ? decode_tc_slices(q.e, q.d, nullptr) : decode_slices(q.e, q.d);
   const int ksp = (q.d + sp - 1) / sp, kso = (q.e + so - 1) / so;
 
   static unsigned long long configured = 0;  // shared-memory ceilings, per device
@@ -354,24 +507,29 @@ cudaError_t step(const DecodeProblem &q) {
     configured |= 1ull << dev;
   }
   const int groups = (q.B + kGroup - 1) / kGroup;
-  if ((err = launch_pdl(gemv_splitk<T, T>, dim3((N + kTileN - 1) / kTileN, sp, groups), dim3(256),
-                        kGemvSmem,
-                        q.stream, (const T *)q.x, q.B, (const T *)q.W_uvz, q.d, N, ksp, q.L.proj,
-                        q.L.pos)) != cudaSuccess)
-    return err;
+  if (tc)
+    err = tc_product(q.x, q.W_uvz, q.B, q.d, N, q.L.proj, q.L.pos, q.L.status, q.stream);
+  else
+    err = launch_pdl(gemv_splitk<T, T>, dim3((N + kTileN - 1) / kTileN, sp, groups), dim3(256),
+                     kGemvSmem, q.stream, (const T *)q.x, q.B, (const T *)q.W_uvz, q.d, N, ksp,
+                     q.L.proj, q.L.pos);
+  if (err != cudaSuccess) return err;
   if ((err = launch_pdl(decode_scores, dim3((q.C + kKeyTile - 1) / kKeyTile, q.B), dim3(256), 0,
                         q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
                         q.local_scale)) != cudaSuccess)
     return err;
   if ((err = launch_pdl(decode_attend, dim3((q.e + kAttCols - 1) / kAttCols, q.B), dim3(32 * kAttW),
-                        0, q.stream,
-                        q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale)) != cudaSuccess)
+                        0, q.stream, q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale,
+                        tc ? (__nv_bfloat16 *)q.L.gated_io : (__nv_bfloat16 *)nullptr)) !=
+      cudaSuccess)
     return err;
-  if ((err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so, groups),
-                        dim3(256),
-                        kGemvSmem, q.stream, (const float *)q.L.gated, q.B, (const T *)q.W_o, q.e, q.d,
-                        kso, q.L.outp, (int *)nullptr)) != cudaSuccess)
-    return err;
+  if (tc)
+    err = tc_product(q.L.gated_io, q.W_o, q.B, q.e, q.d, q.L.outp, nullptr, q.L.status, q.stream);
+  else
+    err = launch_pdl(gemv_splitk<float, T>, dim3((q.d + kTileN - 1) / kTileN, so, groups),
+                     dim3(256), kGemvSmem, q.stream, (const float *)q.L.gated, q.B,
+                     (const T *)q.W_o, q.e, q.d, kso, q.L.outp, (int *)nullptr);
+  if (err != cudaSuccess) return err;
   const int fx = ((q.e > q.d ? q.e : q.d) + 255) / 256;
   return launch_pdl(decode_finish<T>, dim3(fx, (q.s + kFoldRows - 1) / kFoldRows, q.B),
                     dim3(256), 0, q.stream,

@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "flash_gau_internal.h"
@@ -181,13 +182,18 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
   if (B > 65535 || C > 4096 || s > 256 || d > 16384 || e > 16384) return FLASH_GAU_ENOTSUP;
   if (d % 8 != 0 || e % 8 != 0 || s % 8 != 0) return FLASH_GAU_ENOTSUP;
   const size_t N = 2 * (size_t)e + s;
-  const size_t sp = decode_slices(d, (int)N), so = decode_slices(e, d);
+  // slices of the CUDA-core split-K products, or of the tensor-core ones
+  // (bf16), whichever is more
+  const size_t sp = std::max(decode_slices(d, (int)N), decode_tc_slices(d, (int)N, nullptr));
+  const size_t so = std::max(decode_slices(e, d), decode_tc_slices(e, d, nullptr));
+  // the tensor-core products read the gated row in the io type (bf16)
+  const size_t gio = (size_t)B * e * 2;
   size_t off = 0;
   auto take = [&](void **p, size_t bytes) {
     *p = base ? base + off : nullptr;
     off = align_up(off + bytes);
   };
-  void *st, *pos, *pre, *kq, *kl, *vc, *proj, *g, *outp, *hd, *sc;
+  void *st, *pos, *pre, *kq, *kl, *vc, *proj, *g, *gb, *outp, *hd, *sc;
   const size_t f = sizeof(float);
   take(&st, sizeof(int));
   take(&pos, (size_t)B * sizeof(int));
@@ -197,6 +203,7 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
   take(&vc, (size_t)B * C * e * f);
   take(&proj, sp * B * N * f);
   take(&g, (size_t)B * e * f);
+  take(&gb, gio);
   take(&outp, so * B * d * f);
   take(&hd, (size_t)B * 4 * s * f);
   take(&sc, (size_t)B * C * f);
@@ -209,6 +216,7 @@ int decode_layout(int B, int C, int d, int e, int s, char *base, DecodeLayout *L
     L->vc = (float *)vc;
     L->proj = (float *)proj;
     L->gated = (float *)g;
+    L->gated_io = gb;
     L->outp = (float *)outp;
     L->heads = (float *)hd;
     L->score = (float *)sc;

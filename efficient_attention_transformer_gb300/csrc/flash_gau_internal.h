@@ -136,6 +136,7 @@ struct DecodeLayout {
   float *vc;       // [B, C, e] the current chunk's V rows
   float *proj;     // [slices, B, 2e+s] this step's x W_uvz, by depth slice
   float *gated;    // [B, e]
+  void *gated_io;  // [B, e] io-type copy of gated (bf16: the tensor-core projection's operand)
   float *outp;     // [slices, B, d] this step's gated W_o, by depth slice
   float *heads;    // [B, 4, s] this step's four heads
   float *score;    // [B, C] this step's chunk weights a_j (local_scale included)
@@ -152,6 +153,20 @@ inline int decode_slices(int K, int N) {
   if (sl < lo) sl = lo;
   if (sl > hi) sl = hi;
   return sl < 1 ? 1 : sl;
+}
+// The bf16 decode step's projections on the tensor cores: y^T = W^T x^T,
+// 128 weight columns (TMEM lanes) x the sequences (up to 256, padded to 16)
+// per block, over a depth slice of kbs 64-row k-blocks (at most 4), about
+// 150 blocks; returns the number of slices.
+constexpr int kDecodeTcMaxB = 256;
+inline int decode_tc_slices(int K, int N, int *kbs) {
+  const int nkb = (K + 63) / 64, tiles = (N + 127) / 128;
+  int sl = (150 + tiles - 1) / tiles;
+  if (sl > nkb) sl = nkb;
+  int kb = (nkb + sl - 1) / sl;
+  if (kb > 4) kb = 4;
+  if (kbs) *kbs = kb;
+  return (nkb + kb - 1) / kb;
 }
 struct DecodeProblem {
   int B, C, d, e, s;

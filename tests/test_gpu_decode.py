@@ -34,6 +34,10 @@ def _built():
     (17, 20, 128, 256, 128, 8, "bf16", 1.0, 1.0),
     (2, 50, 64, 128, 32, 16, "fp32", 1.0, 0.0),    # GlobalOnly
     (3, 40, 128, 256, 128, 16, "bf16", 1.0, 0.5),
+    # the layer's widths with a batch of 64 sequences: the projections run
+    # as tensor-core products over 64 (and 1) padded sequence rows
+    (64, 260, 768, 1536, 128, 256, "bf16", 1.0 / 256, 1.0),
+    (1, 40, 768, 1536, 128, 16, "bf16", 1.0, 1.0),
 ])
 def test_decode_matches_causal_forward(B, steps, d, e, s, C, dtype, lin_scale, local_scale):
     T = -(-steps // C) * C
