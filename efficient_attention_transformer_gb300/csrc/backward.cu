@@ -251,9 +251,11 @@ __global__ void gate_grad(const float *__restrict__ dA, const float *__restrict_
 // diagonal when causal) as a bf16 operand
 // Four columns per thread (C a multiple of 4), over the rows z*C + i of the
 // [B*G*C, C] score matrices.
+// (P_io carries the factor l = local_scale: both contractions that read it
+// multiply P by l)
 __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_io,
                           const float *__restrict__ relpos, long long rows, int C, int causal,
-                          float inv_c) {
+                          float inv_c, float l) {
   pdl_enter();
   const int C4 = C / 4;
   for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < rows * C4;
@@ -270,8 +272,9 @@ __global__ void score_act(float *__restrict__ S, __nv_bfloat16 *__restrict__ P_i
     const float r0 = fmaxf(v.x, 0.f), r1 = fmaxf(v.y, 0.f), r2 = fmaxf(v.z, 0.f),
                 r3 = fmaxf(v.w, 0.f);
     const bool m = causal != 0;
-    store_bf4(P_io + 4LL * q, (m && j > i) ? 0.f : r0 * r0, (m && j + 1 > i) ? 0.f : r1 * r1,
-              (m && j + 2 > i) ? 0.f : r2 * r2, (m && j + 3 > i) ? 0.f : r3 * r3);
+    store_bf4(P_io + 4LL * q, (m && j > i) ? 0.f : l * (r0 * r0),
+              (m && j + 1 > i) ? 0.f : l * (r1 * r1), (m && j + 2 > i) ? 0.f : l * (r2 * r2),
+              (m && j + 3 > i) ? 0.f : l * (r3 * r3));
   }
 }
 
@@ -505,13 +508,12 @@ __global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__r
   }
 }
 
-// The tensor-core path's forms of the two kernels above: Pre comes as bf16
+// The tensor-core path's forms of the kernels above: Pre comes as bf16
 // (the recompute GEMM's output, in the dPre buffer), four columns per
 // thread (e and s multiples of 4), the sigmoid from the fast exponential
 // and division intrinsics (their errors are far below the bf16 rounding of
-// Pre),
-// and only the bf16 operands that the tensor-core contractions read are
-// written besides U and Z.
+// Pre), and only the bf16 operands that the tensor-core contractions read
+// are written besides Z.
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x); }
 __device__ __forceinline__ float swish_grad_fast(float x) {
@@ -519,28 +521,29 @@ __device__ __forceinline__ float swish_grad_fast(float x) {
   return sg * (1.0f + x * (1.0f - sg));
 }
 
-__global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__restrict__ U,
-                             float *__restrict__ Z, const float *__restrict__ gamma,
-                             const float *__restrict__ beta, long long M, int e, int s,
-                             __nv_bfloat16 *__restrict__ V_io, __nv_bfloat16 *__restrict__ H_io) {
+// The tensor-core path keeps no U: U = swish(Pre_u) is recomputed from
+// the bf16 Pre wherever it is needed (the values are those that U held,
+// swish of the same bf16 inputs).  act_heads_vz writes the V and Z parts'
+// operands (V and the heads in bf16, Z in fp32).
+__global__ void act_heads_vz(const __nv_bfloat16 *__restrict__ pre, float *__restrict__ Z,
+                             const float *__restrict__ gamma, const float *__restrict__ beta,
+                             long long M, int e, int s, __nv_bfloat16 *__restrict__ V_io,
+                             __nv_bfloat16 *__restrict__ H_io) {
   pdl_enter();
-  const int N4 = (2 * e + s) / 4, e4 = e / 4;
+  const int N = 2 * e + s, W4 = (e + s) / 4, e4 = e / 4;  // the V and Z columns
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  // (row, column group) of element i, advanced by the stride without a divide
-  long long m = i0 / N4;
-  int c4 = (int)(i0 - m * N4);
-  const long long dm = stride / N4;
-  const int dc = (int)(stride - dm * N4);
-  for (long long i = i0; i < M * N4; i += stride) {
-    const float4 x = load_bf4(pre + 4 * i);
+  long long m = i0 / W4;
+  int c4 = (int)(i0 - m * W4);
+  const long long dm = stride / W4;
+  const int dc = (int)(stride - dm * W4);
+  for (long long i = i0; i < M * W4; i += stride) {
+    const float4 x = load_bf4(pre + m * N + e + 4 * c4);
     const float4 y = make_float4(swish_fast(x.x), swish_fast(x.y), swish_fast(x.z), swish_fast(x.w));
     if (c4 < e4) {
-      reinterpret_cast<float4 *>(U)[m * e4 + c4] = y;
-    } else if (c4 < 2 * e4) {
-      store_bf4(V_io + m * e + 4 * (c4 - e4), y.x, y.y, y.z, y.w);
+      store_bf4(V_io + m * e + 4 * c4, y.x, y.y, y.z, y.w);
     } else {
-      const int k = 4 * (c4 - 2 * e4);
+      const int k = 4 * (c4 - e4);
       reinterpret_cast<float4 *>(Z + m * s)[k / 4] = y;
       for (int h = 0; h < 4; ++h) {
         const float *g = gamma + h * s + k, *b = beta + h * s + k;
@@ -551,8 +554,89 @@ __global__ void act_heads_v4(const __nv_bfloat16 *__restrict__ pre, float *__res
     }
     m += dm;
     c4 += dc;
-    if (c4 >= N4) {
-      c4 -= N4;
+    if (c4 >= W4) {
+      c4 -= W4;
+      ++m;
+    }
+  }
+}
+
+// A = swish(Pre_u) * Vh as bf16 (Pre row stride N = 2e + s)
+__global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const float4 *__restrict__ Vh,
+                         __nv_bfloat16 *__restrict__ A_io, long long M, int e, int s) {
+  pdl_enter();
+  const int N = 2 * e + s, e4 = e / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  long long m = i0 / e4;
+  int c4 = (int)(i0 - m * e4);
+  const long long dm = stride / e4;
+  const int dc = (int)(stride - dm * e4);
+  for (long long i = i0; i < M * e4; i += stride) {
+    const float4 x = load_bf4(pre + m * N + 4 * c4), v = Vh[i];
+    store_bf4(A_io + 4 * i, swish_fast(x.x) * v.x, swish_fast(x.y) * v.y, swish_fast(x.z) * v.z,
+              swish_fast(x.w) * v.w);
+    m += dm;
+    c4 += dc;
+    if (c4 >= e4) {
+      c4 -= e4;
+      ++m;
+    }
+  }
+}
+
+// The gate's gradient and the U part of dPre in one pass: with u =
+// swish(Pre_u), dVh = dA * u (bf16) and dPre_u = (dA * Vh) * swish'(Pre_u),
+// written in place over Pre_u (bf16); no dU buffer.
+__global__ void gate_grad_pre(const float4 *__restrict__ dA, const float4 *__restrict__ Vh,
+                              __nv_bfloat16 *__restrict__ pre, __nv_bfloat16 *__restrict__ dVh_io,
+                              long long M, int e, int s) {
+  pdl_enter();
+  const int N = 2 * e + s, e4 = e / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  long long m = i0 / e4;
+  int c4 = (int)(i0 - m * e4);
+  const long long dm = stride / e4;
+  const int dc = (int)(stride - dm * e4);
+  for (long long i = i0; i < M * e4; i += stride) {
+    __nv_bfloat16 *pu = pre + m * N + 4 * c4;
+    const float4 a = dA[i], v = Vh[i], x = load_bf4(pu);
+    store_bf4(dVh_io + 4 * i, a.x * swish_fast(x.x), a.y * swish_fast(x.y), a.z * swish_fast(x.z),
+              a.w * swish_fast(x.w));
+    store_bf4(pu, (a.x * v.x) * swish_grad_fast(x.x), (a.y * v.y) * swish_grad_fast(x.y),
+              (a.z * v.z) * swish_grad_fast(x.z), (a.w * v.w) * swish_grad_fast(x.w));
+    m += dm;
+    c4 += dc;
+    if (c4 >= e4) {
+      c4 -= e4;
+      ++m;
+    }
+  }
+}
+
+// The V and Z parts of dPre = d(V | Z) * swish'(Pre), bf16, in place
+__global__ void pre_grad_vz(__nv_bfloat16 *__restrict__ pre_io, const float *__restrict__ dV,
+                            const float *__restrict__ dZ, long long M, int e, int s) {
+  pdl_enter();
+  const int N = 2 * e + s, W4 = (e + s) / 4, e4 = e / 4, s4 = s / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  long long m = i0 / W4;
+  int c4 = (int)(i0 - m * W4);
+  const long long dm = stride / W4;
+  const int dc = (int)(stride - dm * W4);
+  for (long long i = i0; i < M * W4; i += stride) {
+    const float4 g = c4 < e4 ? reinterpret_cast<const float4 *>(dV)[m * e4 + c4]
+                             : reinterpret_cast<const float4 *>(dZ)[m * s4 + c4 - e4];
+    __nv_bfloat16 *px = pre_io + m * N + e + 4 * c4;
+    const float4 x = load_bf4(px);
+    store_bf4(px, g.x * swish_grad_fast(x.x), g.y * swish_grad_fast(x.y),
+              g.z * swish_grad_fast(x.z), g.w * swish_grad_fast(x.w));
+    m += dm;
+    c4 += dc;
+    if (c4 >= W4) {
+      c4 -= W4;
       ++m;
     }
   }
@@ -566,22 +650,6 @@ __global__ void gate_v4(const float4 *__restrict__ U, const float4 *__restrict__
        i += (long long)gridDim.x * blockDim.x) {
     const float4 u = U[i], v = Vh[i];
     store_bf4(A_io + 4 * i, u.x * v.x, u.y * v.y, u.z * v.z, u.w * v.w);
-  }
-}
-
-// dU = dA * Vh (fp32), dVh = dA * U (bf16 only, or also fp32 when dVh is set)
-__global__ void gate_grad_v4(const float4 *__restrict__ dA, const float4 *__restrict__ U,
-                             const float4 *__restrict__ Vh, float4 *__restrict__ dU,
-                             float4 *__restrict__ dVh, __nv_bfloat16 *__restrict__ dVh_io,
-                             long long n4) {
-  pdl_enter();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
-       i += (long long)gridDim.x * blockDim.x) {
-    const float4 a = dA[i], u = U[i], v = Vh[i];
-    dU[i] = make_float4(a.x * v.x, a.y * v.y, a.z * v.z, a.w * v.w);
-    const float4 g = make_float4(a.x * u.x, a.y * u.y, a.z * u.z, a.w * u.w);
-    if (dVh) dVh[i] = g;
-    store_bf4(dVh_io + 4 * i, g.x, g.y, g.z, g.w);
   }
 }
 
@@ -636,11 +704,17 @@ GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int 
   return g;
 }
 
-__global__ void zero_f32(float *p, int n) {
+// the three atomically summed gradients start from zero (one launch)
+__global__ void zero_sums(float *a, int na, float *b, int nb, float *c, int nc) {
   pdl_enter();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0.f;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < na + nb + nc;
+       i += gridDim.x * blockDim.x) {
+    if (i < na) a[i] = 0.f;
+    else if (i < na + nb) b[i - na] = 0.f;
+    else c[i - na - nb] = 0.f;
+  }
 }
+
 
 // blocks of 256 threads over the columns of a row, each block looping over
 // rows: at most 2048 blocks along y
@@ -708,8 +782,8 @@ cudaError_t run(const BackwardProblem &q) {
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
   if (tcc)
-    LAUNCH(act_heads_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, U, Z, q.gamma, q.beta, M, e, s,
-                                                         V_io, H_io)
+    LAUNCH(act_heads_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, Z, q.gamma, q.beta, M, e,
+                                                                  s, V_io, H_io)
   else if (tc)  // bf16 Pre, fp32 heads and V for the CUDA-core chunk contractions
     LAUNCH(act_heads_bf16, blocks_for(M * N), 256, 0, st, dpre_io, U, V, Z, H, q.gamma, q.beta, M, e,
                                                       s)
@@ -721,8 +795,7 @@ cudaError_t run(const BackwardProblem &q) {
   if (tcc) {
     BW_TRY(bt(Qq_io, s, 0, Kq_io, s, 1, S, C, C, s, 1, 1.f, 0));  // raw Qq Kq^T
     LAUNCH(score_act, blocks_for(BG * C * C / 4), 256, 0, st, S, P_io, q.relpos, BG * C, C, q.causal,
-                                                           1.f / C)
-    BW_TRY(bt(P_io, C, 0, V_io, e, 0, Vh, C, e, C, 1, q.local_scale, 0));
+                                                           1.f / C, q.local_scale)
     BW_TRY(bt(Kl_io, s, 1, V_io, e, 0, state, s, e, C, 1, 1.f, 0));
   } else {
     BW_TRY(gemm(st, C, C, s, (int)BG, Qq, op(s, 1, (long long)C * s), Kq,
@@ -734,15 +807,27 @@ cudaError_t run(const BackwardProblem &q) {
   }
   LAUNCH(scan_forward, blocks_for(q.B * se), 256, 0, st, state, tcc ? nullptr : prefix, q.B, G, se,
                                                       q.causal, q.lin_scale, pre_io)
-  // Vh += Q_lin Prefix (a chunk's prefix, or its batch row's total)
+  // Vh (+)= Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
-    BW_TRY(bt(Ql_io, s, 0, pre_io, e, 0, Vh, C, e, s, pdiv, 1.f, 1));
+    // Vh = (l P) V + Q_lin Prefix as one two-product contraction
+    GemmAnyArgs g = tc_args(q, P_io, C, 0, V_io, e, 0, Vh, 0, C, e, C, 0);
+    g.batches = (int)BG;
+    g.A2 = Ql_io;
+    g.lda2 = s;
+    g.a2_mn = 0;
+    g.B2 = pre_io;
+    g.ldb2 = e;
+    g.K2 = s;
+    g.b2_div = pdiv;
+    BW_TRY(tc_gemm_any(g, st));
   } else {
     const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
     BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
-  if (tc)
+  if (tcc)
+    LAUNCH(gate_pre, blocks_for(M * e / 4), 256, 0, st, dpre_io, (const float4 *)Vh, A_io, M, e, s)
+  else if (tc)
     LAUNCH(gate_v4, blocks_for(M * e / 4), 256, 0, st, (const float4 *)U, (const float4 *)Vh, A_io,
                                                     M * e / 4)
   else
@@ -759,15 +844,14 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
   if (tcc)
-    LAUNCH(gate_grad_v4, blocks_for(M * e / 4), 256, 0, st, 
-        (const float4 *)dA, (const float4 *)U, (const float4 *)Vh, (float4 *)dU, nullptr, dVh_io,
-        M * e / 4)
+    LAUNCH(gate_grad_pre, blocks_for(M * e / 4), 256, 0, st, (const float4 *)dA, (const float4 *)Vh,
+                                                          dpre_io, dVh_io, M, e, s)
   else
     LAUNCH(gate_grad, blocks_for(M * e), 256, 0, st, dA, U, Vh, dU, dVh, M * e, nullptr)
   // ---- local part
   if (tcc) {
+    // dV = (l P)^T dVh + K_lin dState comes after the reverse scan
     BW_TRY(bt(dVh_io, e, 0, V_io, e, 1, dP, C, C, e, 1, q.local_scale, 0));
-    BW_TRY(bt(P_io, C, 1, dVh_io, e, 0, dV, C, e, C, 1, q.local_scale, 0));
   } else {
     BW_TRY(gemm(st, C, C, e, (int)BG, dVh, op(e, 1, (long long)C * e), V,
                 op(1, e, (long long)C * e),
@@ -776,7 +860,8 @@ cudaError_t run(const BackwardProblem &q) {
                 op(e, 1, (long long)C * e),
                 StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   }
-  LAUNCH(zero_f32, (2 * C - 1 + 255) / 256, 256, 0, st, q.drelpos, 2 * C - 1)
+  LAUNCH(zero_sums, (2 * C - 1 + 8 * s + 255) / 256, 256, 0, st, q.drelpos, 2 * C - 1, q.dgamma,
+                                                                   4 * s, q.dbeta, 4 * s)
   if (tcc) {
     const long long rpb = 32;  // rows per block
     LAUNCH(score_grad_relpos, (unsigned)((BG * C + rpb - 1) / rpb), 256, (2 * C - 1) * sizeof(float), st, S, dP, dS_io, q.drelpos, BG * C, C, q.causal, rpb)
@@ -808,7 +893,17 @@ cudaError_t run(const BackwardProblem &q) {
   LAUNCH(scan_backward, blocks_for(q.B * se), 256, 0, st, dpre, q.B, G, se, q.causal, dst_io)
   if (tcc) {
     BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
-    BW_TRY(bt(Kl_io, s, 0, dst_io, e, 0, dV, C, e, s, 1, 1.f, 1));
+    // dV = (l P)^T dVh + K_lin dState as one two-product contraction
+    GemmAnyArgs g = tc_args(q, P_io, C, 1, dVh_io, e, 0, dV, 0, C, e, C, 0);
+    g.batches = (int)BG;
+    g.A2 = Kl_io;
+    g.lda2 = s;
+    g.a2_mn = 0;
+    g.B2 = dst_io;
+    g.ldb2 = e;
+    g.K2 = s;
+    g.b2_div = 1;
+    BW_TRY(tc_gemm_any(g, st));
   } else {
     BW_TRY(gemm(st, C, s, e, (int)BG, V, op(e, 1, (long long)C * e), dpre, op(1, e, se),
                 StoreF32{dKl, s, 1, (long long)C * s, 1.f, 0}));
@@ -816,13 +911,13 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
   }
   // ---- heads
-  LAUNCH(zero_f32, (8 * s + 255) / 256, 256, 0, st, q.dgamma, 4 * s)
-  LAUNCH(zero_f32, (8 * s + 255) / 256, 256, 0, st, q.dbeta, 4 * s)
   const int rows = 128;
   LAUNCH(heads_grad, (unsigned)((M + rows - 1) / rows), 256, 0, st, dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows)
   // ---- input side
-  if (tc)
+  if (tcc)  // the U part was written by gate_grad_pre
+    LAUNCH(pre_grad_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, dV, dZ, M, e, s)
+  else if (tc)
     LAUNCH(pre_grad_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, dU, dV, dZ, M, e, s)
   else
     LAUNCH(pre_grad, blocks_for(M * N), 256, 0, st, pre, nullptr, dU, dV, dZ, M, e, s)

@@ -124,6 +124,16 @@ struct GemmAnyArgs {
   int batches = 1;
   int b_div = 1;
   float alpha = 1.f;  // fp32 output: C (+)= alpha * A B
+  // optional second product summed into the same tile: C = A B + A2 B2,
+  // K2 deep (a multiple of 64), A2 of its own majorness, B2 stored as B,
+  // batched like A and B (B2's batch z / b2_div); K2 = 0: none
+  const void *A2 = nullptr;
+  long long lda2 = 0;
+  int a2_mn = 0;
+  const void *B2 = nullptr;
+  long long ldb2 = 0;
+  int K2 = 0;
+  int b2_div = 1;
 };
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 

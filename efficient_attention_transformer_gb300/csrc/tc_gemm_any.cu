@@ -13,6 +13,10 @@
 // operand (a batch never shares a 128-row tile or a 64-deep k-block with
 // the next), one tile list over all of them.
 //
+// Two-product form: C = A B + A2 B2 in one accumulator, the k-blocks of the
+// second product (its own A majorness, B2 stored as B) following those of
+// the first, so that a sum of two contractions needs no second pass over C.
+//
 // One persistent CTA per SM over 128 x 256 output tiles (x split), static
 // round robin.  Warp 0 streams 64-deep k-blocks of A and B into a 4-stage
 // ring of 128-byte-swizzled boxes with TMA; one thread of warp 1 issues
@@ -44,6 +48,7 @@ constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct AnyParams {
   int M, N, K;
+  int K2, a2_mn, b2_div;  // second product: depth, A2 majorness, B2 batch divisor
   int m_tiles, n_tiles, splits, total;
   int kb_split;  // k-blocks per split
   int atomic;    // fp32: add into C (zeroed by the caller) instead of storing
@@ -80,7 +85,7 @@ __device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
   x.nt = rem % p.n_tiles;
   x.mt = (rem / p.n_tiles) % p.m_tiles;
   x.z = rem / (p.n_tiles * p.m_tiles);
-  const int kblocks = p.K / BK;
+  const int kblocks = (p.K + p.K2) / BK;
   x.kb0 = split * p.kb_split;
   x.kb1 = min(kblocks, x.kb0 + p.kb_split);
   return x;
@@ -89,7 +94,8 @@ __device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
 template <bool A_MN, bool B_KM, bool OUT_BF16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const AnyParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB2, const AnyParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,9 +142,12 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x) {
         const Tile x = tile_of(p, t);
         const int m0 = x.mt * BM, n0 = x.nt * BN, nsz = min(BN, p.N - n0);
-        // this batch's first stored row of A and of B
+        // this batch's first stored row of A and of B (and of A2, B2)
         const int za = x.z * (A_MN ? p.K : p.M);
         const int zb = (x.z / p.b_div) * (B_KM ? p.N : p.K);
+        const int za2 = x.z * (p.a2_mn ? p.K2 : p.M);
+        const int zb2 = (x.z / p.b2_div) * (B_KM ? p.N : p.K2);
+        const int kb_one = p.K / BK;  // k-blocks of the first product
         for (int kb = x.kb0; kb < x.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
@@ -152,18 +161,24 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           const uint32_t b_bytes =
               B_KM ? (uint32_t)p.kbox_rows * 128u : (uint32_t)(nsz / 64) * BOX_BYTES;
           mbar_arrive_expect_tx(full, A_BYTES + b_bytes);
-          if (A_MN) {
+          // the first product's k-block, or the second's
+          const bool two = kb >= kb_one;
+          const int k = two ? kb - kb_one : kb;
+          const CUtensorMap *ta = two ? &tmA2 : &tmA, *tb = two ? &tmB2 : &tmB;
+          const bool amn = two ? p.a2_mn != 0 : A_MN;
+          const int zA = two ? za2 : za, zB = two ? zb2 : zb;
+          if (amn) {
             // [K, M] storage: 64 k-rows of two 64-column blocks of M
-            tma_load_2d(smem_u32(sA), &tmA, full, m0, za + kb * BK);
-            tma_load_2d(smem_u32(sA + BOX_BYTES), &tmA, full, m0 + 64, za + kb * BK);
+            tma_load_2d(smem_u32(sA), ta, full, m0, zA + k * BK);
+            tma_load_2d(smem_u32(sA + BOX_BYTES), ta, full, m0 + 64, zA + k * BK);
           } else {
-            tma_load_2d(smem_u32(sA), &tmA, full, kb * BK, za + m0);
+            tma_load_2d(smem_u32(sA), ta, full, k * BK, zA + m0);
           }
           if (B_KM) {
-            tma_load_2d(smem_u32(sB), &tmB, full, kb * BK, zb + n0);
+            tma_load_2d(smem_u32(sB), tb, full, k * BK, zB + n0);
           } else {
             for (int j = 0; j < nsz / 64; ++j)
-              tma_load_2d(smem_u32(sB + j * BOX_BYTES), &tmB, full, n0 + j * 64, zb + kb * BK);
+              tma_load_2d(smem_u32(sB + j * BOX_BYTES), tb, full, n0 + j * 64, zB + k * BK);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -188,9 +203,11 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        const uint32_t idesc = idesc_bf16_f32(BM, nsz, A_MN ? 1 : 0, B_KM ? 0 : 1);
+        const int kb_one = p.K / BK;
         bool ok = true;
         for (int kb = x.kb0; kb < x.kb1; ++kb) {
+          const bool amn = kb >= kb_one ? p.a2_mn != 0 : A_MN;
+          const uint32_t idesc = idesc_bf16_f32(BM, nsz, amn ? 1 : 0, B_KM ? 0 : 1);
           if (!mbar_wait(smem_u32(&sm->full[stage]), phase, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
             ok = false;
@@ -200,12 +217,12 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
           // K-major: 16 elements (32 B) per step inside the swizzle atom;
           // MN-major: 16 k-rows of 128 B per step, 64-wide blocks 8 KB apart
-          const uint64_t da = A_MN ? sw128_desc(sA, BOX_BYTES, 1024) : sw128_desc(sA, 16, 1024);
+          const uint64_t da = amn ? sw128_desc(sA, BOX_BYTES, 1024) : sw128_desc(sA, 16, 1024);
           const uint64_t db = B_KM ? sw128_desc(sA + A_BYTES, 16, 1024)
                                    : sw128_desc(sA + A_BYTES, BOX_BYTES, 1024);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss(d_tmem, desc_advance(da, k * (A_MN ? 2048 : 32)),
+            mma_f16_ss(d_tmem, desc_advance(da, k * (amn ? 2048 : 32)),
                        desc_advance(db, k * (B_KM ? 32 : 2048)), idesc, kb != x.kb0 || k != 0);
           mma_commit(smem_u32(&sm->empty[stage]));
           if (++stage == STAGES) {
@@ -308,7 +325,8 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 template <bool A_MN, bool B_KM, bool OUT_BF16>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                   const AnyParams &p, int num_sms, cudaStream_t stream) {
+                   const CUtensorMap &tmA2, const CUtensorMap &tmB2, const AnyParams &p,
+                   int num_sms, cudaStream_t stream) {
   static unsigned long long configured = 0;  // one bit per device ordinal
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -320,7 +338,8 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
     configured |= 1ull << dev;
   }
   const int grid = p.total < num_sms ? p.total : num_sms;
-  return launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmC, p);
+  return launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmC,
+                    tmA2, tmB2, p);
 }
 
 }  // namespace
@@ -328,6 +347,8 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   if (g.M % BM != 0 || g.N % 64 != 0 || g.K % BK != 0 || g.M <= 0 || g.N <= 0 || g.K <= 0 ||
       g.batches <= 0 || g.b_div <= 0)
+    return cudaErrorInvalidValue;
+  if (g.K2 < 0 || g.K2 % BK != 0 || (g.K2 > 0 && (!g.A2 || !g.B2 || g.b2_div <= 0)))
     return cudaErrorInvalidValue;
   const long long Z = g.batches, ZB = (g.batches + g.b_div - 1) / g.b_div;
   const int kbox = g.N < BN ? g.N : BN;
@@ -345,13 +366,27 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   if (g.c_bf16) err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64);
   else err = make_tmap_f32_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 32);
   if (err != cudaSuccess) return err;
+  // the second product's operands (unused copies of the first's when none)
+  CUtensorMap tmA2 = tmA, tmB2 = tmB;
+  if (g.K2 > 0) {
+    const long long ZB2 = (g.batches + g.b2_div - 1) / g.b2_div;
+    if (g.a2_mn) err = make_tmap_bf16_2d(&tmA2, g.A2, Z * g.K2, g.M, g.lda2, 64, 64);
+    else err = make_tmap_bf16_2d(&tmA2, g.A2, Z * g.M, g.K2, g.lda2, BM, 64);
+    if (err != cudaSuccess) return err;
+    if (g.b_km) err = make_tmap_bf16_2d(&tmB2, g.B2, ZB2 * g.N, g.K2, g.ldb2, kbox, 64);
+    else err = make_tmap_bf16_2d(&tmB2, g.B2, ZB2 * g.K2, g.N, g.ldb2, 64, 64);
+    if (err != cudaSuccess) return err;
+  }
   AnyParams p = {};
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
+  p.K2 = g.K2;
+  p.a2_mn = g.a2_mn;
+  p.b2_div = g.b2_div;
   p.m_tiles = g.M / BM;
   p.n_tiles = (g.N + BN - 1) / BN;
-  const int kblocks = g.K / BK;
+  const int kblocks = (g.K + g.K2) / BK;
   // split K when the output tiles would leave SMs idle (fp32 atomic output
   // only); at least 8 k-blocks a split
   int splits = 1;
@@ -377,14 +412,14 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   }
   const int key = (g.a_mn ? 4 : 0) | (g.b_km ? 2 : 0) | (g.c_bf16 ? 1 : 0);
   switch (key) {
-    case 0: return launch<false, false, false>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 1: return launch<false, false, true>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 2: return launch<false, true, false>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 3: return launch<false, true, true>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 4: return launch<true, false, false>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 5: return launch<true, false, true>(tmA, tmB, tmC, p, g.num_sms, stream);
-    case 6: return launch<true, true, false>(tmA, tmB, tmC, p, g.num_sms, stream);
-    default: return launch<true, true, true>(tmA, tmB, tmC, p, g.num_sms, stream);
+    case 0: return launch<false, false, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 1: return launch<false, false, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 2: return launch<false, true, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 3: return launch<false, true, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 4: return launch<true, false, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 5: return launch<true, false, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 6: return launch<true, true, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    default: return launch<true, true, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
   }
 }
 
