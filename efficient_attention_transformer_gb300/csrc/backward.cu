@@ -419,6 +419,66 @@ __global__ void scan_backward(float *__restrict__ dpre, int B, int G, long long 
   }
 }
 
+// The tensor-core path's scans: four consecutive state elements per thread
+// (se a multiple of 4), the loads of 8 chunks issued together, bf16 out.
+// prefix_io[b][g] = lin_scale * (exclusive sum over chunks, or the total)
+__global__ void scan_forward4(const float4 *__restrict__ state, int B, int G, long long se4,
+                              int causal, float lin_scale, __nv_bfloat16 *__restrict__ prefix_io) {
+  pdl_enter();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long b = i / se4, r = i - b * se4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g0 = 0; g0 < G; g0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (g0 + k < G) v[k] = state[(b * G + g0 + k) * se4 + r];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (g0 + k >= G) continue;
+        if (causal)
+          store_bf4(prefix_io + 4 * ((b * G + g0 + k) * se4 + r), lin_scale * run.x,
+                    lin_scale * run.y, lin_scale * run.z, lin_scale * run.w);
+        run = make_float4(run.x + v[k].x, run.y + v[k].y, run.z + v[k].z, run.w + v[k].w);
+      }
+    }
+    if (!causal)
+      store_bf4(prefix_io + 4 * (b * se4 + r), lin_scale * run.x, lin_scale * run.y,
+                lin_scale * run.z, lin_scale * run.w);
+  }
+}
+
+// dState_h = sum_{g>h} dPrefix_g (causal) or the total, as bf16
+__global__ void scan_backward4(const float4 *__restrict__ dpre, int B, int G, long long se4,
+                               int causal, __nv_bfloat16 *__restrict__ dstate_io) {
+  pdl_enter();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < B * se4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long b = i / se4, r = i - b * se4;
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!causal)
+      for (int g = 0; g < G; ++g) {
+        const float4 v = dpre[(b * G + g) * se4 + r];
+        run = make_float4(run.x + v.x, run.y + v.y, run.z + v.z, run.w + v.w);
+      }
+    for (int g1 = G; g1 > 0; g1 -= 8) {
+      const int g0 = g1 - 8 > 0 ? g1 - 8 : 0;
+      float4 v[8];
+      if (causal)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (g0 + k < g1) v[k] = dpre[(b * G + g0 + k) * se4 + r];
+#pragma unroll
+      for (int k = 7; k >= 0; --k) {
+        if (g0 + k >= g1) continue;
+        store_bf4(dstate_io + 4 * ((b * G + g0 + k) * se4 + r), run.x, run.y, run.z, run.w);
+        if (causal) run = make_float4(run.x + v[k].x, run.y + v[k].y, run.z + v[k].z, run.w + v[k].w);
+      }
+    }
+  }
+}
+
 // dZ = sum_k dH_k * gamma_k; dgamma, dbeta as column sums of dH_k * Z, dH_k
 // (per block partial sums over its rows, added atomically; 256 threads)
 __global__ void __launch_bounds__(256)
@@ -805,8 +865,12 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, s, e, C, (int)BG, Kl, op(1, s, (long long)C * s), V,
                 op(e, 1, (long long)C * e), StoreF32{state, e, 1, se, 1.f, 0}));
   }
-  LAUNCH(scan_forward, blocks_for(q.B * se), 256, 0, st, state, tcc ? nullptr : prefix, q.B, G, se,
-                                                      q.causal, q.lin_scale, pre_io)
+  if (tcc)
+    LAUNCH(scan_forward4, blocks_for(q.B * se / 4), 256, 0, st, (const float4 *)state, q.B, G, se / 4,
+                                                         q.causal, q.lin_scale, pre_io)
+  else
+    LAUNCH(scan_forward, blocks_for(q.B * se), 256, 0, st, state, prefix, q.B, G, se, q.causal,
+                                                        q.lin_scale, pre_io)
   // Vh (+)= Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
     // Vh = (l P) V + Q_lin Prefix as one two-product contraction
@@ -890,7 +954,11 @@ cudaError_t run(const BackwardProblem &q) {
     BW_TRY(gemm(st, s, e, C, (int)BG, Ql, op(1, s, (long long)C * s), dVh,
                 op(e, 1, (long long)C * e), StoreF32{dpre, e, 1, se, q.lin_scale, 0}));
   }
-  LAUNCH(scan_backward, blocks_for(q.B * se), 256, 0, st, dpre, q.B, G, se, q.causal, dst_io)
+  if (tcc)
+    LAUNCH(scan_backward4, blocks_for(q.B * se / 4), 256, 0, st, (const float4 *)dpre, q.B, G,
+                                                          se / 4, q.causal, dst_io)
+  else
+    LAUNCH(scan_backward, blocks_for(q.B * se), 256, 0, st, dpre, q.B, G, se, q.causal, dst_io)
   if (tcc) {
     BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
     // dV = (l P)^T dVh + K_lin dState as one two-product contraction
@@ -911,7 +979,7 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{dV, e, 1, (long long)C * e, 1.f, 1}));
   }
   // ---- heads
-  const int rows = 128;
+  const int rows = 32;  // about 3 blocks a SM at the long workload's 16k rows
   LAUNCH(heads_grad, (unsigned)((M + rows - 1) / rows), 256, 0, st, dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows)
   // ---- input side
