@@ -621,8 +621,8 @@ __global__ void act_heads_vz(const __nv_bfloat16 *__restrict__ pre, float *__res
   }
 }
 
-// A = swish(Pre_u) * Vh as bf16 (Pre row stride N = 2e + s)
-__global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const float4 *__restrict__ Vh,
+// A = swish(Pre_u) * Vh as bf16 (Pre row stride N = 2e + s; Vh bf16)
+__global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const __nv_bfloat16 *__restrict__ Vh,
                          __nv_bfloat16 *__restrict__ A_io, long long M, int e, int s) {
   pdl_enter();
   const int N = 2 * e + s, e4 = e / 4;
@@ -633,7 +633,7 @@ __global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const float4 *__
   const long long dm = stride / e4;
   const int dc = (int)(stride - dm * e4);
   for (long long i = i0; i < M * e4; i += stride) {
-    const float4 x = load_bf4(pre + m * N + 4 * c4), v = Vh[i];
+    const float4 x = load_bf4(pre + m * N + 4 * c4), v = load_bf4(Vh + 4 * i);
     store_bf4(A_io + 4 * i, swish_fast(x.x) * v.x, swish_fast(x.y) * v.y, swish_fast(x.z) * v.z,
               swish_fast(x.w) * v.w);
     m += dm;
@@ -647,10 +647,12 @@ __global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const float4 *__
 
 // The gate's gradient and the U part of dPre in one pass: with u =
 // swish(Pre_u), dVh = dA * u (bf16) and dPre_u = (dA * Vh) * swish'(Pre_u),
-// written in place over Pre_u (bf16); no dU buffer.
-__global__ void gate_grad_pre(const float4 *__restrict__ dA, const float4 *__restrict__ Vh,
-                              __nv_bfloat16 *__restrict__ pre, __nv_bfloat16 *__restrict__ dVh_io,
-                              long long M, int e, int s) {
+// written in place over Pre_u (bf16); no dU buffer.  dA and Vh come as bf16
+// from the contractions that produce them (every product here is rounded
+// to bf16 anyway).
+__global__ void gate_grad_pre(const __nv_bfloat16 *__restrict__ dA,
+                              const __nv_bfloat16 *__restrict__ Vh, __nv_bfloat16 *__restrict__ pre,
+                              __nv_bfloat16 *__restrict__ dVh_io, long long M, int e, int s) {
   pdl_enter();
   const int N = 2 * e + s, e4 = e / 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -661,7 +663,7 @@ __global__ void gate_grad_pre(const float4 *__restrict__ dA, const float4 *__res
   const int dc = (int)(stride - dm * e4);
   for (long long i = i0; i < M * e4; i += stride) {
     __nv_bfloat16 *pu = pre + m * N + 4 * c4;
-    const float4 a = dA[i], v = Vh[i], x = load_bf4(pu);
+    const float4 a = load_bf4(dA + 4 * i), v = load_bf4(Vh + 4 * i), x = load_bf4(pu);
     store_bf4(dVh_io + 4 * i, a.x * swish_fast(x.x), a.y * swish_fast(x.y), a.z * swish_fast(x.z),
               a.w * swish_fast(x.w));
     store_bf4(pu, (a.x * v.x) * swish_grad_fast(x.x), (a.y * v.y) * swish_grad_fast(x.y),
@@ -874,7 +876,7 @@ cudaError_t run(const BackwardProblem &q) {
   // Vh (+)= Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
     // Vh = (l P) V + Q_lin Prefix as one two-product contraction
-    GemmAnyArgs g = tc_args(q, P_io, C, 0, V_io, e, 0, Vh, 0, C, e, C, 0);
+    GemmAnyArgs g = tc_args(q, P_io, C, 0, V_io, e, 0, Vh, 1, C, e, C, 0);  // bf16 Vh
     g.batches = (int)BG;
     g.A2 = Ql_io;
     g.lda2 = s;
@@ -890,7 +892,7 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
   if (tcc)
-    LAUNCH(gate_pre, blocks_for(M * e / 4), 256, 0, st, dpre_io, (const float4 *)Vh, A_io, M, e, s)
+    LAUNCH(gate_pre, blocks_for(M * e / 4), 256, 0, st, dpre_io, (const bf *)Vh, A_io, M, e, s)
   else if (tc)
     LAUNCH(gate_v4, blocks_for(M * e / 4), 256, 0, st, (const float4 *)U, (const float4 *)Vh, A_io,
                                                     M * e / 4)
@@ -900,15 +902,16 @@ cudaError_t run(const BackwardProblem &q) {
   if (tc) {
     // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
     BW_TRY(tc_gemm_any(tc_args(q, A_io, e, 1, dO, d, 0, q.dW_o, 0, e, d, (int)M, 1), st));
-    // dA = dO W_o^T: B the transpose of the stored [e, d] W_o
-    BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, 0, (int)M, e, d, 0), st));
+    // dA = dO W_o^T: B the transpose of the stored [e, d] W_o (bf16 when
+    // the gate's gradient kernel below reads it)
+    BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, tcc ? 1 : 0, (int)M, e, d, 0), st));
   } else {
     BW_TRY(gemm(st, e, d, (int)M, 1, Ag, op(1, e), dO, op(d, 1),
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
   if (tcc)
-    LAUNCH(gate_grad_pre, blocks_for(M * e / 4), 256, 0, st, (const float4 *)dA, (const float4 *)Vh,
+    LAUNCH(gate_grad_pre, blocks_for(M * e / 4), 256, 0, st, (const bf *)dA, (const bf *)Vh,
                                                           dpre_io, dVh_io, M, e, s)
   else
     LAUNCH(gate_grad, blocks_for(M * e), 256, 0, st, dA, U, Vh, dU, dVh, M * e, nullptr)
