@@ -677,8 +677,9 @@ __global__ void gate_grad_pre(const __nv_bfloat16 *__restrict__ dA,
   }
 }
 
-// The V and Z parts of dPre = d(V | Z) * swish'(Pre), bf16, in place
-__global__ void pre_grad_vz(__nv_bfloat16 *__restrict__ pre_io, const float *__restrict__ dV,
+// The V and Z parts of dPre = d(V | Z) * swish'(Pre), bf16, in place (dV
+// comes as bf16 from its contraction)
+__global__ void pre_grad_vz(__nv_bfloat16 *__restrict__ pre_io, const __nv_bfloat16 *__restrict__ dV,
                             const float *__restrict__ dZ, long long M, int e, int s) {
   pdl_enter();
   const int N = 2 * e + s, W4 = (e + s) / 4, e4 = e / 4, s4 = s / 4;
@@ -689,7 +690,7 @@ __global__ void pre_grad_vz(__nv_bfloat16 *__restrict__ pre_io, const float *__r
   const long long dm = stride / W4;
   const int dc = (int)(stride - dm * W4);
   for (long long i = i0; i < M * W4; i += stride) {
-    const float4 g = c4 < e4 ? reinterpret_cast<const float4 *>(dV)[m * e4 + c4]
+    const float4 g = c4 < e4 ? load_bf4(dV + (m * e4 + c4) * 4)
                              : reinterpret_cast<const float4 *>(dZ)[m * s4 + c4 - e4];
     __nv_bfloat16 *px = pre_io + m * N + e + 4 * c4;
     const float4 x = load_bf4(px);
@@ -766,15 +767,23 @@ GemmAnyArgs tc_args(const BackwardProblem &q, const void *A, long long lda, int 
   return g;
 }
 
-// the three atomically summed gradients start from zero (one launch)
-__global__ void zero_sums(float *a, int na, float *b, int nb, float *c, int nc) {
+// The gradients summed by atomic or TMA reduce-adds start from zero, all in
+// one launch: three small ones element by element, and (the tensor-core
+// path's split-K weight gradients, 16-byte aligned, sizes multiples of 4)
+// two large ones in 16-byte stores.
+__global__ void zero_sums(float *a, int na, float *b, int nb, float *c, int nc, float4 *w1,
+                          long long n1, float4 *w2, long long n2) {
   pdl_enter();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < na + nb + nc;
-       i += gridDim.x * blockDim.x) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  for (long long i = i0; i < na + nb + nc; i += stride) {
     if (i < na) a[i] = 0.f;
     else if (i < na + nb) b[i - na] = 0.f;
     else c[i - na - nb] = 0.f;
   }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = i0; i < n1; i += stride) w1[i] = z;
+  for (long long i = i0; i < n2; i += stride) w2[i] = z;
 }
 
 
@@ -837,6 +846,14 @@ cudaError_t run(const BackwardProblem &q) {
     return tc_gemm_any(g, st);
   };
   const int pdiv = q.causal ? 1 : G;  // chunks sharing one prefix state
+  // the summed gradients start from zero (the split-K weight gradients of
+  // the tensor-core path too, so those contractions need no zeroing)
+  {
+    const long long n1 = tc ? (long long)e * d / 4 : 0, n2 = tc ? (long long)d * N / 4 : 0;
+    LAUNCH(zero_sums, blocks_for(n2 > 2 * C + 8 * s ? n2 : 2 * C + 8 * s), 256, 0, st, q.drelpos,
+                      2 * C - 1, q.dgamma, 4 * s, q.dbeta, 4 * s, (float4 *)q.dW_o, n1,
+                      (float4 *)q.dW_uvz, n2)
+  }
   // ---- recompute the forward
   // (the tensor-core path keeps Pre in bf16, in the buffer of dPre)
   if (tc)
@@ -901,7 +918,11 @@ cudaError_t run(const BackwardProblem &q) {
   // ---- output projection and gate
   if (tc) {
     // dW_o = A^T dO: A the transpose of the stored [M, e] gated product
-    BW_TRY(tc_gemm_any(tc_args(q, A_io, e, 1, dO, d, 0, q.dW_o, 0, e, d, (int)M, 1), st));
+    {
+      GemmAnyArgs g = tc_args(q, A_io, e, 1, dO, d, 0, q.dW_o, 0, e, d, (int)M, 1);
+      g.c_zeroed = 1;
+      BW_TRY(tc_gemm_any(g, st));
+    }
     // dA = dO W_o^T: B the transpose of the stored [e, d] W_o (bf16 when
     // the gate's gradient kernel below reads it)
     BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, tcc ? 1 : 0, (int)M, e, d, 0), st));
@@ -927,8 +948,6 @@ cudaError_t run(const BackwardProblem &q) {
                 op(e, 1, (long long)C * e),
                 StoreF32{dV, e, 1, (long long)C * e, q.local_scale, 0}));
   }
-  LAUNCH(zero_sums, (2 * C - 1 + 8 * s + 255) / 256, 256, 0, st, q.drelpos, 2 * C - 1, q.dgamma,
-                                                                   4 * s, q.dbeta, 4 * s)
   if (tcc) {
     const long long rpb = 32;  // rows per block
     LAUNCH(score_grad_relpos, (unsigned)((BG * C + rpb - 1) / rpb), 256, (2 * C - 1) * sizeof(float), st, S, dP, dS_io, q.drelpos, BG * C, C, q.causal, rpb)
@@ -965,7 +984,7 @@ cudaError_t run(const BackwardProblem &q) {
   if (tcc) {
     BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
     // dV = (l P)^T dVh + K_lin dState as one two-product contraction
-    GemmAnyArgs g = tc_args(q, P_io, C, 1, dVh_io, e, 0, dV, 0, C, e, C, 0);
+    GemmAnyArgs g = tc_args(q, P_io, C, 1, dVh_io, e, 0, dV, 1, C, e, C, 0);  // bf16 dV
     g.batches = (int)BG;
     g.A2 = Kl_io;
     g.lda2 = s;
@@ -987,7 +1006,8 @@ cudaError_t run(const BackwardProblem &q) {
                                                                 q.dbeta, M, s, rows)
   // ---- input side
   if (tcc)  // the U part was written by gate_grad_pre
-    LAUNCH(pre_grad_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, dV, dZ, M, e, s)
+    LAUNCH(pre_grad_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, (const bf *)dV, dZ, M, e,
+                                                                   s)
   else if (tc)
     LAUNCH(pre_grad_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, dU, dV, dZ, M, e, s)
   else
@@ -995,7 +1015,9 @@ cudaError_t run(const BackwardProblem &q) {
   if (tc) {
     // dX = dPre W_uvz^T (bf16 out); dW_uvz = X^T dPre
     BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
-    BW_TRY(tc_gemm_any(tc_args(q, X, d, 1, dpre_io, N, 0, q.dW_uvz, 0, d, N, (int)M, 1), st));
+    GemmAnyArgs g = tc_args(q, X, d, 1, dpre_io, N, 0, q.dW_uvz, 0, d, N, (int)M, 1);
+    g.c_zeroed = 1;
+    BW_TRY(tc_gemm_any(g, st));
   } else {
     BW_TRY(gemm(st, (int)M, d, N, 1, (const float *)pre, op(N, 1), Wuvz, op(1, N),
                 StoreIo<T>{(T *)q.dX, d}));

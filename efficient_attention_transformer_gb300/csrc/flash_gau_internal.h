@@ -116,6 +116,7 @@ struct GemmAnyArgs {
   int M, N, K;
   int accumulate;   // fp32: add into C
   int allow_split;  // fp32: split K across CTAs when the tiles are few
+  int c_zeroed = 0; // C is known to be zero: a split needs no zeroing first
   int num_sms;
   int *status;
   // batched: `batches` independent products, each operand's batch z stored

@@ -404,7 +404,7 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   p.kbox_rows = kbox;
   p.atomic = p.splits > 1 || g.accumulate;
   p.status = g.status;
-  if (p.atomic && !g.accumulate) {
+  if (p.atomic && !g.accumulate && !g.c_zeroed) {
     // the split partial sums add into a zeroed output
     if ((err = cudaMemsetAsync(g.C, 0, (size_t)Z * g.M * g.N * sizeof(float), stream)) !=
         cudaSuccess)
