@@ -856,7 +856,9 @@ cudaError_t run(const BackwardProblem &q) {
   }
   // ---- recompute the forward
   // (the tensor-core path keeps Pre in bf16, in the buffer of dPre)
-  if (tc)
+  if (tcc)  // the forward's 2-SM pair GEMM with its plain bf16 store
+    BW_TRY(pair_gemm_bf16(X, Wuvz, 0, dpre_io, (int)M, N, d, L.status, q.num_sms, st));
+  else if (tc)
     BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, dpre_io, 1, (int)M, N, d, 0), st));
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
@@ -925,7 +927,10 @@ cudaError_t run(const BackwardProblem &q) {
     }
     // dA = dO W_o^T: B the transpose of the stored [e, d] W_o (bf16 when
     // the gate's gradient kernel below reads it)
-    BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, tcc ? 1 : 0, (int)M, e, d, 0), st));
+    if (tcc)  // bf16 dA on the pair GEMM
+      BW_TRY(pair_gemm_bf16(dO, Wo, 1, dA, (int)M, e, d, L.status, q.num_sms, st));
+    else
+      BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, 0, (int)M, e, d, 0), st));
   } else {
     BW_TRY(gemm(st, e, d, (int)M, 1, Ag, op(1, e), dO, op(d, 1),
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
@@ -1014,7 +1019,10 @@ cudaError_t run(const BackwardProblem &q) {
     LAUNCH(pre_grad, blocks_for(M * N), 256, 0, st, pre, nullptr, dU, dV, dZ, M, e, s)
   if (tc) {
     // dX = dPre W_uvz^T (bf16 out); dW_uvz = X^T dPre
-    BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
+    if (tcc)  // on the pair GEMM (d a multiple of 128)
+      BW_TRY(pair_gemm_bf16(dpre_io, Wuvz, 1, q.dX, (int)M, d, N, L.status, q.num_sms, st));
+    else
+      BW_TRY(tc_gemm_any(tc_args(q, dpre_io, N, 0, Wuvz, N, 1, q.dX, 1, (int)M, d, N, 0), st));
     GemmAnyArgs g = tc_args(q, X, d, 1, dpre_io, N, 0, q.dW_uvz, 0, d, N, (int)M, 1);
     g.c_zeroed = 1;
     BW_TRY(tc_gemm_any(g, st));

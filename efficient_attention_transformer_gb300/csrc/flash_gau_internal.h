@@ -138,6 +138,13 @@ struct GemmAnyArgs {
 };
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 
+// C[M, N] = A[M, K] B[K, N], bf16 operands and output, on the 2-SM pair
+// GEMM of the forward (tc_gemm_pair.cu): A and C row-major, B a row-major
+// [K, N] matrix or (b_km) the transpose of a row-major [N, K] one; M a
+// multiple of 128, N of 128, K of 64.
+cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int M, int N, int K,
+                           int *status, int num_sms, cudaStream_t stream);
+
 // Decode step (decode.cu): the per-sequence state, all fp32 but pos.
 struct DecodeLayout {
   int *status;     // the state's first slot

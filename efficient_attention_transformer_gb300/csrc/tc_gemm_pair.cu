@@ -143,7 +143,10 @@ __device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (
   }
 }
 
-template <int EPI>
+// B_KM: B is the transpose of a row-major [N, K] matrix (K-major), each
+// CTA's half of the tile's columns one box of up to 128 rows x 64 k;
+// otherwise B is a row-major [K, N] matrix (N-major), 64-column boxes.
+template <int EPI, bool B_KM = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC0,
@@ -232,11 +235,18 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t full_leader = mapa_shared(full_own, 0);
           uint8_t *sA = tiles + stage * STAGE_BYTES;
           uint8_t *sB = sA + A_BYTES;
-          if (leader) mbar_arrive_expect_tx(full_own, 2 * (A_BYTES + hboxes * B_BOX_BYTES));
+          // a K-major B box is always 128 rows (rows past the tile's half
+          // are read and unused)
+          const uint32_t b_bytes = B_KM ? 2 * B_BOX_BYTES : hboxes * B_BOX_BYTES;
+          if (leader) mbar_arrive_expect_tx(full_own, 2 * (A_BYTES + b_bytes));
           tma_load_2d_pair(smem_u32(sA), &tmA, full_leader, kb * BK, arow);
-          for (int j = 0; j < hboxes; ++j)
-            tma_load_2d_pair(smem_u32(sB + j * B_BOX_BYTES), &tmB, full_leader,
-                             n0 + rank * half + j * 64, kb * BK);
+          if (B_KM) {
+            tma_load_2d_pair(smem_u32(sB), &tmB, full_leader, kb * BK, n0 + rank * half);
+          } else {
+            for (int j = 0; j < hboxes; ++j)
+              tma_load_2d_pair(smem_u32(sB + j * B_BOX_BYTES), &tmB, full_leader,
+                               n0 + rank * half + j * 64, kb * BK);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -260,7 +270,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-        const uint32_t idesc = idesc_bf16_f32(2 * BM, nsz, 0, 1);
+        const uint32_t idesc = idesc_bf16_f32(2 * BM, nsz, 0, B_KM ? 0 : 1);
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&sm->full[stage]), phase, &sm->abort_flag)) {
@@ -271,13 +281,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           tc_fence_after();
           const uint32_t sA = smem_u32(tiles + stage * STAGE_BYTES);
           // A: K-major, 16 elements (32 B) per step inside the swizzle atom;
-          // B: N-major, 16 rows of 128 B per step, 64-column boxes 8 KB apart
+          // B: N-major, 16 rows of 128 B per step, 64-column boxes 8 KB
+          // apart (or K-major like A)
           const uint64_t da = sw128_desc(sA, 16, 1024);
-          const uint64_t db = sw128_desc(sA + A_BYTES, B_BOX_BYTES, 1024);
+          const uint64_t db = B_KM ? sw128_desc(sA + A_BYTES, 16, 1024)
+                                   : sw128_desc(sA + A_BYTES, B_BOX_BYTES, 1024);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_f16_ss_pair(d_tmem, desc_advance(da, k * 32), desc_advance(db, k * 2048), idesc,
-                            (kb | k) != 0);
+            mma_f16_ss_pair(d_tmem, desc_advance(da, k * 32),
+                            desc_advance(db, B_KM ? k * 32 : k * 2048), idesc, (kb | k) != 0);
           mma_commit_pair_mc(smem_u32(&sm->empty[stage]), kPair);
           if (++stage == STAGES) {
             stage = 0;
@@ -427,7 +439,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
-template <int EPI>
+template <int EPI, bool B_KM = false>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &c0,
                    const CUtensorMap &c1, const CUtensorMap &c2, const Params &p,
                    const Problem &pr) {
@@ -437,7 +449,7 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kernel = tc_gemm_pair_kernel<EPI>;
+  auto kernel = tc_gemm_pair_kernel<EPI, B_KM>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -507,6 +519,26 @@ cudaError_t tc_projection_bf16(const Problem &pr) {
   p.causal = pr.causal;
   if (pr.rope) return launch<EPI_PROJ_ROPE>(tmA, tmB, tU, tV, tH, p, pr);
   return launch<EPI_PROJ>(tmA, tmB, tU, tV, tH, p, pr);
+}
+
+cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int M, int N, int K,
+                           int *status, int num_sms, cudaStream_t stream) {
+  if (M % BM != 0 || N % (2 * 64) != 0 || K % BK != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tC;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, A, M, K, K, BM, 64)) != cudaSuccess) return err;
+  if (b_km) err = make_tmap_bf16_2d(&tmB, B, N, K, K, BN / 2, 64);
+  else err = make_tmap_bf16_2d(&tmB, B, K, N, N, BK, 64);
+  if (err != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tC, C, M, N, N, 32, 64)) != cudaSuccess) return err;
+  Problem pr = {};
+  pr.M = M;
+  pr.status = status;
+  pr.stream = stream;
+  pr.num_sms = num_sms;
+  const Params p = base_params(pr, N, K);
+  if (b_km) return launch<EPI_STORE, true>(tmA, tmB, tC, tC, tC, p, pr);
+  return launch<EPI_STORE>(tmA, tmB, tC, tC, tC, p, pr);
 }
 
 cudaError_t tc_output_bf16(const Problem &pr) {
