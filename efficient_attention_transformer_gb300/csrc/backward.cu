@@ -856,13 +856,20 @@ cudaError_t run(const BackwardProblem &q) {
   }
   // ---- recompute the forward
   // (the tensor-core path keeps Pre in bf16, in the buffer of dPre)
-  if (tcc)  // the forward's 2-SM pair GEMM with its plain bf16 store
+  // the forward's 2-SM pair GEMM: with e a multiple of 256 its epilogue also
+  // forms V, Z and the heads (then no separate activation pass)
+  const bool fused_act = tcc && e % 256 == 0 && s == 128;
+  if (fused_act)
+    BW_TRY(pair_recompute_bf16(X, Wuvz, q.gamma, q.beta, dpre_io, V_io, Z, H_io, (int)M, d, e, s,
+                               L.status, q.num_sms, st));
+  else if (tcc)
     BW_TRY(pair_gemm_bf16(X, Wuvz, 0, dpre_io, (int)M, N, d, L.status, q.num_sms, st));
   else if (tc)
     BW_TRY(tc_gemm_any(tc_args(q, X, d, 0, Wuvz, N, 0, dpre_io, 1, (int)M, N, d, 0), st));
   else
     BW_TRY(gemm(st, (int)M, N, d, 1, X, op(d, 1), Wuvz, op(N, 1), StoreF32{pre, N, 1, 0, 1.f, 0}));
-  if (tcc)
+  if (fused_act) {
+  } else if (tcc)
     LAUNCH(act_heads_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, Z, q.gamma, q.beta, M, e,
                                                                   s, V_io, H_io)
   else if (tc)  // bf16 Pre, fp32 heads and V for the CUDA-core chunk contractions

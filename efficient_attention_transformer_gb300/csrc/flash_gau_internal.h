@@ -144,6 +144,14 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 // multiple of 128, N of 128, K of 64.
 cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int M, int N, int K,
                            int *status, int num_sms, cudaStream_t stream);
+// The backward's recompute on the pair GEMM: Pre = X W_uvz as bf16 [M,
+// 2e + s], and from its bf16 values V_io = swish (bf16 [M, e]), Z = swish
+// (fp32 [M, s]) and the four heads H_io = Z gamma_h + beta_h (bf16 [4, M,
+// s]); M a multiple of 128, e of 256, s = 128.
+cudaError_t pair_recompute_bf16(const void *X, const void *W_uvz, const float *gamma,
+                                const float *beta, void *pre, void *V_io, float *Z, void *H_io,
+                                int M, int d, int e, int s, int *status, int num_sms,
+                                cudaStream_t stream);
 
 // Decode step (decode.cu): the per-sequence state, all fp32 but pos.
 struct DecodeLayout {

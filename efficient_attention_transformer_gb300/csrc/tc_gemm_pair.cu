@@ -48,7 +48,10 @@ constexpr uint16_t kPair = 0x3, kLeader = 0x1;
 
 // EPI_PROJ_ROPE: the projection with the flash_block RoPE of the heads, a
 // separate instance so that its register needs stay out of the plain one.
-enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2 };
+// EPI_RECOMPUTE: the backward pass's recompute of X W_uvz: Pre in bf16 for
+// every column, and from its bf16 values the V activations (row-major bf16),
+// Z (fp32) and the four heads (bf16) that the backward's contractions read.
+enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2, EPI_RECOMPUTE = 3 };
 
 struct Params {
   int N, K;        // output columns, contraction depth
@@ -70,6 +73,8 @@ struct Params {
   const uint32_t *rope_cs;  // [s / 2][T] half2 (cos, sin)
   // output (flash_block): the shortcut added to O, or null
   const __nv_bfloat16 *residual;
+  // recompute: Z in fp32, [M, s]
+  float *zf;
 };
 
 struct Smem {
@@ -193,7 +198,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   // grid has completed (the first after its griddepcontrol.wait, the second
   // once every CTA of the first has passed that wait), and the previous
   // forward's kernels had all completed before this one got past its wait.
-  if (EPI != EPI_STORE && blockIdx.x == 0) {
+  if ((EPI == EPI_PROJ || EPI == EPI_PROJ_ROPE) && blockIdx.x == 0) {
     if (threadIdx.x == 0) {
       p.sched[kNextUnitWord] = 0;
       p.sched[kGridBarrierWord] = 0;
@@ -334,7 +339,52 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm->acc_empty[acc]), 0));
         }
         if (!valid) continue;
-        if constexpr (EPI == EPI_STORE) {
+        if constexpr (EPI == EPI_RECOMPUTE) {
+          const int n = n0 + c0;
+          uint4 w[8];
+          pack64(ra, rb, [](float x, int) { return x; }, w);
+          {
+            uint8_t *b = st.begin();
+            st.put(b, w);
+            st.finish(b, &tmC0, n, row0);
+          }
+          if (n >= p.e) {
+            // swish of the bf16 Pre, with the backward's sigmoid
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float xa = __bfloat162float(__float2bfloat16_rn(__uint_as_float(ra[j])));
+              const float xb = __bfloat162float(__float2bfloat16_rn(__uint_as_float(rb[j])));
+              ra[j] = __float_as_uint(xa * __fdividef(1.0f, 1.0f + __expf(-xa)));
+              rb[j] = __float_as_uint(xb * __fdividef(1.0f, 1.0f + __expf(-xb)));
+            }
+            if (n < 2 * p.e) {
+              pack64(ra, rb, [](float x, int) { return x; }, w);
+              uint8_t *b = st.begin();
+              st.put(b, w);
+              st.finish(b, &tmC1, n - p.e, row0);
+            } else {
+              const int c = n - 2 * p.e;  // column inside Z
+              float4 *zr = reinterpret_cast<float4 *>(p.zf + (size_t)(row0 + lane) * p.s + c);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {  // columns 4q.. from ra, 32 + 4q.. from rb
+                zr[q] = make_float4(__uint_as_float(ra[4 * q]), __uint_as_float(ra[4 * q + 1]),
+                                    __uint_as_float(ra[4 * q + 2]), __uint_as_float(ra[4 * q + 3]));
+                zr[8 + q] = make_float4(__uint_as_float(rb[4 * q]), __uint_as_float(rb[4 * q + 1]),
+                                        __uint_as_float(rb[4 * q + 2]), __uint_as_float(rb[4 * q + 3]));
+              }
+#pragma unroll 1
+              for (int h = 0; h < 4; ++h) {
+                const float *g = p.gamma + h * p.s + c;
+                const float *be = p.beta + h * p.s + c;
+                pack64(ra, rb, [&](float z, int col) { return fmaf(z, __ldg(g + col), __ldg(be + col)); },
+                       w);
+                uint8_t *b = st.begin();
+                st.put(b, w);
+                st.finish(b, &tmC2, c, h * p.M_tokens + row0);
+              }
+            }
+          }
+        } else if constexpr (EPI == EPI_STORE) {
           uint4 w[8];
           if (p.residual) {
             // the block's shortcut: this thread's row, 64 columns of X
@@ -539,6 +589,33 @@ cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int 
   const Params p = base_params(pr, N, K);
   if (b_km) return launch<EPI_STORE, true>(tmA, tmB, tC, tC, tC, p, pr);
   return launch<EPI_STORE>(tmA, tmB, tC, tC, tC, p, pr);
+}
+
+cudaError_t pair_recompute_bf16(const void *X, const void *W_uvz, const float *gamma,
+                                const float *beta, void *pre, void *V_io, float *Z, void *H_io,
+                                int M, int d, int e, int s, int *status, int num_sms,
+                                cudaStream_t stream) {
+  const int N = 2 * e + s;
+  if (M % BM != 0 || e % BN != 0 || s != 128 || d % BK != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tP, tV, tH;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, X, M, d, d, BM, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tmB, W_uvz, d, N, N, BK, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tP, pre, M, N, N, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tV, V_io, M, e, e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tH, H_io, 4LL * M, s, s, 32, 64)) != cudaSuccess) return err;
+  Problem pr = {};
+  pr.M = M;
+  pr.e = e;
+  pr.s = s;
+  pr.status = status;
+  pr.stream = stream;
+  pr.num_sms = num_sms;
+  Params p = base_params(pr, N, d);
+  p.gamma = gamma;
+  p.beta = beta;
+  p.zf = Z;
+  return launch<EPI_RECOMPUTE>(tmA, tmB, tP, tV, tH, p, pr);
 }
 
 cudaError_t tc_output_bf16(const Problem &pr) {
