@@ -113,6 +113,7 @@ struct AttnParams {
   const float *bias;  // [2C-1] relpos, -inf at causally masked offsets
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
+  int lin_off;     // no global term: no Q_lin or prefix loads, no Q_lin Prefix MMA
 };
 
 // Agents that consume each queued unit index: the MMA thread, the relu^2
@@ -308,7 +309,11 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         mbar_arrive(smem_u32(&bar->uq_full[q & 3]));
         return true;
       };
-      bool prefix_ready = false;
+      // Without a global term the kernel before this one is the projection
+      // itself (the chunk-state stage launches nothing): wait for it before
+      // the first ticket, as the projection zeroes the work counter.
+      bool prefix_ready = p.lin_off != 0;
+      if (prefix_ready) griddep_wait();
       for (int i = 0;; ++i) {
         int u = atomicAdd(p.next_unit, 1);
         if (u >= p.total) u = -1;
@@ -328,6 +333,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             ok = ok && load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB, col, ncb)) &&
                  load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB + 64, col, ncb));
           }
+          if (p.lin_off) continue;  // local term only
           if (ok && t == 0) {
             // the global term last: the prefix states come from the kernel
             // launched just before this one, which may still be running
@@ -457,14 +463,17 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
             ok = issue_b_tmem(pcol, kb == 0) && issue_b_tmem(pcol + 64, false);
             if (ok && last_t) mma_commit(smem_u32(&bar->sb_free[sb]));
           }
-          if (ok && t == 0) {
-            ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
-            if (ok) tc_fence_after();
+          if (!p.lin_off) {
+            if (ok && t == 0) {
+              ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
+              if (ok) tc_fence_after();
+            }
+            // with no key blocks the global term opens the accumulator
+            ok = ok && issue_b_smem(sQL, x.nkb == 0) && issue_b_smem(sQL + ATOM_BYTES, false);
+            if (!ok) break;
+            if (last_t) mma_commit(smem_u32(&bar->ql_empty));
           }
-          // with no key blocks the global term opens the accumulator
-          ok = ok && issue_b_smem(sQL, x.nkb == 0) && issue_b_smem(sQL + ATOM_BYTES, false);
           if (!ok) break;
-          if (last_t) mma_commit(smem_u32(&bar->ql_empty));
           mma_commit(smem_u32(&bar->acc_full[v & 1]));
         }
         if (!ok) break;
@@ -671,6 +680,7 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.bias = pr.bias;
   p.status = pr.status;
   p.next_unit = pr.status + kNextUnitWord;
+  p.lin_off = pr.lin_off;
   const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;
   return launch_pdl(chunk_attention_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
                     tQq, tKq, tQl, tV, tPre, tU, tG, p);

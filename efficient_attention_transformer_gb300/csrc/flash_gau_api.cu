@@ -345,6 +345,10 @@ int run_forward(const void *X, const flash_gau_weights *w, const flash_gau_block
   p.seg_ids = seg ? seg->ids : nullptr;
   p.chunk_average = (seg && seg->average) ? 1 : 0;
   p.per_chunk = (causal || p.seg_ids) ? 1 : 0;
+  p.lin_off = (dtype == FLASH_GAU_BF16 && !p.seg_ids && !p.chunk_average &&
+               p.local_scale != 0.f && (p.lin_scale == 0.f || (causal && p.G == 1)))
+                  ? 1
+                  : 0;
   p.X = X;
   p.W_uvz = w->W_uvz;
   p.W_o = w->W_o;

@@ -47,6 +47,10 @@ struct Problem {
   long long M;  // B * T tokens
   float lin_scale;
   float local_scale;  // factor on the local term; 0 = global term only
+  // bf16 without a chunk mask whose global term is zero for every chunk
+  // (lin_scale 0, or causal with a single chunk, where the only prefix is
+  // the empty sum) and whose local term is not: no chunk states, no prefix
+  int lin_off;
   // chunk mask of the global term: segment ids [B, G] (null: one segment)
   // and row normalisation; per_chunk: a prefix state per chunk (causal or
   // segmented), else one per batch row

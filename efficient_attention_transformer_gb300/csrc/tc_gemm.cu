@@ -463,6 +463,8 @@ GemmParams base_params(const Problem &pr) {
 }  // namespace
 
 cudaError_t tc_chunk_state_scan_bf16(const Problem &pr) {
+  // a zero global term: nothing to compute (the attention reads no prefix)
+  if (pr.lin_off) return cudaSuccess;
   // batch = chunk (b*G + g): State[chunk] = K_lin[chunk rows]^T V[chunk rows]
   const __nv_bfloat16 *Kl = (const __nv_bfloat16 *)pr.heads + 3 * pr.M * pr.s;
   CUtensorMap tmA, tmB, tS;
