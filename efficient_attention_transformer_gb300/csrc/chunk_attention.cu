@@ -114,6 +114,10 @@ struct AttnParams {
   int *status;
   int *next_unit;  // work counter, zeroed by the projection kernel
   int lin_off;     // no global term: no Q_lin or prefix loads, no Q_lin Prefix MMA
+  // chunks longer than the two S/P buffers (C > 256): a unit's value tiles
+  // all take each key block's P in turn (key blocks outer), so that one S
+  // and its relu^2 serve ng value tiles
+  int kb_outer;
 };
 
 // Agents that consume each queued unit index: the MMA thread, the relu^2
@@ -215,6 +219,9 @@ __device__ __forceinline__ void relu2_half(uint32_t sbuf, const AttnParams &p, i
   tmem_st16(sbuf + c0 + 16, hi);
 }
 
+// KB_OUTER: chunks longer than 256 with key blocks outer (p.kb_outer); a
+// separate instance, so that the other keeps its code as it is
+template <bool KB_OUTER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
                        const __grid_constant__ CUtensorMap tmKq,
@@ -324,6 +331,37 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const long long pre_row0 = (long long)(p.per_chunk ? x.chunk : x.b) * SD;
         const long long ncb = 2LL * p.n_et;  // 64-column blocks of e
         if (x.nkb > 0) ok = load_atoms(&tmQq, qrow) && load_atoms(&tmKq, x.tok0);
+        if constexpr (KB_OUTER) {
+          // per key block: the next K block, then this block's V rows of
+          // every value tile; then Q_lin and every value tile's prefix
+          for (int kb = 0; ok && kb < x.nkb; ++kb) {
+            if (kb + 1 < x.nkb)
+              ok = (!x.q_per_block || load_atoms(&tmQq, qrow)) &&
+                   load_atoms(&tmKq, x.tok0 + (kb + 1) * KB);
+            for (int t = 0; ok && t < x.ng; ++t) {
+              const int col = (x.et0 + t) * ET;
+              ok = load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB, col, ncb)) &&
+                   load(&tmV, 1, 0, rb64_row(x.tok0 + kb * KB + 64, col, ncb));
+            }
+          }
+          if (ok && !p.lin_off) {
+            if (!prefix_ready) {
+              griddep_wait();
+              prefix_ready = true;
+            }
+            ok = mbar_wait(smem_u32(&bar->ql_empty), (i & 1) ^ 1, abort);
+            if (!ok) break;
+            const uint32_t f = smem_u32(&bar->ql_full);
+            mbar_arrive_expect_tx(f, Q_BYTES);
+            tma_load_2d(smem_u32(tiles + OFF_QL), &tmQl, f, 0, (int)qrow);
+            tma_load_2d(smem_u32(tiles + OFF_QL + ATOM_BYTES), &tmQl, f, 64, (int)qrow);
+            for (int t = 0; ok && t < x.ng; ++t) {
+              const int col = (x.et0 + t) * ET;
+              ok = load(&tmPre, 1, 0, rb64_row(pre_row0, col, ncb)) &&
+                   load(&tmPre, 1, 0, rb64_row(pre_row0 + 64, col, ncb));
+            }
+          }
+        } else {
         for (int t = 0; ok && t < x.ng; ++t) {
           const int col = (x.et0 + t) * ET;
           for (int kb = 0; ok && kb < x.nkb; ++kb) {
@@ -350,6 +388,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           }
           ok = ok && load(&tmPre, 1, 0, rb64_row(pre_row0, col, ncb)) &&
                load(&tmPre, 1, 0, rb64_row(pre_row0 + 64, col, ncb));
+        }
         }
         if (!ok) break;
       }
@@ -440,6 +479,40 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
         const Unit x = unit_of(p, u);
         const int n0 = n;
         if (x.nkb > 0) ok = issue_s(true, x.q_per_block || x.nkb == 1);
+        if constexpr (KB_OUTER) {
+          // every accumulator of the unit drained by the epilogue first (the
+          // first S above overlaps that)
+          for (int t = 0; ok && t < x.ng; ++t)
+            ok = mbar_wait(smem_u32(&bar->acc_empty[(v + t) & 1]), (((v + t) >> 1) & 1) ^ 1, abort);
+          if (!ok) break;
+          tc_fence_after();
+          for (int kb = 0; ok && kb < x.nkb; ++kb) {
+            const int si = n0 + kb, sb = si & 1;
+            if (kb + 1 < x.nkb) ok = issue_s(x.q_per_block, x.q_per_block || kb + 2 == x.nkb);
+            ok = ok && mbar_wait(smem_u32(&bar->p_full[sb]), (si >> 1) & 1, abort);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t pcol = TM_S + sb * KB;
+            for (int t = 0; ok && t < x.ng; ++t) {
+              acc_col = TM_ACC + ((v + t) & 1) * ET;
+              ok = issue_b_tmem(pcol, kb == 0) && issue_b_tmem(pcol + 64, false);
+            }
+            if (ok) mma_commit(smem_u32(&bar->sb_free[sb]));
+          }
+          if (ok && !p.lin_off) {
+            ok = mbar_wait(smem_u32(&bar->ql_full), i & 1, abort);
+            if (ok) tc_fence_after();
+            for (int t = 0; ok && t < x.ng; ++t) {
+              acc_col = TM_ACC + ((v + t) & 1) * ET;
+              // with no key blocks the global term opens the accumulator
+              ok = issue_b_smem(sQL, x.nkb == 0) && issue_b_smem(sQL + ATOM_BYTES, false);
+            }
+            if (ok) mma_commit(smem_u32(&bar->ql_empty));
+          }
+          if (!ok) break;
+          for (int t = 0; t < x.ng; ++t) mma_commit(smem_u32(&bar->acc_full[(v + t) & 1]));
+          v += x.ng;
+        } else {
         // P of the unit's key blocks stays in TMEM for all its value tiles
         for (int t = 0; ok && t < x.ng; ++t, ++v) {
           const bool last_t = t + 1 == x.ng;
@@ -475,6 +548,7 @@ chunk_attention_kernel(const __grid_constant__ CUtensorMap tmQq,
           }
           if (!ok) break;
           mma_commit(smem_u32(&bar->acc_full[v & 1]));
+        }
         }
         if (!ok) break;
         release(i);
@@ -644,8 +718,11 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev < 64 && !(configured & (1ull << dev))) {
-    err = cudaFuncSetAttribute(chunk_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
+    err = cudaFuncSetAttribute(chunk_attention_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(chunk_attention_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
     configured |= 1ull << dev;
   }
@@ -666,6 +743,13 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
       p.ng = ng;
       break;
     }
+  // Longer chunks: key blocks outer, two value tiles a unit (the two
+  // accumulators), when that still leaves about two units per SM
+  p.kb_outer = 0;
+  if (pr.C > 2 * KB && p.n_et % 2 == 0 && tiles / 2 >= 2LL * pr.num_sms) {
+    p.kb_outer = 1;
+    p.ng = 2;
+  }
   p.n_vg = p.n_et / p.ng;
   // the last chunks as single-tile units: about one per SM
   const int BG = pr.B * pr.G, per_chunk = p.n_qt * p.n_et;
@@ -682,8 +766,11 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   p.next_unit = pr.status + kNextUnitWord;
   p.lin_off = pr.lin_off;
   const int grid = p.total < pr.num_sms ? p.total : pr.num_sms;
-  return launch_pdl(chunk_attention_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, pr.stream,
-                    tQq, tKq, tQl, tV, tPre, tU, tG, p);
+  if (p.kb_outer)
+    return launch_pdl(chunk_attention_kernel<true>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES,
+                      pr.stream, tQq, tKq, tQl, tV, tPre, tU, tG, p);
+  return launch_pdl(chunk_attention_kernel<false>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES,
+                    pr.stream, tQq, tKq, tQl, tV, tPre, tU, tG, p);
 }
 
 }  // namespace flashgau
