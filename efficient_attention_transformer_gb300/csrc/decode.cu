@@ -322,13 +322,18 @@ decode_scores(DecodeLayout L, const float *__restrict__ gamma, const float *__re
 }
 
 // one block per (128 value columns, sequence), 8 warps: gathers the
-// projection's slices into this block's U and V columns, then (warp w
-// taking keys j = w, w + 8, .. and linear-cache rows k = w, w + 8, ..;
-// each lane 4 consecutive columns, 16-byte loads) the weighted sum of the
-// cached V rows, the linear term and the gate; the warps' sums meet in a
-// fixed order
+// projection's slices into this block's U and V columns, then the weighted
+// sum over the chunk's cached V rows (weights a_j) and the rows of the
+// linear cache (weights lin_scale q_lin), each lane on 4 consecutive
+// columns (16-byte loads): warp w takes rows w, w + 8, .. of each, eight
+// loads in flight per lane.  MANY (many sequences, more than two blocks an
+// SM): the eight rows land in registers before one accumulator takes them
+// (64 registers, four blocks an SM); else each row has an accumulator of its
+// own (two blocks an SM, but shorter dependences per warp).  Then the gate.
+// The warps' sums meet in a fixed order.
 constexpr int kAttW = 8;
 constexpr int kAttCols = 128;  // value columns per block: 4 per lane
+constexpr int kAttBatch = 8;   // loads in flight per lane
 __device__ __forceinline__ float4 fma4(float a, float4 v, float4 acc) {
   return make_float4(fmaf(a, v.x, acc.x), fmaf(a, v.y, acc.y), fmaf(a, v.z, acc.z),
                      fmaf(a, v.w, acc.w));
@@ -337,6 +342,7 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
+template <bool MANY>
 __global__ void __launch_bounds__(32 * kAttW)
 decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_scale,
               __nv_bfloat16 *gated_io) {
@@ -352,6 +358,7 @@ decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_
   const float *ql = L.heads + ((long long)b * 4 + 2) * s;
   const float *sa = L.score + (long long)b * C;
   float *v_c = L.vc + (long long)b * C * e;
+  const float *pre = L.prefix + (long long)b * s * e + c;
   const bool on = c < e;  // e is a multiple of 8: all 4 columns or none
   float4 pu = make_float4(0.f, 0.f, 0.f, 0.f), pv = pu;
   if (on)
@@ -363,35 +370,71 @@ decode_attend(DecodeLayout L, int B, int C, int e, int s, int slices, float lin_
   const float4 vnew = make_float4(swish(pv.x), swish(pv.y), swish(pv.z), swish(pv.w));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (on) {
-    // eight independent 16-byte loads in flight per lane, one accumulator each
-    float4 a8[8], l8[8];
+    if constexpr (MANY) {
+      // the chunk's cached V rows j < i, then the linear cache's rows
+      for (int j0 = warp; j0 < i; j0 += kAttBatch * kAttW) {
+        float4 v[kAttBatch];
+        float a[kAttBatch];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) a8[t] = l8[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = warp; j0 < i; j0 += 8 * kAttW) {
+        for (int t = 0; t < kAttBatch; ++t) {
+          const int j = j0 + t * kAttW;
+          v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+          a[t] = 0.f;
+          if (j < i) {
+            v[t] = *reinterpret_cast<const float4 *>(v_c + (long long)j * e + c);
+            a[t] = sa[j];
+          }
+        }
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int j = j0 + t * kAttW;
-        if (j < i)
-          a8[t] = fma4(sa[j], *reinterpret_cast<const float4 *>(v_c + (long long)j * e + c), a8[t]);
+        for (int t = 0; t < kAttBatch; ++t) acc = fma4(a[t], v[t], acc);
       }
-    }
-    if (i % kAttW == warp) a8[0] = fma4(sa[i], vnew, a8[0]);
-    const float *pre = L.prefix + (long long)b * s * e + c;
-    for (int k0 = warp; k0 < s; k0 += 8 * kAttW) {
+      if (i % kAttW == warp) acc = fma4(sa[i], vnew, acc);
+      for (int k0 = warp; k0 < s; k0 += kAttBatch * kAttW) {
+        float4 v[kAttBatch];
+        float a[kAttBatch];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int k = k0 + t * kAttW;
-        if (k < s)
-          l8[t] = fma4(ql[k], *reinterpret_cast<const float4 *>(pre + (long long)k * e), l8[t]);
+        for (int t = 0; t < kAttBatch; ++t) {
+          const int k = k0 + t * kAttW;
+          v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+          a[t] = 0.f;
+          if (k < s) {
+            v[t] = *reinterpret_cast<const float4 *>(pre + (long long)k * e);
+            a[t] = ql[k];
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kAttBatch; ++t) acc = fma4(lin_scale * a[t], v[t], acc);
       }
-    }
-    float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      float4 a8[kAttBatch], l8[kAttBatch];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      acc = add4(acc, a8[t]);
-      l = add4(l, l8[t]);
+      for (int t = 0; t < kAttBatch; ++t) a8[t] = l8[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = warp; j0 < i; j0 += kAttBatch * kAttW) {
+#pragma unroll
+        for (int t = 0; t < kAttBatch; ++t) {
+          const int j = j0 + t * kAttW;
+          if (j < i)
+            a8[t] = fma4(sa[j], *reinterpret_cast<const float4 *>(v_c + (long long)j * e + c),
+                         a8[t]);
+        }
+      }
+      if (i % kAttW == warp) a8[0] = fma4(sa[i], vnew, a8[0]);
+      for (int k0 = warp; k0 < s; k0 += kAttBatch * kAttW) {
+#pragma unroll
+        for (int t = 0; t < kAttBatch; ++t) {
+          const int k = k0 + t * kAttW;
+          if (k < s)
+            l8[t] = fma4(ql[k], *reinterpret_cast<const float4 *>(pre + (long long)k * e), l8[t]);
+        }
+      }
+      float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int t = 0; t < kAttBatch; ++t) {
+        acc = add4(acc, a8[t]);
+        l = add4(l, l8[t]);
+      }
+      acc = fma4(lin_scale, l, acc);
     }
-    acc = fma4(lin_scale, l, acc);
   }
   red[warp][lane] = acc;
   __syncthreads();
@@ -494,10 +537,14 @@ cudaError_t step(const DecodeProblem &q) {
   const int ksp = (q.d + sp - 1) / sp, kso = (q.e + so - 1) / so;
 
   static unsigned long long configured = 0;  // shared-memory ceilings, per device
+  static int sms[64];                         // and SM counts
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev >= 64) return cudaErrorInvalidDevice;
   if (!(configured & (1ull << dev))) {
+    if ((err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) !=
+        cudaSuccess)
+      return err;
     if ((err = cudaFuncSetAttribute(gemv_splitk<T, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kGemvSmem)) != cudaSuccess ||
         (err = cudaFuncSetAttribute(gemv_splitk<float, T>,
@@ -518,8 +565,11 @@ cudaError_t step(const DecodeProblem &q) {
                         q.stream, q.L, q.gamma, q.beta, q.relpos, q.B, q.C, q.e, q.s, sp,
                         q.local_scale)) != cudaSuccess)
     return err;
-  if ((err = launch_pdl(decode_attend, dim3((q.e + kAttCols - 1) / kAttCols, q.B), dim3(32 * kAttW),
-                        0, q.stream, q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale,
+  // more attention blocks than two an SM: the few-register form
+  const dim3 agrid((q.e + kAttCols - 1) / kAttCols, q.B);
+  const bool many = (long long)agrid.x * agrid.y > 2LL * sms[dev];
+  if ((err = launch_pdl(many ? decode_attend<true> : decode_attend<false>, agrid,
+                        dim3(32 * kAttW), 0, q.stream, q.L, q.B, q.C, q.e, q.s, sp, q.lin_scale,
                         tc ? (__nv_bfloat16 *)q.L.gated_io : (__nv_bfloat16 *)nullptr)) !=
       cudaSuccess)
     return err;

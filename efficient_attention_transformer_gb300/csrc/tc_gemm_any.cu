@@ -81,7 +81,10 @@ struct Tile {
 };
 __device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
   Tile x;
-  const int split = t % p.splits, rem = t / p.splits;
+  // split slowest: the CTAs of one round work on the same K range, whose
+  // operand rows then stay in L2 for every output tile that reads them
+  const int out_tiles = p.total / p.splits;
+  const int split = t / out_tiles, rem = t % out_tiles;
   x.nt = rem % p.n_tiles;
   x.mt = (rem / p.n_tiles) % p.m_tiles;
   x.z = rem / (p.n_tiles * p.m_tiles);
@@ -388,13 +391,25 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   p.n_tiles = (g.N + BN - 1) / BN;
   const int kblocks = (g.K + g.K2) / BK;
   // split K when the output tiles would leave SMs idle (fp32 atomic output
-  // only); at least 8 k-blocks a split
+  // only), at least 8 k-blocks a split: the count with the least estimated
+  // time, the persistent grid's rounds times the k-blocks of a split, plus
+  // for each split an fp32 reduce-add of the whole result (measured on the
+  // weight gradients: about 1.8 k-block times per MB of result)
   int splits = 1;
   const int out_tiles = (int)Z * p.m_tiles * p.n_tiles;
   if (!g.c_bf16 && g.allow_split && out_tiles < g.num_sms) {
-    splits = (2 * g.num_sms + out_tiles - 1) / out_tiles;
+    const double out_mb = (double)Z * g.M * g.N * sizeof(float) / 1e6;
     const int max_splits = kblocks / 8 > 1 ? kblocks / 8 : 1;
-    if (splits > max_splits) splits = max_splits;
+    double best = 0.0;
+    for (int sp = 1; sp <= max_splits; ++sp) {
+      const int kbs = (kblocks + sp - 1) / sp, n = (kblocks + kbs - 1) / kbs;
+      const long long rounds = ((long long)out_tiles * n + g.num_sms - 1) / g.num_sms;
+      const double cost = (double)rounds * kbs + (n > 1 ? 1.8 * n * out_mb : 0.0);
+      if (sp == 1 || cost < best) {
+        best = cost;
+        splits = n;
+      }
+    }
   }
   p.kb_split = (kblocks + splits - 1) / splits;
   p.splits = (kblocks + p.kb_split - 1) / p.kb_split;
