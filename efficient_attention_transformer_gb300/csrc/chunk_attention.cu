@@ -735,11 +735,12 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
   // Value tiles per unit: the unit's P is computed once and stays in TMEM
   // for each of them, which takes a unit's key blocks fitting the two S/P
   // buffers (C <= 256); else one.  As many as divide the value tiles while
-  // leaving about two units per SM for the dynamic scheduler to balance.
+  // leaving at least one unit per SM (the single-tile units at the end of
+  // the schedule balance the SMs' finishing times).
   const long long tiles = (long long)pr.B * pr.G * p.n_qt * p.n_et;
   p.ng = 1;
   for (int ng : {4, 3, 2})
-    if (pr.C <= 2 * KB && p.n_et % ng == 0 && tiles / ng >= 2LL * pr.num_sms) {
+    if (pr.C <= 2 * KB && p.n_et % ng == 0 && tiles / ng >= pr.num_sms) {
       p.ng = ng;
       break;
     }
