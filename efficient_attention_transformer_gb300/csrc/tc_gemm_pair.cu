@@ -55,8 +55,9 @@ enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2, EPI_RECOMPUTE = 3 };
 
 struct Params {
   int N, K;        // output columns, contraction depth
+  int bn;          // columns per pair tile: 256, or 128
   int m_tiles;     // 128-row tiles of the output
-  int n_tiles;     // 256-column pair tiles
+  int n_tiles;     // bn-column pair tiles
   int total;       // ceil(m_tiles / 2) * n_tiles pair tiles
   const float *gamma, *beta;
   int M_tokens;
@@ -230,7 +231,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // an overhanging CTA of the last pair re-reads the last valid rows
         // (its results are discarded) so every box is in bounds
         const int arow = min(mt, p.m_tiles - 1) * BM;
-        const int n0 = nt * BN, half = min(BN, p.N - n0) / 2, hboxes = half / 64;
+        const int n0 = nt * p.bn, half = min(p.bn, p.N - n0) / 2, hboxes = half / 64;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
@@ -267,7 +268,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int local = 0;
       for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
         const int nt = t % p.n_tiles;
-        const int nsz = min(BN, p.N - nt * BN);
+        const int nsz = min(p.bn, p.N - nt * p.bn);
         const int acc = local & 1;
         if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), ((local >> 1) & 1) ^ 1, &sm->abort_flag)) {
           raise_timeout(sm, p.status);
@@ -317,7 +318,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
       const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
       const bool valid = mt < p.m_tiles;
-      const int n0 = nt * BN, nsz = min(BN, p.N - n0);
+      const int n0 = nt * p.bn, nsz = min(p.bn, p.N - n0);
       const int acc = local & 1;
       if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
         raise_timeout(sm, p.status);
@@ -527,12 +528,25 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, c0, c1, c2, p);
 }
 
-Params base_params(const Problem &pr, int N, int K) {
+// Pair tile width for a plain product: 256 columns, or 128 where the pairs'
+// rounds come out fuller.  A 128-column tile takes about 0.6 of a
+// 256-column one (it reads the same A block; the mainloop is bound by shared
+// memory traffic, not by the MMAs): measured on the output projection, 256
+// rows a pair, 768 columns, 1536 deep.
+int store_bn(long long M, int N, int num_sms) {
+  const long long row_pairs = (M / BM + 1) / 2, pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  if (N % (BN / 2) != 0) return BN;
+  auto rounds = [&](int bn) { return (row_pairs * ((N + bn - 1) / bn) + pairs - 1) / pairs; };
+  return 0.6 * rounds(BN / 2) < rounds(BN) ? BN / 2 : BN;
+}
+
+Params base_params(const Problem &pr, int N, int K, int bn = BN) {
   Params p = {};
   p.N = N;
   p.K = K;
+  p.bn = bn;
   p.m_tiles = (int)(pr.M / BM);
-  p.n_tiles = (N + BN - 1) / BN;
+  p.n_tiles = (N + bn - 1) / bn;
   p.total = (p.m_tiles + 1) / 2 * p.n_tiles;
   p.status = pr.status;
   p.M_tokens = (int)pr.M;
@@ -586,7 +600,7 @@ cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int 
   pr.status = status;
   pr.stream = stream;
   pr.num_sms = num_sms;
-  const Params p = base_params(pr, N, K);
+  const Params p = base_params(pr, N, K, store_bn(M, N, num_sms));
   if (b_km) return launch<EPI_STORE, true>(tmA, tmB, tC, tC, tC, p, pr);
   return launch<EPI_STORE>(tmA, tmB, tC, tC, tC, p, pr);
 }
@@ -626,7 +640,7 @@ cudaError_t tc_output_bf16(const Problem &pr) {
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
     return err;
   if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
-  Params p = base_params(pr, pr.d, pr.e);
+  Params p = base_params(pr, pr.d, pr.e, store_bn(pr.M, pr.d, pr.num_sms));
   p.residual = (const __nv_bfloat16 *)pr.residual;
   return launch<EPI_STORE>(tmA, tmB, tO, tO, tO, p, pr);
 }
