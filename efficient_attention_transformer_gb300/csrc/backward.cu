@@ -574,12 +574,6 @@ __global__ void act_heads_bf16(const __nv_bfloat16 *__restrict__ pre, float *__r
 // and division intrinsics (their errors are far below the bf16 rounding of
 // Pre), and only the bf16 operands that the tensor-core contractions read
 // are written besides Z.
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x); }
-__device__ __forceinline__ float swish_grad_fast(float x) {
-  const float sg = sigmoid_fast(x);
-  return sg * (1.0f + x * (1.0f - sg));
-}
 
 // The tensor-core path keeps no U: U = swish(Pre_u) is recomputed from
 // the bf16 Pre wherever it is needed (the values are those that U held,
@@ -621,30 +615,6 @@ __global__ void act_heads_vz(const __nv_bfloat16 *__restrict__ pre, float *__res
   }
 }
 
-// A = swish(Pre_u) * Vh as bf16 (Pre row stride N = 2e + s; Vh bf16)
-__global__ void gate_pre(const __nv_bfloat16 *__restrict__ pre, const __nv_bfloat16 *__restrict__ Vh,
-                         __nv_bfloat16 *__restrict__ A_io, long long M, int e, int s) {
-  pdl_enter();
-  const int N = 2 * e + s, e4 = e / 4;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  long long m = i0 / e4;
-  int c4 = (int)(i0 - m * e4);
-  const long long dm = stride / e4;
-  const int dc = (int)(stride - dm * e4);
-  for (long long i = i0; i < M * e4; i += stride) {
-    const float4 x = load_bf4(pre + m * N + 4 * c4), v = load_bf4(Vh + 4 * i);
-    store_bf4(A_io + 4 * i, swish_fast(x.x) * v.x, swish_fast(x.y) * v.y, swish_fast(x.z) * v.z,
-              swish_fast(x.w) * v.w);
-    m += dm;
-    c4 += dc;
-    if (c4 >= e4) {
-      c4 -= e4;
-      ++m;
-    }
-  }
-}
-
 // The gate's gradient and the U part of dPre in one pass: with u =
 // swish(Pre_u), dVh = dA * u (bf16) and dPre_u = (dA * Vh) * swish'(Pre_u),
 // written in place over Pre_u (bf16); no dU buffer.  dA and Vh come as bf16
@@ -677,31 +647,22 @@ __global__ void gate_grad_pre(const __nv_bfloat16 *__restrict__ dA,
   }
 }
 
-// The V and Z parts of dPre = d(V | Z) * swish'(Pre), bf16, in place (dV
-// comes as bf16 from its contraction)
-__global__ void pre_grad_vz(__nv_bfloat16 *__restrict__ pre_io, const __nv_bfloat16 *__restrict__ dV,
-                            const float *__restrict__ dZ, long long M, int e, int s) {
+// The Z part of dPre = dZ * swish'(Pre_z), bf16, in place (Pre row stride
+// 2e + s; the U and V parts come from the epilogues of the contractions
+// that produce dU and dV)
+__global__ void pre_grad_z(__nv_bfloat16 *__restrict__ pre_io, const float *__restrict__ dZ,
+                           long long M, int e, int s) {
   pdl_enter();
-  const int N = 2 * e + s, W4 = (e + s) / 4, e4 = e / 4, s4 = s / 4;
+  const int N = 2 * e + s, s4 = s / 4;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  long long m = i0 / W4;
-  int c4 = (int)(i0 - m * W4);
-  const long long dm = stride / W4;
-  const int dc = (int)(stride - dm * W4);
-  for (long long i = i0; i < M * W4; i += stride) {
-    const float4 g = c4 < e4 ? load_bf4(dV + (m * e4 + c4) * 4)
-                             : reinterpret_cast<const float4 *>(dZ)[m * s4 + c4 - e4];
-    __nv_bfloat16 *px = pre_io + m * N + e + 4 * c4;
-    const float4 x = load_bf4(px);
-    store_bf4(px, g.x * swish_grad_fast(x.x), g.y * swish_grad_fast(x.y),
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < M * s4; i += stride) {
+    const long long m = i / s4;
+    const int c4 = (int)(i - m * s4);
+    const float4 g = reinterpret_cast<const float4 *>(dZ)[i];
+    __nv_bfloat16 *pz = pre_io + m * N + 2 * e + 4 * c4;
+    const float4 x = load_bf4(pz);
+    store_bf4(pz, g.x * swish_grad_fast(x.x), g.y * swish_grad_fast(x.y),
               g.z * swish_grad_fast(x.z), g.w * swish_grad_fast(x.w));
-    m += dm;
-    c4 += dc;
-    if (c4 >= W4) {
-      c4 -= W4;
-      ++m;
-    }
   }
 }
 
@@ -902,7 +863,8 @@ cudaError_t run(const BackwardProblem &q) {
   // Vh (+)= Q_lin Prefix (a chunk's prefix, or its batch row's total)
   if (tcc) {
     // Vh = (l P) V + Q_lin Prefix as one two-product contraction
-    GemmAnyArgs g = tc_args(q, P_io, C, 0, V_io, e, 0, Vh, 1, C, e, C, 0);  // bf16 Vh
+    // bf16 Vh, and in the epilogue the gated product A = swish(Pre_u) * Vh
+    GemmAnyArgs g = tc_args(q, P_io, C, 0, V_io, e, 0, Vh, 1, C, e, C, 0);
     g.batches = (int)BG;
     g.A2 = Ql_io;
     g.lda2 = s;
@@ -911,15 +873,20 @@ cudaError_t run(const BackwardProblem &q) {
     g.ldb2 = e;
     g.K2 = s;
     g.b2_div = pdiv;
+    g.epi = kEpiGate;
+    g.E = dpre_io;  // Pre's U columns
+    g.lde = N;
+    g.D = A_io;
+    g.ldd = e;
     BW_TRY(tc_gemm_any(g, st));
   } else {
     const Operand opre = q.causal ? op(e, 1, se) : op(e, 1, se, G);
     BW_TRY(gemm(st, C, e, s, (int)BG, Ql, op(s, 1, (long long)C * s), prefix, opre,
                 StoreF32{Vh, e, 1, (long long)C * e, 1.f, 1}));
   }
-  if (tcc)
-    LAUNCH(gate_pre, blocks_for(M * e / 4), 256, 0, st, dpre_io, (const bf *)Vh, A_io, M, e, s)
-  else if (tc)
+  if (tcc) {
+    // the gate was applied in the epilogue above
+  } else if (tc)
     LAUNCH(gate_v4, blocks_for(M * e / 4), 256, 0, st, (const float4 *)U, (const float4 *)Vh, A_io,
                                                     M * e / 4)
   else
@@ -995,8 +962,10 @@ cudaError_t run(const BackwardProblem &q) {
     LAUNCH(scan_backward, blocks_for(q.B * se), 256, 0, st, dpre, q.B, G, se, q.causal, dst_io)
   if (tcc) {
     BW_TRY(bt(V_io, e, 0, dst_io, e, 1, dKl, C, s, e, 1, 1.f, 0));
-    // dV = (l P)^T dVh + K_lin dState as one two-product contraction
-    GemmAnyArgs g = tc_args(q, P_io, C, 1, dVh_io, e, 0, dV, 1, C, e, C, 0);  // bf16 dV
+    // dV = (l P)^T dVh + K_lin dState as one two-product contraction; its
+    // epilogue writes the V part of dPre = dV * swish'(Pre_v) in place over
+    // Pre_v (bf16), so dV itself is never stored
+    GemmAnyArgs g = tc_args(q, P_io, C, 1, dVh_io, e, 0, nullptr, 1, C, e, C, 0);
     g.batches = (int)BG;
     g.A2 = Kl_io;
     g.lda2 = s;
@@ -1005,6 +974,11 @@ cudaError_t run(const BackwardProblem &q) {
     g.ldb2 = e;
     g.K2 = s;
     g.b2_div = 1;
+    g.epi = kEpiSwishGrad;
+    g.E = dpre_io + e;
+    g.lde = N;
+    g.D = dpre_io + e;
+    g.ldd = N;
     BW_TRY(tc_gemm_any(g, st));
   } else {
     BW_TRY(gemm(st, C, s, e, (int)BG, V, op(e, 1, (long long)C * e), dpre, op(1, e, se),
@@ -1017,9 +991,8 @@ cudaError_t run(const BackwardProblem &q) {
   LAUNCH(heads_grad, (unsigned)((M + rows - 1) / rows), 256, 0, st, dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows)
   // ---- input side
-  if (tcc)  // the U part was written by gate_grad_pre
-    LAUNCH(pre_grad_vz, blocks_for(M * (e + s) / 4), 256, 0, st, dpre_io, (const bf *)dV, dZ, M, e,
-                                                                   s)
+  if (tcc)  // the U part came from gate_grad_pre, the V part from the dV contraction
+    LAUNCH(pre_grad_z, blocks_for(M * s / 4), 256, 0, st, dpre_io, dZ, M, e, s)
   else if (tc)
     LAUNCH(pre_grad_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, dU, dV, dZ, M, e, s)
   else

@@ -108,6 +108,21 @@ constexpr int kGridBarrierWord = 17;
 
 
 // General tcgen05 GEMM (tc_gemm_any.cu): C[M, N] = A B, bf16 operands.
+enum { kEpiNone = 0, kEpiGate = 1, kEpiSwishGrad = 2 };
+
+#ifdef __CUDACC__
+// The backward's activation arithmetic: the sigmoid from the fast
+// exponential and reciprocal
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+__device__ __forceinline__ float swish_fast(float x) { return x * sigmoid_fast(x); }
+__device__ __forceinline__ float swish_grad_fast(float x) {
+  const float sg = sigmoid_fast(x);
+  return sg * (1.0f + x * (1.0f - sg));
+}
+#endif
+
 struct GemmAnyArgs {
   const void *A;
   long long lda;
@@ -139,6 +154,16 @@ struct GemmAnyArgs {
   long long ldb2 = 0;
   int K2 = 0;
   int b2_div = 1;
+  // optional elementwise epilogue (bf16 C only) with an operand E and a
+  // result D, both bf16 with C's rows and columns (leading dimensions lde,
+  // ldd): kEpiGate stores C and D = swish(E) * C; kEpiSwishGrad stores
+  // D = C * swish'(E) only (C is then not written, and D may be E itself).
+  // C's values enter as rounded to bf16.
+  int epi = 0;
+  const void *E = nullptr;
+  long long lde = 0;
+  void *D = nullptr;
+  long long ldd = 0;
 };
 cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream);
 

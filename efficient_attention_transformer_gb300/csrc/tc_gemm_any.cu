@@ -17,6 +17,12 @@
 // second product (its own A majorness, B2 stored as B) following those of
 // the first, so that a sum of two contractions needs no second pass over C.
 //
+// Elementwise epilogues (bf16 C): each epilogue warp loads the box of an
+// operand E with C's coordinates by TMA into its second staging buffer (the
+// next box's load issued as soon as the current one is read) and stores
+// D = swish(E) * C (with C) or D = C * swish'(E) (instead of C): the gate
+// of the layer and the activation's gradient, without a separate pass.
+//
 // One persistent CTA per SM over 128 x 256 output tiles (x split), static
 // round robin.  Warp 0 streams 64-deep k-blocks of A and B into a 4-stage
 // ring of 128-byte-swizzled boxes with TMA; one thread of warp 1 issues
@@ -62,6 +68,7 @@ struct Smem {
   uint64_t full[STAGES], empty[STAGES];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t drain;
+  uint64_t ebar[4];  // per epilogue warp: its E box landed
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -94,11 +101,13 @@ __device__ __forceinline__ Tile tile_of(const AnyParams &p, int t) {
   return x;
 }
 
-template <bool A_MN, bool B_KM, bool OUT_BF16>
+template <bool A_MN, bool B_KM, bool OUT_BF16, int EPI = kEpiNone>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmA2,
-                   const __grid_constant__ CUtensorMap tmB2, const AnyParams p) {
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmE,
+                   const __grid_constant__ CUtensorMap tmD, const AnyParams p) {
+  static_assert(EPI == kEpiNone || OUT_BF16, "elementwise epilogues take a bf16 C");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -115,6 +124,7 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       mbar_init(smem_u32(&sm->acc_empty[i]), 4);  // one arrival per epilogue warp
     }
     mbar_init(smem_u32(&sm->drain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sm->ebar[i]), 1);
     sm->abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -244,6 +254,20 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     uint8_t *stg = tiles + STG_OFF + (warp - 2) * 2 * STG_BYTES;
+    // elementwise epilogues: this warp's E boxes land in its second buffer
+    uint8_t *ebox = stg + STG_BYTES;
+    const uint32_t ebar = smem_u32(&sm->ebar[warp - 2]);
+    uint32_t e_issued = 0, e_used = 0;
+    auto load_e = [&](int t) {  // box 0 of tile t, or nothing past the list
+      if (t >= p.total) return;
+      const Tile y = tile_of(p, t);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(ebar, STG_BYTES);
+        tma_load_2d(smem_u32(ebox), &tmE, ebar, y.nt * BN, y.z * p.M + y.mt * BM + quarter * 32);
+      }
+      ++e_issued;
+    };
+    if constexpr (EPI != kEpiNone) load_e(blockIdx.x);
     int local = 0, nbox = 0;
     for (int t = blockIdx.x; t < p.total && !sm->abort_flag; t += gridDim.x, ++local) {
       const Tile x = tile_of(p, t);
@@ -267,24 +291,75 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
           if (lane == 0) mbar_arrive(smem_u32(&sm->acc_empty[acc]));
         }
         if constexpr (OUT_BF16) {
-          // this row's 64 columns into the swizzled box, then one TMA store
-          if (lane == 0) tma_store_wait_read<0>();
-          __syncwarp();
+          // this row's 64 columns as bf16
+          uint4 w[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const uint32_t *v = q < 4 ? &ra[8 * q] : &rb[8 * (q - 4)];
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            w.y = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            w.z = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            w.w = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            *reinterpret_cast<uint4 *>(stg + sw128_offset(lane, q)) = w;
+            w[q].x = pack_bf16(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            w[q].y = pack_bf16(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            w[q].z = pack_bf16(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            w[q].w = pack_bf16(__uint_as_float(v[6]), __uint_as_float(v[7]));
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, smem_u32(stg), n0 + c0, row0);
-            tma_store_commit();
+          if constexpr (EPI != kEpiSwishGrad) {
+            // into the swizzled box, then one TMA store
+            if (lane == 0) tma_store_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(stg + sw128_offset(lane, q)) = w[q];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, smem_u32(stg), n0 + c0, row0);
+              tma_store_commit();
+            }
+          }
+          if constexpr (EPI != kEpiNone) {
+            if (!mbar_wait(ebar, e_used & 1, &sm->abort_flag)) {
+              raise_timeout(sm, p.status);
+              break;
+            }
+            ++e_used;
+            // D from this row's E and C values
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 ev = *reinterpret_cast<const uint4 *>(ebox + sw128_offset(lane, q));
+              const uint32_t eu[4] = {ev.x, ev.y, ev.z, ev.w};
+              uint32_t cu[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 ef = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&eu[j]));
+                const float2 cf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&cu[j]));
+                if constexpr (EPI == kEpiGate)
+                  cu[j] = pack_bf16(swish_fast(ef.x) * cf.x, swish_fast(ef.y) * cf.y);
+                else
+                  cu[j] = pack_bf16(cf.x * swish_grad_fast(ef.x), cf.y * swish_grad_fast(ef.y));
+              }
+              w[q] = make_uint4(cu[0], cu[1], cu[2], cu[3]);
+            }
+            // the E buffer is free: the next box's load (this tile's, or the
+            // first of this warp's next tile)
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (c0 + 64 < nsz) {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(ebar, STG_BYTES);
+                tma_load_2d(smem_u32(ebox), &tmE, ebar, n0 + c0 + 64, row0);
+              }
+              ++e_issued;
+            } else {
+              load_e(t + gridDim.x);
+            }
+            if (lane == 0) tma_store_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(stg + sw128_offset(lane, q)) = w[q];
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, smem_u32(stg), n0 + c0, row0);
+              tma_store_commit();
+            }
           }
         } else {
           // two 32-column fp32 boxes, alternating between the warp's two
@@ -314,6 +389,10 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
       }
     }
+    // an E load still in flight (a prefetch past an early exit) lands
+    // before the shared memory is given up
+    if constexpr (EPI != kEpiNone)
+      if (e_issued > e_used) mbar_wait(ebar, e_used & 1);
     if (lane == 0) tma_store_wait<0>();
     __syncwarp();
   }
@@ -326,15 +405,15 @@ tc_gemm_any_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   }
 }
 
-template <bool A_MN, bool B_KM, bool OUT_BF16>
+template <bool A_MN, bool B_KM, bool OUT_BF16, int EPI = kEpiNone>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                   const CUtensorMap &tmA2, const CUtensorMap &tmB2, const AnyParams &p,
-                   int num_sms, cudaStream_t stream) {
+                   const CUtensorMap &tmA2, const CUtensorMap &tmB2, const CUtensorMap &tmE,
+                   const CUtensorMap &tmD, const AnyParams &p, int num_sms, cudaStream_t stream) {
   static unsigned long long configured = 0;  // one bit per device ordinal
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  auto kernel = tc_gemm_any_kernel<A_MN, B_KM, OUT_BF16>;
+  auto kernel = tc_gemm_any_kernel<A_MN, B_KM, OUT_BF16, EPI>;
   if (dev < 64 && !(configured & (1ull << dev))) {
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (err != cudaSuccess) return err;
@@ -342,7 +421,7 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   }
   const int grid = p.total < num_sms ? p.total : num_sms;
   return launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tmA, tmB, tmC,
-                    tmA2, tmB2, p);
+                    tmA2, tmB2, tmE, tmD, p);
 }
 
 }  // namespace
@@ -366,9 +445,22 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
   if (g.b_km) err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.N, g.K, g.ldb, kbox, 64);
   else err = make_tmap_bf16_2d(&tmB, g.B, ZB * g.K, g.N, g.ldb, 64, 64);
   if (err != cudaSuccess) return err;
-  if (g.c_bf16) err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64);
+  // elementwise epilogues: E and D boxes as C's (C unused by kEpiSwishGrad)
+  if (g.epi != kEpiNone &&
+      (!g.c_bf16 || !g.E || !g.D || (g.epi != kEpiGate && g.epi != kEpiSwishGrad) ||
+       (g.epi == kEpiGate && !g.C)))
+    return cudaErrorInvalidValue;
+  CUtensorMap tmE, tmD;
+  if (g.epi != kEpiNone) {
+    if ((err = make_tmap_bf16_2d(&tmE, g.E, Z * g.M, g.N, g.lde, 32, 64)) != cudaSuccess ||
+        (err = make_tmap_bf16_2d(&tmD, g.D, Z * g.M, g.N, g.ldd, 32, 64)) != cudaSuccess)
+      return err;
+  }
+  if (g.epi == kEpiSwishGrad) tmC = tmD;
+  else if (g.c_bf16) err = make_tmap_bf16_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 64);
   else err = make_tmap_f32_2d(&tmC, g.C, Z * g.M, g.N, g.N, 32, 32);
   if (err != cudaSuccess) return err;
+  if (g.epi == kEpiNone) tmE = tmD = tmC;
   // the second product's operands (unused copies of the first's when none)
   CUtensorMap tmA2 = tmA, tmB2 = tmB;
   if (g.K2 > 0) {
@@ -425,17 +517,32 @@ cudaError_t tc_gemm_any(const GemmAnyArgs &g, cudaStream_t stream) {
         cudaSuccess)
       return err;
   }
+  // the epilogue forms exist for an N-major B (the backward's Vh and dV)
+  if (g.epi != kEpiNone && g.b_km) return cudaErrorInvalidValue;
+  if (g.epi == kEpiGate)
+    return g.a_mn ? launch<true, false, true, kEpiGate>(tmA, tmB, tmC, tmA2, tmB2, tmE, tmD, p,
+                                                          g.num_sms, stream)
+                  : launch<false, false, true, kEpiGate>(tmA, tmB, tmC, tmA2, tmB2, tmE, tmD, p,
+                                                           g.num_sms, stream);
+  if (g.epi == kEpiSwishGrad)
+    return g.a_mn ? launch<true, false, true, kEpiSwishGrad>(tmA, tmB, tmC, tmA2, tmB2, tmE, tmD,
+                                                               p, g.num_sms, stream)
+                  : launch<false, false, true, kEpiSwishGrad>(tmA, tmB, tmC, tmA2, tmB2, tmE, tmD,
+                                                                p, g.num_sms, stream);
   const int key = (g.a_mn ? 4 : 0) | (g.b_km ? 2 : 0) | (g.c_bf16 ? 1 : 0);
+#define ANY_LAUNCH(am, bk, cb) \
+  launch<am, bk, cb>(tmA, tmB, tmC, tmA2, tmB2, tmE, tmD, p, g.num_sms, stream)
   switch (key) {
-    case 0: return launch<false, false, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 1: return launch<false, false, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 2: return launch<false, true, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 3: return launch<false, true, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 4: return launch<true, false, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 5: return launch<true, false, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    case 6: return launch<true, true, false>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
-    default: return launch<true, true, true>(tmA, tmB, tmC, tmA2, tmB2, p, g.num_sms, stream);
+    case 0: return ANY_LAUNCH(false, false, false);
+    case 1: return ANY_LAUNCH(false, false, true);
+    case 2: return ANY_LAUNCH(false, true, false);
+    case 3: return ANY_LAUNCH(false, true, true);
+    case 4: return ANY_LAUNCH(true, false, false);
+    case 5: return ANY_LAUNCH(true, false, true);
+    case 6: return ANY_LAUNCH(true, true, false);
+    default: return ANY_LAUNCH(true, true, true);
   }
+#undef ANY_LAUNCH
 }
 
 }  // namespace flashgau
