@@ -615,38 +615,6 @@ __global__ void act_heads_vz(const __nv_bfloat16 *__restrict__ pre, float *__res
   }
 }
 
-// The gate's gradient and the U part of dPre in one pass: with u =
-// swish(Pre_u), dVh = dA * u (bf16) and dPre_u = (dA * Vh) * swish'(Pre_u),
-// written in place over Pre_u (bf16); no dU buffer.  dA and Vh come as bf16
-// from the contractions that produce them (every product here is rounded
-// to bf16 anyway).
-__global__ void gate_grad_pre(const __nv_bfloat16 *__restrict__ dA,
-                              const __nv_bfloat16 *__restrict__ Vh, __nv_bfloat16 *__restrict__ pre,
-                              __nv_bfloat16 *__restrict__ dVh_io, long long M, int e, int s) {
-  pdl_enter();
-  const int N = 2 * e + s, e4 = e / 4;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long i0 = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  long long m = i0 / e4;
-  int c4 = (int)(i0 - m * e4);
-  const long long dm = stride / e4;
-  const int dc = (int)(stride - dm * e4);
-  for (long long i = i0; i < M * e4; i += stride) {
-    __nv_bfloat16 *pu = pre + m * N + 4 * c4;
-    const float4 a = load_bf4(dA + 4 * i), v = load_bf4(Vh + 4 * i), x = load_bf4(pu);
-    store_bf4(dVh_io + 4 * i, a.x * swish_fast(x.x), a.y * swish_fast(x.y), a.z * swish_fast(x.z),
-              a.w * swish_fast(x.w));
-    store_bf4(pu, (a.x * v.x) * swish_grad_fast(x.x), (a.y * v.y) * swish_grad_fast(x.y),
-              (a.z * v.z) * swish_grad_fast(x.z), (a.w * v.w) * swish_grad_fast(x.w));
-    m += dm;
-    c4 += dc;
-    if (c4 >= e4) {
-      c4 -= e4;
-      ++m;
-    }
-  }
-}
-
 // The Z part of dPre = dZ * swish'(Pre_z), bf16, in place (Pre row stride
 // 2e + s; the U and V parts come from the epilogues of the contractions
 // that produce dU and dV)
@@ -899,10 +867,12 @@ cudaError_t run(const BackwardProblem &q) {
       g.c_zeroed = 1;
       BW_TRY(tc_gemm_any(g, st));
     }
-    // dA = dO W_o^T: B the transpose of the stored [e, d] W_o (bf16 when
-    // the gate's gradient kernel below reads it)
-    if (tcc)  // bf16 dA on the pair GEMM
-      BW_TRY(pair_gemm_bf16(dO, Wo, 1, dA, (int)M, e, d, L.status, q.num_sms, st));
+    // dA = dO W_o^T: B the transpose of the stored [e, d] W_o.  The
+    // tensor-core chunk path forms it on the pair GEMM, whose epilogue
+    // takes it straight into the gate's gradient (dVh, and dPre_u over Pre_u)
+    if (tcc)
+      BW_TRY(pair_gate_grad_bf16(dO, Wo, dpre_io, Vh, dVh_io, (int)M, e, s, d, L.status,
+                                 q.num_sms, st));
     else
       BW_TRY(tc_gemm_any(tc_args(q, dO, d, 0, Wo, d, 1, dA, 0, (int)M, e, d, 0), st));
   } else {
@@ -910,10 +880,7 @@ cudaError_t run(const BackwardProblem &q) {
                 StoreF32{q.dW_o, d, 1, 0, 1.f, 0}));
     BW_TRY(gemm(st, (int)M, e, d, 1, dO, op(d, 1), Wo, op(1, d), StoreF32{dA, e, 1, 0, 1.f, 0}));
   }
-  if (tcc)
-    LAUNCH(gate_grad_pre, blocks_for(M * e / 4), 256, 0, st, (const bf *)dA, (const bf *)Vh,
-                                                          dpre_io, dVh_io, M, e, s)
-  else
+  if (!tcc)
     LAUNCH(gate_grad, blocks_for(M * e), 256, 0, st, dA, U, Vh, dU, dVh, M * e, nullptr)
   // ---- local part
   if (tcc) {
@@ -991,7 +958,7 @@ cudaError_t run(const BackwardProblem &q) {
   LAUNCH(heads_grad, (unsigned)((M + rows - 1) / rows), 256, 0, st, dH, Z, q.gamma, dZ, q.dgamma,
                                                                 q.dbeta, M, s, rows)
   // ---- input side
-  if (tcc)  // the U part came from gate_grad_pre, the V part from the dV contraction
+  if (tcc)  // the U part came from the dA contraction, the V part from the dV one
     LAUNCH(pre_grad_z, blocks_for(M * s / 4), 256, 0, st, dpre_io, dZ, M, e, s)
   else if (tc)
     LAUNCH(pre_grad_v4, blocks_for(M * N / 4), 256, 0, st, dpre_io, dU, dV, dZ, M, e, s)

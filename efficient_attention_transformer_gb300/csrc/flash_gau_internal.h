@@ -177,6 +177,12 @@ cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int 
 // 2e + s], and from its bf16 values V_io = swish (bf16 [M, e]), Z = swish
 // (fp32 [M, s]) and the four heads H_io = Z gamma_h + beta_h (bf16 [4, M,
 // s]); M a multiple of 128, e of 256, s = 128.
+// dVh = dA * swish(Pre_u) and dPre_u = (dA * Vh) * swish'(Pre_u) (over Pre_u
+// in place, Pre's rows 2e + s wide) with dA = dO W_o^T formed on the pair
+// GEMM and not stored; M a multiple of 128, e of 128, d of 64
+cudaError_t pair_gate_grad_bf16(const void *dO, const void *W_o, void *pre, const void *Vh,
+                                void *dVh, int M, int e, int s, int d, int *status, int num_sms,
+                                cudaStream_t stream);
 cudaError_t pair_recompute_bf16(const void *X, const void *W_uvz, const float *gamma,
                                 const float *beta, void *pre, void *V_io, float *Z, void *H_io,
                                 int M, int d, int e, int s, int *status, int num_sms,

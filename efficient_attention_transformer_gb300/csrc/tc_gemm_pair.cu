@@ -41,9 +41,9 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);  // producer, MMA issuer, epilogue
 constexpr int STG_BYTES = 32 * 128;                // one 32-row x 128-byte store box
-constexpr int STG_OFF = STAGES * STAGE_BYTES;      // one staging box per epilogue warp
-constexpr int TILE_BYTES = STG_OFF + EPI_WARPS * STG_BYTES;
-constexpr int SMEM_BYTES = TILE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// Shared memory of an instance: the stage ring, then each epilogue warp's
+// staging boxes (one; the gate-gradient epilogue three: its two operand
+// boxes and a store box, with a shorter ring to make room)
 constexpr uint16_t kPair = 0x3, kLeader = 0x1;
 
 // EPI_PROJ_ROPE: the projection with the flash_block RoPE of the heads, a
@@ -51,7 +51,21 @@ constexpr uint16_t kPair = 0x3, kLeader = 0x1;
 // EPI_RECOMPUTE: the backward pass's recompute of X W_uvz: Pre in bf16 for
 // every column, and from its bf16 values the V activations (row-major bf16),
 // Z (fp32) and the four heads (bf16) that the backward's contractions read.
-enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2, EPI_RECOMPUTE = 3 };
+// EPI_GATE_GRAD: the backward's dA = dO W_o^T, and from it in the epilogue
+// (with Pre_u and Vh boxes loaded by TMA) the gate's gradient:
+// dVh = dA * swish(Pre_u) and the U part of dPre = (dA * Vh) * swish'(Pre_u),
+// the latter in place over Pre_u; dA itself is not stored.
+enum Epi { EPI_PROJ = 0, EPI_STORE = 1, EPI_PROJ_ROPE = 2, EPI_RECOMPUTE = 3, EPI_GATE_GRAD = 4 };
+
+template <int EPI>
+struct Layout {
+  static constexpr int stages = EPI == EPI_GATE_GRAD ? 4 : STAGES;
+  static constexpr int boxes = EPI == EPI_GATE_GRAD ? 3 : 1;  // staging boxes per epilogue warp
+  static constexpr int stg_off = stages * STAGE_BYTES;
+  static constexpr int tile_bytes = stg_off + EPI_WARPS * boxes * STG_BYTES;
+  static constexpr int smem_bytes = tile_bytes + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(smem_bytes <= 227 * 1024, "shared memory of one CTA");
+};
 
 struct Params {
   int N, K;        // output columns, contraction depth
@@ -84,6 +98,7 @@ struct Smem {
   uint64_t acc_full[2];    // both: an accumulator is ready
   uint64_t acc_empty[2];   // leader: both CTAs drained an accumulator
   uint64_t drain;
+  uint64_t ebar[EPI_WARPS];  // gate gradient: an epilogue warp's operand boxes landed
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -161,16 +176,18 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem *sm = reinterpret_cast<Smem *>(tiles + TILE_BYTES);
+  using L = Layout<EPI>;
+  Smem *sm = reinterpret_cast<Smem *>(tiles + L::tile_bytes);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rank = (int)cluster_ctarank();  // 0 = leader of the pair
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < L::stages; ++i) {
       mbar_init(smem_u32(&sm->full[i]), 1);
       mbar_init(smem_u32(&sm->empty[i]), 1);
     }
+    for (int i = 0; i < EPI_WARPS; ++i) mbar_init(smem_u32(&sm->ebar[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm->acc_full[i]), 1);
       mbar_init(smem_u32(&sm->acc_empty[i]), 2 * EPI_WARPS);  // all epilogue warps, 2 CTAs
@@ -253,7 +270,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               tma_load_2d_pair(smem_u32(sB + j * B_BOX_BYTES), &tmB, full_leader,
                                n0 + rank * half + j * 64, kb * BK);
           }
-          if (++stage == STAGES) {
+          if (++stage == L::stages) {
             stage = 0;
             phase ^= 1;
           }
@@ -297,7 +314,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mma_f16_ss_pair(d_tmem, desc_advance(da, k * 32),
                             desc_advance(db, B_KM ? k * 32 : k * 2048), idesc, (kb | k) != 0);
           mma_commit_pair_mc(smem_u32(&sm->empty[stage]), kPair);
-          if (++stage == STAGES) {
+          if (++stage == L::stages) {
             stage = 0;
             phase ^= 1;
           }
@@ -313,7 +330,96 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // -------------------------------------------------- epilogue (both)
     const int quarter = warp & 3;       // TMEM lanes 32*quarter .. +31
     const int half = (warp - 2) >> 2;   // which half of the tile's columns
-    Stager st{tiles + STG_OFF + (warp - 2) * STG_BYTES, lane};
+    Stager st{tiles + L::stg_off + (warp - 2) * L::boxes * STG_BYTES, lane};
+    if constexpr (EPI == EPI_GATE_GRAD) {
+      // boxes: st.buf carries dVh; xb is Pre_u, then dPre_u in place; vb is Vh
+      uint8_t *xb = st.buf + STG_BYTES, *vb = st.buf + 2 * STG_BYTES;
+      const uint32_t ebar = smem_u32(&sm->ebar[warp - 2]);
+      uint32_t e_issued = 0, e_used = 0;
+      auto load_e = [&](int col, int row) {
+        if (lane == 0) {
+          tma_store_wait_read<0>();  // the previous box's stores have read xb
+          mbar_arrive_expect_tx(ebar, 2 * STG_BYTES);
+          tma_load_2d(smem_u32(xb), &tmC1, ebar, col, row);
+          tma_load_2d(smem_u32(vb), &tmC2, ebar, col, row);
+        }
+        ++e_issued;
+      };
+      int local = 0;
+      for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
+        const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
+        const bool valid = mt < p.m_tiles;
+        const int n0 = nt * p.bn, nsz = min(p.bn, p.N - n0);
+        const int acc = local & 1;
+        const int row0 = mt * BM + quarter * 32;
+        const int cbeg = half * (nsz / 2), cend = (half + 1) * (nsz / 2);
+        // the first box's operands load while the accumulator fills
+        if (valid) load_e(n0 + cbeg, row0);
+        if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
+          raise_timeout(sm, p.status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * ACC_COLS;
+        bool ok = true;
+        for (int c0 = cbeg; c0 < cend; c0 += 64) {
+          if (valid && c0 != cbeg) load_e(n0 + c0, row0);
+          uint32_t ra[32], rb[32];
+          tmem_ld32(taddr + c0, ra);
+          tmem_ld32(taddr + c0 + 32, rb);
+          tmem_ld_wait();
+          if (c0 + 64 >= cend) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sm->acc_empty[acc]), 0));
+          }
+          if (!valid) continue;
+          if (!mbar_wait(ebar, e_used & 1, &sm->abort_flag)) {
+            raise_timeout(sm, p.status);
+            ok = false;
+            break;
+          }
+          ++e_used;
+          // dA as bf16 (as the separate kernel read it), with this row's Pre_u and Vh
+          uint4 w[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t *src = q < 4 ? &ra[8 * q] : &rb[8 * (q - 4)];
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xb + sw128_offset(lane, q));
+            const uint4 vv = *reinterpret_cast<const uint4 *>(vb + sw128_offset(lane, q));
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+            uint32_t dvh[4], dpu[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 a = __bfloat1622float2(__floats2bfloat162_rn(
+                  __uint_as_float(src[2 * j]), __uint_as_float(src[2 * j + 1])));
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xw[j]));
+              const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&vw[j]));
+              dvh[j] = pack_bf16(a.x * swish_fast(x.x), a.y * swish_fast(x.y));
+              dpu[j] = pack_bf16((a.x * v.x) * swish_grad_fast(x.x), (a.y * v.y) * swish_grad_fast(x.y));
+            }
+            w[q] = make_uint4(dvh[0], dvh[1], dvh[2], dvh[3]);
+            *reinterpret_cast<uint4 *>(xb + sw128_offset(lane, q)) =
+                make_uint4(dpu[0], dpu[1], dpu[2], dpu[3]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(st.buf + sw128_offset(lane, q)) = w[q];
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC0, smem_u32(st.buf), n0 + c0, row0);
+            tma_store_2d(&tmC1, smem_u32(xb), n0 + c0, row0);
+            tma_store_commit();
+          }
+        }
+        if (!ok) break;
+      }
+      // operands still in flight (an early exit) land before the shared
+      // memory is given up
+      if (e_issued > e_used) mbar_wait(ebar, e_used & 1);
+      if (lane == 0) tma_store_wait<0>();
+      __syncwarp();
+    } else {
     int local = 0;
     for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
       const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
@@ -479,6 +585,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
     }
     st.drain();
+    }
   }
 
   tc_fence_before();
@@ -510,12 +617,13 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Layout<EPI>::smem_bytes;
   cfg.stream = pr.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (max_pairs[dev] == 0) {
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Layout<EPI>::smem_bytes);
     if (err != cudaSuccess) return err;
     int n = 0;
     cfg.gridDim = dim3(2 * (pr.num_sms / 2));
@@ -603,6 +711,28 @@ cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int 
   const Params p = base_params(pr, N, K, store_bn(M, N, num_sms));
   if (b_km) return launch<EPI_STORE, true>(tmA, tmB, tC, tC, tC, p, pr);
   return launch<EPI_STORE>(tmA, tmB, tC, tC, tC, p, pr);
+}
+
+cudaError_t pair_gate_grad_bf16(const void *dO, const void *W_o, void *pre, const void *Vh,
+                                void *dVh, int M, int e, int s, int d, int *status, int num_sms,
+                                cudaStream_t stream) {
+  const int N = 2 * e + s;  // Pre's row: U, V, Z
+  if (M % BM != 0 || e % (2 * 64) != 0 || d % BK != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tD, tX, tV;
+  cudaError_t err;
+  if ((err = make_tmap_bf16_2d(&tmA, dO, M, d, d, BM, 64)) != cudaSuccess) return err;
+  // B = W_o^T: the stored [e, d] W_o read K-major
+  if ((err = make_tmap_bf16_2d(&tmB, W_o, e, d, d, BN / 2, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tD, dVh, M, e, e, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tX, pre, M, e, N, 32, 64)) != cudaSuccess) return err;
+  if ((err = make_tmap_bf16_2d(&tV, Vh, M, e, e, 32, 64)) != cudaSuccess) return err;
+  Problem pr = {};
+  pr.M = M;
+  pr.status = status;
+  pr.stream = stream;
+  pr.num_sms = num_sms;
+  const Params p = base_params(pr, e, d, store_bn(M, e, num_sms));
+  return launch<EPI_GATE_GRAD, true>(tmA, tmB, tD, tX, tV, p, pr);
 }
 
 cudaError_t pair_recompute_bf16(const void *X, const void *W_uvz, const float *gamma,
