@@ -23,12 +23,15 @@
 // The contractions run on one batched, strided GEMM kernel (64 x 64 tiles,
 // 4 x 4 per thread), so transposed views cost no copies; the rest are
 // elementwise or column-reduction kernels.  For bf16 io, when the shapes
-// tile, every contraction runs on the tensor cores instead (tc_gemm_any.cu):
-// the five large ones (Pre, dW_o, dA, dX, dW_uvz) and, batched over the
-// chunks, the chunk-level ones, with their operands (the gated product,
-// dPre, V, the heads, P, dS, dVh, the prefix states and their gradients)
-// rounded to bf16 by the kernels that produce them; sums, scans and the
-// elementwise steps stay fp32.
+// tile, every contraction runs on the tensor cores instead: the five large
+// ones (Pre, dW_o, dA, dX, dW_uvz) on the 2-SM pair GEMM or the general one
+// (tc_gemm_pair.cu, tc_gemm_any.cu) and, batched over the chunks, the
+// chunk-level ones, with their operands (the gated product, dPre, V, the
+// heads, P, dS, dVh, the prefix states and their gradients) rounded to
+// bf16 by the kernels that produce them.  There the elementwise steps that
+// follow a contraction run in its epilogue: V, Z and the heads in the
+// recompute's, A = U * Vh in Vh's, the gate's gradient in dA's (dA is not
+// stored), dV * swish'(Pre_v) in dV's; sums and scans stay fp32.
 #include <cuda_bf16.h>
 
 #include "flash_gau_internal.h"

@@ -289,9 +289,9 @@ int flash_gau_forward_segmented(const void *X, const flash_gau_weights *w,
  * tcgen05 tensor cores with bf16 operands and fp32 accumulation (with C or
  * s not multiples of 128, the chunk-level ones run on the CUDA cores);
  * fp32 io, and other bf16 shapes, run the contractions in fp32 on the
- * CUDA cores.  Sums, scans and the
- * elementwise steps are fp32 in both cases.  Gradients are written, not
- * added.                                                                   */
+ * CUDA cores.  Sums and scans are fp32 in both cases; on the tensor-core
+ * path the elementwise steps run in fp32 on bf16 operands, most of them in
+ * the epilogues of the contractions.  Gradients are written, not added.    */
 typedef struct flash_gau_grads {
   void *dX;          /* device [B, T, d], io type                           */
   float *dW_uvz;     /* device [d, 2e+s] fp32, columns as in W_uvz          */
