@@ -276,6 +276,21 @@ decode_scores(DecodeLayout L, const float *__restrict__ gamma, const float *__re
   if (j0 > i && blockIdx.x != 0) return;
   const float *yp = L.proj + (long long)b * N;
   const long long sstride = (long long)B * N;
+  const float *kq_c = L.kq + (long long)b * C * s;
+  constexpr int KW = kKeyTile / 8;  // keys per warp
+  constexpr int MS = kMaxS / 32;    // key elements per lane
+  float kv[KW][MS];
+  // the cached keys first: they do not depend on this step's projection
+#pragma unroll
+  for (int t = 0; t < KW; ++t) {
+    const int j = j0 + warp * KW + t;
+#pragma unroll
+    for (int m = 0; m < MS; ++m) {
+      const int k = lane + 32 * m;
+      kv[t][m] = 0.f;
+      if (j < i && k < s) kv[t][m] = kq_c[(long long)j * s + k];
+    }
+  }
   for (int k = threadIdx.x; k < s; k += blockDim.x) {
     float pz = 0.f;
     for (int q = 0; q < slices; ++q) pz += yp[q * sstride + 2 * e + k];
@@ -288,19 +303,14 @@ decode_scores(DecodeLayout L, const float *__restrict__ gamma, const float *__re
   }
   __syncthreads();
   if (j0 > i) return;
-  const float *kq_c = L.kq + (long long)b * C * s;
   const float inv_c = 1.0f / (float)C;
-  constexpr int KW = kKeyTile / 8;  // keys per warp
-  constexpr int MS = kMaxS / 32;    // key elements per lane
-  float kv[KW][MS];
 #pragma unroll
   for (int t = 0; t < KW; ++t) {
     const int j = j0 + warp * KW + t;
 #pragma unroll
     for (int m = 0; m < MS; ++m) {
       const int k = lane + 32 * m;
-      kv[t][m] = 0.f;
-      if (j <= i && k < s) kv[t][m] = j < i ? kq_c[(long long)j * s + k] : kq_new[k];
+      if (j == i && k < s) kv[t][m] = kq_new[k];
     }
   }
 #pragma unroll
@@ -478,7 +488,7 @@ decode_finish(DecodeLayout L, T *__restrict__ out, int B, int C, int d, int e, i
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (blockIdx.y == 0 && c < d) {
     float v = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int q = 0; q < slices; ++q) v += L.outp[((long long)q * B + b) * d + c];
     out[(long long)b * d + c] = from_f<T>(v);
   }
