@@ -141,27 +141,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
       : "memory");
 }
 
-// L2 eviction priority policies for bulk tensor copies: evict_last keeps the
-// lines a later kernel reads again ahead of other data; evict_first lets a
-// last read leave first.
+// L2 eviction priority policy for bulk tensor stores: evict_last keeps the
+// lines a later kernel reads again ahead of other data.
 __device__ __forceinline__ uint64_t l2_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
-}
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-// tma_load_2d with an L2 policy
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, uint32_t bar,
-                                                 int x, int y, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(pol)
-      : "memory");
 }
 
 // ------------------------------------------------------------- clusters
