@@ -38,6 +38,8 @@ def _built():
     # as tensor-core products over 64 (and 1) padded sequence rows
     (64, 260, 768, 1536, 128, 256, "bf16", 1.0 / 256, 1.0),
     (1, 40, 768, 1536, 128, 16, "bf16", 1.0, 1.0),
+    # more attention blocks than two an SM in fp32: the one-accumulator form
+    (32, 20, 256, 1536, 64, 16, "fp32", 1.0, 1.0),
 ])
 def test_decode_matches_causal_forward(B, steps, d, e, s, C, dtype, lin_scale, local_scale):
     T = -(-steps // C) * C
