@@ -5,6 +5,9 @@
 //                ("Transformer Quality in Linear Time", Method, eq. 5 and
 //                 the four heads of mixed chunk attention)
 //   output       O = gated W_o                   (display after eq. 8)
+// and for the backward pass's weight-sized ones: the recompute of X W_uvz
+// (with V, Z and the heads), dA = dO W_o^T with the gate's gradient in its
+// epilogue, and dX = dPre W_uvz^T (a K-major B).
 //
 // A cluster of two CTAs on neighbouring SMs computes 256 x 256 output tiles
 // with tcgen05.mma.cta_group::2 (M = 256): each CTA holds its own 128 rows
