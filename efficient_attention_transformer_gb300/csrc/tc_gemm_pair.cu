@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <vector>
+
 #include "flash_gau_internal.h"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
@@ -72,10 +74,13 @@ struct Layout {
 
 struct Params {
   int N, K;        // output columns, contraction depth
-  int bn;          // columns per pair tile: 256, or 128
+  int bn;          // columns per pair tile of the first rp_split row pairs: 256 or 128
   int m_tiles;     // 128-row tiles of the output
-  int n_tiles;     // bn-column pair tiles
-  int total;       // ceil(m_tiles / 2) * n_tiles pair tiles
+  int n_tiles;     // bn-column pair tiles per row pair
+  // the row pairs from rp_split on (a last, partial round of tiles) in
+  // 128-column tiles, n_tiles2 per row pair, from tile index t_split on
+  int rp_split, n_tiles2, t_split;
+  int total;       // pair tiles
   const float *gamma, *beta;
   int M_tokens;
   int e, s;
@@ -170,7 +175,9 @@ __device__ __forceinline__ void pack64(const uint32_t (&a)[32], const uint32_t (
 // B_KM: B is the transpose of a row-major [N, K] matrix (K-major), each
 // CTA's half of the tile's columns one box of up to 128 rows x 64 k;
 // otherwise B is a row-major [K, N] matrix (N-major), 64-column boxes.
-template <int EPI, bool B_KM = false>
+// TAIL: the launch's last row pairs run 128-column tiles (plan_tiles); a
+// separate instance, so that launches without one keep the plain mapping
+template <int EPI, bool B_KM = false, bool TAIL = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC0,
@@ -233,12 +240,25 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const uint32_t tmem_base = sm->tmem_base;
   const int kblocks = p.K / BK;
   const int first = blockIdx.x / 2, step = gridDim.x / 2;
-  // Pair tile t covers row pair row_pair(t), n-tile t % n_tiles.  The output
-  // projection walks the rows last first: the attention kernel wrote the
-  // last rows of the gated product most recently, so they are still in L2.
-  auto row_pair = [&](int t) {
-    const int rp = t / p.n_tiles;
-    return EPI == EPI_STORE ? (p.m_tiles + 1) / 2 - 1 - rp : rp;
+  // Pair tile t: row pair rp, columns n0 .. n0 + nsz.  Tiles before t_split
+  // are bn wide (row pairs in order, n-tiles fastest), the rest 128 wide.
+  // The output projection walks the rows last first: the attention kernel
+  // wrote the last rows of the gated product most recently, so they are
+  // still in L2.
+  auto geom = [&](int t, int &rp, int &n0, int &nsz) {
+    int w;
+    if (!TAIL || t < p.t_split) {
+      rp = t / p.n_tiles;
+      n0 = (t % p.n_tiles) * p.bn;
+      w = p.bn;
+    } else {
+      const int u = t - p.t_split;
+      rp = p.rp_split + u / p.n_tiles2;
+      n0 = (u % p.n_tiles2) * (BN / 2);
+      w = BN / 2;
+    }
+    nsz = min(w, p.N - n0);
+    if (EPI == EPI_STORE) rp = (p.m_tiles + 1) / 2 - 1 - rp;
   };
 
   if (warp == 0) {
@@ -247,11 +267,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       for (int t = first; t < p.total && !sm->abort_flag; t += step) {
-        const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
+        int rp, n0, nsz;
+        geom(t, rp, n0, nsz);
+        const int mt = rp * 2 + rank;
         // an overhanging CTA of the last pair re-reads the last valid rows
         // (its results are discarded) so every box is in bounds
         const int arow = min(mt, p.m_tiles - 1) * BM;
-        const int n0 = nt * p.bn, half = min(p.bn, p.N - n0) / 2, hboxes = half / 64;
+        const int half = nsz / 2, hboxes = half / 64;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, &sm->abort_flag)) {
             raise_timeout(sm, p.status);
@@ -287,8 +309,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0;
       int local = 0;
       for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
-        const int nt = t % p.n_tiles;
-        const int nsz = min(p.bn, p.N - nt * p.bn);
+        int rp, n0, nsz;
+        geom(t, rp, n0, nsz);
         const int acc = local & 1;
         if (!mbar_wait(smem_u32(&sm->acc_empty[acc]), ((local >> 1) & 1) ^ 1, &sm->abort_flag)) {
           raise_timeout(sm, p.status);
@@ -350,9 +372,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       };
       int local = 0;
       for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
-        const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
+        int rp, n0, nsz;
+        geom(t, rp, n0, nsz);
+        const int mt = rp * 2 + rank;
         const bool valid = mt < p.m_tiles;
-        const int n0 = nt * p.bn, nsz = min(p.bn, p.N - n0);
         const int acc = local & 1;
         const int row0 = mt * BM + quarter * 32;
         const int cbeg = half * (nsz / 2), cend = (half + 1) * (nsz / 2);
@@ -425,9 +448,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
     int local = 0;
     for (int t = first; t < p.total && !sm->abort_flag; t += step, ++local) {
-      const int mt = row_pair(t) * 2 + rank, nt = t % p.n_tiles;
+      int rp, n0, nsz;
+      geom(t, rp, n0, nsz);
+      const int mt = rp * 2 + rank;
       const bool valid = mt < p.m_tiles;
-      const int n0 = nt * p.bn, nsz = min(p.bn, p.N - n0);
       const int acc = local & 1;
       if (!mbar_wait(smem_u32(&sm->acc_full[acc]), (local >> 1) & 1, &sm->abort_flag)) {
         raise_timeout(sm, p.status);
@@ -600,17 +624,21 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   }
 }
 
-template <int EPI, bool B_KM = false>
+template <int EPI, bool B_KM = false, bool TAIL = false>
 cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &c0,
                    const CUtensorMap &c1, const CUtensorMap &c2, const Params &p,
                    const Problem &pr) {
+  // plain products may carry a tail of 128-column tiles (plan_tiles)
+  if constexpr (!TAIL && (EPI == EPI_STORE || EPI == EPI_GATE_GRAD)) {
+    if (p.t_split < p.total) return launch<EPI, B_KM, true>(tmA, tmB, c0, c1, c2, p, pr);
+  }
   // per device: shared-memory attribute set, and how many pairs fit at once
   static int max_pairs[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  auto kernel = tc_gemm_pair_kernel<EPI, B_KM>;
+  auto kernel = tc_gemm_pair_kernel<EPI, B_KM, TAIL>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -639,26 +667,82 @@ cudaError_t launch(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtenso
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, c0, c1, c2, p);
 }
 
-// Pair tile width for a plain product: 256 columns, or 128 where the pairs'
-// rounds come out fuller.  A 128-column tile takes about 0.6 of a
-// 256-column one (it reads the same A block; the mainloop is bound by shared
-// memory traffic, not by the MMAs): measured on the output projection, 256
-// rows a pair, 768 columns, 1536 deep.
-int store_bn(long long M, int N, int num_sms) {
-  const long long row_pairs = (M / BM + 1) / 2, pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
-  if (N % (BN / 2) != 0) return BN;
-  auto rounds = [&](int bn) { return (row_pairs * ((N + bn - 1) / bn) + pairs - 1) / pairs; };
-  return 0.6 * rounds(BN / 2) < rounds(BN) ? BN / 2 : BN;
+// The tile plan of a launch: bn-column tiles (256 or 128) for the first
+// rp_split row pairs, 128-column tiles for the rest, chosen to minimise the
+// busiest pair's work when tile t goes to pair t % pairs.  A 128-column
+// tile counts about 0.6 of a 256-column one: it reads the same A block, and
+// the mainloop is bound by shared-memory traffic rather than by the MMAs
+// (measured on the output projection, 256 rows a pair, 768 columns, 1536
+// deep).  So a last, partial round of 256-column tiles is cut into twice
+// as many 128-column ones when they fit one round, or every tile is 128
+// wide when that fills the rounds better.  Plain products only: the
+// projection's epilogue makes its narrow tiles dearer (a 128-column tail
+// measured slower there), so it keeps 256-column tiles.
+struct Plan {
+  int bn;
+  int rp_split;
+};
+
+double plan_makespan(int row_pairs, int N, int pairs, int bn, int rp_split,
+                     std::vector<double> &load) {
+  load.assign(pairs, 0.0);
+  long long t = 0;
+  auto add = [&](int w, int rows) {
+    for (int r = 0; r < rows; ++r)
+      for (int n0 = 0; n0 < N; n0 += w, ++t) load[t % pairs] += (N - n0 >= BN) && w == BN ? 1.0 : 0.6;
+  };
+  add(bn, rp_split);
+  add(BN / 2, row_pairs - rp_split);
+  double m = 0.0;
+  for (double v : load) m = v > m ? v : m;
+  return m;
 }
 
-Params base_params(const Problem &pr, int N, int K, int bn = BN) {
+Plan plan_tiles(long long M, int N, int num_sms) {
+  const int row_pairs = (int)((M / BM + 1) / 2), pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  Plan best = {BN, row_pairs};
+  if (N % (BN / 2) != 0) return best;
+  const int n256 = (N + BN - 1) / BN, n128 = N / (BN / 2);
+  // large launches: the last round is a small part of the work
+  if ((long long)row_pairs * n256 > 16LL * pairs) return best;
+  thread_local struct {
+    long long M;
+    int N, sms;
+    Plan plan;
+  } cache[8];
+  thread_local int next = 0;
+  for (const auto &c : cache)
+    if (c.M == M && c.N == N && c.sms == num_sms) return c.plan;
+  std::vector<double> load;
+  double cost = plan_makespan(row_pairs, N, pairs, BN, row_pairs, load);
+  auto consider = [&](int bn, int rp_split) {
+    const double c = plan_makespan(row_pairs, N, pairs, bn, rp_split, load);
+    if (c < cost - 1e-9) {
+      cost = c;
+      best = {bn, rp_split};
+    }
+  };
+  consider(BN / 2, row_pairs);
+  // a tail of row pairs in 128-column tiles, at most two rounds of them
+  for (int k = 1; k <= row_pairs && (long long)k * n128 <= 2LL * pairs; ++k)
+    consider(BN, row_pairs - k);
+  cache[next] = {M, N, num_sms, best};
+  next = (next + 1) % 8;
+  return best;
+}
+
+Params base_params(const Problem &pr, int N, int K, Plan plan = {BN, 1 << 30}) {
   Params p = {};
   p.N = N;
   p.K = K;
-  p.bn = bn;
+  p.bn = plan.bn;
   p.m_tiles = (int)(pr.M / BM);
-  p.n_tiles = (N + bn - 1) / bn;
-  p.total = (p.m_tiles + 1) / 2 * p.n_tiles;
+  const int row_pairs = (p.m_tiles + 1) / 2;
+  p.n_tiles = (N + plan.bn - 1) / plan.bn;
+  p.rp_split = plan.rp_split < row_pairs ? plan.rp_split : row_pairs;
+  p.n_tiles2 = (N + BN / 2 - 1) / (BN / 2);
+  p.t_split = p.rp_split * p.n_tiles;
+  p.total = p.t_split + (row_pairs - p.rp_split) * p.n_tiles2;
   p.status = pr.status;
   p.M_tokens = (int)pr.M;
   p.e = pr.e;
@@ -711,7 +795,7 @@ cudaError_t pair_gemm_bf16(const void *A, const void *B, int b_km, void *C, int 
   pr.status = status;
   pr.stream = stream;
   pr.num_sms = num_sms;
-  const Params p = base_params(pr, N, K, store_bn(M, N, num_sms));
+  const Params p = base_params(pr, N, K, plan_tiles(M, N, num_sms));
   if (b_km) return launch<EPI_STORE, true>(tmA, tmB, tC, tC, tC, p, pr);
   return launch<EPI_STORE>(tmA, tmB, tC, tC, tC, p, pr);
 }
@@ -734,7 +818,7 @@ cudaError_t pair_gate_grad_bf16(const void *dO, const void *W_o, void *pre, cons
   pr.status = status;
   pr.stream = stream;
   pr.num_sms = num_sms;
-  const Params p = base_params(pr, e, d, store_bn(M, e, num_sms));
+  const Params p = base_params(pr, e, d, plan_tiles(M, e, num_sms));
   return launch<EPI_GATE_GRAD, true>(tmA, tmB, tD, tX, tV, p, pr);
 }
 
@@ -773,7 +857,7 @@ cudaError_t tc_output_bf16(const Problem &pr) {
   if ((err = make_tmap_bf16_2d(&tmB, pr.W_o, pr.e, pr.d, pr.d, BK, 64)) != cudaSuccess)
     return err;
   if ((err = make_tmap_bf16_2d(&tO, pr.out, pr.M, pr.d, pr.d, 32, 64)) != cudaSuccess) return err;
-  Params p = base_params(pr, pr.d, pr.e, store_bn(pr.M, pr.d, pr.num_sms));
+  Params p = base_params(pr, pr.d, pr.e, plan_tiles(pr.M, pr.d, pr.num_sms));
   p.residual = (const __nv_bfloat16 *)pr.residual;
   return launch<EPI_STORE>(tmA, tmB, tO, tO, tO, p, pr);
 }
