@@ -752,9 +752,10 @@ cudaError_t tc_chunk_attention_bf16(const Problem &pr) {
     p.ng = 2;
   }
   p.n_vg = p.n_et / p.ng;
-  // the last chunks as single-tile units: about one per SM
+  // the last chunks as single-tile units: about one for every two SMs (one
+  // per SM, or two, ended the schedule later on the long workload)
   const int BG = pr.B * pr.G, per_chunk = p.n_qt * p.n_et;
-  int singles = p.ng > 1 ? (pr.num_sms + per_chunk - 1) / per_chunk : BG;
+  int singles = p.ng > 1 ? (pr.num_sms / 2 + per_chunk - 1) / per_chunk : BG;
   if (singles > BG) singles = BG;
   p.g_split = BG - singles;
   p.n_grouped = p.g_split * p.n_qt * p.n_vg;
