@@ -81,6 +81,9 @@ def _run(B, T, d, e, s, C, causal, dtype, lin_scale, seed, local_scale=1.0):
     # take several rounds of tiles
     ((1, 2048, 768, 1536, 128, 256), True, "bf16", 1.0),
     ((2, 1024, 768, 1536, 128, 256), False, "bf16", 1.0),
+    # 40 row pairs of 256: the dA (gate gradient) and dX pair GEMMs run a
+    # last partial round of their tiles as 128-column tiles
+    ((5, 2048, 512, 512, 128, 256), True, "bf16", 1.0),
 ])
 def test_backward_matches_oracle(shape, causal, dtype, lin_scale):
     B, T, d, e, s, C = shape
